@@ -1,0 +1,384 @@
+"""Benchmark of the TurboQuant KV-cache hot path on GB300.
+
+One step = one decode step of the 32K long-context workload (batch 1, 64 query
+heads / 8 KV heads, head_dim 128, 8-bit K / 3-bit V, 32768 cached tokens):
+  1. encode the step's new token (K and V of every KV head) into the cache,
+  2. fused split-K decode attention over the whole packed cache.
+value = packed-KV bytes attended per second (GB/s), L2 flushed before every
+step.  The roofline object is the decode-attention kernel alone (CUDA events
+around its launch); `e2e` adds the host->device copy of the step's inputs (q,
+new K/V, lengths) from pinned memory and the device->host read of the output.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
+
+--impl reference times the CPU oracle (the plain, slow implementation the tests
+compare against) on the host cores over a bounded sample of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica (the method has
+no exchange step); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import tq_inputs  # noqa: E402
+
+WORKLOAD = "c4_long_k8v3"
+METRIC = "fused decode-attend GB/s of packed KV (% of HBM peak); encode Mvec/s"
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _source_sha():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "quantized_kv_cache_10_gb300", "csrc", "*"))):
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_name):
+    """DRAM bytes per launch from a committed ncu summary, if taken on the current source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_name)
+    if not e or e.get("source_sha") != _source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class Clocks:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- CPU oracle (baseline arm)
+class OracleSample:
+    """The oracle's decode attention over a token prefix of every (b, kvh) unit of a
+    workload, on a thread pool (ctypes releases the GIL during each oracle call)."""
+
+    def __init__(self, w, seconds_target=12.0, threads=None):
+        import oracle
+        self.oracle = oracle
+        self.w = w
+        self.threads = threads or len(os.sched_getaffinity(0))
+        self.ok_k = oracle.Codec(w.d, w.k_bits, w.rot_seed)
+        self.ok_v = oracle.Codec(w.d, w.v_bits, w.rot_seed)
+        self.units = [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+        self.q = w.q()
+        self.n = 256
+        self._prep()
+        dt = self.run()
+        n = int(min(w.S, max(256, self.n * seconds_target / max(dt, 1e-3))))
+        self.n = max(256, n // 8 * 8)
+        self._prep()
+        self.used = min(self.threads, len(self.units))
+
+    def _prep(self):
+        w, n = self.w, self.n
+        self.data = []
+        for b, h in self.units:
+            K, V = w.k_slice(b, h, n), w.v_slice(b, h, n)
+            kc, kn = (K, None) if w.k_bits == 16 else self.ok_k.encode(K)[:2]
+            vc, vn = self.ok_v.encode(V)[:2]
+            self.data.append((b, h, kc, kn, vc, vn))
+
+    def run(self):
+        from concurrent.futures import ThreadPoolExecutor
+        w, n = self.w, self.n
+
+        def one(t):
+            b, h, kc, kn, vc, vn = t
+            self.oracle.attention_unit(self.ok_k, self.ok_v, self.q[b, h * w.G:(h + 1) * w.G], kc, kn, vc, vn, n,
+                                       1 / math.sqrt(w.d))
+
+        t0 = time.perf_counter()
+        with ThreadPoolExecutor(min(self.threads, len(self.data))) as ex:
+            list(ex.map(one, self.data))
+        return time.perf_counter() - t0
+
+    def bytes(self):
+        w = self.w
+        kb = w.d * 2 if w.k_bits == 16 else w.d * w.k_bits // 8 + 2
+        vb = w.d * w.v_bits // 8 + 2
+        return self.n * len(self.units) * (kb + vb)
+
+    def describe(self):
+        w = self.w
+        return (f"oracle decode attention over the first {self.n} of {w.S} tokens of all {len(self.units)} "
+                f"(batch, kv-head) units of {w.name} on {self.used} threads")
+
+
+def reference_arm(args):
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return
+    w = tq_inputs.WORKLOADS[args.workload]
+    per_step = max(0.5, min(args.ref_seconds, 150.0 / (args.steps + args.warmup)))
+    smp = OracleSample(w, seconds_target=per_step)
+    per = []
+    for i in range(args.warmup + args.steps):
+        dt = smp.run()
+        if i >= args.warmup:
+            per.append(smp.bytes() / dt / 1e9)
+    v = statistics.median(per)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d{w.d} S{w.S} K{w.k_bits}/V{w.v_bits}"},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "cores": smp.used, "kind": "oracle",
+                             "sample": smp.describe()},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def gpu_arm(args):
+    import torch
+    ws_, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if ws_ > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import quantized_kv_cache_10_gb300 as tq
+
+    w = tq_inputs.WORKLOADS[args.workload]
+    ck = tq.tq_codec_create(w.d, w.k_bits, w.rot_seed)
+    cv = tq.tq_codec_create(w.d, w.v_bits, w.rot_seed)
+    # prefill: generate K/V on the host, encode the whole cache on the GPU
+    K, V = w.kv("k", 16), w.kv("v", 16)
+    n = w.B * w.Hkv * w.S
+    kc = torch.empty((w.B, w.Hkv, w.S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
+    kn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
+    vc = torch.empty((w.B, w.Hkv, w.S, cv.bytes_per_vec), dtype=torch.uint8, device=dev)
+    vn = torch.empty_like(kn)
+    Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    # encode throughput of the prefill (one launch per tensor), events on this stream
+    enc_times = []
+    for i in range(4):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        tq.tq_encode(ck, Kd.view(n, w.d), kc.view(n, -1), kn.view(-1))
+        tq.tq_encode(cv, Vd.view(n, w.d), vc.view(n, -1), vn.view(-1))
+        e1.record()
+        torch.cuda.synchronize()
+        if i > 0:
+            enc_times.append(e0.elapsed_time(e1) * 1e-3)
+    enc_mvec = 2 * n / statistics.median(enc_times) / 1e6
+    del Kd, Vd
+    q = torch.from_numpy(w.q()).to(dev)
+    lens = torch.from_numpy(w.lengths()).to(dev)
+    pos = (lens - 1).to(torch.int32)                         # the step's token is the last cached one
+    k_new = torch.from_numpy(np.ascontiguousarray(K[:, :, -1:])).to(dev)
+    v_new = torch.from_numpy(np.ascontiguousarray(V[:, :, -1:])).to(dev)
+    out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16, device=dev)
+    wsb = torch.empty(tq.tq_decode_attend_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.d), dtype=torch.uint8, device=dev)
+    tq.tq_workspace_init(wsb)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        tq.tq_encode_append(ck, k_new, pos, kc, kn)
+        tq.tq_encode_append(cv, v_new, pos, vc, vn)
+
+    def attend():
+        tq.tq_decode_attend(ck, cv, q, kc, kn, vc, vn, lens, out, wsb)
+
+    launches_per_step = 3
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+        attend()
+    torch.cuda.synchronize()
+    if ws_ > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    step_t, dec_t = [], []
+    with Clocks(local) as clk:
+        for _ in range(args.steps):
+            flush.zero_()
+            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            attend()
+            e2.record(stream)
+            torch.cuda.synchronize()
+            step_t.append(e0.elapsed_time(e2) * 1e-3)
+            dec_t.append(e1.elapsed_time(e2) * 1e-3)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(wsb) == 0
+    tot = sum(step_t)
+    if ws_ > 1:
+        t = torch.tensor([tot], device=dev, dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        tot = float(t.item())
+        torch.distributed.barrier()
+    bytes_step = w.packed_kv_bytes()
+    value = ws_ * bytes_step * args.steps / tot / 1e9
+    dec_mean = statistics.mean(dec_t)
+    peak, peak_kind = _peaks()
+    achieved = bytes_step / dec_mean / 1e9
+
+    # ---- end to end through the public API: pinned host inputs in, output back ----
+    h_q = torch.from_numpy(w.q()).pin_memory()
+    h_k = torch.from_numpy(np.ascontiguousarray(K[:, :, -1:])).pin_memory()
+    h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -1:])).pin_memory()
+    h_len = torch.from_numpy(w.lengths()).pin_memory()
+    h_out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16).pin_memory()
+    e2e_t = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        lens.copy_(h_len, non_blocking=True)
+        torch.sub(lens, 1, out=pos)
+        step()
+        attend()
+        h_out.copy_(out, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= args.warmup:
+            e2e_t.append(e0.elapsed_time(e1) * 1e-3)
+    h2d = h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_len.numel() * 4
+    d2h = h_out.numel() * 2
+    e2e_v = ws_ * bytes_step / statistics.mean(e2e_t) / 1e9
+
+    if rank != 0:
+        if ws_ > 1:
+            torch.distributed.destroy_process_group()
+        return
+    cpu = None
+    if ws_ == 1 and not args.no_cpu_baseline:
+        smp = OracleSample(w, seconds_target=args.ref_seconds)
+        dt = smp.run()
+        cpu = {"value": smp.bytes() / dt / 1e9, "unit": "GB/s", "cores": smp.used, "kind": "oracle",
+               "sample": smp.describe()}
+    kname = "decode_attend"
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d{w.d} S{w.S} K{w.k_bits}/V{w.v_bits}",
+                   "step": "encode new token (K,V) + fused decode attention",
+                   "packed_kv_bytes": bytes_step, "l2": "flushed before every step (write of 2x L2)",
+                   "parallelism": f"replicas x{ws_}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": _traffic(kname), "peak_kind": peak_kind,
+                     "kernel": kname, "decode_us": dec_mean * 1e6},
+        "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": 2 * n, "dim": w.d},
+        "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if ws_ > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(tq_inputs.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

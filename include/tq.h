@@ -1,0 +1,212 @@
+/*
+ * tq.h -- C ABI of libtq, the GB300 (sm_103a) TurboQuant KV-cache hot path.
+ *
+ * What the library computes follows these pages (titles and sections):
+ *  [PR]  "add TurboQuant KV cache compression" (mlx-swift-lm pull request #232):
+ *        "Schemes" (asymmetric K/V bit widths, raw-fp16 keys) and "Design"
+ *        (WHT for power-of-two head dims, dense fallback otherwise, one
+ *        rotation and codebook shared per (dim, bits, seed), pending tokens
+ *        encoded in batches).
+ *  [VQ]  VeloxQuant-MLX, "How I built VeloxQuant-MLX": "Stage 1: Random
+ *        Rotation", "Stage 2: Lloyd-Max Scalar Quantization" (norm kept as
+ *        fp16), "The Core Idea" (Lloyd-Max conditions), "The Bit-Packing
+ *        Problem" (LSB-first packing).
+ *  [RVQ] VeloxQuant-MLX RVQ post, "The Throughput Problem": O(d log d)
+ *        Hadamard rotation; quantisation by counting the midpoints a value
+ *        exceeds.
+ *  [TW]  "anyone still talking about mlx-swift-lm?": fused single-dispatch
+ *        decode -- score, softmax and inline dequant in one kernel, K read
+ *        once in its rotated basis, GQA served without expanding K/V.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named as device memory must point to memory of the device that
+ *    is current when the call is made; host pointers are plain host memory.
+ *  - fp16 values are passed as uint16_t bit patterns (IEEE binary16).
+ *  - `stream` is a cudaStream_t cast to void* (NULL = the legacy default
+ *    stream).  Every compute call only enqueues work on that stream and
+ *    returns; nothing allocates device memory except tq_codec_create.
+ *  - Arguments are checked before any launch; a failed check returns a
+ *    status and enqueues nothing.  Violations that can only be seen on the
+ *    device (lengths or positions read from device memory) are clamped and
+ *    recorded in a device error word (see tq_get_device_error); kernels never
+ *    trap and never wait on other blocks.
+ *  - Inputs holding Inf/NaN are outside the contract.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ_OK = 0,
+    TQ_ERR_INVALID_ARG = 1,   /* a pointer, size, stride or alignment is invalid */
+    TQ_ERR_UNSUPPORTED = 2,   /* a valid request this build has no kernel for */
+    TQ_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    TQ_ERR_OOM = 4,           /* tq_codec_create could not allocate */
+    TQ_ERR_WORKSPACE = 5,     /* workspace missing or smaller than required */
+    TQ_ERR_DEVICE_CHECK = 6   /* a device-side check fired (tq_get_device_error) */
+} tq_status;
+
+/* Device error codes (bit flags) recorded by kernels. */
+#define TQ_DEVERR_SEQ_LEN   1   /* seq_lens[b] < 0 or > max_seq: clamped */
+#define TQ_DEVERR_POSITION  2   /* encode_append position outside [0, max_seq): row skipped */
+
+typedef struct tq_codec tq_codec;   /* opaque; immutable after creation */
+
+/* Library version as 10000*major + 100*minor + patch. */
+int tq_version(void);
+
+/* Short English text for a status code (static storage). */
+const char *tq_status_string(tq_status s);
+
+/*
+ * Codec: the rotation and codebook shared by every layer that uses the same
+ * (dim, bits, seed) ([PR] Design, "Shared codecs").
+ *   dim   head dimension, a multiple of 32 in [32, 512].  Powers of two use
+ *         the randomised Walsh-Hadamard rotation R = H diag(s) / sqrt(dim)
+ *         with Rademacher signs s drawn from SplitMix64(seed) ([VQ] Stage 1,
+ *         [RVQ]); other sizes use a dense orthogonal Q, the QR factor of a
+ *         seeded Gaussian matrix ([PR] Design; [VQ] Stage 1).
+ *   bits  2, 3, 4 or 8: Lloyd-Max codebook of N(0,1) with 2^bits levels
+ *         ([VQ] The Core Idea); 16: raw fp16 keys, no codebook ([PR] Schemes,
+ *         turbo0v*; such a codec may only be passed as the K codec of
+ *         tq_decode_attend).
+ *   seed  selects the signs / the dense matrix.
+ * The codec is built on the host (fp64) and its tables are copied to the
+ * current device, which the codec then belongs to.  *out receives a handle
+ * owned by the caller (free with tq_codec_destroy).  Thread-safe to use from
+ * several threads once created.
+ * Errors: TQ_ERR_INVALID_ARG (dim/bits/out), TQ_ERR_OOM, TQ_ERR_CUDA.
+ */
+tq_status tq_codec_create(int dim, int bits, uint64_t seed, tq_codec **out);
+
+/* Frees the codec and its device tables (NULL is ignored).  The caller must
+ * ensure no enqueued work still uses it. */
+void tq_codec_destroy(tq_codec *codec);
+
+/* Codec parameters; any output pointer may be NULL.  bytes_per_vec is the
+ * packed row size dim*bits/8 (dim*2 for bits == 16); is_wht is 1 for the
+ * Hadamard rotation, 0 for the dense one. */
+tq_status tq_codec_info(const tq_codec *codec, int *dim, int *bits, int *bytes_per_vec,
+                        int *is_wht);
+
+/* Copies the codec's host tables out (any pointer may be NULL):
+ *   signs      [dim] int8 (+1/-1), WHT codecs only (left untouched otherwise)
+ *   dense_q    [dim*dim] fp32 row-major Q (z = Q k), dense codecs only
+ *   centroids  [2^bits] fp32 ascending (not for bits == 16)
+ *   midpoints  [2^bits - 1] fp64, (c_i + c_{i+1}) / 2
+ * These are the tables the kernels use; tests compare them with tables an
+ * independent implementation builds from the same (dim, bits, seed). */
+tq_status tq_codec_export(const tq_codec *codec, int8_t *signs, float *dense_q, float *centroids,
+                          double *midpoints);
+
+/*
+ * Encode n_vec fp16 vectors ([VQ] Stage 1 + Stage 2; [RVQ] boundary-count
+ * quantisation; [VQ] The Bit-Packing Problem), bit-exactly:
+ *   k_i = x_i * 2^24 exactly; S = sum k_i^2 exactly; D = RN64(sqrt(RN64(S)));
+ *   WHT: w = H (s . k) exactly, code_j = #{ i : w_j > RN64(m_i * D) };
+ *   dense: z_j = fp64 fma chain of Q[j][i] * k_i over ascending i,
+ *          code_j = #{ i : z_j > RN64(m_i * RN64(D / RN64(sqrt(dim)))) };
+ *   codes packed LSB-first (bit j*bits + t of the row = bit t of code_j);
+ *   norms[v] = RN16(D * 2^-24) (the L2 norm of the fp16 vector).
+ *   x       device, fp16, row v at x + v * x_row_stride (elements)
+ *   codes   device, row v at codes + v * code_row_stride (bytes), each row
+ *           bytes_per_vec long, written completely
+ *   norms   device, fp16 [n_vec]
+ * Requirements: x 4-byte aligned and x_row_stride even; codes 4-byte aligned
+ * and code_row_stride a multiple of 4; bits != 16.  n_vec == 0 is a no-op.
+ */
+tq_status tq_encode(const tq_codec *codec, const uint16_t *x, int64_t n_vec, int64_t x_row_stride,
+                    uint8_t *codes, int64_t code_row_stride, uint16_t *norms, void *stream);
+
+/*
+ * Encode a pending-token batch straight into a cache ([PR] Design, "Batch
+ * recompression": pending tokens encoded together).
+ *   x          device fp16 [B, n_kv_heads, T, dim] contiguous
+ *   start_pos  device int32 [B]: token t of sequence b goes to position
+ *              start_pos[b] + t
+ *   codes      device cache [B, n_kv_heads, max_seq, bytes_per_vec]
+ *   norms      device cache [B, n_kv_heads, max_seq] fp16
+ *   dev_error  optional device int32 word; positions outside [0, max_seq)
+ *              are skipped and TQ_DEVERR_POSITION is OR-ed into it.
+ * Same arithmetic and alignment rules as tq_encode.
+ */
+tq_status tq_encode_append(const tq_codec *codec, const uint16_t *x, int B, int n_kv_heads, int T,
+                           const int32_t *start_pos, int64_t max_seq, uint8_t *codes,
+                           uint16_t *norms, int32_t *dev_error, void *stream);
+
+/*
+ * Dequantise (debugging aid): out[v] = n16_v * R^T (c[codes_v] / sqrt(dim)),
+ * fp32, computed with a fp32 butterfly (WHT) or fp32 Q^T product (dense).
+ *   codes device [n_vec, bytes_per_vec] contiguous; norms device fp16
+ *   [n_vec]; out device fp32 [n_vec, dim].  Requires codes 4-byte aligned.
+ */
+tq_status tq_dequant(const tq_codec *codec, const uint8_t *codes, const uint16_t *norms,
+                     int64_t n_vec, float *out, void *stream);
+
+/*
+ * Bytes of device workspace tq_decode_attend needs for this shape on the
+ * current device (0 on invalid arguments).  The workspace holds a device
+ * error word, one arrival counter per (batch, KV head) and the split-K
+ * partial results.
+ */
+size_t tq_decode_attend_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
+                                        int dim);
+
+/* Zeroes a workspace on `stream`.  Required once before the first
+ * tq_decode_attend that uses it; kernels leave the counters at zero again. */
+tq_status tq_workspace_init(void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Fused single-dispatch decode attention over the packed cache ([TW]; [PR]
+ * Design): one query per sequence,
+ *   out[b,h] = sum_n softmax_n(scale * <q[b,h], K^[b,kvh,n]>) V^[b,kvh,n],
+ *   n < seq_lens[b], kvh = h / (n_q_heads / n_kv_heads) (each KV head serves
+ *   its contiguous group of query heads without expanding K/V),
+ * where K^ and V^ are the dequantised cache (K^ = raw fp16 when the K codec
+ * has bits == 16).  The query is rotated once, scores and P.V are computed
+ * in the rotated basis against codebook values, the softmax is online and
+ * split over the sequence (flash-decoding), and one inverse V rotation is
+ * applied to each output head.  seq_lens[b] == 0 gives a zero output.
+ *   ck, cv     K and V codecs: same dim; cv->bits != 16
+ *   q          device fp16 [B, n_q_heads, dim]
+ *   k          device: packed K codes [B, n_kv_heads, max_seq, ck bytes_per_vec]
+ *              or raw fp16 K [B, n_kv_heads, max_seq, dim] (ck bits == 16)
+ *   k_norms    device fp16 [B, n_kv_heads, max_seq] (NULL for raw K)
+ *   v_codes    device [B, n_kv_heads, max_seq, cv bytes_per_vec]
+ *   v_norms    device fp16 [B, n_kv_heads, max_seq]
+ *   seq_lens   device int32 [B]; values outside [0, max_seq] are clamped and
+ *              flagged with TQ_DEVERR_SEQ_LEN
+ *   scale      softmax scale (1/sqrt(dim) in the usual model)
+ *   out        device fp16 [B, n_q_heads, dim]
+ *   workspace  device, >= tq_decode_attend_workspace_bytes(...) bytes,
+ *              256-byte aligned, zeroed once by tq_workspace_init; one
+ *              workspace must not be used by two calls that can overlap.
+ * Requirements: n_q_heads % n_kv_heads == 0; max_seq % 8 == 0; every cache
+ * pointer 16-byte aligned.  Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED,
+ * TQ_ERR_WORKSPACE, TQ_ERR_CUDA.
+ */
+tq_status tq_decode_attend(const tq_codec *ck, const tq_codec *cv, const uint16_t *q,
+                           const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                           const uint16_t *v_norms, const int32_t *seq_lens, int B, int n_q_heads,
+                           int n_kv_heads, int64_t max_seq, float scale, uint16_t *out,
+                           void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * Reads and clears the device error word of a decode workspace (or of any
+ * int32 word passed as dev_error to tq_encode_append).  Synchronises
+ * `stream`.  *code receives the OR of TQ_DEVERR_* flags seen since the last
+ * read; returns TQ_ERR_DEVICE_CHECK when it is non-zero.
+ */
+tq_status tq_get_device_error(void *error_word, void *stream, int *code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

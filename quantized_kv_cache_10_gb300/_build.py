@@ -1,0 +1,91 @@
+"""Builds libtq.so (the C-ABI library) in-tree with nvcc for sm_103a.
+
+Every translation unit is compiled in parallel; objects live in ``_build/``
+next to this file and ``libtq.so`` lands in the package directory.  ptxas
+resource usage (registers, spills, shared memory) of each kernel is kept in
+``_build/ptxas.log``.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+import sys
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INC = os.path.join(ROOT, "include")
+BUILD = os.path.join(PKG, "_build")
+LIB = os.path.join(PKG, "libtq.so")
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _cuda_home() -> str:
+    home = os.environ.get("CUDA_HOME") or "/usr/local/cuda"
+    if not os.path.exists(os.path.join(home, "bin", "nvcc")):
+        nv = shutil.which("nvcc")
+        if nv:
+            home = os.path.dirname(os.path.dirname(os.path.realpath(nv)))
+    return home
+
+
+def _headers():
+    return glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
+        [os.path.join(INC, "tq.h")]
+
+
+def _stale(obj: str, src: str) -> bool:
+    if not os.path.exists(obj):
+        return True
+    t = os.path.getmtime(obj)
+    return any(os.path.getmtime(f) > t for f in [src] + _headers())
+
+
+def _compile(src: str, cuda: str) -> tuple[str, str]:
+    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+    if not _stale(obj, src):
+        return obj, ""
+    nvcc = os.path.join(cuda, "bin", "nvcc")
+    common = ["-O3", "-std=c++17", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    if src.endswith(".cu"):
+        cmd = [nvcc, *ARCH, "-lineinfo", "--expt-relaxed-constexpr", "-Xptxas", "-v", *common,
+               "-c", src, "-o", obj]
+    else:
+        cmd = [nvcc, *common, "-x", "c++", "-c", src, "-o", obj]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"compile failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    return obj, r.stderr
+
+
+def build(verbose: bool = False) -> str:
+    """Compile every csrc/*.cu and *.cpp and link libtq.so; returns its path."""
+    cuda = _cuda_home()
+    os.makedirs(BUILD, exist_ok=True)
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
+    with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
+        results = list(ex.map(lambda s: _compile(s, cuda), srcs))
+    objs = [o for o, _ in results]
+    logs = [log for _, log in results if log]
+    if logs:
+        with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+            f.write("\n".join(logs))
+    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+        tmp = LIB + f".tmp{os.getpid()}"
+        cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+               "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, LIB)
+    if verbose:
+        print(LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(verbose="-v" in sys.argv)

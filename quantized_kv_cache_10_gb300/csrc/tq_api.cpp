@@ -1,0 +1,123 @@
+// tq_api.cpp -- argument checking and dispatch for the C ABI in include/tq.h.
+// Every check happens before anything is enqueued; a failed check returns a
+// status and leaves the stream untouched.
+#include <cstdint>
+
+#include "tq_internal.h"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+tq_status from_cuda(cudaError_t e) {
+    if (e == cudaSuccess) return TQ_OK;
+    if (e == cudaErrorNotSupported) return TQ_ERR_UNSUPPORTED;
+    return TQ_ERR_CUDA;
+}
+
+bool on_codec_device(const tq_codec* c) {
+    int d = -1;
+    return cudaGetDevice(&d) == cudaSuccess && d == c->device;
+}
+
+}  // namespace
+
+extern "C" {
+
+tq_status tq_encode(const tq_codec* c, const uint16_t* x, int64_t n_vec, int64_t x_row_stride, uint8_t* codes,
+                    int64_t code_row_stride, uint16_t* norms, void* stream) {
+    if (!c || c->bits == 16 || n_vec < 0) return TQ_ERR_INVALID_ARG;
+    if (n_vec == 0) return TQ_OK;
+    if (!x || !codes || !norms) return TQ_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || (x_row_stride & 1) || x_row_stride < c->dim) return TQ_ERR_INVALID_ARG;
+    if (!aligned(codes, 4) || (code_row_stride & 3) || code_row_stride < c->bytes_per_vec)
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned(norms, 2) || !on_codec_device(c)) return TQ_ERR_INVALID_ARG;
+    return from_cuda(tq::launch_encode(c, x, n_vec, x_row_stride, codes, code_row_stride, norms, 0, 0, 0, nullptr,
+                                       0, nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_encode_append(const tq_codec* c, const uint16_t* x, int B, int n_kv_heads, int T,
+                           const int32_t* start_pos, int64_t max_seq, uint8_t* codes, uint16_t* norms,
+                           int32_t* dev_error, void* stream) {
+    if (!c || c->bits == 16 || B < 0 || n_kv_heads < 0 || T < 0 || max_seq <= 0) return TQ_ERR_INVALID_ARG;
+    if (B == 0 || n_kv_heads == 0 || T == 0) return TQ_OK;
+    if (!x || !start_pos || !codes || !norms) return TQ_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(codes, 4) || !aligned(norms, 2) || !aligned(start_pos, 4))
+        return TQ_ERR_INVALID_ARG;
+    if (dev_error && !aligned(dev_error, 4)) return TQ_ERR_INVALID_ARG;
+    if (!on_codec_device(c)) return TQ_ERR_INVALID_ARG;
+    return from_cuda(tq::launch_encode(c, x, 0, c->dim, codes, c->bytes_per_vec, norms, B, n_kv_heads, T,
+                                       start_pos, max_seq, dev_error, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_dequant(const tq_codec* c, const uint8_t* codes, const uint16_t* norms, int64_t n_vec, float* out,
+                     void* stream) {
+    if (!c || c->bits == 16 || n_vec < 0) return TQ_ERR_INVALID_ARG;
+    if (n_vec == 0) return TQ_OK;
+    if (!codes || !norms || !out || !aligned(codes, 4) || !aligned(norms, 2) || !aligned(out, 4))
+        return TQ_ERR_INVALID_ARG;
+    if (!on_codec_device(c)) return TQ_ERR_INVALID_ARG;
+    return from_cuda(tq::launch_dequant(c, codes, norms, n_vec, out, static_cast<cudaStream_t>(stream)));
+}
+
+size_t tq_decode_attend_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int64_t max_seq, int dim) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dim < 32 || dim > 512 || dim % 32) return 0;
+    tq::DecodePlan p;
+    if (!tq::make_decode_plan(dim, dev, B, n_q_heads, n_kv_heads, max_seq, p)) return 0;
+    return p.ws_bytes;
+}
+
+tq_status tq_workspace_init(void* ws, size_t bytes, void* stream) {
+    if (!ws || bytes == 0) return TQ_ERR_INVALID_ARG;
+    return from_cuda(cudaMemsetAsync(ws, 0, bytes, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_decode_attend(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, const void* k,
+                           const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
+                           const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
+                           float scale, uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
+    if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
+    if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
+    if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
+    if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned(q, 4) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
+    if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
+    tq::DecodePlan p;
+    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
+    tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
+                     B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (tq::decode_mma_supported(ck, cv, p.G)) {
+        p.kernel = 1;
+        cudaError_t e = tq::launch_decode_mma(a, p, st);
+        if (e != cudaErrorNotSupported) return from_cuda(e);
+        p.kernel = 0;
+    }
+    return from_cuda(tq::launch_decode_simt(a, p, st));
+}
+
+tq_status tq_get_device_error(void* error_word, void* stream, int* code) {
+    if (!error_word || !code) return TQ_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, error_word, sizeof(v), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return TQ_ERR_CUDA;
+    *code = v;
+    if (v != 0) {
+        e = cudaMemsetAsync(error_word, 0, sizeof(v), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return TQ_ERR_CUDA;
+        return TQ_ERR_DEVICE_CHECK;
+    }
+    return TQ_OK;
+}
+
+}  // extern "C"

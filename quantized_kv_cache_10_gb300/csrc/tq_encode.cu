@@ -1,0 +1,339 @@
+// tq_encode.cu -- bit-exact TurboQuant encode on sm_103a.
+//
+// Per vector ("How I built VeloxQuant-MLX", Stage 1 + Stage 2; RVQ post,
+// "The Throughput Problem"; "add TurboQuant KV cache compression", Design):
+//   k_i = x_i * 2^24 (exact int64), S = sum k_i^2 (exact 128-bit),
+//   D = RN64(sqrt(RN64(S))), norm = RN16(D * 2^-24);
+//   WHT dims: w = H (s . k) by an exact int64 butterfly (registers, then
+//   warp shuffles), code_j = #{ i : w_j > RN64(m_i * D) };
+//   other dims: z_j = fp64 fma chain of Q[j][i] k_i over ascending i,
+//   code_j = #{ i : z_j > RN64(m_i * RN64(D / RN64(sqrt(d)))) };
+//   codes packed LSB-first into 32-bit words.
+// One warp per vector: lane l owns elements [l*E, (l+1)*E), E = d / 32.  The
+// 2^b - 1 thresholds of a vector are computed once per warp (spread over its
+// lanes) into shared memory and each coordinate finds its code by a b-step
+// binary search over them ("number of boundaries exceeded").
+#include <cuda_fp16.h>
+#include <math_constants.h>
+
+#include "tq_internal.h"
+
+namespace tq {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+struct EncParams {
+    const uint16_t* x;
+    int64_t n;
+    int64_t xstride;
+    uint8_t* codes;
+    int64_t cstride;
+    uint16_t* norms;
+    // append mode when B > 0
+    int B, H, T;
+    const int32_t* start_pos;
+    int64_t max_seq;
+    int32_t* dev_error;
+    // codec
+    const double* mid;
+    const uint32_t* sign_bits;
+    const float* qt;  // Q^T row-major (dense)
+    int bits;
+    int dim;
+};
+
+__device__ __forceinline__ int64_t f16_exact(uint32_t h) {
+    const int e = (h >> 10) & 31;
+    const int64_t m = h & 1023;
+    const int64_t k = (e == 0) ? m : ((m | 1024) << (e - 1));
+    return (h & 0x8000u) ? -k : k;
+}
+
+// Correctly rounded conversion of the unsigned 128-bit integer hi:lo.
+__device__ __forceinline__ double u128_to_f64_rn(uint64_t hi, uint64_t lo) {
+    if (hi == 0) return __ull2double_rn(lo);
+    const int nz = __clzll(static_cast<long long>(hi));
+    uint64_t top, rest;
+    if (nz == 0) {
+        top = hi;
+        rest = lo;
+    } else {
+        top = (hi << nz) | (lo >> (64 - nz));
+        rest = lo << nz;
+    }
+    top |= (rest != 0) ? 1ull : 0ull;  // sticky bit below the rounding position
+    return ldexp(__ull2double_rn(top), 64 - nz);
+}
+
+// Exact sum of squares of the warp's values, returned as RN64 on all lanes.
+template <int E>
+__device__ __forceinline__ double warp_sumsq_rn(const int64_t (&k)[E], int E_rt) {
+    uint64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (e < E_rt) {
+            const uint64_t a = static_cast<uint64_t>(k[e] < 0 ? -k[e] : k[e]);
+            const uint64_t plo = a * a, phi = __umul64hi(a, a);
+            const uint64_t nlo = lo + plo;
+            hi += phi + (nlo < lo ? 1ull : 0ull);
+            lo = nlo;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t olo = __shfl_xor_sync(kFull, lo, off);
+        const uint64_t ohi = __shfl_xor_sync(kFull, hi, off);
+        const uint64_t nlo = lo + olo;
+        hi += ohi + (nlo < lo ? 1ull : 0ull);
+        lo = nlo;
+    }
+    return u128_to_f64_rn(hi, lo);
+}
+
+// Source row, destination row, and whether the row is written.
+__device__ __forceinline__ bool map_row(const EncParams& p, int64_t v, const uint16_t*& src,
+                                        int64_t& dst) {
+    if (p.B <= 0) {
+        src = p.x + v * p.xstride;
+        dst = v;
+        return true;
+    }
+    const int64_t per_b = static_cast<int64_t>(p.H) * p.T;
+    const int64_t b = v / per_b;
+    const int64_t rem = v - b * per_b;
+    const int64_t h = rem / p.T;
+    const int64_t t = rem - h * p.T;
+    src = p.x + v * p.dim;
+    const int64_t pos = static_cast<int64_t>(__ldg(p.start_pos + b)) + t;
+    if (pos < 0 || pos >= p.max_seq) return false;
+    dst = (b * p.H + h) * p.max_seq + pos;
+    return true;
+}
+
+template <int E>
+__device__ __forceinline__ void load_row(const uint16_t* src, int lane, int E_rt, uint32_t (&hv)[E]) {
+    const uint16_t* s = src + lane * E_rt;
+    if ((E_rt & 1) == 0) {
+        const uint32_t* s32 = reinterpret_cast<const uint32_t*>(s);
+#pragma unroll
+        for (int e = 0; e < E; e += 2) {
+            if (e < E_rt) {
+                const uint32_t u = __ldg(s32 + e / 2);
+                hv[e] = u & 0xffffu;
+                if (e + 1 < E) hv[e + 1] = u >> 16;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if (e < E_rt) hv[e] = __ldg(s + e);
+    }
+}
+
+// Packs the lane's E codes into the warp's shared word buffer and writes the
+// row (d*b/32 words) with coalesced 32-bit stores.
+template <int E>
+__device__ __forceinline__ void pack_store(const int (&code)[E], int E_rt, int lane, int bits, int dim,
+                                           uint32_t* buf, uint8_t* dst_row) {
+    const int W = dim * bits / 32;
+    for (int i = lane; i < W; i += 32) buf[i] = 0u;
+    __syncwarp();
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (e < E_rt) {
+            const int p = (lane * E_rt + e) * bits;
+            const int word = p >> 5, sh = p & 31;
+            const uint32_t c = static_cast<uint32_t>(code[e]);
+            atomicOr(buf + word, c << sh);
+            if (sh + bits > 32) atomicOr(buf + word + 1, c >> (32 - sh));
+        }
+    }
+    __syncwarp();
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(dst_row);
+    for (int i = lane; i < W; i += 32) d32[i] = buf[i];
+    __syncwarp();
+}
+
+constexpr int kWarps = 8;
+
+// Power-of-two dims: E = dim / 32 in {1, 2, 4, 8, 16}.
+template <int E>
+__global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams p) {
+    __shared__ int64_t s_thr[kWarps][256];
+    __shared__ uint32_t s_pack[kWarps][128];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = 1 << p.bits;
+    int64_t* thr = s_thr[warp];
+    uint32_t* pk = s_pack[warp];
+    // signs of this lane's elements as a bit mask
+    uint32_t smask = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int j = lane * E + e;
+        smask |= ((__ldg(p.sign_bits + (j >> 5)) >> (j & 31)) & 1u) << e;
+    }
+    const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kWarps + warp; v < total;
+         v += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const uint16_t* src;
+        int64_t dst;
+        if (!map_row(p, v, src, dst)) {
+            if (lane == 0 && p.dev_error) atomicOr(p.dev_error, TQ_DEVERR_POSITION);
+            continue;
+        }
+        uint32_t hv[E];
+        load_row<E>(src, lane, E, hv);
+        int64_t k[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) k[e] = f16_exact(hv[e]);
+        const double D = __dsqrt_rn(warp_sumsq_rn<E>(k, E));
+        // thresholds F_i = floor(RN64(m_i * D)); w > F_i  <=>  w > RN64(m_i * D)
+        for (int i = lane; i < L; i += 32)
+            thr[i] = (i < L - 1) ? __double2ll_rd(__dmul_rn(__ldg(p.mid + i), D)) : INT64_MAX;
+        // w = H (s . k): in-lane stages, then cross-lane stages
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+            if ((smask >> e) & 1u) k[e] = -k[e];
+#pragma unroll
+        for (int h = 1; h < E; h <<= 1) {
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                if ((e & h) == 0) {
+                    const int64_t a = k[e], b = k[e + h];
+                    k[e] = a + b;
+                    k[e + h] = a - b;
+                }
+            }
+        }
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const bool upper = (lane & m) != 0;
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const int64_t o = __shfl_xor_sync(kFull, k[e], m);
+                k[e] = upper ? (o - k[e]) : (k[e] + o);
+            }
+        }
+        __syncwarp();
+        int code[E];
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            int pos = 0;
+            for (int s = L >> 1; s > 0; s >>= 1)
+                if (thr[pos + s - 1] < k[e]) pos += s;
+            code[e] = pos;
+        }
+        pack_store<E>(code, E, lane, p.bits, p.dim, pk, p.codes + dst * p.cstride);
+        if (lane == 0) p.norms[dst] = __half_as_ushort(__double2half(ldexp(D, -24)));
+    }
+}
+
+constexpr int kDenseWarps = 4;
+constexpr int kDenseMaxE = 15;
+
+// Other dims (multiple of 32, not a power of two): E = dim / 32 at run time.
+__global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const EncParams p) {
+    __shared__ double s_thr[kDenseWarps][256];
+    __shared__ uint32_t s_pack[kDenseWarps][128];
+    __shared__ double s_k[kDenseWarps][kDenseMaxE * 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int L = 1 << p.bits;
+    const int E = p.dim >> 5;
+    double* thr = s_thr[warp];
+    uint32_t* pk = s_pack[warp];
+    double* kk = s_k[warp];
+    const double sqrt_d = __dsqrt_rn(static_cast<double>(p.dim));
+    const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kDenseWarps + warp; v < total;
+         v += static_cast<int64_t>(gridDim.x) * kDenseWarps) {
+        const uint16_t* src;
+        int64_t dst;
+        if (!map_row(p, v, src, dst)) {
+            if (lane == 0 && p.dev_error) atomicOr(p.dev_error, TQ_DEVERR_POSITION);
+            continue;
+        }
+        uint32_t hv[kDenseMaxE];
+        load_row<kDenseMaxE>(src, lane, E, hv);
+        int64_t k[kDenseMaxE];
+#pragma unroll
+        for (int e = 0; e < kDenseMaxE; ++e) {
+            k[e] = (e < E) ? f16_exact(hv[e]) : 0;
+            if (e < E) kk[lane * E + e] = static_cast<double>(k[e]);  // exact: |k| < 2^40
+        }
+        const double D = __dsqrt_rn(warp_sumsq_rn<kDenseMaxE>(k, E));
+        const double sc = __ddiv_rn(D, sqrt_d);
+        for (int i = lane; i < L; i += 32)
+            thr[i] = (i < L - 1) ? __dmul_rn(__ldg(p.mid + i), sc) : CUDART_INF;
+        __syncwarp();
+        int code[kDenseMaxE];
+#pragma unroll
+        for (int e = 0; e < kDenseMaxE; ++e) {
+            code[e] = 0;
+            if (e < E) {
+                const int j = lane * E + e;
+                double acc = 0.0;
+                for (int i = 0; i < p.dim; ++i)
+                    acc = __fma_rn(static_cast<double>(__ldg(p.qt + static_cast<int64_t>(i) * p.dim + j)),
+                                   kk[i], acc);
+                int pos = 0;
+                for (int s = L >> 1; s > 0; s >>= 1)
+                    if (thr[pos + s - 1] < acc) pos += s;
+                code[e] = pos;
+            }
+        }
+        pack_store<kDenseMaxE>(code, E, lane, p.bits, p.dim, pk, p.codes + dst * p.cstride);
+        if (lane == 0) p.norms[dst] = __half_as_ushort(__double2half(ldexp(D, -24)));
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride,
+                          uint8_t* codes, int64_t cstride, uint16_t* norms, int B, int H, int T,
+                          const int32_t* start_pos, int64_t max_seq, int32_t* dev_error,
+                          cudaStream_t st) {
+    EncParams p{};
+    p.x = x;
+    p.n = n;
+    p.xstride = xstride;
+    p.codes = codes;
+    p.cstride = cstride;
+    p.norms = norms;
+    p.B = B;
+    p.H = H;
+    p.T = T;
+    p.start_pos = start_pos;
+    p.max_seq = max_seq;
+    p.dev_error = dev_error;
+    p.mid = c->d_midpoints;
+    p.sign_bits = c->d_sign_bits;
+    p.qt = c->d_qt;
+    p.bits = c->bits;
+    p.dim = c->dim;
+    const int64_t total = (B > 0) ? static_cast<int64_t>(B) * H * T : n;
+    if (total <= 0) return cudaSuccess;
+    const int sms = num_sms(c->device);
+    if (c->is_wht) {
+        const int64_t want = (total + kWarps - 1) / kWarps;
+        const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+        const int E = c->dim / 32;
+        switch (E) {
+            case 1: encode_wht_kernel<1><<<grid, kWarps * 32, 0, st>>>(p); break;
+            case 2: encode_wht_kernel<2><<<grid, kWarps * 32, 0, st>>>(p); break;
+            case 4: encode_wht_kernel<4><<<grid, kWarps * 32, 0, st>>>(p); break;
+            case 8: encode_wht_kernel<8><<<grid, kWarps * 32, 0, st>>>(p); break;
+            case 16: encode_wht_kernel<16><<<grid, kWarps * 32, 0, st>>>(p); break;
+            default: return cudaErrorInvalidValue;
+        }
+    } else {
+        if (c->dim / 32 > kDenseMaxE) return cudaErrorInvalidValue;
+        const int64_t want = (total + kDenseWarps - 1) / kDenseWarps;
+        const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+        encode_dense_kernel<<<grid, kDenseWarps * 32, 0, st>>>(p);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace tq

@@ -1,0 +1,119 @@
+// tq_internal.h -- declarations shared by the libtq translation units.
+// Not part of the public ABI (include/tq.h is).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "tq.h"
+
+// Codec: host tables (fp64 construction, see tq_codec.cpp) and their device
+// copies.  Immutable after tq_codec_create.
+struct tq_codec {
+    int dim = 0;
+    int bits = 0;          // 2, 3, 4, 8, or 16 (raw fp16 keys)
+    int is_wht = 0;
+    int bytes_per_vec = 0;
+    int device = 0;
+    uint64_t seed = 0;
+
+    std::vector<int8_t> signs;        // [dim] (WHT)
+    std::vector<float> dense_q;       // [dim*dim] row-major, z = Q k (dense)
+    std::vector<float> centroids;     // [2^bits]
+    std::vector<double> midpoints;    // [2^bits - 1]
+
+    // Device copies (owned).
+    float* d_centroids = nullptr;     // [2^bits] fp32
+    double* d_midpoints = nullptr;    // [2^bits - 1] fp64
+    uint32_t* d_sign_bits = nullptr;  // [dim/32] bit j%32 of word j/32 set <=> s_j = -1
+    float* d_q = nullptr;             // [dim*dim] Q row-major (dense)
+    float* d_qt = nullptr;            // [dim*dim] Q^T row-major (dense)
+    // Decode tables in compact form (see tq_decode_mma.cu):
+    //  d_ktab: K-role entries for fp16 hi/lo split of centroid values;
+    //  d_vtab: V-role entries (fp16 hi).
+    uint32_t* d_ktab = nullptr;
+    uint32_t* d_vtab = nullptr;
+    int ktab_words = 0;
+    int vtab_words = 0;
+};
+
+namespace tq {
+
+// Host-side codebook / rotation construction (tq_codec.cpp).
+void lloyd_max_gaussian(int bits, std::vector<double>& c64);
+int dense_rotation(int dim, uint64_t seed, std::vector<float>& q);
+void rademacher_signs(int dim, uint64_t seed, std::vector<int8_t>& s);
+
+int num_sms(int device);
+
+// Launchers (tq_encode.cu / tq_dequant.cu / tq_decode_*.cu).  All return
+// cudaGetLastError() of the launch.
+cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride,
+                          uint8_t* codes, int64_t cstride, uint16_t* norms,
+                          // append mode (B > 0): x is [B, H, T, d], destination rows from start_pos
+                          int B, int H, int T, const int32_t* start_pos, int64_t max_seq,
+                          int32_t* dev_error, cudaStream_t st);
+
+cudaError_t launch_dequant(const tq_codec* c, const uint8_t* codes, const uint16_t* norms,
+                           int64_t n, float* out, cudaStream_t st);
+
+// Split-K plan for decode attention, shared by the workspace-size query and
+// the launcher so both agree for a given device and shape.
+struct DecodePlan {
+    int kernel;          // 0 = SIMT (general), 1 = tensor-core (mma.sync) kernel
+    int n_units;         // B * n_kv_heads
+    int G;               // query heads per KV head
+    int q_chunks;        // SIMT: query groups of at most 8 per unit
+    int n_split;         // CTAs per unit along the sequence
+    int64_t chunk;       // tokens per split (multiple of 8 / tile)
+    size_t ws_bytes;     // total workspace bytes
+    size_t part_offset;  // byte offset of partials
+    size_t ticket_offset;
+};
+
+// Split-K plan (independent of the kernel chosen, so the workspace size only
+// depends on the shape and the device).  plan.kernel is set by the caller.
+bool make_decode_plan(int dim, int device, int B, int Hq, int Hkv, int64_t max_seq, DecodePlan& plan);
+
+// By-value view of a codec for kernels (host structs are not visible on the
+// device).
+struct DevCodec {
+    int dim, bits, is_wht, bpv;
+    const float* centroids;
+    const uint32_t* sign_bits;
+    const float* q;    // Q row-major (dense)
+    const float* qt;   // Q^T row-major (dense)
+    const uint32_t* ktab;
+    const uint32_t* vtab;
+};
+
+inline DevCodec dev_view(const tq_codec* c) {
+    return DevCodec{c->dim,        c->bits,          c->is_wht, c->bytes_per_vec, c->d_centroids,
+                    c->d_sign_bits, c->d_q,          c->d_qt,   c->d_ktab,        c->d_vtab};
+}
+
+struct DecodeArgs {
+    DevCodec ck;
+    DevCodec cv;
+    const uint16_t* q;
+    const void* k;
+    const uint16_t* k_norms;
+    const uint8_t* v_codes;
+    const uint16_t* v_norms;
+    const int32_t* seq_lens;
+    int B, Hq, Hkv;
+    int64_t max_seq;
+    float scale;
+    uint16_t* out;
+    void* ws;
+};
+
+cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+// Returns cudaErrorNotSupported when no tensor-core instantiation matches.
+cudaError_t launch_decode_mma(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G);
+
+}  // namespace tq

@@ -1,0 +1,146 @@
+"""Fused decode attention on the GPU (through the C ABI) against the CPU oracle's
+dequantise-then-softmax attention: max-abs <= 2e-3 and relative L2 <= 1e-3.
+
+Small shapes are compared on every output; the five workloads run at full size
+(the launch configuration the bench times) and are compared on sampled
+(batch, KV head) units the oracle computes one by one."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import tq_inputs
+from tq_helpers import (check_close, codecs, decode, encode_cache, oracle_codecs, oracle_unit_reference,
+                        torch_mods)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_small(w, lens=None, scale=None):
+    ck, cv = codecs(w)
+    ok_k, ok_v = oracle_codecs(w)
+    K, V, q = w.kv("k", 1), w.kv("v", 1), w.q()
+    kc, kn, vc, vn = encode_cache(w, ck, cv, K, V)
+    lens = w.lengths() if lens is None else np.asarray(lens, np.int32)
+    got, ws = decode(w, ck, cv, q, kc, kn, vc, vn, lens, scale)
+    sc = 1.0 / math.sqrt(w.d) if scale is None else scale
+    ref = np.zeros_like(got)
+    G = w.G
+    for b in range(w.B):
+        for h in range(w.Hkv):
+            r, (kk, kkn, vcc, vnn) = oracle_unit_reference(w, ok_k, ok_v, q, K, V, b, h, lens)
+            if scale is not None:
+                r = oracle.attention_unit(ok_k, ok_v, q[b, h * G:(h + 1) * G], kk, kkn, vcc, vnn, int(lens[b]), sc)
+            ref[b, h * G:(h + 1) * G] = r
+    return got, ref, ws
+
+
+@pytest.mark.parametrize("G", [1, 3, 4, 8, 16])
+@pytest.mark.parametrize("kb,vb", [(4, 4), (4, 2), (8, 3), (3, 3), (16, 4), (2, 2)])
+def test_decode_small_all_outputs(G, kb, vb):
+    w = tq_inputs.Workload("t", B=2, Hq=2 * G, Hkv=2, d=128, S=520, k_bits=kb, v_bits=vb, k_outliers=True)
+    got, ref, _ = _run_small(w, lens=[517, 64])
+    check_close(got, ref, f"G={G} K{kb}V{vb}")
+
+
+@pytest.mark.parametrize("d", [64, 96, 256, 32])
+def test_decode_head_dims(d):
+    w = tq_inputs.Workload("t", B=1, Hq=8, Hkv=2, d=d, S=384, k_bits=4, v_bits=3, k_outliers=True)
+    got, ref, _ = _run_small(w, lens=[383])
+    check_close(got, ref, f"d={d}")
+
+
+@pytest.mark.parametrize("lens", [[0, 1], [63, 64], [65, 8], [1, 520]])
+def test_decode_edge_lengths(lens):
+    w = tq_inputs.Workload("t", B=2, Hq=8, Hkv=2, d=128, S=520, k_bits=8, v_bits=3, k_outliers=True)
+    got, ref, _ = _run_small(w, lens=lens)
+    for b, L in enumerate(lens):
+        if L == 0:
+            assert np.all(got[b] == 0)
+    check_close(got, ref, f"lens={lens}")
+
+
+def test_decode_single_token_is_dequantised_value():
+    w = tq_inputs.Workload("t", B=1, Hq=4, Hkv=1, d=128, S=64, k_bits=4, v_bits=4, k_outliers=False)
+    got, ref, _ = _run_small(w, lens=[1])
+    ok_v = oracle.Codec(128, 4, w.rot_seed)
+    vc, vn, _, _ = ok_v.encode(w.kv("v", 1)[0, 0, :1])
+    v0 = ok_v.dequant(vc, vn)[0]
+    np.testing.assert_allclose(got[0], np.repeat(v0[None], 4, 0), atol=2e-3, rtol=1e-3)
+
+
+def test_decode_scale_and_repeat_calls_reuse_workspace():
+    w = tq_inputs.Workload("t", B=2, Hq=8, Hkv=2, d=128, S=1024, k_bits=4, v_bits=4, k_outliers=True)
+    got, ref, _ = _run_small(w, lens=[1000, 777], scale=0.3)
+    check_close(got, ref, "scale=0.3")
+    # the arrival counters are back at zero: a second call on the same workspace is identical
+    torch, tq = torch_mods()
+    ck, cv = codecs(w)
+    K, V, q = w.kv("k", 1), w.kv("v", 1), w.q()
+    kc, kn, vc, vn = encode_cache(w, ck, cv, K, V)
+    dev = torch.device("cuda")
+    ws = torch.empty(tq.tq_decode_attend_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.d), dtype=torch.uint8, device=dev)
+    tq.tq_workspace_init(ws)
+    outs = []
+    for _ in range(3):
+        out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16, device=dev)
+        tq.tq_decode_attend(ck, cv, torch.from_numpy(q).to(dev), kc, kn, vc, vn,
+                            torch.tensor([1000, 777], dtype=torch.int32, device=dev), out, ws)
+        outs.append(out.cpu().numpy())
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[1], outs[2])
+    ticks = ws[256:256 + 4 * w.B * w.Hkv].view(torch.int32).cpu().numpy()
+    assert np.all(ticks == 0)
+
+
+def test_decode_bad_lengths_are_clamped_and_flagged():
+    torch, tq = torch_mods()
+    w = tq_inputs.Workload("t", B=2, Hq=4, Hkv=2, d=128, S=256, k_bits=4, v_bits=4, k_outliers=False)
+    ck, cv = codecs(w)
+    K, V, q = w.kv("k", 1), w.kv("v", 1), w.q()
+    kc, kn, vc, vn = encode_cache(w, ck, cv, K, V)
+    got, ws = decode(w, ck, cv, q, kc, kn, vc, vn, lens=[300, -5])
+    assert tq.tq_get_device_error(ws) == tq.TQ_DEVERR_SEQ_LEN
+    assert np.all(got[1] == 0)
+    full, _ = decode(w, ck, cv, q, kc, kn, vc, vn, lens=[256, 0])
+    np.testing.assert_array_equal(got, full)
+
+
+# --------------------------------------------------------------------------- full-size workloads
+FULL = {
+    "c1_tiny": None,                       # every unit
+    "c2_llama3b": None,
+    "c3_turbo4v2_ragged": [(0, 0), (3, 5), (7, 7)],
+    "c4_long_k8v3": [(0, 0), (0, 5)],
+    "c4_long_k8v3_d96": [(0, 3)],
+    "c5_turbo0v4_d256": [(0, 0), (31, 7)],
+    "c5_turbo3_d256": [(5, 2)],
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_decode_workload_full_size(name):
+    w = tq_inputs.WORKLOADS[name]
+    ck, cv = codecs(w)
+    ok_k, ok_v = oracle_codecs(w)
+    K, V, q = w.kv("k", 16), w.kv("v", 16), w.q()
+    kc, kn, vc, vn = encode_cache(w, ck, cv, K, V)
+    lens = w.lengths()
+    got, ws = decode(w, ck, cv, q, kc, kn, vc, vn, lens)
+    torch, tq = torch_mods()
+    assert tq.tq_get_device_error(ws) == 0
+    units = FULL[name] or [(b, h) for b in range(w.B) for h in range(w.Hkv)]
+    G = w.G
+    gs, rs = [], []
+    kcc = None if w.k_bits == 16 else kc.cpu().numpy()
+    vcc = vc.cpu().numpy()
+    for b, h in units:
+        ref, (kk, kkn, vv, vvn) = oracle_unit_reference(w, ok_k, ok_v, q, K, V, b, h, lens)
+        L = int(lens[b])
+        # the cache the GPU attended is the oracle's encoding, bit for bit
+        if kcc is not None:
+            np.testing.assert_array_equal(kcc[b, h, :L], kk[:L])
+        np.testing.assert_array_equal(vcc[b, h, :L], vv[:L])
+        gs.append(got[b, h * G:(h + 1) * G])
+        rs.append(ref)
+    check_close(np.array(gs), np.array(rs), name)
