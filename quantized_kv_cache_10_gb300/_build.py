@@ -10,6 +10,7 @@ from __future__ import annotations
 import concurrent.futures as cf
 import glob
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -18,7 +19,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INC = os.path.join(ROOT, "include")
-BUILD = os.path.join(PKG, "_build")
+BUILD = os.path.join(PKG, "_build", platform.machine())   # objects per host architecture
 LIB = os.path.join(PKG, "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -74,7 +75,10 @@ def build(verbose: bool = False) -> str:
     if logs:
         with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
             f.write("\n".join(logs))
-    if not os.path.exists(LIB) or any(os.path.getmtime(o) > os.path.getmtime(LIB) for o in objs):
+    stamp = os.path.join(BUILD, "libtq.stamp")     # the library was linked from this architecture's objects
+    fresh = os.path.exists(LIB) and os.path.exists(stamp) and \
+        all(os.path.getmtime(o) <= os.path.getmtime(LIB) for o in objs)
+    if not fresh:
         tmp = LIB + f".tmp{os.getpid()}"
         cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")]
@@ -82,6 +86,8 @@ def build(verbose: bool = False) -> str:
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
         os.replace(tmp, LIB)
+        with open(stamp, "w") as f:
+            f.write(LIB + "\n")
     if verbose:
         print(LIB)
     return LIB
