@@ -55,6 +55,7 @@ typedef enum {
 /* Device error codes (bit flags) recorded by kernels. */
 #define TQ_DEVERR_SEQ_LEN   1   /* seq_lens[b] < 0 or > max_seq: clamped */
 #define TQ_DEVERR_POSITION  2   /* encode_append position outside [0, max_seq): row skipped */
+#define TQ_DEVERR_TIMEOUT   4   /* a bounded wait inside a kernel gave up; its outputs are invalid */
 
 typedef struct tq_codec tq_codec;   /* opaque; immutable after creation */
 

@@ -1,26 +1,133 @@
-// tq_decode_mma.cu -- tensor-core fused decode attention (filled in below).
-#include "tq_decode_common.cuh"
+// tq_decode_mma.cu -- host side of the tensor-core fused decode attention for GQA groups of up
+// to 8 query heads ("anyone still talking about mlx-swift-lm?": one dispatch,
+// K read once in its rotated basis, inline dequant; "add TurboQuant KV cache
+// compression", review of the NR0 path: every query head of a KV head's group
+// served from one read of that head's cache).
+//
+// Per CTA: one (batch, KV head, sequence split).  One producer warp streams
+// tiles of TS tokens (packed K codes, packed V codes, both norm vectors) into
+// an NSTAGE-deep shared-memory ring with 1-D TMA bulk copies
+// (cp.async.bulk ... mbarrier::complete_tx); eight consumer warps each take
+// 16*MT tokens of a tile:
+//   scores  S[16 tok x 8 col] += Khat[16 x 16 dims] * Q'[16 dims x 8 col]
+//           (mma.sync m16n8k16, fp16 in, fp32 accumulate), Khat built in
+//           registers from the codes through replicated shared-memory tables
+//           holding each centroid as fp16 hi + fp16 lo, and q' split the same
+//           way into separate columns, so the product keeps ~fp32 accuracy;
+//   softmax online in fp32 (exp2 of log2-scaled scores);
+//   P.V     O^T[16 dims x 8 col] += Vhat^T[16 dims x 16 tok] * P[16 tok x 8]
+//           with P moved from the score layout by movmatrix.trans and Vhat
+//           looked up two tokens at a time from a pair table.
+// Warps merge in shared memory in a fixed order, then the CTA publishes its
+// split-K partial and the last CTA of the unit combines and applies the single
+// inverse V rotation (tq_decode_common.cuh).
+//
+// Register/shared layouts (thread = 4*g + t in its warp):
+//   K role (A of the score mma, rows = tokens): thread t owns dims
+//     [(D/4) t, (D/4)(t+1)); k-tile kt uses dims (D/4) t + 4 kt + {0,1,2,3}
+//     for the k columns {2t, 2t+1, 2t+8, 2t+9}.  The q' B fragment uses the
+//     same map.
+//   V role (A of the P.V mma, rows = dims): thread g owns dims
+//     [(D/8) g, (D/8)(g+1)); m-tile dm rows g / g+8 are dims (D/8) g + 2 dm + 0/1.
+//   Query columns: NT == 2 (5..8 heads): column j of n-tile 0 / 1 = q_hi / q_lo
+//     of head j; NT == 1 (<= 4 heads): column 2j / 2j+1 = q_hi / q_lo of head j,
+//     and in P.V head j sits in column 2j.
+#include <cuda_fp16.h>
+
+#include "tq_decode_mma.cuh"
 
 namespace tq {
 
+// ---------------------------------------------------------------------------
+// Host: compact decode tables, built once per codec.
+//   ktab: K role.  bits <= 4: per pair index p = c0 | c1 << bits two words
+//         {hi(c0) | hi(c1) << 16, lo(c0) | lo(c1) << 16};  bits == 8: one word
+//         per code {hi | lo << 16}.  hi = fp16(c), lo = fp16(c - hi).
+//   vtab: V role.  bits <= 4: per pair index one word hi(c0) | hi(c1) << 16;
+//         bits == 8: one word per code hi | hi << 16.
+// ---------------------------------------------------------------------------
+namespace {
+
+uint16_t f16_bits(float x) {
+    __half h = __float2half_rn(x);
+    return __half_as_ushort(h);
+}
+
+float f16_val(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+}  // namespace
+
 void build_decode_tables(const tq_codec& c, std::vector<uint32_t>& ktab, std::vector<uint32_t>& vtab) {
-    (void)c;
     ktab.clear();
     vtab.clear();
+    if (c.bits == 16) return;
+    const int L = 1 << c.bits;
+    std::vector<uint16_t> hi(L), lo(L);
+    for (int i = 0; i < L; ++i) {
+        hi[i] = f16_bits(c.centroids[i]);
+        lo[i] = f16_bits(c.centroids[i] - f16_val(hi[i]));
+    }
+    if (c.bits <= 4) {
+        for (int p = 0; p < L * L; ++p) {
+            const int c0 = p & (L - 1), c1 = p >> c.bits;
+            ktab.push_back(uint32_t(hi[c0]) | (uint32_t(hi[c1]) << 16));
+            ktab.push_back(uint32_t(lo[c0]) | (uint32_t(lo[c1]) << 16));
+            vtab.push_back(uint32_t(hi[c0]) | (uint32_t(hi[c1]) << 16));
+        }
+    } else {
+        for (int i = 0; i < L; ++i) {
+            ktab.push_back(uint32_t(hi[i]) | (uint32_t(lo[i]) << 16));
+            vtab.push_back(uint32_t(hi[i]) | (uint32_t(hi[i]) << 16));
+        }
+    }
 }
 
 bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G) {
-    (void)ck;
-    (void)cv;
-    (void)G;
+    if (G < 1 || G > 8 || ck->bits == 16 || cv->bits == 16 || ck->dim != cv->dim) return false;
+    const int d = cv->dim;
+    if (d != 64 && d != 96 && d != 128 && d != 256) return false;
+    for (const auto& s : mma_detail::kSchemes)
+        if (s[0] == ck->bits && s[1] == cv->bits) return mma_detail::mma_fits(d, ck->bits, cv->bits);
     return false;
 }
 
-cudaError_t launch_decode_mma(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    (void)a;
-    (void)p;
-    (void)st;
-    return cudaErrorNotSupported;
+template <int D>
+cudaError_t launch_mma_d_extern(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
+// defined in tq_decode_mma_d{64,96,128,256}.cu
+template <>
+cudaError_t launch_mma_d_extern<64>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+template <>
+cudaError_t launch_mma_d_extern<96>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+template <>
+cudaError_t launch_mma_d_extern<128>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+template <>
+cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+
+cudaError_t launch_decode_mma(const DecodeArgs& a, const DecodePlan& p0, cudaStream_t st) {
+    // one CTA per SM: as many splits per (batch, KV head) as fill the SMs once
+    DecodePlan p = p0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int64_t sms = num_sms(dev);
+    int64_t ns = (sms + p.n_units - 1) / p.n_units;
+    const int64_t cap = (a.max_seq + 255) / 256;
+    if (ns > cap) ns = cap;
+    if (ns < 1) ns = 1;
+    int64_t chunk = (a.max_seq + ns - 1) / ns;
+    chunk = (chunk + 63) / 64 * 64;
+    ns = (a.max_seq + chunk - 1) / chunk;
+    if (ns <= p0.n_split) {  // the workspace was sized for p0.n_split splits
+        p.n_split = static_cast<int>(ns);
+        p.chunk = chunk;
+    }
+    const int nt = p.G > 4 ? 2 : 1;
+    switch (a.cv.dim) {
+        case 64: return launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st);
+        case 96: return launch_mma_d_extern<96>(a, p, a.ck.bits, a.cv.bits, nt, st);
+        case 128: return launch_mma_d_extern<128>(a, p, a.ck.bits, a.cv.bits, nt, st);
+        case 256: return launch_mma_d_extern<256>(a, p, a.ck.bits, a.cv.bits, nt, st);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace tq

@@ -1,0 +1,713 @@
+// tq_decode_mma.cuh -- the tensor-core fused decode-attention kernel template
+// (instantiated per head dim in tq_decode_mma_d*.cu).
+//
+// Per CTA: one (batch, KV head, sequence split).  One producer warp streams
+// tiles of TS tokens (packed K codes, packed V codes, both norm vectors) into
+// an NSTAGE-deep shared-memory ring with 1-D TMA bulk copies
+// (cp.async.bulk ... mbarrier::complete_tx); eight consumer warps each take
+// 16*MT tokens of a tile:
+//   scores  S[16 tok x 8 col] += Khat[16 x 16 dims] * Q'[16 dims x 8 col]
+//           (mma.sync m16n8k16, fp16 in, fp32 accumulate), Khat built in
+//           registers from the codes through replicated shared-memory tables
+//           holding each centroid as fp16 hi + fp16 lo, and q' split the same
+//           way into separate columns, so the product keeps ~fp32 accuracy;
+//   softmax online in fp32 (exp2 of log2-scaled scores);
+//   P.V     O^T[16 dims x 8 col] += Vhat^T[16 dims x 16 tok] * P[16 tok x 8]
+//           with P moved from the score layout by movmatrix.trans and Vhat
+//           looked up two tokens at a time from a pair table.
+// Warps merge in shared memory in a fixed order, then the CTA publishes its
+// split-K partial and the last CTA of the unit combines and applies the single
+// inverse V rotation (tq_decode_common.cuh).  Every wait is bounded: a wait that
+// gives up records TQ_DEVERR_TIMEOUT and the CTA drains its copies and exits.
+//
+// Register/shared layouts (thread = 4*g + t in its warp):
+//   K role (A of the score mma, rows = tokens): thread t owns dims
+//     [(D/4) t, (D/4)(t+1)); k-tile kt uses dims (D/4) t + 4 kt + {0,1,2,3}
+//     for the k columns {2t, 2t+1, 2t+8, 2t+9}.  The q' B fragment uses the
+//     same map.
+//   V role (A of the P.V mma, rows = dims): thread g owns dims
+//     [(D/8) g, (D/8)(g+1)); m-tile dm rows g / g+8 are dims (D/8) g + 2 dm + 0/1.
+//   Query columns: NT == 2 (5..8 heads): column j of n-tile 0 / 1 = q_hi / q_lo
+//     of head j; NT == 1 (<= 4 heads): column 2j / 2j+1 = q_hi / q_lo of head j,
+//     and in P.V head j sits in column 2j.
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include <atomic>
+
+#include "tq_decode_common.cuh"
+
+namespace tq {
+namespace mma_detail {
+// ---------------------------------------------------------------------------
+// PTX helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait (about a second of SM clock); false on timeout.
+constexpr long long kWaitCycles = 2000000000LL;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitCycles) return false;
+    return true;
+}
+
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ uint32_t lds32(uint32_t addr) {
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
+    asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
+}
+
+// 32 bits of the little-endian word array w starting at bit s (compile-time s).
+template <int NW>
+__device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int s) {
+    const int i = s >> 5, sh = s & 31;
+    const uint32_t lo = (i < NW) ? w[i] : 0u;
+    const uint32_t hi = (i + 1 < NW) ? w[i + 1] : 0u;
+    return sh ? __funnelshift_r(lo, hi, sh) : lo;
+}
+
+// ---------------------------------------------------------------------------
+// Configuration
+// ---------------------------------------------------------------------------
+constexpr int kNWC = 8;                    // consumer warps
+constexpr int kThreads = (kNWC + 1) * 32;  // + one producer warp
+constexpr int kSmemLimit = 227 * 1024;
+
+constexpr int al16(int x) { return (x + 15) / 16 * 16; }
+constexpr int al128(int x) { return (x + 127) / 128 * 128; }
+
+template <int D, int KB, int VB>
+struct TableBytes {
+    static constexpr int KROWS = (KB <= 4) ? (1 << (2 * KB)) : 256;
+    static constexpr int VROWS = (VB <= 4) ? (1 << (2 * VB)) : 256;
+    static constexpr int KTAB = KROWS * 256;   // 32 lanes x 8 B (pairs) or 32 x 4 B in a 256-B row
+    static constexpr int VTAB = VROWS * 128;   // 32 lanes x 4 B
+    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024;
+    static constexpr int stage(int ts) {
+        return al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
+    }
+    // two m-tiles per warp per stage when two such stages fit, else one
+    static constexpr int MT = (FIXED + 2 * stage(kNWC * 32) <= kSmemLimit && D <= 128) ? 2 : 1;
+    // whether the kernel fits at all (two stages of one m-tile per warp)
+    static constexpr bool FITS = FIXED + 2 * stage(kNWC * 16) <= kSmemLimit;
+};
+
+// Same test for run-time (d, bits) on the host.
+inline bool mma_fits(int D, int KB, int VB) {
+    const int krows = (KB <= 4) ? (1 << (2 * KB)) : 256, vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
+    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024;
+    const int ts = kNWC * 16;
+    const int stage = al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
+    return fixed + 2 * stage <= kSmemLimit;
+}
+
+template <int D, int KB, int VB, int NT>
+struct Cfg {
+    using TB = TableBytes<D, KB, VB>;
+    static constexpr int MT = TB::MT;               // m-tiles of 16 tokens per warp per stage
+    static constexpr int TS = kNWC * 16 * MT;       // tokens per stage
+    static constexpr int BPK = D * KB / 8;
+    static constexpr int BPV = D * VB / 8;
+    static constexpr int KT = D / 16;               // score k-tiles == P.V dim m-tiles
+    static constexpr bool KPAIR = KB <= 4;
+    static constexpr bool VPAIR = VB <= 4;
+    static constexpr int KROWS = TB::KROWS;
+    static constexpr int KTAB = TB::KTAB;
+    static constexpr int VROWS = TB::VROWS;
+    static constexpr int VTAB = TB::VTAB;
+    // per-thread chunk of one row, in bits and 32-bit words
+    static constexpr int KCB = (D / 4) * KB;        // K role: thread t, dims (D/4) t ...
+    static constexpr int KCW = (KCB + 31) / 32;
+    static constexpr int VCB = (D / 8) * VB;        // V role: thread g, dims (D/8) g ...
+    static constexpr int VCW = (VCB + 31) / 32;
+    // stage buffers (+16 B slack: chunk loads may read one word past a row)
+    static constexpr int KBUF = al128(TS * BPK + 16);
+    static constexpr int VBUF = al128(TS * BPV + 16);
+    static constexpr int NBUF = al128(TS * 2);
+    static constexpr int STAGE = KBUF + VBUF + 2 * NBUF;
+    static constexpr int QBYTES = kGP * D * 4;      // q' fp32, later the merged O
+    static constexpr int MISC = 1024;               // barriers, m/l exchange
+    static constexpr int FIXED = TB::FIXED;
+    static constexpr int NSTAGE_RAW = (kSmemLimit - FIXED) / STAGE;
+    static constexpr int NSTAGE = NSTAGE_RAW > 4 ? 4 : NSTAGE_RAW;
+    static constexpr int SMEM = FIXED + NSTAGE * STAGE;
+    static_assert(STAGE == TB::stage(TS), "stage size");
+    static_assert(NSTAGE >= 2, "shared memory too small for two stages");
+    // epilogue scratch (per-warp O slices, combine weights) lives in the stage ring
+    static_assert(NSTAGE * STAGE >= kNWC * kGP * D * 4, "stage ring too small for the warp merge");
+};
+
+// ---------------------------------------------------------------------------
+// Dequant: K role (pairs of neighbouring dims of one token)
+// ---------------------------------------------------------------------------
+// For k-tile kt of one token row whose chunk words are w: A registers for dims
+// base+0,1 (rlo) and base+2,3 (rhi), hi and lo parts.
+template <int KB, int KCW>
+__device__ __forceinline__ void k_role(const uint32_t (&w)[KCW], int kt, uint32_t tab, uint32_t lane_off,
+                                       uint32_t& hi01, uint32_t& hi23, uint32_t& lo01, uint32_t& lo23) {
+    if constexpr (KB == 8) {
+        // four single-code lookups; row stride 256 B so the byte can be placed with one prmt
+        const uint32_t word = w[kt];
+        const uint32_t a0 = __byte_perm(word, lane_off, 0x5504);
+        const uint32_t a1 = __byte_perm(word, lane_off, 0x5514);
+        const uint32_t a2 = __byte_perm(word, lane_off, 0x5524);
+        const uint32_t a3 = __byte_perm(word, lane_off, 0x5534);
+        const uint32_t v0 = lds32(tab + a0), v1 = lds32(tab + a1), v2 = lds32(tab + a2), v3 = lds32(tab + a3);
+        hi01 = __byte_perm(v0, v1, 0x5410);
+        lo01 = __byte_perm(v0, v1, 0x7632);
+        hi23 = __byte_perm(v2, v3, 0x5410);
+        lo23 = __byte_perm(v2, v3, 0x7632);
+    } else {
+        // pair lookups: index = 2*KB bits at bit 4*KB*kt (and + 2*KB); rows of 256 B
+        const int s0 = 4 * KB * kt;
+        const uint32_t x0 = bits_at<KCW>(w, s0), x1 = bits_at<KCW>(w, s0 + 2 * KB);
+        const uint32_t m = (1u << (2 * KB)) - 1u;
+        const uint32_t a0 = ((x0 & m) << 8) | lane_off;
+        const uint32_t a1 = ((x1 & m) << 8) | lane_off;
+        lds64(tab + a0, hi01, lo01);
+        lds64(tab + a1, hi23, lo23);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Dequant: V role (one dim of two tokens a, b)
+// ---------------------------------------------------------------------------
+template <int VB, int VCW>
+__device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint32_t (&wb)[VCW], int j,
+                                           uint32_t tab, uint32_t lane4) {
+    const int s = VB * j;
+    const uint32_t m = (1u << VB) - 1u;
+    if constexpr (VB <= 4) {
+        const uint32_t ca = bits_at<VCW>(wa, s) & m;
+        const uint32_t cb = bits_at<VCW>(wb, s) & m;
+        return lds32(tab + (((ca | (cb << VB)) << 7) | lane4));
+    } else {
+        const uint32_t ca = bits_at<VCW>(wa, s) & m;
+        const uint32_t cb = bits_at<VCW>(wb, s) & m;
+        const uint32_t va = lds32(tab + ((ca << 7) | lane4));
+        const uint32_t vb = lds32(tab + ((cb << 7) | lane4));
+        return __byte_perm(va, vb, 0x7610);
+    }
+}
+
+// Loads NW 32-bit words of a row chunk starting at bit `bit` of the row (row
+// 4-byte aligned).  One word past the chunk may be read (stage slack).
+template <int NW>
+__device__ __forceinline__ void load_chunk(const uint8_t* row, int bit, uint32_t (&w)[NW]) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + (bit >> 5);
+    const int sh = bit & 31;
+    if (sh == 0) {
+#pragma unroll
+        for (int i = 0; i < NW; ++i) w[i] = p[i];
+    } else {
+        uint32_t prev = p[0];
+#pragma unroll
+        for (int i = 0; i < NW; ++i) {
+            const uint32_t nxt = p[i + 1];
+            w[i] = __funnelshift_r(prev, nxt, sh);
+            prev = nxt;
+        }
+    }
+}
+
+// K row chunk: thread t's dims of token row `row`.  For 32 B chunks at D=128,
+// odd rows load their two 16-byte halves in the opposite order so a quarter
+// warp never hits the same banks twice.
+template <int D, int KB, int KCW>
+__device__ __forceinline__ void load_k_chunk(const uint8_t* kbuf, int row, int t, uint32_t (&w)[KCW]) {
+    constexpr int BPK = D * KB / 8;
+    constexpr int KCB = (D / 4) * KB;
+    if constexpr (KCB % 128 == 0) {
+        const uint4* p = reinterpret_cast<const uint4*>(kbuf + row * BPK + t * (KCB / 8));
+        constexpr int NV = KCW / 4;
+        const int rot = row & 1;
+#pragma unroll
+        for (int i = 0; i < NV; ++i) {
+            const int ii = (i + rot) % NV;
+            const uint4 v = p[ii];
+            // select by compile-time index to keep w in registers
+#pragma unroll
+            for (int jj = 0; jj < NV; ++jj)
+                if (jj == ii) {
+                    w[4 * jj] = v.x;
+                    w[4 * jj + 1] = v.y;
+                    w[4 * jj + 2] = v.z;
+                    w[4 * jj + 3] = v.w;
+                }
+        }
+    } else {
+        load_chunk<KCW>(kbuf + row * BPK, t * KCB, w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int D, int KB, int VB, int NT>
+__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArgs a, const DecodePlan p) {
+    using C = Cfg<D, KB, VB, NT>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    uint8_t* ktab_s = smem;
+    uint8_t* vtab_s = ktab_s + C::KTAB;
+    float* qs = reinterpret_cast<float*>(vtab_s + C::VTAB);              // [kGP][D]
+    uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE]
+    uint64_t* empty = full + 4;                                          // [NSTAGE]
+    float* wm = reinterpret_cast<float*>(misc + 64);                     // [kNWC][kGP]
+    float* wl = wm + kNWC * kGP;                                         // [kNWC][kGP]
+    float* cm = wl + kNWC * kGP;                                         // [kGP]
+    float* cl = cm + kGP;                                                // [kGP]
+    int* s_flag = reinterpret_cast<int*>(cl + kGP);
+    int* s_abort = s_flag + 1;
+    uint8_t* ring = misc + C::MISC;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int u = blockIdx.y, split = blockIdx.x;
+    const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+    const int G = p.G;
+    const int h0 = kvh * G;
+    const int64_t len = clamped_len(a, b);
+    const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
+    const int64_t t1 = min(len, t0 + p.chunk);
+    const int ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+    const int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
+
+    if (tid == 0) {
+        for (int s = 0; s < C::NSTAGE; ++s) {
+            mbar_init(full + s, 1);
+            mbar_init(empty + s, kNWC);
+        }
+        *s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    int issued = 0;  // tiles whose copies the producer has started (producer lane 0)
+    if (warp == kNWC) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint8_t* kg = static_cast<const uint8_t*>(a.k);
+            for (int it = 0; it < ntiles; ++it) {
+                const int s = it % C::NSTAGE;
+                if (it >= C::NSTAGE && !mbar_wait(empty + s, ((it / C::NSTAGE) - 1) & 1)) {
+                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                    break;
+                }
+                const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
+                const int64_t nv = min(static_cast<int64_t>(C::TS), t1 - ts);
+                const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
+                uint8_t* st = ring + s * C::STAGE;
+                const uint32_t kbytes = n8 * C::BPK, vbytes = n8 * C::BPV, nbytes = n8 * 2;
+                mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes);
+                bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
+                bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
+                bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
+                bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
+                issued = it + 1;
+            }
+        }
+        __syncwarp();  // reconverge the producer warp before the block-wide barriers
+    } else {
+        // ------------------------------------------------------------ consumers: prologue
+        const int ctid = tid;  // 0 .. 255
+        {
+            // replicate the compact tables across the 32 lanes
+            const uint32_t* kt = a.ck.ktab;
+            if constexpr (C::KPAIR) {
+                for (int i = ctid; i < C::KROWS * 32; i += kNWC * 32) {
+                    const int r = i >> 5, l = i & 31;
+                    uint2 v = make_uint2(__ldg(kt + 2 * r), __ldg(kt + 2 * r + 1));
+                    *reinterpret_cast<uint2*>(ktab_s + r * 256 + l * 8) = v;
+                }
+            } else {
+                for (int i = ctid; i < C::KROWS * 32; i += kNWC * 32) {
+                    const int r = i >> 5, l = i & 31;
+                    *reinterpret_cast<uint32_t*>(ktab_s + r * 256 + l * 4) = __ldg(kt + r);
+                }
+            }
+            const uint32_t* vt = a.cv.vtab;
+            for (int i = ctid; i < C::VROWS * 32; i += kNWC * 32) {
+                const int r = i >> 5, l = i & 31;
+                *reinterpret_cast<uint32_t*>(vtab_s + r * 128 + l * 4) = __ldg(vt + r);
+            }
+            if (warp < G) rotate_query_warp(a, b, h0 + warp, qs + warp * D);
+            for (int i = G * D + ctid; i < kGP * D; i += kNWC * 32) qs[i] = 0.0f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+
+        const int g = lane >> 2, t = lane & 3;
+        // q' B fragments: Bq[kt][nt][2]
+        uint32_t Bq[C::KT][NT][2];
+#pragma unroll
+        for (int kt = 0; kt < C::KT; ++kt) {
+            const int base = (D / 4) * t + 4 * kt;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float v[4];
+                bool lo_part;
+                int qh;
+                if constexpr (NT == 2) {
+                    qh = g;
+                    lo_part = (nt == 1);
+                } else {
+                    qh = g >> 1;
+                    lo_part = (g & 1) != 0;
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float x = qs[qh * D + base + e];
+                    const float hi = __half2float(__float2half_rn(x));
+                    v[e] = lo_part ? (x - hi) : x;
+                }
+                Bq[kt][nt][0] = pack_f16(v[0], v[1]);
+                Bq[kt][nt][1] = pack_f16(v[2], v[3]);
+            }
+        }
+
+        float O[C::KT][4];
+#pragma unroll
+        for (int i = 0; i < C::KT; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
+        float m_run[NT], l_run[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            m_run[j] = -CUDART_INF_F;
+            l_run[j] = 0.0f;
+        }
+        const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
+        const uint32_t koff = C::KPAIR ? uint32_t(lane * 8) : uint32_t(lane * 4);
+        const uint32_t lane4 = uint32_t(lane * 4);
+
+        // ------------------------------------------------------------ main loop
+        for (int it = 0; it < ntiles; ++it) {
+            const int s = it % C::NSTAGE;
+            // the warp decides together so every later barrier is reached convergently
+            const bool ok = __all_sync(kFullMask, mbar_wait(full + s, (it / C::NSTAGE) & 1));
+            if (!ok) {
+                if (lane == 0) {
+                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                }
+                break;
+            }
+            const uint8_t* st = ring + s * C::STAGE;
+            const uint8_t* kbuf = st;
+            const uint8_t* vbuf = st + C::KBUF;
+            const __half* knrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF);
+            const __half* vnrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF + C::NBUF);
+            const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
+            const int nvalid = static_cast<int>(min(static_cast<int64_t>(C::TS), t1 - ts));
+            const int r0 = warp * 16 * C::MT;
+            if (r0 < nvalid) {
+                // ---- scores for MT m-tiles ----
+                float sc[C::MT][NT][4];
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
+                    const int ra = r0 + 16 * mt + g, rb = ra + 8;
+                    uint32_t wa[C::KCW], wb[C::KCW];
+                    load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
+                    load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
+#pragma unroll
+                    for (int kt = 0; kt < C::KT; ++kt) {
+                        uint32_t ah01, ah23, al01, al23, bh01, bh23, bl01, bl23;
+                        k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23, al01, al23);
+                        k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23, bl01, bl23);
+                        // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
+                        mma16816(sc[mt][0], ah01, bh01, ah23, bh23, Bq[kt][0][0], Bq[kt][0][1]);
+                        mma16816(sc[mt][0], al01, bl01, al23, bl23, Bq[kt][0][0], Bq[kt][0][1]);
+                        if constexpr (NT == 2)
+                            mma16816(sc[mt][1], ah01, bh01, ah23, bh23, Bq[kt][1][0], Bq[kt][1][1]);
+                    }
+                }
+                // ---- scale by K norms, mask, tile max ----
+                float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
+                float tmax[NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) tmax[j] = -CUDART_INF_F;
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int r = r0 + 16 * mt + g + 8 * hr;
+                        const bool ok = r < nvalid;
+                        const float nk = __half2float(knrm[r]);
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            float x;
+                            if constexpr (NT == 2)
+                                x = sc[mt][0][2 * hr + j] + sc[mt][1][2 * hr + j];
+                            else
+                                x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
+                            x = ok ? x * nk : -CUDART_INF_F;
+                            sv[mt][hr][j] = x;
+                            tmax[j] = fmaxf(tmax[j], x);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 4));
+                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 8));
+                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 16));
+                }
+                float alpha[NT], muse[NT];
+                bool rescale = false;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const float mn = fmaxf(m_run[j], tmax[j]);
+                    muse[j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
+                    alpha[j] = exp2f(m_run[j] - muse[j]);
+                    rescale |= (alpha[j] != 1.0f);
+                    m_run[j] = mn;
+                    l_run[j] *= alpha[j];
+                }
+                if (__any_sync(kFullMask, rescale)) {
+                    const float a1 = (NT == 2) ? alpha[NT - 1] : 1.0f;
+#pragma unroll
+                    for (int i = 0; i < C::KT; ++i) {
+                        O[i][0] *= alpha[0];
+                        O[i][1] *= a1;
+                        O[i][2] *= alpha[0];
+                        O[i][3] *= a1;
+                    }
+                }
+                // ---- probabilities, P' = p * n16_V, P.V ----
+#pragma unroll
+                for (int mt = 0; mt < C::MT; ++mt) {
+                    const int rbase = r0 + 16 * mt;
+                    if (rbase >= nvalid) break;
+                    float pv[2][NT];
+#pragma unroll
+                    for (int hr = 0; hr < 2; ++hr) {
+                        const int r = rbase + g + 8 * hr;
+                        const bool ok = r < nvalid;
+                        const float nvv = __half2float(vnrm[r]);
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            const float pp = exp2f(sv[mt][hr][j] - muse[j]);
+                            l_run[j] += pp;
+                            pv[hr][j] = ok ? pp * nvv : 0.0f;
+                        }
+                    }
+                    uint32_t x0, x1;
+                    if constexpr (NT == 2) {
+                        x0 = pack_f16(pv[0][0], pv[0][1]);
+                        x1 = pack_f16(pv[1][0], pv[1][1]);
+                    } else {
+                        x0 = pack_f16(pv[0][0], 0.0f);
+                        x1 = pack_f16(pv[1][0], 0.0f);
+                    }
+                    const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
+                    // V chunks of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile
+                    uint32_t v0[C::VCW], v1[C::VCW], v2[C::VCW], v3[C::VCW];
+                    const int vb = g * C::VCB;
+                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t) * C::BPV, vb, v0);
+                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vb, v1);
+                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vb, v2);
+                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
+#pragma unroll
+                    for (int dm = 0; dm < C::KT; ++dm) {
+                        const uint32_t a0 = v_role<VB, C::VCW>(v0, v1, 2 * dm, vtab_a, lane4);
+                        const uint32_t a1 = v_role<VB, C::VCW>(v0, v1, 2 * dm + 1, vtab_a, lane4);
+                        const uint32_t a2 = v_role<VB, C::VCW>(v2, v3, 2 * dm, vtab_a, lane4);
+                        const uint32_t a3 = v_role<VB, C::VCW>(v2, v3, 2 * dm + 1, vtab_a, lane4);
+                        mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty + s);
+        }
+        // ------------------------------------------------------------ warp totals
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 4);
+            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 8);
+            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 16);
+        }
+        if (g == 0) {
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int q = (NT == 2) ? 2 * t + j : t;
+                wm[warp * kGP + q] = m_run[j];
+                wl[warp * kGP + q] = l_run[j];
+            }
+            if constexpr (NT == 1) {
+                wm[warp * kGP + 4 + t] = -CUDART_INF_F;
+                wl[warp * kGP + 4 + t] = 0.0f;
+            }
+        }
+        // every consumer is done with the ring; wm / wl are visible
+        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        float f[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int q = (NT == 2) ? 2 * t + j : t;
+            float M = -CUDART_INF_F;
+            for (int w = 0; w < kNWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+            f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M);
+        }
+        float* slice = reinterpret_cast<float*>(ring) + warp * kGP * D;
+#pragma unroll
+        for (int dm = 0; dm < C::KT; ++dm) {
+            const int d0 = (D / 8) * g + 2 * dm;
+            if constexpr (NT == 2) {
+                slice[(2 * t) * D + d0] = f[0] * O[dm][0];
+                slice[(2 * t + 1) * D + d0] = f[1] * O[dm][1];
+                slice[(2 * t) * D + d0 + 1] = f[0] * O[dm][2];
+                slice[(2 * t + 1) * D + d0 + 1] = f[1] * O[dm][3];
+            } else {
+                slice[t * D + d0] = f[0] * O[dm][0];
+                slice[t * D + d0 + 1] = f[0] * O[dm][2];
+                slice[(4 + t) * D + d0] = 0.0f;
+                slice[(4 + t) * D + d0 + 1] = 0.0f;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        // fixed-order sum of the warp slices -> qs (the CTA's unnormalised o)
+        const float* all = reinterpret_cast<const float*>(ring);
+        for (int i = tid; i < kGP * D; i += kNWC * 32) {
+            float acc = 0.0f;
+#pragma unroll
+            for (int w = 0; w < kNWC; ++w) acc += all[w * kGP * D + i];
+            qs[i] = acc;
+        }
+        if (tid < kGP) {
+            const int q = tid;
+            float M = -CUDART_INF_F;
+            for (int w = 0; w < kNWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+            float L = 0.0f;
+            for (int w = 0; w < kNWC; ++w) {
+                const float mw = wm[w * kGP + q];
+                if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
+            }
+            cm[q] = (q < G) ? M : -CUDART_INF_F;
+            cl[q] = (q < G) ? L : 0.0f;
+        }
+    }
+    __syncthreads();
+    if (warp == kNWC && lane == 0 && *s_abort) {
+        // a wait gave up: let every copy this CTA issued land before shared memory is released
+        for (int it = (issued > C::NSTAGE ? issued - C::NSTAGE : 0); it < issued; ++it) {
+            const long long c0 = clock64();
+            while (!mbar_try_wait(full + (it % C::NSTAGE), (it / C::NSTAGE) & 1) && clock64() - c0 < kWaitCycles) {
+            }
+        }
+    }
+    __syncthreads();
+    publish_and_combine(a, p, u, split, b, h0, G, qs, cm, cl, reinterpret_cast<float*>(ring), s_flag);
+}
+
+
+// Launch of one instantiation; split plan for one CTA per SM.
+template <int D, int KB, int VB, int NT>
+cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    using C = Cfg<D, KB, VB, NT>;
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
+    dim3 grid(p.n_split, p.n_units);
+    decode_mma_kernel<D, KB, VB, NT><<<grid, kThreads, C::SMEM, st>>>(a, p);
+    return cudaGetLastError();
+}
+
+#define TQ_MMA_CASE(KB_, VB_)                                                                 \
+    if constexpr (TableBytes<D, KB_, VB_>::FITS) {                                            \
+        if (kb == KB_ && vb == VB_)                                                           \
+            return nt == 2 ? launch_inst<D, KB_, VB_, 2>(a, p, st) : launch_inst<D, KB_, VB_, 1>(a, p, st); \
+    }
+
+// The (K bits, V bits) schemes with a tensor-core instantiation.
+constexpr int kSchemes[][2] = {{4, 4}, {3, 3}, {2, 2}, {4, 2}, {4, 3}, {8, 3}, {8, 4}, {8, 8}, {8, 2}, {3, 2}};
+
+template <int D>
+cudaError_t launch_mma_d(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
+    TQ_MMA_CASE(4, 4)
+    TQ_MMA_CASE(3, 3)
+    TQ_MMA_CASE(2, 2)
+    TQ_MMA_CASE(4, 2)
+    TQ_MMA_CASE(4, 3)
+    TQ_MMA_CASE(8, 3)
+    TQ_MMA_CASE(8, 4)
+    TQ_MMA_CASE(8, 8)
+    TQ_MMA_CASE(8, 2)
+    TQ_MMA_CASE(3, 2)
+    return cudaErrorNotSupported;
+}
+
+#undef TQ_MMA_CASE
+
+}  // namespace mma_detail
+}  // namespace tq

@@ -1,0 +1,16 @@
+// tq_decode_mma_d128.cu -- tensor-core decode-attention instantiations for head dim 128
+// (one translation unit per head dim so they compile in parallel).
+#include "tq_decode_mma.cuh"
+
+namespace tq {
+
+template <int D>
+cudaError_t launch_mma_d_extern(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
+
+template <>
+cudaError_t launch_mma_d_extern<128>(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt,
+                                     cudaStream_t st) {
+    return mma_detail::launch_mma_d<128>(a, p, kb, vb, nt, st);
+}
+
+}  // namespace tq

@@ -127,16 +127,21 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
             wl[warp * kGP + g] = l[g];
         }
     __syncthreads();
+    // fixed warp order, so repeated calls give identical bits
+    for (int w = 0; w < kWarps; ++w) {
+        if (warp == w) {
 #pragma unroll
-    for (int g = 0; g < kGP; ++g) {
-        if (g < Gc) {
-            float M = -CUDART_INF_F;
-            for (int w = 0; w < kWarps; ++w) M = fmaxf(M, wm[w * kGP + g]);
-            const float f = (m[g] == -CUDART_INF_F) ? 0.0f : exp2f(m[g] - M);
-            if (f != 0.0f)
+            for (int g = 0; g < kGP; ++g) {
+                if (g < Gc) {
+                    float M = -CUDART_INF_F;
+                    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, wm[w2 * kGP + g]);
+                    const float f = (m[g] == -CUDART_INF_F) ? 0.0f : exp2f(m[g] - M);
 #pragma unroll
-                for (int e = 0; e < E; ++e) atomicAdd(so + g * d + lane * E + e, o[g][e] * f);
+                    for (int e = 0; e < E; ++e) so[g * d + lane * E + e] += o[g][e] * f;
+                }
+            }
         }
+        __syncthreads();
     }
     if (tid < kGP) {
         const int g = tid;
