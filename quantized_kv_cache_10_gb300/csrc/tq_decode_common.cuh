@@ -94,7 +94,7 @@ __device__ inline void rotate_query_warp(const DecodeArgs& a, int b, int h, floa
 // Publishes this CTA's partial (already in smem: so[kGP][d], sm[kGP], sl[kGP])
 // and, if it is the last CTA of the virtual unit, combines all partials,
 // applies the inverse V rotation and writes the fp16 outputs.
-// Must be called by all threads of the block.  scratch: >= kGP*d floats.
+// Must be called by all threads of the block.  scratch: >= kGP*(d + 2*n_split + 1) floats.
 __device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan& p, int vu, int split,
                                            int b, int h0, int Gc, const float* so, const float* sm,
                                            const float* sl, float* scratch, int* s_flag) {
@@ -116,30 +116,41 @@ __device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan
     if (*s_flag == 0) return;
     __threadfence();
     // ---- last CTA of this unit: merge partials ----
-    float* wts = scratch + kGP * d;  // [n_split][kGP] weights, then [kGP] 1/L
+    // All (m, l) pairs are fetched at once, the per-split weights exp2(m_s - M)
+    // are formed in shared memory, and each output element then reads its
+    // n_split partial values with independent (unrolled) loads.
+    const int ns = p.n_split;
+    float* pm = scratch + kGP * d;   // [ns][kGP]: m, then the weights
+    float* pl = pm + ns * kGP;       // [ns][kGP]: l
+    float* inv = pl + ns * kGP;      // [kGP]: 1 / L
     const float* base = partial_ptr(a.ws, p, vu, 0, d);
     const int rec = kGP * (d + 2);
-    for (int g = tid; g < kGP; g += nth) {
+    for (int i = tid; i < ns * kGP; i += nth) {
+        const int sp = i / kGP, g = i - sp * kGP;
+        pm[i] = __ldcg(base + sp * rec + kGP * d + g);
+        pl[i] = __ldcg(base + sp * rec + kGP * d + kGP + g);
+    }
+    __syncthreads();
+    if (tid < kGP) {
+        const int g = tid;
         float M = -CUDART_INF_F;
-        for (int s = 0; s < p.n_split; ++s) M = fmaxf(M, __ldcg(base + s * rec + kGP * d + g));
+        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, pm[sp * kGP + g]);
         float L = 0.0f;
-        for (int s = 0; s < p.n_split; ++s) {
-            const float ms = __ldcg(base + s * rec + kGP * d + g);
+        for (int sp = 0; sp < ns; ++sp) {
+            const float ms = pm[sp * kGP + g];
             const float w = (ms == -CUDART_INF_F) ? 0.0f : exp2f(ms - M);
-            wts[s * kGP + g] = w;
-            L += w * __ldcg(base + s * rec + kGP * d + kGP + g);
+            pm[sp * kGP + g] = w;
+            L += w * pl[sp * kGP + g];
         }
-        wts[p.n_split * kGP + g] = (L > 0.0f) ? 1.0f / L : 0.0f;
+        inv[g] = (L > 0.0f) ? 1.0f / L : 0.0f;
     }
     __syncthreads();
     for (int i = tid; i < kGP * d; i += nth) {
         const int g = i / d;
         float acc = 0.0f;
-        for (int s = 0; s < p.n_split; ++s) {
-            const float w = wts[s * kGP + g];
-            if (w != 0.0f) acc = fmaf(w, __ldcg(base + s * rec + i), acc);
-        }
-        scratch[i] = acc * wts[p.n_split * kGP + g];
+#pragma unroll 8
+        for (int sp = 0; sp < ns; ++sp) acc = fmaf(pm[sp * kGP + g], __ldcg(base + sp * rec + i), acc);
+        scratch[i] = acc * inv[g];
     }
     __syncthreads();
     // ---- inverse V rotation, fp16 store ----

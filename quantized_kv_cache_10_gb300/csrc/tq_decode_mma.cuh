@@ -129,6 +129,19 @@ __device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int s) {
     return sh ? __funnelshift_r(lo, hi, sh) : lo;
 }
 
+// 32 bits of w starting at bit s, where s may be negative (low bits then zero).
+template <int NW>
+__device__ __forceinline__ uint32_t bits_from(const uint32_t (&w)[NW], int s) {
+    return (s >= 0) ? bits_at<NW>(w, s) : (w[0] << (-s));
+}
+
+// ((field of `width` bits at bit s) << dst) | lane_off, in two instructions.
+template <int NW>
+__device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int s, int width, int dst, uint32_t lane_off) {
+    const uint32_t m = ((1u << width) - 1u) << dst;
+    return (bits_from<NW>(w, s - dst) & m) | lane_off;
+}
+
 // ---------------------------------------------------------------------------
 // Configuration
 // ---------------------------------------------------------------------------
@@ -171,7 +184,11 @@ struct Cfg {
     static constexpr int TS = kNWC * 16 * MT;       // tokens per stage
     static constexpr int BPK = D * KB / 8;
     static constexpr int BPV = D * VB / 8;
-    static constexpr int KT = D / 16;               // score k-tiles == P.V dim m-tiles
+    static constexpr int KT = D / 16;               // P.V dim m-tiles
+    // 8-bit K: each dim contributes two k elements (K_hi, K_lo) against (q, q), so the
+    // table word is the mma operand as it stands; other widths pair neighbouring dims.
+    static constexpr bool KEXP = (KB == 8);
+    static constexpr int KTS = KEXP ? D / 8 : D / 16;  // score k-tiles
     static constexpr bool KPAIR = KB <= 4;
     static constexpr bool VPAIR = VB <= 4;
     static constexpr int KROWS = TB::KROWS;
@@ -223,10 +240,8 @@ __device__ __forceinline__ void k_role(const uint32_t (&w)[KCW], int kt, uint32_
     } else {
         // pair lookups: index = 2*KB bits at bit 4*KB*kt (and + 2*KB); rows of 256 B
         const int s0 = 4 * KB * kt;
-        const uint32_t x0 = bits_at<KCW>(w, s0), x1 = bits_at<KCW>(w, s0 + 2 * KB);
-        const uint32_t m = (1u << (2 * KB)) - 1u;
-        const uint32_t a0 = ((x0 & m) << 8) | lane_off;
-        const uint32_t a1 = ((x1 & m) << 8) | lane_off;
+        const uint32_t a0 = field_addr<KCW>(w, s0, 2 * KB, 8, lane_off);
+        const uint32_t a1 = field_addr<KCW>(w, s0 + 2 * KB, 2 * KB, 8, lane_off);
         lds64(tab + a0, hi01, lo01);
         lds64(tab + a1, hi23, lo23);
     }
@@ -251,6 +266,46 @@ __device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint
         const uint32_t vb = lds32(tab + ((cb << 7) | lane4));
         return __byte_perm(va, vb, 0x7610);
     }
+}
+
+// V role for 2-4 bit codes.  Two tokens' chunks of up to 16 dims (a, b as
+// 64-bit values) are interleaved once into z_even / z_odd whose field i
+// (2*VB bits) is code_a | code_b << VB of dim 2i / 2i+1; each pair is then one
+// shift and one mask.
+template <int VB>
+struct VPairs {
+    static constexpr uint64_t even_mask() {
+        uint64_t m = 0;
+        for (int i = 0; i < 16; i += 2) m |= ((1ull << VB) - 1ull) << (i * VB);
+        return m;
+    }
+    uint64_t ze, zo;
+    __device__ __forceinline__ VPairs(uint64_t a, uint64_t b) {
+        constexpr uint64_t me = even_mask();
+        ze = (a & me) | ((b << VB) & ~me);
+        zo = ((a >> VB) & me) | (b & ~me);
+    }
+    // shared-memory address of the pair-table slot for dim j (0..15) of the chunk
+    __device__ __forceinline__ uint32_t addr(int j, uint32_t tab, uint32_t lane4) const {
+        const uint64_t z = (j & 1) ? zo : ze;
+        const int s = VB * (j & ~1);
+        const uint32_t x = (s >= 7) ? static_cast<uint32_t>(z >> (s - 7)) : static_cast<uint32_t>(z << (7 - s));
+        return tab + ((x & (((1u << (2 * VB)) - 1u) << 7)) | lane4);
+    }
+};
+
+// 64 bits of a row starting at bit `bit` (row 4-byte aligned; may read 12 bytes past).
+__device__ __forceinline__ uint64_t load_bits64(const uint8_t* row, int bit) {
+    const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + (bit >> 5);
+    const int sh = bit & 31;
+    const uint32_t w0 = p[0], w1 = p[1];
+    uint32_t lo = w0, hi = w1;
+    if (sh) {
+        const uint32_t w2 = p[2];
+        lo = __funnelshift_r(w0, w1, sh);
+        hi = __funnelshift_r(w1, w2, sh);
+    }
+    return (static_cast<uint64_t>(hi) << 32) | lo;
 }
 
 // Loads NW 32-bit words of a row chunk starting at bit `bit` of the row (row
@@ -300,6 +355,119 @@ __device__ __forceinline__ void load_k_chunk(const uint8_t* kbuf, int row, int t
         }
     } else {
         load_chunk<KCW>(kbuf + row * BPK, t * KCB, w);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Prologue helpers (consumer threads 0..255)
+// ---------------------------------------------------------------------------
+// Replicates the compact decode tables into one slot per lane.  Thread ctid
+// loads one table row and writes spt = rows * 32 / 256 of its lane slots,
+// rotated by lane so a warp's stores spread over the banks.
+template <typename C, int ROWS, int ENTRY_WORDS, int ROW_BYTES>
+__device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst, int ctid) {
+    constexpr int NTH = kNWC * 32;
+    constexpr int SPT = (ROWS * 32 + NTH - 1) / NTH;     // slots per thread
+    constexpr int RPP = (ROWS < NTH) ? ROWS : NTH;        // rows per pass
+    constexpr int PASSES = (ROWS + NTH - 1) / NTH;
+    const int lane = ctid & 31;
+#pragma unroll
+    for (int ps = 0; ps < PASSES; ++ps) {
+        const int r = ps * NTH + (ctid % RPP);
+        if (r < ROWS) {
+            const int l0 = (ROWS >= NTH) ? 0 : (ctid / RPP) * SPT;
+            uint32_t e0 = __ldg(src + ENTRY_WORDS * r), e1 = 0;
+            if constexpr (ENTRY_WORDS == 2) e1 = __ldg(src + 2 * r + 1);
+            const int spt = (ROWS >= NTH) ? 32 : SPT;
+#pragma unroll
+            for (int j = 0; j < ((ROWS >= NTH) ? 32 : SPT); ++j) {
+                const int l = l0 + ((j + lane) % spt);
+                if constexpr (ENTRY_WORDS == 2)
+                    *reinterpret_cast<uint2*>(dst + r * ROW_BYTES + l * 8) = make_uint2(e0, e1);
+                else
+                    *reinterpret_cast<uint32_t*>(dst + r * ROW_BYTES + l * 4) = e0;
+            }
+        }
+    }
+}
+
+template <typename C>
+__device__ __forceinline__ void replicate_tables(const DecodeArgs& a, uint8_t* ktab_s, uint8_t* vtab_s, int ctid) {
+    replicate_one<C, C::KROWS, C::KPAIR ? 2 : 1, 256>(a.ck.ktab, ktab_s, ctid);
+    replicate_one<C, C::VROWS, 1, 128>(a.cv.vtab, vtab_s, ctid);
+}
+
+// q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
+// qs[kGP][D] (rows >= G zero), with every global load in flight at once.
+template <int D>
+__device__ __forceinline__ void rotate_queries(const DecodeArgs& a, int b, int h0, int G, float* qs, int warp,
+                                               int lane, int ctid) {
+    constexpr int NTH = kNWC * 32;
+    const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D;
+    if (a.ck.is_wht) {
+        if (warp < G) {
+            float* dst = qs + warp * D;
+            uint32_t hv[D / 32], sw[D / 32];
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+                hv[k] = qg[warp * D + lane + 32 * k];
+                sw[k] = __ldg(a.ck.sign_bits + k);
+            }
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) {
+                const float v = __half2float(__ushort_as_half(static_cast<uint16_t>(hv[k])));
+                dst[lane + 32 * k] = ((sw[k] >> lane) & 1u) ? -v : v;
+            }
+            __syncwarp();
+#pragma unroll
+            for (int hh = 1; hh < D; hh <<= 1) {
+#pragma unroll
+                for (int i0 = 0; i0 < D / 2; i0 += 32) {
+                    const int i = i0 + lane;
+                    const int lo = (i / hh) * (2 * hh) + (i % hh);
+                    const float x = dst[lo], y = dst[lo + hh];
+                    dst[lo] = x + y;
+                    dst[lo + hh] = x - y;
+                }
+                __syncwarp();
+            }
+            const float f = kLog2e * a.scale / static_cast<float>(D);
+#pragma unroll
+            for (int k = 0; k < D / 32; ++k) dst[lane + 32 * k] *= f;
+        }
+        for (int i = G * D + ctid; i < kGP * D; i += NTH) qs[i] = 0.0f;
+    } else {
+        // dense: stage q in qs, then each thread forms whole columns j of Q q
+        for (int i = ctid; i < kGP * D; i += NTH)
+            qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) : 0.0f;
+        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        constexpr int CPT = (D + NTH - 1) / NTH;  // columns per thread
+        float acc[CPT][kGP];
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            const int j = ctid + NTH * c;
+#pragma unroll
+            for (int g = 0; g < kGP; ++g) acc[c][g] = 0.0f;
+            if (j < D) {
+                float col[D];
+#pragma unroll
+                for (int i = 0; i < D; ++i) col[i] = __ldg(a.ck.qt + static_cast<int64_t>(i) * D + j);
+#pragma unroll
+                for (int g = 0; g < kGP; ++g)
+                    if (g < G)
+#pragma unroll
+                        for (int i = 0; i < D; ++i) acc[c][g] = fmaf(col[i], qs[g * D + i], acc[c][g]);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        const float f = kLog2e * a.scale * rsqrtf(static_cast<float>(D));
+#pragma unroll
+        for (int c = 0; c < CPT; ++c) {
+            const int j = ctid + NTH * c;
+            if (j < D)
+#pragma unroll
+                for (int g = 0; g < kGP; ++g) qs[g * D + j] = acc[c][g] * f;
+        }
     }
 }
 
@@ -375,56 +543,51 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         // ------------------------------------------------------------ consumers: prologue
         const int ctid = tid;  // 0 .. 255
         {
-            // replicate the compact tables across the 32 lanes
-            const uint32_t* kt = a.ck.ktab;
-            if constexpr (C::KPAIR) {
-                for (int i = ctid; i < C::KROWS * 32; i += kNWC * 32) {
-                    const int r = i >> 5, l = i & 31;
-                    uint2 v = make_uint2(__ldg(kt + 2 * r), __ldg(kt + 2 * r + 1));
-                    *reinterpret_cast<uint2*>(ktab_s + r * 256 + l * 8) = v;
-                }
-            } else {
-                for (int i = ctid; i < C::KROWS * 32; i += kNWC * 32) {
-                    const int r = i >> 5, l = i & 31;
-                    *reinterpret_cast<uint32_t*>(ktab_s + r * 256 + l * 4) = __ldg(kt + r);
-                }
-            }
-            const uint32_t* vt = a.cv.vtab;
-            for (int i = ctid; i < C::VROWS * 32; i += kNWC * 32) {
-                const int r = i >> 5, l = i & 31;
-                *reinterpret_cast<uint32_t*>(vtab_s + r * 128 + l * 4) = __ldg(vt + r);
-            }
-            if (warp < G) rotate_query_warp(a, b, h0 + warp, qs + warp * D);
-            for (int i = G * D + ctid; i < kGP * D; i += kNWC * 32) qs[i] = 0.0f;
+            // Every prologue read of global memory is issued at once (one memory
+            // latency for the CTA, not one per loop iteration).
+            replicate_tables<C>(a, ktab_s, vtab_s, ctid);
+            rotate_queries<D>(a, b, h0, G, qs, warp, lane, ctid);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
 
         const int g = lane >> 2, t = lane & 3;
         // q' B fragments: Bq[kt][nt][2]
-        uint32_t Bq[C::KT][NT][2];
+        uint32_t Bq[C::KTS][NT][2];
 #pragma unroll
-        for (int kt = 0; kt < C::KT; ++kt) {
-            const int base = (D / 4) * t + 4 * kt;
+        for (int kt = 0; kt < C::KTS; ++kt) {
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                float v[4];
-                bool lo_part;
-                int qh;
-                if constexpr (NT == 2) {
-                    qh = g;
-                    lo_part = (nt == 1);
-                } else {
-                    qh = g >> 1;
-                    lo_part = (g & 1) != 0;
-                }
+                const int qh = (NT == 2) ? g : (g >> 1);
+                const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
+                if constexpr (C::KEXP) {
+                    // dims d0, d1 = (D/4) t + 2 kt + {0, 1}; k pair = (K_hi, K_lo) of one dim
+                    const int d0 = (D / 4) * t + 2 * kt;
+                    float v[2];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float x = qs[qh * D + base + e];
-                    const float hi = __half2float(__float2half_rn(x));
-                    v[e] = lo_part ? (x - hi) : x;
+                    for (int e = 0; e < 2; ++e) {
+                        const float x = qs[qh * D + d0 + e];
+                        const float hi = __half2float(__float2half_rn(x));
+                        v[e] = lo_part ? (x - hi) : x;
+                    }
+                    if (NT == 2 && lo_part) {  // q_lo multiplies K_hi only
+                        Bq[kt][nt][0] = pack_f16(v[0], 0.0f);
+                        Bq[kt][nt][1] = pack_f16(v[1], 0.0f);
+                    } else {
+                        Bq[kt][nt][0] = pack_f16(v[0], v[0]);
+                        Bq[kt][nt][1] = pack_f16(v[1], v[1]);
+                    }
+                } else {
+                    const int base = (D / 4) * t + 4 * kt;
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float x = qs[qh * D + base + e];
+                        const float hi = __half2float(__float2half_rn(x));
+                        v[e] = lo_part ? (x - hi) : x;
+                    }
+                    Bq[kt][nt][0] = pack_f16(v[0], v[1]);
+                    Bq[kt][nt][1] = pack_f16(v[2], v[3]);
                 }
-                Bq[kt][nt][0] = pack_f16(v[0], v[1]);
-                Bq[kt][nt][1] = pack_f16(v[2], v[3]);
             }
         }
 
@@ -472,16 +635,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                     uint32_t wa[C::KCW], wb[C::KCW];
                     load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
                     load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
+                    if constexpr (C::KEXP) {
 #pragma unroll
-                    for (int kt = 0; kt < C::KT; ++kt) {
-                        uint32_t ah01, ah23, al01, al23, bh01, bh23, bl01, bl23;
-                        k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23, al01, al23);
-                        k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23, bl01, bl23);
-                        // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
-                        mma16816(sc[mt][0], ah01, bh01, ah23, bh23, Bq[kt][0][0], Bq[kt][0][1]);
-                        mma16816(sc[mt][0], al01, bl01, al23, bl23, Bq[kt][0][0], Bq[kt][0][1]);
-                        if constexpr (NT == 2)
-                            mma16816(sc[mt][1], ah01, bh01, ah23, bh23, Bq[kt][1][0], Bq[kt][1][1]);
+                        for (int kt = 0; kt < C::KTS; ++kt) {
+                            // bytes 2(kt&1), 2(kt&1)+1 of word kt/2 are dims d0, d1 of this k-tile
+                            const uint32_t wA = wa[kt >> 1], wB = wb[kt >> 1];
+                            const uint32_t sel0 = 0x5504u + ((2u * (kt & 1)) << 4);
+                            const uint32_t sel1 = sel0 + 0x10u;
+                            const uint32_t r0v = lds32(ktab_a + __byte_perm(wA, koff, sel0));
+                            const uint32_t r1v = lds32(ktab_a + __byte_perm(wB, koff, sel0));
+                            const uint32_t r2v = lds32(ktab_a + __byte_perm(wA, koff, sel1));
+                            const uint32_t r3v = lds32(ktab_a + __byte_perm(wB, koff, sel1));
+                            mma16816(sc[mt][0], r0v, r1v, r2v, r3v, Bq[kt][0][0], Bq[kt][0][1]);
+                            if constexpr (NT == 2)
+                                mma16816(sc[mt][1], r0v, r1v, r2v, r3v, Bq[kt][1][0], Bq[kt][1][1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kt = 0; kt < C::KTS; ++kt) {
+                            uint32_t ah01, ah23, al01, al23, bh01, bh23, bl01, bl23;
+                            k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23, al01, al23);
+                            k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23, bl01, bl23);
+                            // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
+                            mma16816(sc[mt][0], ah01, bh01, ah23, bh23, Bq[kt][0][0], Bq[kt][0][1]);
+                            mma16816(sc[mt][0], al01, bl01, al23, bl23, Bq[kt][0][0], Bq[kt][0][1]);
+                            if constexpr (NT == 2)
+                                mma16816(sc[mt][1], ah01, bh01, ah23, bh23, Bq[kt][1][0], Bq[kt][1][1]);
+                        }
                     }
                 }
                 // ---- scale by K norms, mask, tile max ----
@@ -563,20 +743,44 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                         x1 = pack_f16(pv[1][0], 0.0f);
                     }
                     const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
-                    // V chunks of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile
-                    uint32_t v0[C::VCW], v1[C::VCW], v2[C::VCW], v3[C::VCW];
-                    const int vb = g * C::VCB;
-                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t) * C::BPV, vb, v0);
-                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vb, v1);
-                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vb, v2);
-                    load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
+                    // V of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile, thread g's dims
+                    if constexpr (C::VPAIR) {
+                        constexpr int NSUB = (D / 8 + 15) / 16;  // chunks of up to 16 dims
 #pragma unroll
-                    for (int dm = 0; dm < C::KT; ++dm) {
-                        const uint32_t a0 = v_role<VB, C::VCW>(v0, v1, 2 * dm, vtab_a, lane4);
-                        const uint32_t a1 = v_role<VB, C::VCW>(v0, v1, 2 * dm + 1, vtab_a, lane4);
-                        const uint32_t a2 = v_role<VB, C::VCW>(v2, v3, 2 * dm, vtab_a, lane4);
-                        const uint32_t a3 = v_role<VB, C::VCW>(v2, v3, 2 * dm + 1, vtab_a, lane4);
-                        mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                        for (int sub = 0; sub < NSUB; ++sub) {
+                            const int vbit = g * C::VCB + 16 * VB * sub;
+                            const VPairs<VB> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
+                                                 load_bits64(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
+                            const VPairs<VB> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
+                                                 load_bits64(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
+                            constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
+#pragma unroll
+                            for (int k = 0; k < DM_PER_SUB; ++k) {
+                                const int dm = sub * DM_PER_SUB + k;
+                                if (dm < C::KT) {
+                                    const uint32_t a0 = lds32(p01.addr(2 * k, vtab_a, lane4));
+                                    const uint32_t a1 = lds32(p01.addr(2 * k + 1, vtab_a, lane4));
+                                    const uint32_t a2 = lds32(p89.addr(2 * k, vtab_a, lane4));
+                                    const uint32_t a3 = lds32(p89.addr(2 * k + 1, vtab_a, lane4));
+                                    mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                                }
+                            }
+                        }
+                    } else {
+                        uint32_t v0[C::VCW], v1[C::VCW], v2[C::VCW], v3[C::VCW];
+                        const int vb = g * C::VCB;
+                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t) * C::BPV, vb, v0);
+                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vb, v1);
+                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vb, v2);
+                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
+#pragma unroll
+                        for (int dm = 0; dm < C::KT; ++dm) {
+                            const uint32_t a0 = v_role<VB, C::VCW>(v0, v1, 2 * dm, vtab_a, lane4);
+                            const uint32_t a1 = v_role<VB, C::VCW>(v0, v1, 2 * dm + 1, vtab_a, lane4);
+                            const uint32_t a2 = v_role<VB, C::VCW>(v2, v3, 2 * dm, vtab_a, lane4);
+                            const uint32_t a3 = v_role<VB, C::VCW>(v2, v3, 2 * dm + 1, vtab_a, lane4);
+                            mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                        }
                     }
                 }
             }

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     float* wl = wm + kWarps * kGP;       // [kWarps][kGP]
     float* cm = wl + kWarps * kGP;       // [kGP]
     float* cl = cm + kGP;                // [kGP]
-    float* scratch = cl + kGP;           // [kGP*d + (n_split+1)*kGP]
+    float* scratch = cl + kGP;           // [kGP*d + (2*n_split+1)*kGP]
     __shared__ int s_flag;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
 }
 
 size_t simt_smem_bytes(int d, int n_split) {
-    return sizeof(float) * (size_t(kGP) * d * 3 + 512 + 2 * kWarps * kGP + 2 * kGP + size_t(n_split + 1) * kGP);
+    return sizeof(float) * (size_t(kGP) * d * 3 + 512 + 2 * kWarps * kGP + 2 * kGP + size_t(2 * n_split + 1) * kGP);
 }
 
 template <int E>
