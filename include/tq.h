@@ -199,6 +199,37 @@ tq_status tq_decode_attend(const tq_codec *ck, const tq_codec *cv, const uint16_
                            void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * Decode attention for callers that cannot allocate device memory.  The
+ * pages have no counterpart of this entry point; it exists for code that must
+ * not call cudaMalloc where it attends -- work recorded into a CUDA graph it
+ * does not own, plugins whose host engine owns every allocation, loops where
+ * allocating is forbidden -- and so cannot provide the workspace
+ * tq_decode_attend needs.
+ *
+ * Same arguments, arithmetic and results as tq_decode_attend, without the
+ * workspace.  The split-K scratch is instead a fixed 8 MiB array in the
+ * library's own device memory, one per GPU that loads the library, held until
+ * the process exits.  Shapes whose workspace
+ * (tq_decode_attend_workspace_bytes) would exceed 8 MiB are rejected with
+ * TQ_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no
+ * cudaMalloc/cudaFree, no allocating library call; each call enqueues one
+ * cudaMemsetAsync that clears the scratch's arrival counters and error word
+ * (the scratch keeps the previous call's contents otherwise), then the
+ * decode-attention kernel.
+ * The first call on a device looks up the scratch's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call on a device shares the
+ * same scratch, so calls that can overlap on the GPU (different streams
+ * without ordering) race and must not be issued.  Device-side length errors
+ * are clamped as in tq_decode_attend but are not reported by this entry point.
+ */
+tq_status tq_decode_attend_noalloc(const tq_codec *ck, const tq_codec *cv, const uint16_t *q,
+                                   const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                                   const uint16_t *v_norms, const int32_t *seq_lens, int B,
+                                   int n_q_heads, int n_kv_heads, int64_t max_seq, float scale,
+                                   uint16_t *out, void *stream);
+
+/*
  * Reads and clears the device error word of a decode workspace (or of any
  * int32 word passed as dev_error to tq_encode_append).  Synchronises
  * `stream`.  *code receives the OR of TQ_DEVERR_* flags seen since the last

@@ -18,7 +18,7 @@ __all__ = [
     "TQError", "Codec", "tq_version", "tq_codec_create", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
-    "tq_get_device_error", "parse_scheme", "bytes_per_vec", "LIB_PATH",
+    "tq_get_device_error", "tq_decode_attend_noalloc", "parse_scheme", "bytes_per_vec", "LIB_PATH",
     "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION",
 ]
 
@@ -47,6 +47,8 @@ _sig = {
     "tq_decode_attend": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, C.c_float,
                                 _vp, _vp, _sz, _vp]),
     "tq_get_device_error": (_i32, [_vp, _vp, C.POINTER(_i32)]),
+    "tq_decode_attend_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, C.c_float,
+                                        _vp, _vp]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -246,3 +248,25 @@ def tq_get_device_error(error_word: torch.Tensor, stream=None) -> int:
     if st not in (0, 6):
         raise TQError(st, "tq_get_device_error")
     return code.value
+
+
+def tq_decode_attend_noalloc(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor, k_norms: torch.Tensor | None,
+                             v_codes: torch.Tensor, v_norms: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                             scale: float | None = None, stream=None):
+    """tq_decode_attend without a workspace, for callers that cannot allocate device memory: the
+    split-K scratch is a fixed 8 MiB array inside the library (see include/tq.h)."""
+    B, Hq, d = q.shape
+    Hkv, S = v_codes.shape[1], v_codes.shape[2]
+    for t, nm in ((q, "q"), (k, "k"), (v_codes, "v_codes"), (v_norms, "v_norms"), (seq_lens, "seq_lens"),
+                  (out, "out")):
+        _contig(t, nm)
+    if ck.bits == 16:
+        kp, kn = _dev(k, torch.float16, "k"), None
+    else:
+        kp, kn = _dev(k, torch.uint8, "k"), _dev(k_norms, torch.float16, "k_norms")
+    if scale is None:
+        scale = d ** -0.5
+    _check(_lib.tq_decode_attend_noalloc(ck.handle, cv.handle, _dev(q, torch.float16, "q"), kp, kn,
+                                         _dev(v_codes, torch.uint8, "v_codes"), _dev(v_norms, torch.float16, "v_norms"),
+                                         _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, S, float(scale),
+                                         _dev(out, torch.float16, "out"), _stream(stream)), "tq_decode_attend_noalloc")
