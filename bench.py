@@ -2,10 +2,11 @@
 
 One step = one decode step of the 32K long-context workload (batch 1, 64 query
 heads / 8 KV heads, head_dim 128, 8-bit K / 3-bit V, 32768 cached tokens):
-  1. encode the step's new token (K and V of every KV head) into the cache,
-  2. fused split-K decode attention over the whole packed cache.
-value = packed-KV bytes attended per second (GB/s), L2 flushed before every
-step.  The roofline object is the decode-attention kernel alone (CUDA events
+fused split-K decode attention over the whole packed cache; every 64th step
+also encodes the pending batch of 64 tokens (K and V of every KV head) into
+the cache first ("add TurboQuant KV cache compression", Design: pending tokens
+are encoded in batches of 64).  value = packed-KV bytes attended per second
+(GB/s) over all timed steps, L2 flushed before every step.  The roofline object is the decode-attention kernel alone (CUDA events
 around its launch); `e2e` adds the host->device copy of the step's inputs (q,
 new K/V, lengths) from pinned memory and the device->host read of the output.
 
@@ -231,29 +232,37 @@ def gpu_arm(args):
     # prefill: generate K/V on the host, encode the whole cache on the GPU
     K, V = w.kv("k", 16), w.kv("v", 16)
     n = w.B * w.Hkv * w.S
-    kc = torch.empty((w.B, w.Hkv, w.S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
-    kn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
     vc = torch.empty((w.B, w.Hkv, w.S, cv.bytes_per_vec), dtype=torch.uint8, device=dev)
-    vn = torch.empty_like(kn)
+    vn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
     Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
+    if w.k_bits == 16:                                       # raw fp16 keys (turbo0v*): stored as they are
+        kc, kn = Kd, None
+    else:
+        kc = torch.empty((w.B, w.Hkv, w.S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
+        kn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
     # encode throughput of the prefill (one launch per tensor), events on this stream
     enc_times = []
+    n_enc = n if w.k_bits == 16 else 2 * n
     for i in range(4):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
-        tq.tq_encode(ck, Kd.view(n, w.d), kc.view(n, -1), kn.view(-1))
+        if w.k_bits != 16:
+            tq.tq_encode(ck, Kd.view(n, w.d), kc.view(n, -1), kn.view(-1))
         tq.tq_encode(cv, Vd.view(n, w.d), vc.view(n, -1), vn.view(-1))
         e1.record()
         torch.cuda.synchronize()
         if i > 0:
             enc_times.append(e0.elapsed_time(e1) * 1e-3)
-    enc_mvec = 2 * n / statistics.median(enc_times) / 1e6
-    del Kd, Vd
+    enc_mvec = n_enc / statistics.median(enc_times) / 1e6
+    if w.k_bits != 16:
+        del Kd
+    del Vd
     q = torch.from_numpy(w.q()).to(dev)
     lens = torch.from_numpy(w.lengths()).to(dev)
-    pos = (lens - 1).to(torch.int32)                         # the step's token is the last cached one
-    k_new = torch.from_numpy(np.ascontiguousarray(K[:, :, -1:])).to(dev)
-    v_new = torch.from_numpy(np.ascontiguousarray(V[:, :, -1:])).to(dev)
+    PB = 64                                                  # pending-token batch
+    pos = (lens - PB).to(torch.int32)                        # the batch is the last 64 cached tokens
+    k_new = torch.from_numpy(np.ascontiguousarray(K[:, :, -PB:])).to(dev)
+    v_new = torch.from_numpy(np.ascontiguousarray(V[:, :, -PB:])).to(dev)
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16, device=dev)
     wsb = torch.empty(tq.tq_decode_attend_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.d), dtype=torch.uint8, device=dev)
     tq.tq_workspace_init(wsb)
@@ -261,31 +270,38 @@ def gpu_arm(args):
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        tq.tq_encode_append(ck, k_new, pos, kc, kn)
+    def encode_batch():
+        if w.k_bits == 16:
+            kc[:, :, -PB:].copy_(k_new)                      # raw fp16 keys are stored as they are
+        else:
+            tq.tq_encode_append(ck, k_new, pos, kc, kn)
         tq.tq_encode_append(cv, v_new, pos, vc, vn)
 
     def attend():
         tq.tq_decode_attend(ck, cv, q, kc, kn, vc, vn, lens, out, wsb)
 
-    launches_per_step = 3
-    for _ in range(args.warmup):
+    for i in range(args.warmup):
         flush.zero_()
-        step()
+        if i % PB == 0:
+            encode_batch()
         attend()
     torch.cuda.synchronize()
     if ws_ > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     step_t, dec_t = [], []
+    launches = 0
     with Clocks(local) as clk:
-        for _ in range(args.steps):
+        for i in range(args.steps):
             flush.zero_()
             e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
             e0.record(stream)
-            step()
+            if i % PB == 0:
+                encode_batch()
+                launches += 1 if w.k_bits == 16 else 2
             e1.record(stream)
             attend()
+            launches += 1
             e2.record(stream)
             torch.cuda.synchronize()
             step_t.append(e0.elapsed_time(e2) * 1e-3)
@@ -306,28 +322,32 @@ def gpu_arm(args):
 
     # ---- end to end through the public API: pinned host inputs in, output back ----
     h_q = torch.from_numpy(w.q()).pin_memory()
-    h_k = torch.from_numpy(np.ascontiguousarray(K[:, :, -1:])).pin_memory()
-    h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -1:])).pin_memory()
+    h_k = torch.from_numpy(np.ascontiguousarray(K[:, :, -PB:])).pin_memory()
+    h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -PB:])).pin_memory()
     h_len = torch.from_numpy(w.lengths()).pin_memory()
     h_out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16).pin_memory()
-    e2e_t = []
+    e2e_t, h2d_tot = [], 0
     for i in range(args.warmup + args.steps):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         q.copy_(h_q, non_blocking=True)
-        k_new.copy_(h_k, non_blocking=True)
-        v_new.copy_(h_v, non_blocking=True)
         lens.copy_(h_len, non_blocking=True)
-        torch.sub(lens, 1, out=pos)
-        step()
+        h2d = h_q.numel() * 2 + h_len.numel() * 4
+        if i % PB == 0:
+            k_new.copy_(h_k, non_blocking=True)
+            v_new.copy_(h_v, non_blocking=True)
+            torch.sub(lens, PB, out=pos)
+            encode_batch()
+            h2d += h_k.numel() * 2 + h_v.numel() * 2
         attend()
         h_out.copy_(out, non_blocking=True)
         e1.record(stream)
         torch.cuda.synchronize()
         if i >= args.warmup:
             e2e_t.append(e0.elapsed_time(e1) * 1e-3)
-    h2d = h_q.numel() * 2 + h_k.numel() * 2 + h_v.numel() * 2 + h_len.numel() * 4
+            h2d_tot += h2d
+    h2d = h2d_tot / args.steps
     d2h = h_out.numel() * 2
     e2e_v = ws_ * bytes_step / statistics.mean(e2e_t) / 1e9
 
@@ -347,15 +367,15 @@ def gpu_arm(args):
         "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d{w.d} S{w.S} K{w.k_bits}/V{w.v_bits}",
-                   "step": "encode new token (K,V) + fused decode attention",
+                   "step": "fused decode attention; every 64th step first encodes the 64-token pending batch (K,V)",
                    "packed_kv_bytes": bytes_step, "l2": "flushed before every step (write of 2x L2)",
                    "parallelism": f"replicas x{ws_}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic(kname), "peak_kind": peak_kind,
                      "kernel": kname, "decode_us": dec_mean * 1e6},
-        "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": 2 * n, "dim": w.d},
+        "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": launches,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,
     }
@@ -367,7 +387,7 @@ def gpu_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=64)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(tq_inputs.WORKLOADS))
