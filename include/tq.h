@@ -188,8 +188,8 @@ tq_status tq_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  *   workspace  device, >= tq_decode_attend_workspace_bytes(...) bytes,
  *              256-byte aligned, zeroed once by tq_workspace_init; one
  *              workspace must not be used by two calls that can overlap.
- * Requirements: n_q_heads % n_kv_heads == 0; max_seq % 8 == 0; every cache
- * pointer 16-byte aligned.  Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED,
+ * Requirements: n_q_heads % n_kv_heads == 0; max_seq % 8 == 0; q and every
+ * cache pointer 16-byte aligned.  Errors: TQ_ERR_INVALID_ARG, TQ_ERR_UNSUPPORTED,
  * TQ_ERR_WORKSPACE, TQ_ERR_CUDA.
  */
 tq_status tq_decode_attend(const tq_codec *ck, const tq_codec *cv, const uint16_t *q,

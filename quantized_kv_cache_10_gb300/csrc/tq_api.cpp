@@ -86,7 +86,7 @@ tq_status tq_decode_attend(const tq_codec* ck, const tq_codec* cv, const uint16_
     if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
         return TQ_ERR_INVALID_ARG;
-    if (!aligned(q, 4) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
     if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
     tq::DecodePlan p;
     if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;

@@ -273,7 +273,7 @@ tq_status tq_codec_create(int dim, int bits, uint64_t seed, tq_codec** out) {
         if (e == cudaSuccess) e = upload(&c->d_midpoints, c->midpoints.data(), c->midpoints.size());
     }
     if (e == cudaSuccess && c->is_wht) {
-        std::vector<uint32_t> sb(dim / 32, 0u);
+        std::vector<uint32_t> sb(dim / 32 < 4 ? 4 : dim / 32, 0u);  // >= 16 B: read by 16-byte bulk copies
         for (int j = 0; j < dim; ++j)
             if (c->signs[j] < 0) sb[j / 32] |= 1u << (j % 32);
         e = upload(&c->d_sign_bits, sb.data(), sb.size());

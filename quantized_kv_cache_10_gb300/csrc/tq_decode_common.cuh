@@ -91,13 +91,61 @@ __device__ inline void rotate_query_warp(const DecodeArgs& a, int b, int h, floa
     }
 }
 
+// Inverse V rotation and fp16 store of the normalised rotated outputs x[g][0..d)
+// of query heads h0 + g, g < Gc (x in shared memory, overwritten).  `signs` are
+// the V codec's sign words, in shared memory when the caller has them there.
+__device__ inline void write_outputs(const DecodeArgs& a, int b, int h0, int Gc, float* x_all,
+                                     const uint32_t* signs) {
+    const int d = a.cv.dim;
+    const int tid = threadIdx.x, nth = blockDim.x;
+    const DevCodec& cv = a.cv;
+    const int warp = tid >> 5, lane = tid & 31, nw = nth >> 5;
+    if (cv.is_wht) {
+        for (int g = warp; g < Gc; g += nw) {
+            float* x = x_all + g * d;
+            for (int hh = 1; hh < d; hh <<= 1) {
+                for (int i = lane; i < d / 2; i += 32) {
+                    const int lo = ((i & ~(hh - 1)) << 1) | (i & (hh - 1));
+                    const float u = x[lo], v = x[lo + hh];
+                    x[lo] = u + v;
+                    x[lo + hh] = u - v;
+                }
+                __syncwarp();
+            }
+            const float f = 1.0f / static_cast<float>(d);
+            uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h0 + g) * d;
+            for (int j = lane; j < d; j += 32) {
+                const float v = x[j] * f;
+                const bool neg = (signs[j >> 5] >> (j & 31)) & 1u;
+                o[j] = __half_as_ushort(__float2half_rn(neg ? -v : v));
+            }
+        }
+    } else {
+        const float f = rsqrtf(static_cast<float>(d));
+        for (int i = tid; i < Gc * d; i += nth) {
+            const int g = i / d, col = i - g * d;
+            const float* x = x_all + g * d;
+            float acc = 0.0f;
+#pragma unroll 8
+            for (int j = 0; j < d; ++j) acc = fmaf(__ldg(cv.q + static_cast<int64_t>(j) * d + col), x[j], acc);
+            a.out[(static_cast<int64_t>(b) * a.Hq + h0 + g) * d + col] = __half_as_ushort(__float2half_rn(acc * f));
+        }
+    }
+}
+
 // Publishes this CTA's partial (already in smem: so[kGP][d], sm[kGP], sl[kGP])
 // and, if it is the last CTA of the virtual unit, combines all partials,
 // applies the inverse V rotation and writes the fp16 outputs.
+// The last CTA's path is a chain of L2 round trips, so it is kept short: one
+// release atomic for the ticket, every partial of a group of outputs requested
+// in one batch (CH splits at a time) together with the (m, l) pairs, and the
+// sign words taken from shared memory (`signs`) when the caller has them.
 // Must be called by all threads of the block.  scratch: >= kGP*(d + 2*n_split + 1) floats.
+template <int CH>
 __device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan& p, int vu, int split,
                                            int b, int h0, int Gc, const float* so, const float* sm,
-                                           const float* sl, float* scratch, int* s_flag) {
+                                           const float* sl, float* scratch, int* s_flag,
+                                           const uint32_t* signs) {
     const int d = a.cv.dim;
     const int tid = threadIdx.x, nth = blockDim.x;
     float* part = partial_ptr(a.ws, p, vu, split, d);
@@ -106,30 +154,42 @@ __device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan
         part[kGP * d + g] = sm[g];
         part[kGP * d + kGP + g] = sl[g];
     }
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
-        const uint32_t prev = atomicAdd(ticket_ptr(a.ws, p, vu), 1u);
-        *s_flag = (prev == static_cast<uint32_t>(p.n_split - 1)) ? 1 : 0;
+        // the barrier orders the block's partial stores before this release atomic
+        uint32_t prev;
+        asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;"
+                     : "=r"(prev)
+                     : "l"(ticket_ptr(a.ws, p, vu))
+                     : "memory");
+        const int last = (prev == static_cast<uint32_t>(p.n_split - 1)) ? 1 : 0;
+        if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire the other CTAs' partials
+        *s_flag = last;
     }
     __syncthreads();
     if (*s_flag == 0) return;
-    __threadfence();
     // ---- last CTA of this unit: merge partials ----
-    // All (m, l) pairs are fetched at once, the per-split weights exp2(m_s - M)
-    // are formed in shared memory, and each output element then reads its
-    // n_split partial values with independent (unrolled) loads.
     const int ns = p.n_split;
     float* pm = scratch + kGP * d;   // [ns][kGP]: m, then the weights
     float* pl = pm + ns * kGP;       // [ns][kGP]: l
     float* inv = pl + ns * kGP;      // [kGP]: 1 / L
     const float* base = partial_ptr(a.ws, p, vu, 0, d);
     const int rec = kGP * (d + 2);
+    const int nout = kGP * d;
+    constexpr int OPT = 4;           // outputs per thread per group
     for (int i = tid; i < ns * kGP; i += nth) {
         const int sp = i / kGP, g = i - sp * kGP;
         pm[i] = __ldcg(base + sp * rec + kGP * d + g);
         pl[i] = __ldcg(base + sp * rec + kGP * d + kGP + g);
     }
+    float ov[OPT][CH];
+#pragma unroll
+    for (int k = 0; k < OPT; ++k)
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int i = tid + nth * k;
+            ov[k][j] = (i < nout && j < ns) ? __ldcg(base + j * rec + i) : 0.0f;
+        }
     __syncthreads();
     if (tid < kGP) {
         const int g = tid;
@@ -145,47 +205,40 @@ __device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan
         inv[g] = (L > 0.0f) ? 1.0f / L : 0.0f;
     }
     __syncthreads();
-    for (int i = tid; i < kGP * d; i += nth) {
-        const int g = i / d;
-        float acc = 0.0f;
-#pragma unroll 8
-        for (int sp = 0; sp < ns; ++sp) acc = fmaf(pm[sp * kGP + g], __ldcg(base + sp * rec + i), acc);
-        scratch[i] = acc * inv[g];
+    int grp = 0;
+    for (int i0 = tid; i0 < nout; i0 += nth * OPT, ++grp) {
+        float acc[OPT];
+#pragma unroll
+        for (int k = 0; k < OPT; ++k) acc[k] = 0.0f;
+        for (int c0 = 0; c0 < ns; c0 += CH) {
+            if (grp > 0 || c0 > 0) {
+#pragma unroll
+                for (int k = 0; k < OPT; ++k)
+#pragma unroll
+                    for (int j = 0; j < CH; ++j) {
+                        const int i = i0 + nth * k;
+                        ov[k][j] = (i < nout && c0 + j < ns) ? __ldcg(base + (c0 + j) * rec + i) : 0.0f;
+                    }
+            }
+#pragma unroll
+            for (int k = 0; k < OPT; ++k) {
+                const int i = i0 + nth * k;
+                if (i < nout) {
+                    const int g = i / d;
+#pragma unroll
+                    for (int j = 0; j < CH; ++j)
+                        if (c0 + j < ns) acc[k] = fmaf(pm[(c0 + j) * kGP + g], ov[k][j], acc[k]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < OPT; ++k) {
+            const int i = i0 + nth * k;
+            if (i < nout) scratch[i] = acc[k] * inv[i / d];
+        }
     }
     __syncthreads();
-    // ---- inverse V rotation, fp16 store ----
-    const DevCodec& cv = a.cv;
-    const int warp = tid >> 5, lane = tid & 31, nw = nth >> 5;
-    if (cv.is_wht) {
-        for (int g = warp; g < Gc; g += nw) {
-            float* x = scratch + g * d;
-            for (int hh = 1; hh < d; hh <<= 1) {
-                for (int i = lane; i < d / 2; i += 32) {
-                    const int lo = (i / hh) * (2 * hh) + (i % hh);
-                    const float u = x[lo], v = x[lo + hh];
-                    x[lo] = u + v;
-                    x[lo + hh] = u - v;
-                }
-                __syncwarp();
-            }
-            const float f = 1.0f / static_cast<float>(d);
-            uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h0 + g) * d;
-            for (int j = lane; j < d; j += 32) {
-                const float v = x[j] * f;
-                const bool neg = (__ldg(cv.sign_bits + (j >> 5)) >> (j & 31)) & 1u;
-                o[j] = __half_as_ushort(__float2half_rn(neg ? -v : v));
-            }
-        }
-    } else {
-        const float f = rsqrtf(static_cast<float>(d));
-        for (int i = tid; i < Gc * d; i += nth) {
-            const int g = i / d, col = i - g * d;
-            const float* x = scratch + g * d;
-            float acc = 0.0f;
-            for (int j = 0; j < d; ++j) acc = fmaf(__ldg(cv.q + static_cast<int64_t>(j) * d + col), x[j], acc);
-            a.out[(static_cast<int64_t>(b) * a.Hq + h0 + g) * d + col] = __half_as_ushort(__float2half_rn(acc * f));
-        }
-    }
+    write_outputs(a, b, h0, Gc, scratch, signs ? signs : a.cv.sign_bits);
     if (tid == 0) *ticket_ptr(a.ws, p, vu) = 0u;  // every CTA of this unit has arrived
 }
 

@@ -158,7 +158,11 @@ struct TableBytes {
     static constexpr int VROWS = (VB <= 4) ? (1 << (2 * VB)) : 256;
     static constexpr int KTAB = KROWS * 256;   // 32 lanes x 8 B (pairs) or 32 x 4 B in a 256-B row
     static constexpr int VTAB = VROWS * 128;   // 32 lanes x 4 B
-    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024;
+    // TMA landing area for the prologue: compact K / V tables, the query block, sign words
+    static constexpr int KW = (KB <= 4) ? 2 * KROWS : KROWS;   // compact K table words
+    static constexpr int VW = VROWS;                           // compact V table words
+    static constexpr int PRO = al128(KW * 4) + al128(VW * 4) + al128(kGP * D * 2) + 128;
+    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024 + PRO;
     static constexpr int stage(int ts) {
         return al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
     }
@@ -171,7 +175,9 @@ struct TableBytes {
 // Same test for run-time (d, bits) on the host.
 inline bool mma_fits(int D, int KB, int VB) {
     const int krows = (KB <= 4) ? (1 << (2 * KB)) : 256, vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
-    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024;
+    const int kw = (KB <= 4) ? 2 * krows : krows;
+    const int pro = al128(kw * 4) + al128(vrows * 4) + al128(kGP * D * 2) + 128;
+    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024 + pro;
     const int ts = kNWC * 16;
     const int stage = al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
     return fixed + 2 * stage <= kSmemLimit;
@@ -189,6 +195,10 @@ struct Cfg {
     // table word is the mma operand as it stands; other widths pair neighbouring dims.
     static constexpr bool KEXP = (KB == 8);
     static constexpr int KTS = KEXP ? D / 8 : D / 16;  // score k-tiles
+    // score n-tiles: 8-bit K with 5..8 query heads scores against q_hi only --
+    // (K_hi, K_lo) x q_hi keeps K exact to ~2^-22 and leaves only q's fp16
+    // rounding (~2^-12 relative), for 1.5 instead of 2.5 mma per token.
+    static constexpr int NTS = (KEXP && NT == 2) ? 1 : NT;
     static constexpr bool KPAIR = KB <= 4;
     static constexpr bool VPAIR = VB <= 4;
     static constexpr int KROWS = TB::KROWS;
@@ -206,6 +216,11 @@ struct Cfg {
     static constexpr int NBUF = al128(TS * 2);
     static constexpr int STAGE = KBUF + VBUF + 2 * NBUF;
     static constexpr int QBYTES = kGP * D * 4;      // q' fp32, later the merged O
+    static constexpr int KW = TB::KW, VW = TB::VW;
+    static constexpr int PRO_K = 0;                              // offsets inside the prologue area
+    static constexpr int PRO_V = al128(KW * 4);
+    static constexpr int PRO_Q = PRO_V + al128(VW * 4);
+    static constexpr int PRO_S = PRO_Q + al128(kGP * D * 2);
     static constexpr int MISC = 1024;               // barriers, m/l exchange
     static constexpr int FIXED = TB::FIXED;
     static constexpr int NSTAGE_RAW = (kSmemLimit - FIXED) / STAGE;
@@ -376,8 +391,8 @@ __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst,
         const int r = ps * NTH + (ctid % RPP);
         if (r < ROWS) {
             const int l0 = (ROWS >= NTH) ? 0 : (ctid / RPP) * SPT;
-            uint32_t e0 = __ldg(src + ENTRY_WORDS * r), e1 = 0;
-            if constexpr (ENTRY_WORDS == 2) e1 = __ldg(src + 2 * r + 1);
+            uint32_t e0 = src[ENTRY_WORDS * r], e1 = 0;
+            if constexpr (ENTRY_WORDS == 2) e1 = src[2 * r + 1];
             const int spt = (ROWS >= NTH) ? 32 : SPT;
 #pragma unroll
             for (int j = 0; j < ((ROWS >= NTH) ? 32 : SPT); ++j) {
@@ -392,18 +407,18 @@ __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst,
 }
 
 template <typename C>
-__device__ __forceinline__ void replicate_tables(const DecodeArgs& a, uint8_t* ktab_s, uint8_t* vtab_s, int ctid) {
-    replicate_one<C, C::KROWS, C::KPAIR ? 2 : 1, 256>(a.ck.ktab, ktab_s, ctid);
-    replicate_one<C, C::VROWS, 1, 128>(a.cv.vtab, vtab_s, ctid);
+__device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const uint32_t* vcompact, uint8_t* ktab_s,
+                                                 uint8_t* vtab_s, int ctid) {
+    replicate_one<C, C::KROWS, C::KPAIR ? 2 : 1, 256>(kcompact, ktab_s, ctid);
+    replicate_one<C, C::VROWS, 1, 128>(vcompact, vtab_s, ctid);
 }
 
 // q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
 // qs[kGP][D] (rows >= G zero), with every global load in flight at once.
 template <int D>
-__device__ __forceinline__ void rotate_queries(const DecodeArgs& a, int b, int h0, int G, float* qs, int warp,
-                                               int lane, int ctid) {
+__device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint32_t* signs, int G,
+                                               float* qs, int warp, int lane, int ctid) {
     constexpr int NTH = kNWC * 32;
-    const uint16_t* qg = a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D;
     if (a.ck.is_wht) {
         if (warp < G) {
             float* dst = qs + warp * D;
@@ -411,7 +426,7 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, int b, int h
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) {
                 hv[k] = qg[warp * D + lane + 32 * k];
-                sw[k] = __ldg(a.ck.sign_bits + k);
+                sw[k] = signs[k];
             }
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) {
@@ -484,13 +499,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE]
     uint64_t* empty = full + 4;                                          // [NSTAGE]
-    float* wm = reinterpret_cast<float*>(misc + 64);                     // [kNWC][kGP]
+    uint64_t* setup = full + 8;                                          // prologue copies
+    float* wm = reinterpret_cast<float*>(misc + 128);                    // [kNWC][kGP]
     float* wl = wm + kNWC * kGP;                                         // [kNWC][kGP]
     float* cm = wl + kNWC * kGP;                                         // [kGP]
     float* cl = cm + kGP;                                                // [kGP]
     int* s_flag = reinterpret_cast<int*>(cl + kGP);
     int* s_abort = s_flag + 1;
-    uint8_t* ring = misc + C::MISC;
+    uint8_t* pro = misc + C::MISC;                                       // prologue landing area
+    uint8_t* ring = pro + C::TB::PRO;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int u = blockIdx.y, split = blockIdx.x;
@@ -508,6 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             mbar_init(full + s, 1);
             mbar_init(empty + s, kNWC);
         }
+        mbar_init(setup, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -517,6 +535,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     if (warp == kNWC) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
+            // prologue data first: compact tables, this unit's query block, sign words
+            const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
+            // sign words: K codec's at PRO_S, V codec's at PRO_S + 64 (<= 64 B each, D <= 512)
+            const uint32_t sbytes = a.ck.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
+            const uint32_t vsbytes = a.cv.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
+            mbar_arrive_expect_tx(setup, C::KW * 4 + C::VW * 4 + qbytes + sbytes + vsbytes);
+            bulk_g2s(pro + C::PRO_K, a.ck.ktab, C::KW * 4, setup);
+            bulk_g2s(pro + C::PRO_V, a.cv.vtab, C::VW * 4, setup);
+            bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup);
+            if (sbytes) bulk_g2s(pro + C::PRO_S, a.ck.sign_bits, sbytes, setup);
+            if (vsbytes) bulk_g2s(pro + C::PRO_S + 64, a.cv.sign_bits, vsbytes, setup);
             const uint8_t* kg = static_cast<const uint8_t*>(a.k);
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it % C::NSTAGE;
@@ -545,18 +574,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         {
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
-            replicate_tables<C>(a, ktab_s, vtab_s, ctid);
-            rotate_queries<D>(a, b, h0, G, qs, warp, lane, ctid);
+            if (!__all_sync(kFullMask, mbar_wait(setup, 0))) {
+                if (lane == 0) {
+                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                }
+            }
+            replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
+                                reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
+            rotate_queries<D>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
+                              reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp, lane, ctid);
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
 
         const int g = lane >> 2, t = lane & 3;
         // q' B fragments: Bq[kt][nt][2]
-        uint32_t Bq[C::KTS][NT][2];
+        uint32_t Bq[C::KTS][C::NTS][2];
 #pragma unroll
         for (int kt = 0; kt < C::KTS; ++kt) {
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
+            for (int nt = 0; nt < C::NTS; ++nt) {
                 const int qh = (NT == 2) ? g : (g >> 1);
                 const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
                 if constexpr (C::KEXP) {
@@ -626,11 +663,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             const int r0 = warp * 16 * C::MT;
             if (r0 < nvalid) {
                 // ---- scores for MT m-tiles ----
-                float sc[C::MT][NT][4];
+                float sc[C::MT][C::NTS][4];
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
+                    for (int nt = 0; nt < C::NTS; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
                     const int ra = r0 + 16 * mt + g, rb = ra + 8;
                     uint32_t wa[C::KCW], wb[C::KCW];
                     load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
@@ -647,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                             const uint32_t r2v = lds32(ktab_a + __byte_perm(wA, koff, sel1));
                             const uint32_t r3v = lds32(ktab_a + __byte_perm(wB, koff, sel1));
                             mma16816(sc[mt][0], r0v, r1v, r2v, r3v, Bq[kt][0][0], Bq[kt][0][1]);
-                            if constexpr (NT == 2)
+                            if constexpr (C::NTS == 2)
                                 mma16816(sc[mt][1], r0v, r1v, r2v, r3v, Bq[kt][1][0], Bq[kt][1][1]);
                         }
                     } else {
@@ -659,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                             // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
                             mma16816(sc[mt][0], ah01, bh01, ah23, bh23, Bq[kt][0][0], Bq[kt][0][1]);
                             mma16816(sc[mt][0], al01, bl01, al23, bl23, Bq[kt][0][0], Bq[kt][0][1]);
-                            if constexpr (NT == 2)
+                            if constexpr (C::NTS == 2)
                                 mma16816(sc[mt][1], ah01, bh01, ah23, bh23, Bq[kt][1][0], Bq[kt][1][1]);
                         }
                     }
@@ -679,8 +716,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
 #pragma unroll
                         for (int j = 0; j < NT; ++j) {
                             float x;
-                            if constexpr (NT == 2)
+                            if constexpr (C::NTS == 2)
                                 x = sc[mt][0][2 * hr + j] + sc[mt][1][2 * hr + j];
+                            else if constexpr (NT == 2)
+                                x = sc[mt][0][2 * hr + j];
                             else
                                 x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
                             x = ok ? x * nk : -CUDART_INF_F;
@@ -864,7 +903,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         }
     }
     __syncthreads();
-    publish_and_combine(a, p, u, split, b, h0, G, qs, cm, cl, reinterpret_cast<float*>(ring), s_flag);
+    // the V codec's sign words (WHT) in shared memory: K and V codecs share the dim,
+    // but not the seed, so they are fetched only when the caller's V codec is WHT
+    publish_and_combine<20>(a, p, u, split, b, h0, G, qs, cm, cl, reinterpret_cast<float*>(ring), s_flag,
+                            a.cv.is_wht ? reinterpret_cast<const uint32_t*>(pro + C::PRO_S + 64) : nullptr);
 }
 
 

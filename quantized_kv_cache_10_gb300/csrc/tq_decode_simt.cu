@@ -156,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
         cl[g] = (g < Gc) ? L : 0.0f;
     }
     __syncthreads();
-    publish_and_combine(a, p, vu, split, b, h0, Gc, so, cm, cl, scratch, &s_flag);
+    publish_and_combine<16>(a, p, vu, split, b, h0, Gc, so, cm, cl, scratch, &s_flag, nullptr);
 }
 
 size_t simt_smem_bytes(int d, int n_split) {

@@ -62,7 +62,7 @@ tq_status tq_decode_attend_noalloc(const tq_codec* ck, const tq_codec* cv, const
     if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
         return TQ_ERR_INVALID_ARG;
-    if (!aligned(q, 4) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != ck->device || dev != cv->device) return TQ_ERR_INVALID_ARG;
     tq::DecodePlan p;

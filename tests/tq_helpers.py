@@ -2,6 +2,7 @@
 from __future__ import annotations
 
 import math
+import os
 
 import numpy as np
 
@@ -64,6 +65,10 @@ def check_close(got, ref, what=""):
     mx = float(np.abs(err).max()) if err.size else 0.0
     nrm = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(err) / nrm) if nrm > 0 else float(np.linalg.norm(err))
+    log = os.environ.get("TQ_PARITY_LOG")      # optional record of the measured errors
+    if log:
+        with open(log, "a") as f:
+            f.write(f"{what}\tmax_abs {mx:.3e}\trel_l2 {rel:.3e}\n")
     assert mx <= ATOL and rel <= RTOL_L2, f"{what}: max-abs {mx:.3e} (<= {ATOL}), rel-L2 {rel:.3e} (<= {RTOL_L2})"
     return mx, rel
 
