@@ -301,7 +301,7 @@ def gpu_arm(args):
                 launches += 1 if w.k_bits == 16 else 2
             e1.record(stream)
             attend()
-            launches += 1
+            launches += 2                                  # decode kernel + split-K combine kernel
             e2.record(stream)
             torch.cuda.synchronize()
             step_t.append(e0.elapsed_time(e2) * 1e-3)

@@ -153,14 +153,13 @@ tq_status tq_dequant(const tq_codec *codec, const uint8_t *codes, const uint16_t
 /*
  * Bytes of device workspace tq_decode_attend needs for this shape on the
  * current device (0 on invalid arguments).  The workspace holds a device
- * error word, one arrival counter per (batch, KV head) and the split-K
- * partial results.
+ * error word and the split-K partial results.
  */
 size_t tq_decode_attend_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
                                         int dim);
 
 /* Zeroes a workspace on `stream`.  Required once before the first
- * tq_decode_attend that uses it; kernels leave the counters at zero again. */
+ * tq_decode_attend that uses it (the device error word must start at zero). */
 tq_status tq_workspace_init(void *workspace, size_t ws_bytes, void *stream);
 
 /*
@@ -174,6 +173,10 @@ tq_status tq_workspace_init(void *workspace, size_t ws_bytes, void *stream);
  * in the rotated basis against codebook values, the softmax is online and
  * split over the sequence (flash-decoding), and one inverse V rotation is
  * applied to each output head.  seq_lens[b] == 0 gives a zero output.
+ * Two kernels are enqueued: the decode kernel, which writes one partial per
+ * sequence split, and the combine kernel, launched with programmatic stream
+ * serialization so it is resident before the decode kernel ends, which merges
+ * the splits and writes `out`.
  *   ck, cv     K and V codecs: same dim; cv->bits != 16
  *   q          device fp16 [B, n_q_heads, dim]
  *   k          device: packed K codes [B, n_kv_heads, max_seq, ck bytes_per_vec]
@@ -213,9 +216,8 @@ tq_status tq_decode_attend(const tq_codec *ck, const tq_codec *cv, const uint16_
  * (tq_decode_attend_workspace_bytes) would exceed 8 MiB are rejected with
  * TQ_ERR_WORKSPACE before anything is enqueued.  Nothing is allocated: no
  * cudaMalloc/cudaFree, no allocating library call; each call enqueues one
- * cudaMemsetAsync that clears the scratch's arrival counters and error word
- * (the scratch keeps the previous call's contents otherwise), then the
- * decode-attention kernel.
+ * cudaMemsetAsync that clears the scratch's error word (the scratch keeps the
+ * previous call's contents otherwise), then the decode-attention kernels.
  * The first call on a device looks up the scratch's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
  * first call before any stream capture.  Every call on a device shares the

@@ -94,13 +94,17 @@ tq_status tq_decode_attend(const tq_codec* ck, const tq_codec* cv, const uint16_
     tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
                      B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorNotSupported;
     if (tq::decode_mma_supported(ck, cv, p.G)) {
         p.kernel = 1;
-        cudaError_t e = tq::launch_decode_mma(a, p, st);
-        if (e != cudaErrorNotSupported) return from_cuda(e);
-        p.kernel = 0;
+        e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
     }
-    return from_cuda(tq::launch_decode_simt(a, p, st));
+    if (e == cudaErrorNotSupported) {
+        p.kernel = 0;
+        e = tq::launch_decode_simt(a, p, st);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(tq::launch_decode_combine(a, p, st));
 }
 
 tq_status tq_get_device_error(void* error_word, void* stream, int* code) {

@@ -1,0 +1,229 @@
+// tq_decode_combine.cu -- split-K (flash-decoding) combine of the decode
+// partials, the single inverse V rotation and the fp16 store.
+//
+// The decode kernels leave one record per (virtual unit, sequence split):
+// o[kGP][d] relative to the split's running max m, with m and the weight sum l
+// ("anyone still talking about mlx-swift-lm?": online softmax, P . V in the
+// rotated basis).  This kernel merges them exactly as the online softmax
+// would have: M = max_s m_s, w_s = 2^(m_s - M), L = sum_s w_s l_s,
+// acc = sum_s w_s o_s / L, and returns acc to the original basis once
+// ("add TurboQuant KV cache compression": R^T applied to the output, not to
+// every cached vector): diag(s) H acc / d for the Walsh-Hadamard rotation,
+// Q^T acc / sqrt(d) for the dense one.
+//
+// One CTA per (batch, query head).  It is launched with programmatic stream
+// serialization: its CTAs may be resident before the decode grid finishes,
+// and griddepcontrol.wait holds them until that grid has completed and its
+// partial records are visible.  Every head is merged in parallel, each in one
+// round of loads, instead of all heads of a unit by one last-arriving CTA.
+#include "tq_decode_common.cuh"
+
+namespace tq {
+namespace {
+
+constexpr int kCombineWarps = 4;
+
+template <int N>
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[N]) {
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N / 4; ++i) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(p) + i);
+            v[4 * i] = x.x;
+            v[4 * i + 1] = x.y;
+            v[4 * i + 2] = x.z;
+            v[4 * i + 3] = x.w;
+        }
+    } else if constexpr (N % 2 == 0) {
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float2 x = __ldcg(reinterpret_cast<const float2*>(p) + i);
+            v[2 * i] = x.x;
+            v[2 * i + 1] = x.y;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) v[i] = __ldcg(p + i);
+    }
+}
+
+// Online merge of one more partial (m_s, l_s, o_s) into (m, l, acc).
+template <int VPL>
+__device__ __forceinline__ void merge_state(float& m, float& l, float (&acc)[VPL], float ms, float ls,
+                                            const float (&os)[VPL]) {
+    if (ms == -CUDART_INF_F) return;  // empty split
+    const float mn = fmaxf(m, ms);
+    const float a = exp2f(m - mn);    // 0 while m is -inf
+    const float w = exp2f(ms - mn);
+    l = fmaf(l, a, ls * w);
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] = fmaf(acc[v], a, os[v] * w);
+    m = mn;
+}
+
+// One CTA per (batch, query head); VPL = d / 32 dims per lane: lane owns dims
+// [VPL lane, VPL (lane + 1)).  Warp w merges splits w, w + 4, ... in one pass
+// (every load of a batch in flight at once, no separate max pass), then warp 0
+// merges the four warp states in a fixed order and writes the head's output.
+template <int VPL>
+__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
+    constexpr int D = 32 * VPL;
+    __shared__ __align__(16) float s_o[kCombineWarps][D];
+    __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+    // wait for the decode grid (and the visibility of its records)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int pair = blockIdx.x;
+    const int u = pair / p.G, hl = pair - (pair / p.G) * p.G;  // unit, head within its group
+    const int qc = hl / kGP, g = hl - qc * kGP;
+    const int vu = u * p.q_chunks + qc;
+    const int b = u / a.Hkv;
+    const int h = (u - b * a.Hkv) * p.G + hl;
+    const int ns = p.n_split;
+    const int rec = kGP * (D + 2);
+    const float* base = partial_ptr(a.ws, p, vu, 0, D);
+    const float* ob = base + g * D + lane * VPL;
+
+    constexpr int CH = VPL <= 4 ? 8 : (VPL <= 8 ? 4 : 2);
+    float m = -CUDART_INF_F, l = 0.0f, acc[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] = 0.0f;
+    for (int s0 = warp; s0 < ns; s0 += kCombineWarps * CH) {
+        float ov[CH][VPL], mv[CH], lv[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) {
+            const int sp = s0 + j * kCombineWarps;
+            mv[j] = -CUDART_INF_F;
+            lv[j] = 0.0f;
+            if (sp < ns) {
+                const float* r = base + static_cast<int64_t>(sp) * rec;
+                mv[j] = __ldcg(r + kGP * D + g);
+                lv[j] = __ldcg(r + kGP * D + kGP + g);
+                load_vec<VPL>(ob + static_cast<int64_t>(sp) * rec, ov[j]);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < CH; ++j) merge_state<VPL>(m, l, acc, mv[j], lv[j], ov[j]);
+    }
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) s_o[warp][lane * VPL + v] = acc[v];
+    if (lane == 0) {
+        s_m[warp] = m;
+        s_l[warp] = l;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    m = -CUDART_INF_F;
+    l = 0.0f;
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kCombineWarps; ++w) {
+        float os[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) os[v] = s_o[w][lane * VPL + v];
+        merge_state<VPL>(m, l, acc, s_m[w], s_l[w], os);
+    }
+    const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;  // seq_len 0: zero output
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) acc[v] *= inv;
+
+    float res[VPL];
+    bool done = false;
+    if constexpr ((VPL & (VPL - 1)) == 0) {
+        if (a.cv.is_wht) {
+            // H acc: butterflies of stride < VPL inside the lane, the rest across lanes
+#pragma unroll
+            for (int hh = 1; hh < VPL; hh <<= 1)
+#pragma unroll
+                for (int v = 0; v < VPL; ++v)
+                    if (!(v & hh)) {
+                        const float x = acc[v], y = acc[v + hh];
+                        acc[v] = x + y;
+                        acc[v + hh] = x - y;
+                    }
+#pragma unroll
+            for (int lm = 1; lm < 32; lm <<= 1) {
+                const bool upper = (lane & lm) != 0;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                    const float y = __shfl_xor_sync(kFullMask, acc[v], lm);
+                    acc[v] = upper ? (y - acc[v]) : (acc[v] + y);
+                }
+            }
+            const float f = 1.0f / static_cast<float>(D);
+            const uint32_t sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
+            const int sb = (lane * VPL) & 31;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                const float x = acc[v] * f;
+                res[v] = ((sw >> (sb + v)) & 1u) ? -x : x;
+            }
+            done = true;
+        }
+    }
+    if (!done) {
+        // Q^T acc / sqrt(d): column c of the output is sum_j Q[j][c] acc[j], j ascending
+        const float f = rsqrtf(static_cast<float>(D));
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) res[v] = 0.0f;
+        const float* qcol = a.cv.q + lane * VPL;
+        for (int src = 0; src < 32; ++src) {
+#pragma unroll
+            for (int w = 0; w < VPL; ++w) {
+                const float xj = __shfl_sync(kFullMask, acc[w], src);
+                const float* qrow = qcol + static_cast<int64_t>(src * VPL + w) * D;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) res[v] = fmaf(__ldg(qrow + v), xj, res[v]);
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) res[v] *= f;
+    }
+    uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
+    if constexpr (VPL % 2 == 0) {
+        // out is 4-byte aligned and VPL lane offsets are even: 32-bit stores
+        uint32_t* o32 = reinterpret_cast<uint32_t*>(o);
+#pragma unroll
+        for (int v = 0; v < VPL; v += 2)
+            o32[v / 2] = uint32_t(__half_as_ushort(__float2half_rn(res[v]))) |
+                         (uint32_t(__half_as_ushort(__float2half_rn(res[v + 1]))) << 16);
+    } else {
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) o[v] = __half_as_ushort(__float2half_rn(res[v]));
+    }
+}
+
+template <int VPL>
+cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_units * p.G);
+    cfg.blockDim = dim3(kCombineWarps * 32);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<VPL>, a, p);
+}
+
+}  // namespace
+
+cudaError_t launch_decode_combine(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    switch (a.cv.dim / 32) {
+        case 1: return launch_vpl<1>(a, p, st);
+        case 2: return launch_vpl<2>(a, p, st);
+        case 3: return launch_vpl<3>(a, p, st);
+        case 4: return launch_vpl<4>(a, p, st);
+        case 5: return launch_vpl<5>(a, p, st);
+        case 6: return launch_vpl<6>(a, p, st);
+        case 7: return launch_vpl<7>(a, p, st);
+        case 8: return launch_vpl<8>(a, p, st);
+        case 16: return launch_vpl<16>(a, p, st);
+        default: return cudaErrorNotSupported;
+    }
+}
+
+}  // namespace tq

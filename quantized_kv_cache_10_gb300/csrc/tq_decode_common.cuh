@@ -1,6 +1,7 @@
 // tq_decode_common.cuh -- pieces shared by the decode-attention kernels:
-// workspace layout, query rotation, split-K partial publication and the
-// last-arriving-CTA combine with the single inverse rotation.
+// workspace layout, query rotation and the split-K partial records that the
+// combine kernel (tq_decode_combine.cu) merges before the single inverse
+// rotation.
 //
 // Scores are kept in log2 units: with q' = R q * (log2(e) * scale / sqrt(d)),
 // s2_n = n16_K[n] * sum_j q'_j c_K[code_nj] equals log2(e) * scale * <q, K^_n>
@@ -26,10 +27,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 __device__ __forceinline__ float* partial_ptr(void* ws, const DecodePlan& p, int vu, int split, int d) {
     float* base = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_offset);
     return base + (static_cast<int64_t>(vu) * p.n_split + split) * (kGP * (d + 2));
-}
-
-__device__ __forceinline__ uint32_t* ticket_ptr(void* ws, const DecodePlan& p, int vu) {
-    return reinterpret_cast<uint32_t*>(static_cast<char*>(ws) + p.ticket_offset) + vu;
 }
 
 __device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int32_t*>(ws); }
@@ -91,155 +88,29 @@ __device__ inline void rotate_query_warp(const DecodeArgs& a, int b, int h, floa
     }
 }
 
-// Inverse V rotation and fp16 store of the normalised rotated outputs x[g][0..d)
-// of query heads h0 + g, g < Gc (x in shared memory, overwritten).  `signs` are
-// the V codec's sign words, in shared memory when the caller has them there.
-__device__ inline void write_outputs(const DecodeArgs& a, int b, int h0, int Gc, float* x_all,
-                                     const uint32_t* signs) {
-    const int d = a.cv.dim;
-    const int tid = threadIdx.x, nth = blockDim.x;
-    const DevCodec& cv = a.cv;
-    const int warp = tid >> 5, lane = tid & 31, nw = nth >> 5;
-    if (cv.is_wht) {
-        for (int g = warp; g < Gc; g += nw) {
-            float* x = x_all + g * d;
-            for (int hh = 1; hh < d; hh <<= 1) {
-                for (int i = lane; i < d / 2; i += 32) {
-                    const int lo = ((i & ~(hh - 1)) << 1) | (i & (hh - 1));
-                    const float u = x[lo], v = x[lo + hh];
-                    x[lo] = u + v;
-                    x[lo + hh] = u - v;
-                }
-                __syncwarp();
-            }
-            const float f = 1.0f / static_cast<float>(d);
-            uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h0 + g) * d;
-            for (int j = lane; j < d; j += 32) {
-                const float v = x[j] * f;
-                const bool neg = (signs[j >> 5] >> (j & 31)) & 1u;
-                o[j] = __half_as_ushort(__float2half_rn(neg ? -v : v));
-            }
-        }
-    } else {
-        const float f = rsqrtf(static_cast<float>(d));
-        for (int i = tid; i < Gc * d; i += nth) {
-            const int g = i / d, col = i - g * d;
-            const float* x = x_all + g * d;
-            float acc = 0.0f;
-#pragma unroll 8
-            for (int j = 0; j < d; ++j) acc = fmaf(__ldg(cv.q + static_cast<int64_t>(j) * d + col), x[j], acc);
-            a.out[(static_cast<int64_t>(b) * a.Hq + h0 + g) * d + col] = __half_as_ushort(__float2half_rn(acc * f));
-        }
-    }
+// Lets the combine kernel that follows on the stream (launched with
+// programmatic stream serialization) be scheduled while this grid still runs;
+// the combine kernel waits for this grid's completion before it reads.
+__device__ __forceinline__ void allow_dependent_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Publishes this CTA's partial (already in smem: so[kGP][d], sm[kGP], sl[kGP])
-// and, if it is the last CTA of the virtual unit, combines all partials,
-// applies the inverse V rotation and writes the fp16 outputs.
-// The last CTA's path is a chain of L2 round trips, so it is kept short: one
-// release atomic for the ticket, every partial of a group of outputs requested
-// in one batch (CH splits at a time) together with the (m, l) pairs, and the
-// sign words taken from shared memory (`signs`) when the caller has them.
-// Must be called by all threads of the block.  scratch: >= kGP*(d + 2*n_split + 1) floats.
-template <int CH>
-__device__ inline void publish_and_combine(const DecodeArgs& a, const DecodePlan& p, int vu, int split,
-                                           int b, int h0, int Gc, const float* so, const float* sm,
-                                           const float* sl, float* scratch, int* s_flag,
-                                           const uint32_t* signs) {
+// Writes this CTA's split-K partial: so[kGP][d] (unnormalised, relative to the
+// CTA's max), sm[kGP] (max, log2 units), sl[kGP] (sum of weights).  Every CTA
+// writes its record, also when its split is empty (sm = -inf), so the combine
+// reads n_split complete records.  Must be called by `nth` threads tid < nth.
+__device__ inline void write_partial(const DecodeArgs& a, const DecodePlan& p, int vu, int split, const float* so,
+                                     const float* sm, const float* sl, int tid, int nth) {
     const int d = a.cv.dim;
-    const int tid = threadIdx.x, nth = blockDim.x;
     float* part = partial_ptr(a.ws, p, vu, split, d);
-    for (int i = tid; i < kGP * d; i += nth) part[i] = so[i];
+    // d is a multiple of 32 and records are 16-byte aligned: float4 copies
+    const float4* s4 = reinterpret_cast<const float4*>(so);
+    float4* p4 = reinterpret_cast<float4*>(part);
+    for (int i = tid; i < kGP * d / 4; i += nth) p4[i] = s4[i];
     for (int g = tid; g < kGP; g += nth) {
         part[kGP * d + g] = sm[g];
         part[kGP * d + kGP + g] = sl[g];
     }
-    __syncthreads();
-    if (tid == 0) {
-        // the barrier orders the block's partial stores before this release atomic
-        uint32_t prev;
-        asm volatile("atom.add.release.gpu.global.u32 %0, [%1], 1;"
-                     : "=r"(prev)
-                     : "l"(ticket_ptr(a.ws, p, vu))
-                     : "memory");
-        const int last = (prev == static_cast<uint32_t>(p.n_split - 1)) ? 1 : 0;
-        if (last) asm volatile("fence.acq_rel.gpu;" ::: "memory");  // acquire the other CTAs' partials
-        *s_flag = last;
-    }
-    __syncthreads();
-    if (*s_flag == 0) return;
-    // ---- last CTA of this unit: merge partials ----
-    const int ns = p.n_split;
-    float* pm = scratch + kGP * d;   // [ns][kGP]: m, then the weights
-    float* pl = pm + ns * kGP;       // [ns][kGP]: l
-    float* inv = pl + ns * kGP;      // [kGP]: 1 / L
-    const float* base = partial_ptr(a.ws, p, vu, 0, d);
-    const int rec = kGP * (d + 2);
-    const int nout = kGP * d;
-    constexpr int OPT = 4;           // outputs per thread per group
-    for (int i = tid; i < ns * kGP; i += nth) {
-        const int sp = i / kGP, g = i - sp * kGP;
-        pm[i] = __ldcg(base + sp * rec + kGP * d + g);
-        pl[i] = __ldcg(base + sp * rec + kGP * d + kGP + g);
-    }
-    float ov[OPT][CH];
-#pragma unroll
-    for (int k = 0; k < OPT; ++k)
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-            const int i = tid + nth * k;
-            ov[k][j] = (i < nout && j < ns) ? __ldcg(base + j * rec + i) : 0.0f;
-        }
-    __syncthreads();
-    if (tid < kGP) {
-        const int g = tid;
-        float M = -CUDART_INF_F;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, pm[sp * kGP + g]);
-        float L = 0.0f;
-        for (int sp = 0; sp < ns; ++sp) {
-            const float ms = pm[sp * kGP + g];
-            const float w = (ms == -CUDART_INF_F) ? 0.0f : exp2f(ms - M);
-            pm[sp * kGP + g] = w;
-            L += w * pl[sp * kGP + g];
-        }
-        inv[g] = (L > 0.0f) ? 1.0f / L : 0.0f;
-    }
-    __syncthreads();
-    int grp = 0;
-    for (int i0 = tid; i0 < nout; i0 += nth * OPT, ++grp) {
-        float acc[OPT];
-#pragma unroll
-        for (int k = 0; k < OPT; ++k) acc[k] = 0.0f;
-        for (int c0 = 0; c0 < ns; c0 += CH) {
-            if (grp > 0 || c0 > 0) {
-#pragma unroll
-                for (int k = 0; k < OPT; ++k)
-#pragma unroll
-                    for (int j = 0; j < CH; ++j) {
-                        const int i = i0 + nth * k;
-                        ov[k][j] = (i < nout && c0 + j < ns) ? __ldcg(base + (c0 + j) * rec + i) : 0.0f;
-                    }
-            }
-#pragma unroll
-            for (int k = 0; k < OPT; ++k) {
-                const int i = i0 + nth * k;
-                if (i < nout) {
-                    const int g = i / d;
-#pragma unroll
-                    for (int j = 0; j < CH; ++j)
-                        if (c0 + j < ns) acc[k] = fmaf(pm[(c0 + j) * kGP + g], ov[k][j], acc[k]);
-                }
-            }
-        }
-#pragma unroll
-        for (int k = 0; k < OPT; ++k) {
-            const int i = i0 + nth * k;
-            if (i < nout) scratch[i] = acc[k] * inv[i / d];
-        }
-    }
-    __syncthreads();
-    write_outputs(a, b, h0, Gc, scratch, signs ? signs : a.cv.sign_bits);
-    if (tid == 0) *ticket_ptr(a.ws, p, vu) = 0u;  // every CTA of this unit has arrived
 }
 
 }  // namespace tq

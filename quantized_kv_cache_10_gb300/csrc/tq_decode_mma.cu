@@ -18,9 +18,9 @@
 //   P.V     O^T[16 dims x 8 col] += Vhat^T[16 dims x 16 tok] * P[16 tok x 8]
 //           with P moved from the score layout by movmatrix.trans and Vhat
 //           looked up two tokens at a time from a pair table.
-// Warps merge in shared memory in a fixed order, then the CTA publishes its
-// split-K partial and the last CTA of the unit combines and applies the single
-// inverse V rotation (tq_decode_common.cuh).
+// Warps merge in shared memory in a fixed order and the CTA writes its split-K
+// partial; the combine kernel (tq_decode_combine.cu) merges the splits and
+// applies the single inverse V rotation.
 //
 // Register/shared layouts (thread = 4*g + t in its warp):
 //   K role (A of the score mma, rows = tokens): thread t owns dims
@@ -103,9 +103,9 @@ cudaError_t launch_mma_d_extern<128>(const DecodeArgs&, const DecodePlan&, int, 
 template <>
 cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
 
-cudaError_t launch_decode_mma(const DecodeArgs& a, const DecodePlan& p0, cudaStream_t st) {
+cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     // one CTA per SM: as many splits per (batch, KV head) as fill the SMs once
-    DecodePlan p = p0;
+    const DecodePlan p0 = p;
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t sms = num_sms(dev);

@@ -15,9 +15,9 @@
 //   P.V     O^T[16 dims x 8 col] += Vhat^T[16 dims x 16 tok] * P[16 tok x 8]
 //           with P moved from the score layout by movmatrix.trans and Vhat
 //           looked up two tokens at a time from a pair table.
-// Warps merge in shared memory in a fixed order, then the CTA publishes its
-// split-K partial and the last CTA of the unit combines and applies the single
-// inverse V rotation (tq_decode_common.cuh).  Every wait is bounded: a wait that
+// Warps merge in shared memory in a fixed order and the CTA writes its split-K
+// partial; the combine kernel (tq_decode_combine.cu) merges the splits and
+// applies the single inverse V rotation.  Every wait is bounded: a wait that
 // gives up records TQ_DEVERR_TIMEOUT and the CTA drains its copies and exits.
 //
 // Register/shared layouts (thread = 4*g + t in its warp):
@@ -28,8 +28,8 @@
 //   V role (A of the P.V mma, rows = dims): thread g owns dims
 //     [(D/8) g, (D/8)(g+1)); m-tile dm rows g / g+8 are dims (D/8) g + 2 dm + 0/1.
 //   Query columns: NT == 2 (5..8 heads): column j of n-tile 0 / 1 = q_hi / q_lo
-//     of head j; NT == 1 (<= 4 heads): column 2j / 2j+1 = q_hi / q_lo of head j,
-//     and in P.V head j sits in column 2j.
+//     of head j (8-bit K: n-tile 0 only); NT == 1 (<= 4 heads): column 2j / 2j+1
+//     = q_hi / q_lo of head j, and in P.V head j sits in column 2j.
 #pragma once
 
 #include <cuda_fp16.h>
@@ -502,13 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     uint64_t* setup = full + 8;                                          // prologue copies
     float* wm = reinterpret_cast<float*>(misc + 128);                    // [kNWC][kGP]
     float* wl = wm + kNWC * kGP;                                         // [kNWC][kGP]
-    float* cm = wl + kNWC * kGP;                                         // [kGP]
-    float* cl = cm + kGP;                                                // [kGP]
-    int* s_flag = reinterpret_cast<int*>(cl + kGP);
-    int* s_abort = s_flag + 1;
+    int* s_abort = reinterpret_cast<int*>(wl + kNWC * kGP);
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
     uint8_t* ring = pro + C::TB::PRO;
 
+    allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int u = blockIdx.y, split = blockIdx.x;
     const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
@@ -872,13 +870,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
-        // fixed-order sum of the warp slices -> qs (the CTA's unnormalised o)
-        const float* all = reinterpret_cast<const float*>(ring);
-        for (int i = tid; i < kGP * D; i += kNWC * 32) {
-            float acc = 0.0f;
+        // fixed-order sum of the warp slices, straight into this CTA's partial record
+        float* part = partial_ptr(a.ws, p, u, split, D);
+        const float4* all4 = reinterpret_cast<const float4*>(ring);
+        float4* part4 = reinterpret_cast<float4*>(part);
+        for (int i = tid; i < kGP * D / 4; i += kNWC * 32) {
+            float4 acc = all4[i];
 #pragma unroll
-            for (int w = 0; w < kNWC; ++w) acc += all[w * kGP * D + i];
-            qs[i] = acc;
+            for (int w = 1; w < kNWC; ++w) {
+                const float4 x = all4[w * (kGP * D / 4) + i];
+                acc.x += x.x;
+                acc.y += x.y;
+                acc.z += x.z;
+                acc.w += x.w;
+            }
+            part4[i] = acc;
         }
         if (tid < kGP) {
             const int q = tid;
@@ -889,8 +895,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                 const float mw = wm[w * kGP + q];
                 if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
             }
-            cm[q] = (q < G) ? M : -CUDART_INF_F;
-            cl[q] = (q < G) ? L : 0.0f;
+            part[kGP * D + q] = (q < G) ? M : -CUDART_INF_F;
+            part[kGP * D + kGP + q] = (q < G) ? L : 0.0f;
         }
     }
     __syncthreads();
@@ -902,11 +908,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             }
         }
     }
-    __syncthreads();
-    // the V codec's sign words (WHT) in shared memory: K and V codecs share the dim,
-    // but not the seed, so they are fetched only when the caller's V codec is WHT
-    publish_and_combine<20>(a, p, u, split, b, h0, G, qs, cm, cl, reinterpret_cast<float*>(ring), s_flag,
-                            a.cv.is_wht ? reinterpret_cast<const uint32_t*>(pro + C::PRO_S + 64) : nullptr);
 }
 
 

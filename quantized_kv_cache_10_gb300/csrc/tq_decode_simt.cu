@@ -7,9 +7,9 @@
 // the group at once (GQA without expanding K/V: "add TurboQuant KV cache
 // compression", review of the NR0 head mapping), updates an online softmax
 // and accumulates P . dequant(V) in the rotated basis ("anyone still talking
-// about mlx-swift-lm?").  Warp states merge in shared memory, the CTA
-// publishes its split-K partial, and the last CTA of the unit combines and
-// applies the single inverse V rotation (tq_decode_common.cuh).
+// about mlx-swift-lm?").  Warp states merge in shared memory and the CTA
+// writes its split-K partial; the combine kernel (tq_decode_combine.cu)
+// merges the splits and applies the single inverse V rotation.
 //
 // This path is the correctness baseline and the fallback for shapes the
 // tensor-core kernel does not instantiate.
@@ -43,9 +43,8 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     float* wl = wm + kWarps * kGP;       // [kWarps][kGP]
     float* cm = wl + kWarps * kGP;       // [kGP]
     float* cl = cm + kGP;                // [kGP]
-    float* scratch = cl + kGP;           // [kGP*d + (2*n_split+1)*kGP]
-    __shared__ int s_flag;
 
+    allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vu = blockIdx.y, split = blockIdx.x;
     const int u = vu / p.q_chunks, qc = vu - (vu / p.q_chunks) * p.q_chunks;
@@ -156,16 +155,14 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
         cl[g] = (g < Gc) ? L : 0.0f;
     }
     __syncthreads();
-    publish_and_combine<16>(a, p, vu, split, b, h0, Gc, so, cm, cl, scratch, &s_flag, nullptr);
+    write_partial(a, p, vu, split, so, cm, cl, tid, kThreads);
 }
 
-size_t simt_smem_bytes(int d, int n_split) {
-    return sizeof(float) * (size_t(kGP) * d * 3 + 512 + 2 * kWarps * kGP + 2 * kGP + size_t(2 * n_split + 1) * kGP);
-}
+size_t simt_smem_bytes(int d) { return sizeof(float) * (size_t(kGP) * d * 2 + 512 + 2 * kWarps * kGP + 2 * kGP); }
 
 template <int E>
 cudaError_t launch_simt_e(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    const size_t smem = simt_smem_bytes(32 * E, p.n_split);
+    const size_t smem = simt_smem_bytes(32 * E);
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -215,9 +212,7 @@ bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int64_t max_seq
     chunk = (chunk + 63) / 64 * 64;
     plan.chunk = chunk;
     plan.n_split = int((max_seq + chunk - 1) / chunk);
-    plan.ticket_offset = 256;
-    const size_t tick_bytes = (size_t(vunits) * 4 + 255) / 256 * 256;
-    plan.part_offset = plan.ticket_offset + tick_bytes;
+    plan.part_offset = 256;  // after the device error word
     plan.ws_bytes = plan.part_offset + size_t(vunits) * plan.n_split * kGP * (d + 2) * sizeof(float);
     return true;
 }

@@ -70,8 +70,7 @@ struct DecodePlan {
     int n_split;         // CTAs per unit along the sequence
     int64_t chunk;       // tokens per split (multiple of 8 / tile)
     size_t ws_bytes;     // total workspace bytes
-    size_t part_offset;  // byte offset of partials
-    size_t ticket_offset;
+    size_t part_offset;  // byte offset of the split-K partial records
 };
 
 // Split-K plan (independent of the kernel chosen, so the workspace size only
@@ -113,7 +112,13 @@ struct DecodeArgs {
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
 // Returns cudaErrorNotSupported when no tensor-core instantiation matches.
-cudaError_t launch_decode_mma(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
+// May lower p.n_split / raise p.chunk (one CTA per SM); p is then the plan the
+// kernel ran with, which the combine kernel needs.
+cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st);
 bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G);
+// Combine of the split-K partials, inverse V rotation and fp16 store
+// (tq_decode_combine.cu).  Launched right after a decode kernel on the same
+// stream; p must be the plan that kernel ran with.
+cudaError_t launch_decode_combine(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
 
 }  // namespace tq

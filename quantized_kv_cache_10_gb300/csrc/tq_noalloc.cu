@@ -70,8 +70,8 @@ tq_status tq_decode_attend_noalloc(const tq_codec* ck, const tq_codec* cv, const
     if (p.ws_bytes > kScratchBytes) return TQ_ERR_WORKSPACE;  // shape too large for the fixed scratch
     void* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return TQ_ERR_CUDA;
-    // The scratch keeps whatever the previous call left: clear the error word
-    // and the arrival counters, which must start at zero.
+    // The scratch keeps whatever the previous call left: clear the error word,
+    // which must start at zero.
     if (cudaMemsetAsync(ws, 0, p.part_offset, static_cast<cudaStream_t>(stream)) != cudaSuccess) return TQ_ERR_CUDA;
     return tq_decode_attend(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, max_seq,
                             scale, out, ws, kScratchBytes, stream);
