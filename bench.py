@@ -6,9 +6,18 @@ fused split-K decode attention over the whole packed cache; every 64th step
 also encodes the pending batch of 64 tokens (K and V of every KV head) into
 the cache first ("add TurboQuant KV cache compression", Design: pending tokens
 are encoded in batches of 64).  value = packed-KV bytes attended per second
-(GB/s) over all timed steps, L2 flushed before every step.  The roofline object is the decode-attention kernel alone (CUDA events
-around its launch); `e2e` adds the host->device copy of the step's inputs (q,
-new K/V, lengths) from pinned memory and the device->host read of the output.
+(GB/s) over all timed steps.
+
+Inputs larger than L2: the packed cache exists in R replicas (R >= 4 x L2 /
+cache bytes, a power of two) and step i reads replica i mod R, so every read
+comes from HBM.  The steps run back to back, replayed from CUDA graphs of 64
+steps (launch overhead off the host), bracketed by one pair of CUDA events.
+Caches so small that this needs more than 64 replicas are instead timed one
+call at a time after an L2 flush.  The roofline object is the decode-attention
+call alone (decode kernel + combine kernel), timed the same way; `e2e` runs
+the steps eagerly through the public API with the host->device copy of the
+step's inputs (q, lengths, and the new K/V on encode steps) from pinned memory
+and the device->host read of the output in every step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference]
 
@@ -197,7 +206,7 @@ def reference_arm(args):
     if rank != 0:
         return
     w = tq_inputs.WORKLOADS[args.workload]
-    per_step = max(0.5, min(args.ref_seconds, 150.0 / (args.steps + args.warmup)))
+    per_step = min(args.ref_seconds, 150.0 / (args.steps + args.warmup))
     smp = OracleSample(w, seconds_target=per_step)
     per = []
     for i in range(args.warmup + args.steps):
@@ -229,17 +238,29 @@ def gpu_arm(args):
     w = tq_inputs.WORKLOADS[args.workload]
     ck = tq.tq_codec_create(w.d, w.k_bits, w.rot_seed)
     cv = tq.tq_codec_create(w.d, w.v_bits, w.rot_seed)
-    # prefill: generate K/V on the host, encode the whole cache on the GPU
+    bytes_step = w.packed_kv_bytes()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    # Inputs larger than L2: R replicas of the packed cache, cycled, so a replica
+    # is evicted (>= 4x L2 of other traffic) before it is read again.  Caches too
+    # small for that (R > 64) are measured one call at a time after an L2 flush.
+    need = max(2, math.ceil(4 * l2 / bytes_step))
+    R = 1 << (need - 1).bit_length()
+    replica_mode = R <= 64
+    if not replica_mode:
+        R = 1
+    # prefill: generate K/V on the host, encode the whole cache on the GPU (replica 0)
     K, V = w.kv("k", 16), w.kv("v", 16)
     n = w.B * w.Hkv * w.S
-    vc = torch.empty((w.B, w.Hkv, w.S, cv.bytes_per_vec), dtype=torch.uint8, device=dev)
-    vn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
+    vc = torch.empty((R, w.B, w.Hkv, w.S, cv.bytes_per_vec), dtype=torch.uint8, device=dev)
+    vn = torch.empty((R, w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
     Kd, Vd = torch.from_numpy(K).to(dev), torch.from_numpy(V).to(dev)
     if w.k_bits == 16:                                       # raw fp16 keys (turbo0v*): stored as they are
-        kc, kn = Kd, None
+        kc = torch.empty((R, w.B, w.Hkv, w.S, w.d), dtype=torch.float16, device=dev)
+        kc[0].copy_(Kd)
+        kn = None
     else:
-        kc = torch.empty((w.B, w.Hkv, w.S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
-        kn = torch.empty((w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
+        kc = torch.empty((R, w.B, w.Hkv, w.S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
+        kn = torch.empty((R, w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
     # encode throughput of the prefill (one launch per tensor), events on this stream
     enc_times = []
     n_enc = n if w.k_bits == 16 else 2 * n
@@ -247,16 +268,20 @@ def gpu_arm(args):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         if w.k_bits != 16:
-            tq.tq_encode(ck, Kd.view(n, w.d), kc.view(n, -1), kn.view(-1))
-        tq.tq_encode(cv, Vd.view(n, w.d), vc.view(n, -1), vn.view(-1))
+            tq.tq_encode(ck, Kd.view(n, w.d), kc[0].view(n, -1), kn[0].view(-1))
+        tq.tq_encode(cv, Vd.view(n, w.d), vc[0].view(n, -1), vn[0].view(-1))
         e1.record()
         torch.cuda.synchronize()
         if i > 0:
             enc_times.append(e0.elapsed_time(e1) * 1e-3)
     enc_mvec = n_enc / statistics.median(enc_times) / 1e6
-    if w.k_bits != 16:
-        del Kd
-    del Vd
+    del Kd, Vd
+    for r in range(1, R):
+        kc[r].copy_(kc[0])
+        vc[r].copy_(vc[0])
+        vn[r].copy_(vn[0])
+        if kn is not None:
+            kn[r].copy_(kn[0])
     q = torch.from_numpy(w.q()).to(dev)
     lens = torch.from_numpy(w.lengths()).to(dev)
     PB = 64                                                  # pending-token batch
@@ -266,59 +291,120 @@ def gpu_arm(args):
     out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16, device=dev)
     wsb = torch.empty(tq.tq_decode_attend_workspace_bytes(w.B, w.Hq, w.Hkv, w.S, w.d), dtype=torch.uint8, device=dev)
     tq.tq_workspace_init(wsb)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def encode_batch():
+    def encode_batch(r):
         if w.k_bits == 16:
-            kc[:, :, -PB:].copy_(k_new)                      # raw fp16 keys are stored as they are
+            kc[r, :, :, -PB:].copy_(k_new)                   # raw fp16 keys are stored as they are
         else:
-            tq.tq_encode_append(ck, k_new, pos, kc, kn)
-        tq.tq_encode_append(cv, v_new, pos, vc, vn)
+            tq.tq_encode_append(ck, k_new, pos, kc[r], kn[r])
+        tq.tq_encode_append(cv, v_new, pos, vc[r], vn[r])
 
-    def attend():
-        tq.tq_decode_attend(ck, cv, q, kc, kn, vc, vn, lens, out, wsb)
+    def attend(r):
+        tq.tq_decode_attend(ck, cv, q, kc[r], None if kn is None else kn[r], vc[r], vn[r], lens, out, wsb)
+
+    def step(i):
+        if i % PB == 0:
+            encode_batch(i % R)
+        attend(i % R)
+
+    enc_launches = 1 if w.k_bits == 16 else 2               # our kernels per pending-batch encode
+    launches = 2 * args.steps + enc_launches * ((args.steps + PB - 1) // PB)
+
+    def capture(fn, count):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for i in range(count):
+                fn(i)
+        return g
 
     for i in range(args.warmup):
-        flush.zero_()
-        if i % PB == 0:
-            encode_batch()
-        attend()
+        if not replica_mode:
+            flush.zero_()
+        step(i)
     torch.cuda.synchronize()
+    graphs = None
+    if replica_mode:
+        try:
+            tail = args.steps % PB
+            graphs = (capture(step, PB), capture(step, tail) if tail else None,
+                      capture(lambda i: attend(i % R), PB))
+            for g in graphs:
+                if g is not None:
+                    g.replay()
+            torch.cuda.synchronize()
+        except Exception as exc:                             # capture unsupported: eager launches
+            print(f"# CUDA graph capture failed ({exc}); timing eager launches", file=sys.stderr)
+            graphs = None
     if ws_ > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    step_t, dec_t = [], []
-    launches = 0
     with Clocks(local) as clk:
-        for i in range(args.steps):
-            flush.zero_()
-            e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+        if replica_mode:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            if i % PB == 0:
-                encode_batch()
-                launches += 1 if w.k_bits == 16 else 2
+            if graphs:
+                for _ in range(args.steps // PB):
+                    graphs[0].replay()
+                if graphs[1] is not None:
+                    graphs[1].replay()
+            else:
+                for i in range(args.steps):
+                    step(i)
             e1.record(stream)
-            attend()
-            launches += 2                                  # decode kernel + split-K combine kernel
-            e2.record(stream)
             torch.cuda.synchronize()
-            step_t.append(e0.elapsed_time(e2) * 1e-3)
-            dec_t.append(e1.elapsed_time(e2) * 1e-3)
+            tot = e0.elapsed_time(e1) * 1e-3
+            # the decode-attention call alone (no pending-batch encodes), same replicas
+            reps = max(8, args.steps // PB)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for j in range(reps):
+                if graphs:
+                    graphs[2].replay()
+                else:
+                    for i in range(PB):
+                        attend(i % R)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            dec_mean = e0.elapsed_time(e1) * 1e-3 / (reps * PB)
+        else:
+            step_t, dec_t = [], []
+            for i in range(args.steps):
+                flush.zero_()
+                e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                e0.record(stream)
+                if i % PB == 0:
+                    encode_batch(0)
+                e1.record(stream)
+                attend(0)
+                e2.record(stream)
+                torch.cuda.synchronize()
+                step_t.append(e0.elapsed_time(e2) * 1e-3)
+                dec_t.append(e1.elapsed_time(e2) * 1e-3)
+            tot = sum(step_t)
+            dec_mean = statistics.mean(dec_t)
     torch.cuda.synchronize()
     assert tq.tq_get_device_error(wsb) == 0
-    tot = sum(step_t)
     if ws_ > 1:
         t = torch.tensor([tot], device=dev, dtype=torch.float64)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         tot = float(t.item())
         torch.distributed.barrier()
-    bytes_step = w.packed_kv_bytes()
     value = ws_ * bytes_step * args.steps / tot / 1e9
-    dec_mean = statistics.mean(dec_t)
     peak, peak_kind = _peaks()
     achieved = bytes_step / dec_mean / 1e9
+
+    # one call on its own after an L2 flush (latency of an isolated decode step)
+    iso = []
+    for i in range(16):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        attend(0)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        iso.append(e0.elapsed_time(e1) * 1e3)
 
     # ---- end to end through the public API: pinned host inputs in, output back ----
     h_q = torch.from_numpy(w.q()).pin_memory()
@@ -326,11 +412,8 @@ def gpu_arm(args):
     h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -PB:])).pin_memory()
     h_len = torch.from_numpy(w.lengths()).pin_memory()
     h_out = torch.empty((w.B, w.Hq, w.d), dtype=torch.float16).pin_memory()
-    e2e_t, h2d_tot = [], 0
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
+
+    def e2e_step(i):
         q.copy_(h_q, non_blocking=True)
         lens.copy_(h_len, non_blocking=True)
         h2d = h_q.numel() * 2 + h_len.numel() * 4
@@ -338,18 +421,37 @@ def gpu_arm(args):
             k_new.copy_(h_k, non_blocking=True)
             v_new.copy_(h_v, non_blocking=True)
             torch.sub(lens, PB, out=pos)
-            encode_batch()
+            encode_batch(i % R)
             h2d += h_k.numel() * 2 + h_v.numel() * 2
-        attend()
+        attend(i % R)
         h_out.copy_(out, non_blocking=True)
+        return h2d
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    h2d_tot = 0
+    if replica_mode:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            h2d_tot += e2e_step(i)
         e1.record(stream)
         torch.cuda.synchronize()
-        if i >= args.warmup:
-            e2e_t.append(e0.elapsed_time(e1) * 1e-3)
-            h2d_tot += h2d
+        e2e_tot = e0.elapsed_time(e1) * 1e-3
+    else:
+        e2e_tot = 0.0
+        for i in range(args.steps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            h2d_tot += e2e_step(i)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            e2e_tot += e0.elapsed_time(e1) * 1e-3
     h2d = h2d_tot / args.steps
     d2h = h_out.numel() * 2
-    e2e_v = ws_ * bytes_step / statistics.mean(e2e_t) / 1e9
+    e2e_v = ws_ * bytes_step * args.steps / e2e_tot / 1e9
 
     if rank != 0:
         if ws_ > 1:
@@ -362,17 +464,25 @@ def gpu_arm(args):
         cpu = {"value": smp.bytes() / dt / 1e9, "unit": "GB/s", "cores": smp.used, "kind": "oracle",
                "sample": smp.describe()}
     kname = "decode_attend"
+    if replica_mode:
+        l2note = (f"inputs larger than L2: {R} replicas of the packed cache "
+                  f"({R * bytes_step / 1e6:.0f} MB, >= 4x the {l2 / 1e6:.0f} MB L2) cycled, no flush; "
+                  f"steps replayed from CUDA graphs of {PB} steps" if graphs else
+                  f"inputs larger than L2: {R} replicas of the packed cache cycled, no flush; eager launches")
+    else:
+        l2note = "flushed before every step (write of 2x L2), the flush outside the timed events"
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": ws_, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": tot / args.steps * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{w.name}: B{w.B} Hq{w.Hq} Hkv{w.Hkv} d{w.d} S{w.S} K{w.k_bits}/V{w.v_bits}",
                    "step": "fused decode attention; every 64th step first encodes the 64-token pending batch (K,V)",
-                   "packed_kv_bytes": bytes_step, "l2": "flushed before every step (write of 2x L2)",
-                   "parallelism": f"replicas x{ws_}"},
+                   "packed_kv_bytes": bytes_step, "l2": l2note, "parallelism": f"replicas x{ws_}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": _traffic(kname), "peak_kind": peak_kind,
-                     "kernel": kname, "decode_us": dec_mean * 1e6},
+                     "kernel": kname, "decode_us": dec_mean * 1e6,
+                     "note": "one decode-attention call (decode kernel + split-K combine kernel) per launch"},
+        "isolated_call_us": statistics.median(iso),
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
@@ -387,8 +497,8 @@ def gpu_arm(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=16384)
+    ap.add_argument("--warmup", type=int, default=64)
     ap.add_argument("--impl", default="tq", choices=["tq", "reference"])
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(tq_inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")

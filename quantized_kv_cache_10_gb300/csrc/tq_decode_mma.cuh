@@ -120,6 +120,10 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
 
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+
 // 32 bits of the little-endian word array w starting at bit s (compile-time s).
 template <int NW>
 __device__ __forceinline__ uint32_t bits_at(const uint32_t (&w)[NW], int s) {
@@ -145,7 +149,7 @@ __device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int s, i
 // ---------------------------------------------------------------------------
 // Configuration
 // ---------------------------------------------------------------------------
-constexpr int kNWC = 8;                    // consumer warps
+constexpr int kNWC = 11;                   // consumer warps (+ the producer: 3 warps per SM sub-partition)
 constexpr int kThreads = (kNWC + 1) * 32;  // + one producer warp
 constexpr int kSmemLimit = 227 * 1024;
 
@@ -162,12 +166,16 @@ struct TableBytes {
     static constexpr int KW = (KB <= 4) ? 2 * KROWS : KROWS;   // compact K table words
     static constexpr int VW = VROWS;                           // compact V table words
     static constexpr int PRO = al128(KW * 4) + al128(VW * 4) + al128(kGP * D * 2) + 128;
-    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024 + PRO;
+    // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
+    // per (k-tile, n-tile)) instead of registers
+    static constexpr int BQB = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024 + PRO + BQB;
     static constexpr int stage(int ts) {
         return al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
     }
-    // two m-tiles per warp per stage when two such stages fit, else one
-    static constexpr int MT = (FIXED + 2 * stage(kNWC * 32) <= kSmemLimit && D <= 128) ? 2 : 1;
+    // two m-tiles per warp per stage when three such stages fit (so two are in
+    // flight while one is consumed), else one
+    static constexpr int MT = (FIXED + 3 * stage(kNWC * 32) <= kSmemLimit && D <= 128) ? 2 : 1;
     // whether the kernel fits at all (two stages of one m-tile per warp)
     static constexpr bool FITS = FIXED + 2 * stage(kNWC * 16) <= kSmemLimit;
 };
@@ -177,7 +185,8 @@ inline bool mma_fits(int D, int KB, int VB) {
     const int krows = (KB <= 4) ? (1 << (2 * KB)) : 256, vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
     const int kw = (KB <= 4) ? 2 * krows : krows;
     const int pro = al128(kw * 4) + al128(vrows * 4) + al128(kGP * D * 2) + 128;
-    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024 + pro;
+    const int bqb = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024 + pro + bqb;
     const int ts = kNWC * 16;
     const int stage = al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
     return fixed + 2 * stage <= kSmemLimit;
@@ -199,6 +208,7 @@ struct Cfg {
     // (K_hi, K_lo) x q_hi keeps K exact to ~2^-22 and leaves only q's fp16
     // rounding (~2^-12 relative), for 1.5 instead of 2.5 mma per token.
     static constexpr int NTS = (KEXP && NT == 2) ? 1 : NT;
+    static constexpr bool BQ_SMEM = TB::BQB > 0;
     static constexpr bool KPAIR = KB <= 4;
     static constexpr bool VPAIR = VB <= 4;
     static constexpr int KROWS = TB::KROWS;
@@ -374,35 +384,22 @@ __device__ __forceinline__ void load_k_chunk(const uint8_t* kbuf, int row, int t
 }
 
 // ---------------------------------------------------------------------------
-// Prologue helpers (consumer threads 0..255)
+// Prologue helpers (consumer threads)
 // ---------------------------------------------------------------------------
-// Replicates the compact decode tables into one slot per lane.  Thread ctid
-// loads one table row and writes spt = rows * 32 / 256 of its lane slots,
-// rotated by lane so a warp's stores spread over the banks.
+// Replicates the compact decode tables into one slot per lane: slot s of the
+// ROWS * 32 slots is row s / 32, lane s % 32.  A warp writes whole rows (the
+// thread count is a multiple of 32), so its loads of the compact entry are
+// broadcasts and its stores cover all banks.
 template <typename C, int ROWS, int ENTRY_WORDS, int ROW_BYTES>
 __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst, int ctid) {
     constexpr int NTH = kNWC * 32;
-    constexpr int SPT = (ROWS * 32 + NTH - 1) / NTH;     // slots per thread
-    constexpr int RPP = (ROWS < NTH) ? ROWS : NTH;        // rows per pass
-    constexpr int PASSES = (ROWS + NTH - 1) / NTH;
-    const int lane = ctid & 31;
-#pragma unroll
-    for (int ps = 0; ps < PASSES; ++ps) {
-        const int r = ps * NTH + (ctid % RPP);
-        if (r < ROWS) {
-            const int l0 = (ROWS >= NTH) ? 0 : (ctid / RPP) * SPT;
-            uint32_t e0 = src[ENTRY_WORDS * r], e1 = 0;
-            if constexpr (ENTRY_WORDS == 2) e1 = src[2 * r + 1];
-            const int spt = (ROWS >= NTH) ? 32 : SPT;
-#pragma unroll
-            for (int j = 0; j < ((ROWS >= NTH) ? 32 : SPT); ++j) {
-                const int l = l0 + ((j + lane) % spt);
-                if constexpr (ENTRY_WORDS == 2)
-                    *reinterpret_cast<uint2*>(dst + r * ROW_BYTES + l * 8) = make_uint2(e0, e1);
-                else
-                    *reinterpret_cast<uint32_t*>(dst + r * ROW_BYTES + l * 4) = e0;
-            }
-        }
+#pragma unroll 4
+    for (int s = ctid; s < ROWS * 32; s += NTH) {
+        const int r = s >> 5, l = s & 31;
+        if constexpr (ENTRY_WORDS == 2)
+            *reinterpret_cast<uint2*>(dst + r * ROW_BYTES + l * 8) = *reinterpret_cast<const uint2*>(src + 2 * r);
+        else
+            *reinterpret_cast<uint32_t*>(dst + r * ROW_BYTES + l * 4) = src[r];
     }
 }
 
@@ -419,7 +416,8 @@ template <int D>
 __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint32_t* signs, int G,
                                                float* qs, int warp, int lane, int ctid) {
     constexpr int NTH = kNWC * 32;
-    if (a.ck.is_wht) {
+    // power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense one
+    if constexpr ((D & (D - 1)) == 0) {
         if (warp < G) {
             float* dst = qs + warp * D;
             uint32_t hv[D / 32], sw[D / 32];
@@ -486,6 +484,24 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
     }
 }
 
+// q' B fragments of k-tile kt (n-tiles 0 and, when C::NTS == 2, 1): from
+// registers, or from the shared-memory copy when C::BQ_SMEM.
+template <typename C, typename BQ>
+__device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int lane, uint32_t& q00, uint32_t& q01,
+                                       uint32_t& q10, uint32_t& q11) {
+    if constexpr (C::BQ_SMEM) {
+        lds64(bq_a + ((kt * C::NTS) * 32 + lane) * 8, q00, q01);
+        if constexpr (C::NTS == 2) lds64(bq_a + ((kt * C::NTS + 1) * 32 + lane) * 8, q10, q11);
+    } else {
+        q00 = Bq[kt][0][0];
+        q01 = Bq[kt][0][1];
+        if constexpr (C::NTS == 2) {
+            q10 = Bq[kt][1][0];
+            q11 = Bq[kt][1][1];
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -504,7 +520,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     float* wl = wm + kNWC * kGP;                                         // [kNWC][kGP]
     int* s_abort = reinterpret_cast<int*>(wl + kNWC * kGP);
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
-    uint8_t* ring = pro + C::TB::PRO;
+    uint8_t* bq_s = pro + C::TB::PRO;                                    // q' fragments (D > 128)
+    uint8_t* ring = bq_s + C::TB::BQB;
 
     allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -568,7 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         __syncwarp();  // reconverge the producer warp before the block-wide barriers
     } else {
         // ------------------------------------------------------------ consumers: prologue
-        const int ctid = tid;  // 0 .. 255
+        const int ctid = tid;  // 0 .. kNWC * 32 - 1
         {
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
@@ -586,14 +603,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
 
         const int g = lane >> 2, t = lane & 3;
-        // q' B fragments: Bq[kt][nt][2]
-        uint32_t Bq[C::KTS][C::NTS][2];
+        // q' B fragments: Bq[kt][nt][2] (in shared memory for D > 128)
+        uint32_t Bq[C::BQ_SMEM ? 1 : C::KTS][C::NTS][2];
+        const uint32_t bq_a = smem_addr(bq_s);
 #pragma unroll
         for (int kt = 0; kt < C::KTS; ++kt) {
 #pragma unroll
             for (int nt = 0; nt < C::NTS; ++nt) {
                 const int qh = (NT == 2) ? g : (g >> 1);
                 const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
+                uint32_t b0, b1;
                 if constexpr (C::KEXP) {
                     // dims d0, d1 = (D/4) t + 2 kt + {0, 1}; k pair = (K_hi, K_lo) of one dim
                     const int d0 = (D / 4) * t + 2 * kt;
@@ -605,11 +624,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                         v[e] = lo_part ? (x - hi) : x;
                     }
                     if (NT == 2 && lo_part) {  // q_lo multiplies K_hi only
-                        Bq[kt][nt][0] = pack_f16(v[0], 0.0f);
-                        Bq[kt][nt][1] = pack_f16(v[1], 0.0f);
+                        b0 = pack_f16(v[0], 0.0f);
+                        b1 = pack_f16(v[1], 0.0f);
                     } else {
-                        Bq[kt][nt][0] = pack_f16(v[0], v[0]);
-                        Bq[kt][nt][1] = pack_f16(v[1], v[1]);
+                        b0 = pack_f16(v[0], v[0]);
+                        b1 = pack_f16(v[1], v[1]);
                     }
                 } else {
                     const int base = (D / 4) * t + 4 * kt;
@@ -620,11 +639,18 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                         const float hi = __half2float(__float2half_rn(x));
                         v[e] = lo_part ? (x - hi) : x;
                     }
-                    Bq[kt][nt][0] = pack_f16(v[0], v[1]);
-                    Bq[kt][nt][1] = pack_f16(v[2], v[3]);
+                    b0 = pack_f16(v[0], v[1]);
+                    b1 = pack_f16(v[2], v[3]);
+                }
+                if constexpr (C::BQ_SMEM) {
+                    if (warp == 0) sts64(bq_a + ((kt * C::NTS + nt) * 32 + lane) * 8, b0, b1);
+                } else {
+                    Bq[kt][nt][0] = b0;
+                    Bq[kt][nt][1] = b1;
                 }
             }
         }
+        if constexpr (C::BQ_SMEM) asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
 
         float O[C::KT][4];
 #pragma unroll
@@ -681,9 +707,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                             const uint32_t r1v = lds32(ktab_a + __byte_perm(wB, koff, sel0));
                             const uint32_t r2v = lds32(ktab_a + __byte_perm(wA, koff, sel1));
                             const uint32_t r3v = lds32(ktab_a + __byte_perm(wB, koff, sel1));
-                            mma16816(sc[mt][0], r0v, r1v, r2v, r3v, Bq[kt][0][0], Bq[kt][0][1]);
-                            if constexpr (C::NTS == 2)
-                                mma16816(sc[mt][1], r0v, r1v, r2v, r3v, Bq[kt][1][0], Bq[kt][1][1]);
+                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                            mma16816(sc[mt][0], r0v, r1v, r2v, r3v, q00, q01);
+                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], r0v, r1v, r2v, r3v, q10, q11);
                         }
                     } else {
 #pragma unroll
@@ -692,10 +719,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                             k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23, al01, al23);
                             k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23, bl01, bl23);
                             // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
-                            mma16816(sc[mt][0], ah01, bh01, ah23, bh23, Bq[kt][0][0], Bq[kt][0][1]);
-                            mma16816(sc[mt][0], al01, bl01, al23, bl23, Bq[kt][0][0], Bq[kt][0][1]);
-                            if constexpr (C::NTS == 2)
-                                mma16816(sc[mt][1], ah01, bh01, ah23, bh23, Bq[kt][1][0], Bq[kt][1][1]);
+                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                            mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
+                            mma16816(sc[mt][0], al01, bl01, al23, bl23, q00, q01);
+                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
                         }
                     }
                 }
