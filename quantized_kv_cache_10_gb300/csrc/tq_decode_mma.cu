@@ -82,8 +82,36 @@ void build_decode_tables(const tq_codec& c, std::vector<uint32_t>& ktab, std::ve
     }
 }
 
+namespace mma_detail {
+
+cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows) {
+    using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static std::atomic<EncodeFn> fn{nullptr};
+    EncodeFn f = fn.load();
+    if (!f) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        const cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !ptr) return cudaErrorNotSupported;
+        f = reinterpret_cast<EncodeFn>(ptr);
+        fn.store(f);
+    }
+    const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(dim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(dim) * 2};
+    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = f(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(k), gdim, gstride, box, estride,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+}  // namespace mma_detail
+
 bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G) {
-    if (G < 1 || G > 8 || ck->bits == 16 || cv->bits == 16 || ck->dim != cv->dim) return false;
+    if (G < 1 || G > 8 || cv->bits == 16 || ck->dim != cv->dim) return false;
     const int d = cv->dim;
     if (d != 64 && d != 96 && d != 128 && d != 256) return false;
     for (const auto& s : mma_detail::kSchemes)

@@ -32,6 +32,7 @@
 //     = q_hi / q_lo of head j, and in P.V head j sits in column 2j.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_fp16.h>
 
 #include <atomic>
@@ -88,6 +89,21 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
             smem_addr(dst)),
         "l"(src), "r"(bytes), "r"(smem_addr(bar))
         : "memory");
+}
+
+// 2-D tensor copy (TMA) of one box at column x, row y of the tensor map into shared memory.
+__device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -149,54 +165,71 @@ __device__ __forceinline__ uint32_t field_addr(const uint32_t (&w)[NW], int s, i
 // ---------------------------------------------------------------------------
 // Configuration
 // ---------------------------------------------------------------------------
-constexpr int kNWC = 11;                   // consumer warps (+ the producer: 3 warps per SM sub-partition)
-constexpr int kThreads = (kNWC + 1) * 32;  // + one producer warp
 constexpr int kSmemLimit = 227 * 1024;
 
 constexpr int al16(int x) { return (x + 15) / 16 * 16; }
 constexpr int al128(int x) { return (x + 127) / 128 * 128; }
+constexpr int al1024(int x) { return (x + 1023) / 1024 * 1024; }
 
-template <int D, int KB, int VB>
-struct TableBytes {
-    static constexpr int KROWS = (KB <= 4) ? (1 << (2 * KB)) : 256;
-    static constexpr int VROWS = (VB <= 4) ? (1 << (2 * VB)) : 256;
-    static constexpr int KTAB = KROWS * 256;   // 32 lanes x 8 B (pairs) or 32 x 4 B in a 256-B row
-    static constexpr int VTAB = VROWS * 128;   // 32 lanes x 4 B
-    // TMA landing area for the prologue: compact K / V tables, the query block, sign words
-    static constexpr int KW = (KB <= 4) ? 2 * KROWS : KROWS;   // compact K table words
-    static constexpr int VW = VROWS;                           // compact V table words
-    static constexpr int PRO = al128(KW * 4) + al128(VW * 4) + al128(kGP * D * 2) + 128;
-    // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
-    // per (k-tile, n-tile)) instead of registers
-    static constexpr int BQB = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
-    static constexpr int FIXED = KTAB + VTAB + kGP * D * 4 + 1024 + PRO + BQB;
-    static constexpr int stage(int ts) {
-        return al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
-    }
-    // two m-tiles per warp per stage when three such stages fit (so two are in
-    // flight while one is consumed), else one
-    static constexpr int MT = (FIXED + 3 * stage(kNWC * 32) <= kSmemLimit && D <= 128) ? 2 : 1;
-    // whether the kernel fits at all (two stages of one m-tile per warp)
-    static constexpr bool FITS = FIXED + 2 * stage(kNWC * 16) <= kSmemLimit;
+// Consumer warps per CTA (+ one TMA producer warp).  Coded K: 11, three warps
+// per SM sub-partition at a 168-register budget.  Raw fp16 K: 4, whose stages
+// are 4x larger per token, so that four stages of 64 tokens fit.
+constexpr int nwc_for(int KB) { return KB == 16 ? 4 : 11; }
+
+// Bytes of one stage of ts tokens: K codes (raw K: D/64 swizzled column blocks
+// of ts rows x 128 B, each 1024-byte aligned), V codes, K norms, V norms.
+constexpr int stage_bytes(int D, int KB, int VB, int ts) {
+    return KB == 16 ? al1024((D / 64) * al1024(ts * 128) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2))
+                    : al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
+}
+
+// Shared-memory layout of one (D, K bits, V bits) instantiation; the same
+// function serves the kernel (constexpr) and the host's support test.
+struct Layout {
+    int nwc, krows, vrows, ktab, vtab, kw, vw, pro, bqb, fixed, mt, ts, stage, nstage, smem;
 };
 
-// Same test for run-time (d, bits) on the host.
-inline bool mma_fits(int D, int KB, int VB) {
-    const int krows = (KB <= 4) ? (1 << (2 * KB)) : 256, vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
-    const int kw = (KB <= 4) ? 2 * krows : krows;
-    const int pro = al128(kw * 4) + al128(vrows * 4) + al128(kGP * D * 2) + 128;
-    const int bqb = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
-    const int fixed = krows * 256 + vrows * 128 + kGP * D * 4 + 1024 + pro + bqb;
-    const int ts = kNWC * 16;
-    const int stage = al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
-    return fixed + 2 * stage <= kSmemLimit;
+constexpr Layout make_layout(int D, int KB, int VB) {
+    Layout L{};
+    L.nwc = nwc_for(KB);
+    L.krows = (KB == 16) ? 0 : (KB <= 4) ? (1 << (2 * KB)) : 256;
+    L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
+    L.ktab = L.krows * 256;   // 32 lanes x 8 B (pairs) or 32 x 4 B in a 256-B row
+    L.vtab = L.vrows * 128;   // 32 lanes x 4 B
+    // TMA landing area for the prologue: compact K / V tables, the query block, sign words
+    L.kw = (KB == 16) ? 0 : (KB <= 4) ? 2 * L.krows : L.krows;   // compact K table words
+    L.vw = L.vrows;                                              // compact V table words
+    L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
+    // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
+    // per (k-tile, n-tile)) instead of registers
+    L.bqb = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    // (+1024 for raw K: the ring is aligned to 1024 B at run time)
+    L.fixed = L.ktab + L.vtab + kGP * D * 4 + 1024 + L.pro + L.bqb + (KB == 16 ? 1024 : 0);
+    // two m-tiles per warp per stage when three such stages fit (so two are in
+    // flight while one is consumed), else one
+    L.mt = (KB != 16 && D <= 128 && L.fixed + 3 * stage_bytes(D, KB, VB, L.nwc * 32) <= kSmemLimit) ? 2 : 1;
+    L.ts = L.nwc * 16 * L.mt;
+    L.stage = stage_bytes(D, KB, VB, L.ts);
+    const int cap = (KB == 16) ? 6 : 4;
+    const int ns = (kSmemLimit - L.fixed) / L.stage;
+    L.nstage = ns > cap ? cap : ns;
+    L.smem = L.fixed + L.nstage * L.stage;
+    return L;
+}
+
+// Whether an instantiation fits (two stages at least); host and device.
+constexpr bool mma_fits(int D, int KB, int VB) {
+    return (KB != 16 || D % 64 == 0) && make_layout(D, KB, VB).nstage >= 2;
 }
 
 template <int D, int KB, int VB, int NT>
 struct Cfg {
-    using TB = TableBytes<D, KB, VB>;
-    static constexpr int MT = TB::MT;               // m-tiles of 16 tokens per warp per stage
-    static constexpr int TS = kNWC * 16 * MT;       // tokens per stage
+    static constexpr Layout L = make_layout(D, KB, VB);
+    static constexpr int NWC = L.nwc;               // consumer warps
+    static constexpr int NTHREADS = (NWC + 1) * 32;
+    static constexpr int MT = L.mt;                 // m-tiles of 16 tokens per warp per stage
+    static constexpr int TS = L.ts;                 // tokens per stage
+    static constexpr bool KRAW = (KB == 16);        // raw fp16 K rows (no codebook)
     static constexpr int BPK = D * KB / 8;
     static constexpr int BPV = D * VB / 8;
     static constexpr int KT = D / 16;               // P.V dim m-tiles
@@ -208,38 +241,41 @@ struct Cfg {
     // (K_hi, K_lo) x q_hi keeps K exact to ~2^-22 and leaves only q's fp16
     // rounding (~2^-12 relative), for 1.5 instead of 2.5 mma per token.
     static constexpr int NTS = (KEXP && NT == 2) ? 1 : NT;
-    static constexpr bool BQ_SMEM = TB::BQB > 0;
+    static constexpr int BQB = L.bqb;
+    static constexpr bool BQ_SMEM = BQB > 0;
     static constexpr bool KPAIR = KB <= 4;
     static constexpr bool VPAIR = VB <= 4;
-    static constexpr int KROWS = TB::KROWS;
-    static constexpr int KTAB = TB::KTAB;
-    static constexpr int VROWS = TB::VROWS;
-    static constexpr int VTAB = TB::VTAB;
+    static constexpr int KROWS = L.krows;
+    static constexpr int KTAB = L.ktab;
+    static constexpr int VROWS = L.vrows;
+    static constexpr int VTAB = L.vtab;
     // per-thread chunk of one row, in bits and 32-bit words
-    static constexpr int KCB = (D / 4) * KB;        // K role: thread t, dims (D/4) t ...
+    static constexpr int KCB = (D / 4) * (KRAW ? 8 : KB);  // K role: thread t, dims (D/4) t ...
     static constexpr int KCW = (KCB + 31) / 32;
     static constexpr int VCB = (D / 8) * VB;        // V role: thread g, dims (D/8) g ...
     static constexpr int VCW = (VCB + 31) / 32;
     // stage buffers (+16 B slack: chunk loads may read one word past a row)
-    static constexpr int KBUF = al128(TS * BPK + 16);
+    static constexpr int KREG = al1024(TS * 128);   // raw K: one swizzled 64-column block
+    static constexpr int KBUF = KRAW ? (D / 64) * KREG : al128(TS * BPK + 16);
     static constexpr int VBUF = al128(TS * BPV + 16);
     static constexpr int NBUF = al128(TS * 2);
-    static constexpr int STAGE = KBUF + VBUF + 2 * NBUF;
+    static constexpr int STAGE = L.stage;
     static constexpr int QBYTES = kGP * D * 4;      // q' fp32, later the merged O
-    static constexpr int KW = TB::KW, VW = TB::VW;
+    static constexpr int KW = L.kw, VW = L.vw;
+    static constexpr int PRO = L.pro;
     static constexpr int PRO_K = 0;                              // offsets inside the prologue area
     static constexpr int PRO_V = al128(KW * 4);
     static constexpr int PRO_Q = PRO_V + al128(VW * 4);
     static constexpr int PRO_S = PRO_Q + al128(kGP * D * 2);
     static constexpr int MISC = 1024;               // barriers, m/l exchange
-    static constexpr int FIXED = TB::FIXED;
-    static constexpr int NSTAGE_RAW = (kSmemLimit - FIXED) / STAGE;
-    static constexpr int NSTAGE = NSTAGE_RAW > 4 ? 4 : NSTAGE_RAW;
-    static constexpr int SMEM = FIXED + NSTAGE * STAGE;
-    static_assert(STAGE == TB::stage(TS), "stage size");
-    static_assert(NSTAGE >= 2, "shared memory too small for two stages");
+    static constexpr int FIXED = L.fixed;
+    static constexpr int NSTAGE = L.nstage;
+    static constexpr int SMEM = L.smem;
+    static_assert(STAGE >= KBUF + VBUF + 2 * NBUF, "stage size");
+    static_assert(NSTAGE >= 2 && NSTAGE <= 8, "stage count");
+    static_assert(!KRAW || D % 64 == 0, "raw K needs 64-column blocks");
     // epilogue scratch (per-warp O slices, combine weights) lives in the stage ring
-    static_assert(NSTAGE * STAGE >= kNWC * kGP * D * 4, "stage ring too small for the warp merge");
+    static_assert(NSTAGE * STAGE >= NWC * kGP * D * 4, "stage ring too small for the warp merge");
 };
 
 // ---------------------------------------------------------------------------
@@ -392,7 +428,7 @@ __device__ __forceinline__ void load_k_chunk(const uint8_t* kbuf, int row, int t
 // broadcasts and its stores cover all banks.
 template <typename C, int ROWS, int ENTRY_WORDS, int ROW_BYTES>
 __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst, int ctid) {
-    constexpr int NTH = kNWC * 32;
+    constexpr int NTH = C::NWC * 32;
 #pragma unroll 4
     for (int s = ctid; s < ROWS * 32; s += NTH) {
         const int r = s >> 5, l = s & 31;
@@ -412,12 +448,17 @@ __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const
 
 // q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
 // qs[kGP][D] (rows >= G zero), with every global load in flight at once.
-template <int D>
+template <int D, int NWC, bool RAW>
 __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint32_t* signs, int G,
                                                float* qs, int warp, int lane, int ctid) {
-    constexpr int NTH = kNWC * 32;
-    // power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense one
-    if constexpr ((D & (D - 1)) == 0) {
+    constexpr int NTH = NWC * 32;
+    if constexpr (RAW) {
+        // raw fp16 K is scored in the original basis: q' = q * log2(e) * scale
+        const float f = kLog2e * a.scale;
+        for (int i = ctid; i < kGP * D; i += NTH)
+            qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) * f : 0.0f;
+    } else if constexpr ((D & (D - 1)) == 0) {
+        // power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense one
         if (warp < G) {
             float* dst = qs + warp * D;
             uint32_t hv[D / 32], sw[D / 32];
@@ -453,7 +494,7 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
         // dense: stage q in qs, then each thread forms whole columns j of Q q
         for (int i = ctid; i < kGP * D; i += NTH)
             qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) : 0.0f;
-        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(NWC * 32) : "memory");
         constexpr int CPT = (D + NTH - 1) / NTH;  // columns per thread
         float acc[CPT][kGP];
 #pragma unroll
@@ -472,7 +513,7 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
                         for (int i = 0; i < D; ++i) acc[c][g] = fmaf(col[i], qs[g * D + i], acc[c][g]);
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(NWC * 32) : "memory");
         const float f = kLog2e * a.scale * rsqrtf(static_cast<float>(D));
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
@@ -506,22 +547,25 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, int KB, int VB, int NT>
-__global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArgs a, const DecodePlan p) {
+__global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
+    decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT>;
     extern __shared__ __align__(1024) uint8_t smem[];
     uint8_t* ktab_s = smem;
     uint8_t* vtab_s = ktab_s + C::KTAB;
     float* qs = reinterpret_cast<float*>(vtab_s + C::VTAB);              // [kGP][D]
     uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE]
-    uint64_t* empty = full + 4;                                          // [NSTAGE]
-    uint64_t* setup = full + 8;                                          // prologue copies
-    float* wm = reinterpret_cast<float*>(misc + 128);                    // [kNWC][kGP]
-    float* wl = wm + kNWC * kGP;                                         // [kNWC][kGP]
-    int* s_abort = reinterpret_cast<int*>(wl + kNWC * kGP);
+    uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE <= 8]
+    uint64_t* empty = full + 8;                                          // [NSTAGE <= 8]
+    uint64_t* setup = full + 16;                                         // prologue copies
+    float* wm = reinterpret_cast<float*>(misc + 256);                    // [C::NWC][kGP]
+    float* wl = wm + C::NWC * kGP;                                         // [C::NWC][kGP]
+    int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
-    uint8_t* bq_s = pro + C::TB::PRO;                                    // q' fragments (D > 128)
-    uint8_t* ring = bq_s + C::TB::BQB;
+    uint8_t* bq_s = pro + C::PRO;                                    // q' fragments (D > 128)
+    uint8_t* ring = bq_s + C::BQB;
+    if constexpr (C::KRAW)  // the swizzled K blocks need 1024-byte aligned shared addresses
+        ring += (1024u - (smem_addr(ring) & 1023u)) & 1023u;
 
     allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -538,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     if (tid == 0) {
         for (int s = 0; s < C::NSTAGE; ++s) {
             mbar_init(full + s, 1);
-            mbar_init(empty + s, kNWC);
+            mbar_init(empty + s, C::NWC);
         }
         mbar_init(setup, 1);
         *s_abort = 0;
@@ -547,16 +591,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     __syncthreads();
 
     int issued = 0;  // tiles whose copies the producer has started (producer lane 0)
-    if (warp == kNWC) {
+    if (warp == C::NWC) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             // prologue data first: compact tables, this unit's query block, sign words
             const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
             // sign words: K codec's at PRO_S, V codec's at PRO_S + 64 (<= 64 B each, D <= 512)
-            const uint32_t sbytes = a.ck.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
+            const uint32_t sbytes = (a.ck.is_wht && !C::KRAW) ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
             const uint32_t vsbytes = a.cv.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
             mbar_arrive_expect_tx(setup, C::KW * 4 + C::VW * 4 + qbytes + sbytes + vsbytes);
-            bulk_g2s(pro + C::PRO_K, a.ck.ktab, C::KW * 4, setup);
+            if constexpr (C::KW > 0) bulk_g2s(pro + C::PRO_K, a.ck.ktab, C::KW * 4, setup);
             bulk_g2s(pro + C::PRO_V, a.cv.vtab, C::VW * 4, setup);
             bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup);
             if (sbytes) bulk_g2s(pro + C::PRO_S, a.ck.sign_bits, sbytes, setup);
@@ -573,11 +617,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                 const int64_t nv = min(static_cast<int64_t>(C::TS), t1 - ts);
                 const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
                 uint8_t* st = ring + s * C::STAGE;
-                const uint32_t kbytes = n8 * C::BPK, vbytes = n8 * C::BPV, nbytes = n8 * 2;
-                mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes);
-                bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
+                const uint32_t vbytes = n8 * C::BPV, nbytes = n8 * 2;
+                if constexpr (C::KRAW) {
+                    // whole boxes of TS rows per 64-column block (rows past the tensor read as zero)
+                    mbar_arrive_expect_tx(full + s, (D / 64) * C::TS * 128 + vbytes + nbytes);
+#pragma unroll
+                    for (int cb = 0; cb < D / 64; ++cb)
+                        tma_g2s_2d(st + cb * C::KREG, &kmap, 64 * cb, static_cast<int>(row0 + ts), full + s);
+                } else {
+                    const uint32_t kbytes = n8 * C::BPK;
+                    mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes);
+                    bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
+                    bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
+                }
                 bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
-                bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
                 bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
                 issued = it + 1;
             }
@@ -585,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         __syncwarp();  // reconverge the producer warp before the block-wide barriers
     } else {
         // ------------------------------------------------------------ consumers: prologue
-        const int ctid = tid;  // 0 .. kNWC * 32 - 1
+        const int ctid = tid;  // 0 .. C::NWC * 32 - 1
         {
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
@@ -597,10 +650,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             }
             replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
                                 reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
-            rotate_queries<D>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
+            rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
                               reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp, lane, ctid);
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
         const int g = lane >> 2, t = lane & 3;
         // q' B fragments: Bq[kt][nt][2] (in shared memory for D > 128)
@@ -631,11 +684,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                         b1 = pack_f16(v[1], v[1]);
                     }
                 } else {
-                    const int base = (D / 4) * t + 4 * kt;
+                    // coded K: dims (D/4) t + 4 kt + {0..3} (the K-role map); raw K:
+                    // the ldmatrix layout, dims 16 kt + 2 t + {0, 1, 8, 9}
+                    const int base = C::KRAW ? 16 * kt + 2 * t : (D / 4) * t + 4 * kt;
                     float v[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float x = qs[qh * D + base + e];
+                        const float x = qs[qh * D + base + (C::KRAW ? (e & 1) + 8 * (e >> 1) : e)];
                         const float hi = __half2float(__float2half_rn(x));
                         v[e] = lo_part ? (x - hi) : x;
                     }
@@ -650,7 +705,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                 }
             }
         }
-        if constexpr (C::BQ_SMEM) asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        if constexpr (C::BQ_SMEM) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
         float O[C::KT][4];
 #pragma unroll
@@ -693,6 +748,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
 #pragma unroll
                     for (int nt = 0; nt < C::NTS; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
                     const int ra = r0 + 16 * mt + g, rb = ra + 8;
+                    if constexpr (C::KRAW) {
+                        // rows r0 + 16 mt + 0..15 of the swizzled 64-column blocks: lanes 0-7 /
+                        // 8-15 / 16-23 / 24-31 address rows 0-7 / 8-15 / 0-7 / 8-15 at 16-byte
+                        // chunk 2 kl / 2 kl / 2 kl + 1 / 2 kl + 1 of the block, chunk c of
+                        // row r sitting at chunk c ^ (r & 7)
+                        const uint32_t rowa = smem_addr(kbuf) +
+                                              static_cast<uint32_t>((r0 + 16 * mt + (lane & 15)) * 128);
+#pragma unroll
+                        for (int kt = 0; kt < C::KTS; ++kt) {
+                            const int cb = kt >> 2, kl = kt & 3;
+                            const uint32_t chunk = static_cast<uint32_t>(2 * kl) + static_cast<uint32_t>(lane >> 4);
+                            uint32_t a0, a1, a2, a3;
+                            ldmatrix_x4(rowa + cb * C::KREG + ((chunk ^ static_cast<uint32_t>(lane & 7)) << 4), a0, a1,
+                                        a2, a3);
+                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                            mma16816(sc[mt][0], a0, a1, a2, a3, q00, q01);
+                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], a0, a1, a2, a3, q10, q11);
+                        }
+                    } else {
                     uint32_t wa[C::KCW], wb[C::KCW];
                     load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
                     load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
@@ -726,6 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                             if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
                         }
                     }
+                    }
                 }
                 // ---- scale by K norms, mask, tile max ----
                 float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
@@ -738,7 +814,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                     for (int hr = 0; hr < 2; ++hr) {
                         const int r = r0 + 16 * mt + g + 8 * hr;
                         const bool ok = r < nvalid;
-                        const float nk = __half2float(knrm[r]);
+                        const float nk = C::KRAW ? 1.0f : __half2float(knrm[r]);
 #pragma unroll
                         for (int j = 0; j < NT; ++j) {
                             float x;
@@ -872,13 +948,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
             }
         }
         // every consumer is done with the ring; wm / wl are visible
-        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
         float f[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int q = (NT == 2) ? 2 * t + j : t;
             float M = -CUDART_INF_F;
-            for (int w = 0; w < kNWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+            for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
             f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M);
         }
         float* slice = reinterpret_cast<float*>(ring) + warp * kGP * D;
@@ -897,15 +973,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
                 slice[(4 + t) * D + d0 + 1] = 0.0f;
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(kNWC * 32) : "memory");
+        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
         // fixed-order sum of the warp slices, straight into this CTA's partial record
         float* part = partial_ptr(a.ws, p, u, split, D);
         const float4* all4 = reinterpret_cast<const float4*>(ring);
         float4* part4 = reinterpret_cast<float4*>(part);
-        for (int i = tid; i < kGP * D / 4; i += kNWC * 32) {
+        for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
             float4 acc = all4[i];
 #pragma unroll
-            for (int w = 1; w < kNWC; ++w) {
+            for (int w = 1; w < C::NWC; ++w) {
                 const float4 x = all4[w * (kGP * D / 4) + i];
                 acc.x += x.x;
                 acc.y += x.y;
@@ -917,9 +993,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         if (tid < kGP) {
             const int q = tid;
             float M = -CUDART_INF_F;
-            for (int w = 0; w < kNWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+            for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
             float L = 0.0f;
-            for (int w = 0; w < kNWC; ++w) {
+            for (int w = 0; w < C::NWC; ++w) {
                 const float mw = wm[w * kGP + q];
                 if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
             }
@@ -928,7 +1004,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
         }
     }
     __syncthreads();
-    if (warp == kNWC && lane == 0 && *s_abort) {
+    if (warp == C::NWC && lane == 0 && *s_abort) {
         // a wait gave up: let every copy this CTA issued land before shared memory is released
         for (int it = (issued > C::NSTAGE ? issued - C::NSTAGE : 0); it < issued; ++it) {
             const long long c0 = clock64();
@@ -938,6 +1014,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_mma_kernel(const DecodeArg
     }
 }
 
+
+// Tensor map of raw fp16 K for the 2-D TMA copies (host; tq_decode_mma.cu).
+cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows);
 
 // Launch of one instantiation; split plan for one CTA per SM.
 template <int D, int KB, int VB, int NT>
@@ -953,19 +1032,26 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
+    CUtensorMap kmap{};
+    if constexpr (C::KRAW) {
+        // raw K [B * Hkv * max_seq rows, D] fp16 in boxes of TS rows x 64 columns, 128-byte swizzle
+        const cudaError_t e = encode_raw_k_map(&kmap, a.k, D, static_cast<int64_t>(a.B) * a.Hkv * a.max_seq, C::TS);
+        if (e != cudaSuccess) return e;
+    }
     dim3 grid(p.n_split, p.n_units);
-    decode_mma_kernel<D, KB, VB, NT><<<grid, kThreads, C::SMEM, st>>>(a, p);
+    decode_mma_kernel<D, KB, VB, NT><<<grid, C::NTHREADS, C::SMEM, st>>>(a, p, kmap);
     return cudaGetLastError();
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
-    if constexpr (TableBytes<D, KB_, VB_>::FITS) {                                            \
+    if constexpr (mma_fits(D, KB_, VB_)) {                                                    \
         if (kb == KB_ && vb == VB_)                                                           \
             return nt == 2 ? launch_inst<D, KB_, VB_, 2>(a, p, st) : launch_inst<D, KB_, VB_, 1>(a, p, st); \
     }
 
 // The (K bits, V bits) schemes with a tensor-core instantiation.
-constexpr int kSchemes[][2] = {{4, 4}, {3, 3}, {2, 2}, {4, 2}, {4, 3}, {8, 3}, {8, 4}, {8, 8}, {8, 2}, {3, 2}};
+constexpr int kSchemes[][2] = {{4, 4}, {3, 3}, {2, 2}, {4, 2}, {4, 3}, {8, 3}, {8, 4}, {8, 8}, {8, 2}, {3, 2},
+                               {16, 4}, {16, 2}, {16, 3}};
 
 template <int D>
 cudaError_t launch_mma_d(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
@@ -979,6 +1065,9 @@ cudaError_t launch_mma_d(const DecodeArgs& a, const DecodePlan& p, int kb, int v
     TQ_MMA_CASE(8, 8)
     TQ_MMA_CASE(8, 2)
     TQ_MMA_CASE(3, 2)
+    TQ_MMA_CASE(16, 4)
+    TQ_MMA_CASE(16, 2)
+    TQ_MMA_CASE(16, 3)
     return cudaErrorNotSupported;
 }
 

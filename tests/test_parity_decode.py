@@ -51,6 +51,15 @@ def test_decode_head_dims(d):
     check_close(got, ref, f"d={d}")
 
 
+@pytest.mark.parametrize("d,G,vb", [(64, 4, 4), (256, 4, 4), (256, 8, 2), (128, 8, 3), (96, 4, 4)])
+def test_decode_raw_k(d, G, vb):
+    # raw fp16 K (turbo0v*): tensor-core path with 2-D TMA copies of the rows for
+    # d = 64 / 128 / 256, the SIMT path for d = 96; a ragged tail in every split
+    w = tq_inputs.Workload("t", B=2, Hq=2 * G, Hkv=2, d=d, S=1032, k_bits=16, v_bits=vb, k_outliers=True)
+    got, ref, _ = _run_small(w, lens=[1029, 70])
+    check_close(got, ref, f"raw K d={d} G={G} V{vb}")
+
+
 @pytest.mark.parametrize("lens", [[0, 1], [63, 64], [65, 8], [1, 520]])
 def test_decode_edge_lengths(lens):
     w = tq_inputs.Workload("t", B=2, Hq=8, Hkv=2, d=128, S=520, k_bits=8, v_bits=3, k_outliers=True)
