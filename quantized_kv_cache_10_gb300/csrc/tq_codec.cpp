@@ -193,7 +193,7 @@ int num_sms(int device) {
 // ---------------------------------------------------------------------------
 // Decode-table construction lives with the tensor-core kernel that reads it.
 namespace tq {
-void build_decode_tables(const tq_codec& c, std::vector<uint32_t>& ktab, std::vector<uint32_t>& vtab);
+void build_decode_tables(tq_codec& c, std::vector<uint32_t>& ktab, std::vector<uint32_t>& vtab);
 }
 
 namespace {

@@ -34,17 +34,27 @@
 //     and in P.V head j sits in column 2j.
 #include <cuda_fp16.h>
 
+#include <algorithm>
+#include <cmath>
+
 #include "tq_decode_mma.cuh"
 
 namespace tq {
 
 // ---------------------------------------------------------------------------
 // Host: compact decode tables, built once per codec.
-//   ktab: K role.  bits <= 4: per pair index p = c0 | c1 << bits two words
-//         {hi(c0) | hi(c1) << 16, lo(c0) | lo(c1) << 16};  bits == 8: one word
-//         per code {hi | lo << 16}.  hi = fp16(c), lo = fp16(c - hi).
-//   vtab: V role.  bits <= 4: per pair index one word hi(c0) | hi(c1) << 16;
-//         bits == 8: one word per code hi | hi << 16.
+// The tensor cores take fp16 operands, and a centroid rounded to fp16 is off
+// by up to 2^-11 of itself -- a fixed error per code that does not average
+// out.  Every codebook value is therefore stored scaled by a factor alpha in
+// [1, 2) chosen so that the fp16 roundings of alpha * |c_i| are as close to
+// exact as possible (for 2/3/4-bit codebooks the worst relative error drops
+// from ~2^-12 to ~2^-21 / 2^-15.5 / 2^-13.5); the kernel divides alpha out
+// of q' (K) or of the output (V).
+//   ktab: K role.  bits <= 4: per pair index p = c0 | c1 << bits one word
+//         h(c0) | h(c1) << 16 with h(c) = fp16(alpha c);  bits == 8 (alpha 1):
+//         one word per code hi | lo << 16, hi = fp16(c), lo = fp16(c - hi).
+//   vtab: V role.  bits <= 4: per pair index one word h(c0) | h(c1) << 16;
+//         bits == 8: one word per code h | h << 16.
 // ---------------------------------------------------------------------------
 namespace {
 
@@ -55,32 +65,73 @@ uint16_t f16_bits(float x) {
 
 float f16_val(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
+// Relative error of rounding x > 0 to the nearest fp16 (normal range, ties
+// to even do not matter for the maximum), in double arithmetic.
+double f16_rel_err(double x) {
+    int e = 0;
+    std::frexp(x, &e);                         // x = m 2^e, m in [0.5, 1)
+    const double ulp = std::ldexp(1.0, e - 11);
+    return std::fabs(x - std::nearbyint(x / ulp) * ulp) / x;
+}
+
+// alpha = 1 + i / steps minimising the worst relative fp16 rounding error of
+// alpha * |c| over the codebook (first such i on ties).
+float table_alpha(const std::vector<float>& cent, int steps) {
+    std::vector<double> mags;
+    for (float v : cent) {
+        const double m = std::fabs(double(v));
+        if (m > 0.0 && std::find(mags.begin(), mags.end(), m) == mags.end()) mags.push_back(m);
+    }
+    double best = 1e300;
+    int best_i = 0;
+    for (int i = 0; i < steps; ++i) {
+        const double a = 1.0 + double(i) / steps;
+        double worst = 0.0;
+        for (double m : mags) {
+            worst = std::max(worst, f16_rel_err(a * m));
+            if (worst >= best) break;
+        }
+        if (worst < best) {
+            best = worst;
+            best_i = i;
+        }
+    }
+    return float(1.0 + double(best_i) / steps);
+}
+
 }  // namespace
 
-void build_decode_tables(const tq_codec& c, std::vector<uint32_t>& ktab, std::vector<uint32_t>& vtab) {
+void build_decode_tables(tq_codec& c, std::vector<uint32_t>& ktab, std::vector<uint32_t>& vtab) {
     ktab.clear();
     vtab.clear();
+    c.k_alpha = 1.0f;
+    c.v_alpha = 1.0f;
     if (c.bits == 16) return;
     const int L = 1 << c.bits;
-    std::vector<uint16_t> hi(L), lo(L);
+    const float alpha = table_alpha(c.centroids, c.bits <= 4 ? (1 << 18) : (1 << 12));
+    c.v_alpha = alpha;
+    c.k_alpha = c.bits <= 4 ? alpha : 1.0f;
+    std::vector<uint16_t> hk(L), lk(L), hv(L);
     for (int i = 0; i < L; ++i) {
-        hi[i] = f16_bits(c.centroids[i]);
-        lo[i] = f16_bits(c.centroids[i] - f16_val(hi[i]));
+        const float x = c.centroids[i];
+        hk[i] = f16_bits(c.k_alpha * x);
+        lk[i] = f16_bits(x - f16_val(hk[i]));  // used for 8-bit codes only (k_alpha = 1)
+        hv[i] = f16_bits(c.v_alpha * x);
     }
     if (c.bits <= 4) {
         for (int p = 0; p < L * L; ++p) {
             const int c0 = p & (L - 1), c1 = p >> c.bits;
-            ktab.push_back(uint32_t(hi[c0]) | (uint32_t(hi[c1]) << 16));
-            ktab.push_back(uint32_t(lo[c0]) | (uint32_t(lo[c1]) << 16));
-            vtab.push_back(uint32_t(hi[c0]) | (uint32_t(hi[c1]) << 16));
+            ktab.push_back(uint32_t(hk[c0]) | (uint32_t(hk[c1]) << 16));
+            vtab.push_back(uint32_t(hv[c0]) | (uint32_t(hv[c1]) << 16));
         }
     } else {
         for (int i = 0; i < L; ++i) {
-            ktab.push_back(uint32_t(hi[i]) | (uint32_t(lo[i]) << 16));
-            vtab.push_back(uint32_t(hi[i]) | (uint32_t(hi[i]) << 16));
+            ktab.push_back(uint32_t(hk[i]) | (uint32_t(lk[i]) << 16));
+            vtab.push_back(uint32_t(hv[i]) | (uint32_t(hv[i]) << 16));
         }
     }
 }
+
 
 namespace mma_detail {
 

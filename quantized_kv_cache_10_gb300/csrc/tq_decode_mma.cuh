@@ -194,10 +194,12 @@ constexpr Layout make_layout(int D, int KB, int VB) {
     L.nwc = nwc_for(KB);
     L.krows = (KB == 16) ? 0 : (KB <= 4) ? (1 << (2 * KB)) : 256;
     L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
-    L.ktab = L.krows * 256;   // 32 lanes x 8 B (pairs) or 32 x 4 B in a 256-B row
+    // 32 lanes x 4 B: 128-B rows for pair entries, 256-B rows for 8-bit codes
+    // (so the code byte becomes the row with one byte permute)
+    L.ktab = L.krows * ((KB <= 4) ? 128 : 256);
     L.vtab = L.vrows * 128;   // 32 lanes x 4 B
     // TMA landing area for the prologue: compact K / V tables, the query block, sign words
-    L.kw = (KB == 16) ? 0 : (KB <= 4) ? 2 * L.krows : L.krows;   // compact K table words
+    L.kw = L.krows;                                              // compact K table words
     L.vw = L.vrows;                                              // compact V table words
     L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
     // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
@@ -281,31 +283,15 @@ struct Cfg {
 // ---------------------------------------------------------------------------
 // Dequant: K role (pairs of neighbouring dims of one token)
 // ---------------------------------------------------------------------------
-// For k-tile kt of one token row whose chunk words are w: A registers for dims
-// base+0,1 (rlo) and base+2,3 (rhi), hi and lo parts.
+// For k-tile kt of one token row whose chunk words are w (2-4 bit codes): A
+// registers for dims base+0,1 (hi01) and base+2,3 (hi23) from the pair table
+// (index = 2*KB bits at bit 4*KB*kt and 4*KB*kt + 2*KB; rows of 128 B).
 template <int KB, int KCW>
 __device__ __forceinline__ void k_role(const uint32_t (&w)[KCW], int kt, uint32_t tab, uint32_t lane_off,
-                                       uint32_t& hi01, uint32_t& hi23, uint32_t& lo01, uint32_t& lo23) {
-    if constexpr (KB == 8) {
-        // four single-code lookups; row stride 256 B so the byte can be placed with one prmt
-        const uint32_t word = w[kt];
-        const uint32_t a0 = __byte_perm(word, lane_off, 0x5504);
-        const uint32_t a1 = __byte_perm(word, lane_off, 0x5514);
-        const uint32_t a2 = __byte_perm(word, lane_off, 0x5524);
-        const uint32_t a3 = __byte_perm(word, lane_off, 0x5534);
-        const uint32_t v0 = lds32(tab + a0), v1 = lds32(tab + a1), v2 = lds32(tab + a2), v3 = lds32(tab + a3);
-        hi01 = __byte_perm(v0, v1, 0x5410);
-        lo01 = __byte_perm(v0, v1, 0x7632);
-        hi23 = __byte_perm(v2, v3, 0x5410);
-        lo23 = __byte_perm(v2, v3, 0x7632);
-    } else {
-        // pair lookups: index = 2*KB bits at bit 4*KB*kt (and + 2*KB); rows of 256 B
-        const int s0 = 4 * KB * kt;
-        const uint32_t a0 = field_addr<KCW>(w, s0, 2 * KB, 8, lane_off);
-        const uint32_t a1 = field_addr<KCW>(w, s0 + 2 * KB, 2 * KB, 8, lane_off);
-        lds64(tab + a0, hi01, lo01);
-        lds64(tab + a1, hi23, lo23);
-    }
+                                       uint32_t& hi01, uint32_t& hi23) {
+    const int s0 = 4 * KB * kt;
+    hi01 = lds32(tab + field_addr<KCW>(w, s0, 2 * KB, 7, lane_off));
+    hi23 = lds32(tab + field_addr<KCW>(w, s0 + 2 * KB, 2 * KB, 7, lane_off));
 }
 
 // ---------------------------------------------------------------------------
@@ -442,7 +428,7 @@ __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst,
 template <typename C>
 __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const uint32_t* vcompact, uint8_t* ktab_s,
                                                  uint8_t* vtab_s, int ctid) {
-    replicate_one<C, C::KROWS, C::KPAIR ? 2 : 1, 256>(kcompact, ktab_s, ctid);
+    if constexpr (C::KROWS > 0) replicate_one<C, C::KROWS, 1, C::KPAIR ? 128 : 256>(kcompact, ktab_s, ctid);
     replicate_one<C, C::VROWS, 1, 128>(vcompact, vtab_s, ctid);
 }
 
@@ -485,7 +471,7 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
                 }
                 __syncwarp();
             }
-            const float f = kLog2e * a.scale / static_cast<float>(D);
+            const float f = kLog2e * a.scale / (static_cast<float>(D) * a.ck.k_alpha);
 #pragma unroll
             for (int k = 0; k < D / 32; ++k) dst[lane + 32 * k] *= f;
         }
@@ -514,7 +500,7 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(NWC * 32) : "memory");
-        const float f = kLog2e * a.scale * rsqrtf(static_cast<float>(D));
+        const float f = kLog2e * a.scale * rsqrtf(static_cast<float>(D)) / a.ck.k_alpha;
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
             const int j = ctid + NTH * c;
@@ -717,7 +703,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             l_run[j] = 0.0f;
         }
         const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
-        const uint32_t koff = C::KPAIR ? uint32_t(lane * 8) : uint32_t(lane * 4);
+        const uint32_t koff = uint32_t(lane * 4);
         const uint32_t lane4 = uint32_t(lane * 4);
 
         // ------------------------------------------------------------ main loop
@@ -790,14 +776,13 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                     } else {
 #pragma unroll
                         for (int kt = 0; kt < C::KTS; ++kt) {
-                            uint32_t ah01, ah23, al01, al23, bh01, bh23, bl01, bl23;
-                            k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23, al01, al23);
-                            k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23, bl01, bl23);
+                            uint32_t ah01, ah23, bh01, bh23;
+                            k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23);
+                            k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23);
                             // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
                             uint32_t q00, q01, q10 = 0u, q11 = 0u;
                             q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
                             mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
-                            mma16816(sc[mt][0], al01, bl01, al23, bl23, q00, q01);
                             if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
                         }
                     }
@@ -955,7 +940,8 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             const int q = (NT == 2) ? 2 * t + j : t;
             float M = -CUDART_INF_F;
             for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
-            f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M);
+            // the V table holds v_alpha * c: divide it out here, once per output
+            f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M) / a.cv.v_alpha;
         }
         float* slice = reinterpret_cast<float*>(ring) + warp * kGP * D;
 #pragma unroll

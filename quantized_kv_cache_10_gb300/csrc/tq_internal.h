@@ -38,6 +38,8 @@ struct tq_codec {
     uint32_t* d_vtab = nullptr;
     int ktab_words = 0;
     int vtab_words = 0;
+    float k_alpha = 1.0f;   // d_ktab holds fp16(k_alpha * c): the kernel scales q' by 1 / k_alpha
+    float v_alpha = 1.0f;   // d_vtab holds fp16(v_alpha * c): the kernel scales its output by 1 / v_alpha
 };
 
 namespace tq {
@@ -87,11 +89,12 @@ struct DevCodec {
     const float* qt;   // Q^T row-major (dense)
     const uint32_t* ktab;
     const uint32_t* vtab;
+    float k_alpha, v_alpha;
 };
 
 inline DevCodec dev_view(const tq_codec* c) {
-    return DevCodec{c->dim,        c->bits,          c->is_wht, c->bytes_per_vec, c->d_centroids,
-                    c->d_sign_bits, c->d_q,          c->d_qt,   c->d_ktab,        c->d_vtab};
+    return DevCodec{c->dim, c->bits, c->is_wht, c->bytes_per_vec, c->d_centroids, c->d_sign_bits, c->d_q,
+                    c->d_qt, c->d_ktab, c->d_vtab, c->k_alpha, c->v_alpha};
 }
 
 struct DecodeArgs {
