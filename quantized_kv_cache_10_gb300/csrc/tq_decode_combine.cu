@@ -70,7 +70,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
-    // wait for the decode grid (and the visibility of its records)
+    // let the next decode kernel on the stream start its table set-up, then
+    // wait for this call's decode grid (and the visibility of its records)
+    allow_dependent_launch();
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int pair = blockIdx.x;

@@ -543,7 +543,8 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
     uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE <= 8]
     uint64_t* empty = full + 8;                                          // [NSTAGE <= 8]
-    uint64_t* setup = full + 16;                                         // prologue copies
+    uint64_t* setup = full + 16;                                         // codec tables, sign words
+    uint64_t* setup_q = full + 17;                                       // the query block
     float* wm = reinterpret_cast<float*>(misc + 256);                    // [C::NWC][kGP]
     float* wl = wm + C::NWC * kGP;                                         // [C::NWC][kGP]
     int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
@@ -559,11 +560,16 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
     const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
     const int G = p.G;
     const int h0 = kvh * G;
-    const int64_t len = clamped_len(a, b);
-    const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
-    const int64_t t1 = min(len, t0 + p.chunk);
-    const int ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
     const int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
+    const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
+    // This kernel is launched with programmatic stream serialization: it may
+    // start while the previous kernel on the stream (e.g. the combine of the
+    // previous call, which reads this workspace) still runs.  Until
+    // griddepcontrol.wait it touches only the codec's tables and sign words,
+    // which no kernel writes; q, the cache, the lengths and the workspace come
+    // after the wait.
+    int64_t t1 = t0;
+    int ntiles = 0;
 
     if (tid == 0) {
         for (int s = 0; s < C::NSTAGE; ++s) {
@@ -571,6 +577,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             mbar_init(empty + s, C::NWC);
         }
         mbar_init(setup, 1);
+        mbar_init(setup_q, 1);
         *s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -585,12 +592,16 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             // sign words: K codec's at PRO_S, V codec's at PRO_S + 64 (<= 64 B each, D <= 512)
             const uint32_t sbytes = (a.ck.is_wht && !C::KRAW) ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
             const uint32_t vsbytes = a.cv.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
-            mbar_arrive_expect_tx(setup, C::KW * 4 + C::VW * 4 + qbytes + sbytes + vsbytes);
+            mbar_arrive_expect_tx(setup, C::KW * 4 + C::VW * 4 + sbytes + vsbytes);
             if constexpr (C::KW > 0) bulk_g2s(pro + C::PRO_K, a.ck.ktab, C::KW * 4, setup);
             bulk_g2s(pro + C::PRO_V, a.cv.vtab, C::VW * 4, setup);
-            bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup);
             if (sbytes) bulk_g2s(pro + C::PRO_S, a.ck.sign_bits, sbytes, setup);
             if (vsbytes) bulk_g2s(pro + C::PRO_S + 64, a.cv.sign_bits, vsbytes, setup);
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            t1 = min(clamped_len(a, b), t0 + p.chunk);
+            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+            mbar_arrive_expect_tx(setup_q, qbytes);
+            bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup_q);
             const uint8_t* kg = static_cast<const uint8_t*>(a.k);
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it % C::NSTAGE;
@@ -628,14 +639,17 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
         {
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
-            if (!__all_sync(kFullMask, mbar_wait(setup, 0))) {
-                if (lane == 0) {
-                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
-                    *s_abort = 1;
-                }
-            }
+            bool ok = __all_sync(kFullMask, mbar_wait(setup, 0));
             replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
                                 reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            t1 = min(clamped_len(a, b), t0 + p.chunk);
+            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+            ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
+            if (!ok && lane == 0) {
+                atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                *s_abort = 1;
+            }
             rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
                               reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp, lane, ctid);
         }
@@ -1024,9 +1038,17 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
         const cudaError_t e = encode_raw_k_map(&kmap, a.k, D, static_cast<int64_t>(a.B) * a.Hkv * a.max_seq, C::TS);
         if (e != cudaSuccess) return e;
     }
-    dim3 grid(p.n_split, p.n_units);
-    decode_mma_kernel<D, KB, VB, NT><<<grid, C::NTHREADS, C::SMEM, st>>>(a, p, kmap);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.n_split, p.n_units);
+    cfg.blockDim = dim3(C::NTHREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT>, a, p, kmap);
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
