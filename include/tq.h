@@ -56,6 +56,8 @@ typedef enum {
 #define TQ_DEVERR_SEQ_LEN   1   /* seq_lens[b] < 0 or > max_seq: clamped */
 #define TQ_DEVERR_POSITION  2   /* encode_append position outside [0, max_seq): row skipped */
 #define TQ_DEVERR_TIMEOUT   4   /* a bounded wait inside a kernel gave up; its outputs are invalid */
+#define TQ_DEVERR_LAYOUT    8   /* the GPU's shared-memory window does not match the layout the
+                                   decode kernel was built for; its outputs are invalid */
 
 typedef struct tq_codec tq_codec;   /* opaque; immutable after creation */
 

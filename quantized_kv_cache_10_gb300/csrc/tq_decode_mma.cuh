@@ -187,9 +187,62 @@ constexpr int stage_bytes(int D, int KB, int VB, int ts) {
 // function serves the kernel (constexpr) and the host's support test.
 struct Layout {
     int nwc, krows, vrows, ktab, vtab, kw, vw, pro, bqb, fixed, mt, ts, stage, nstage, smem;
+    // 8-bit K ("table block"): both lookup tables share one 64 KB block at the
+    // fixed shared address kTBlock -- K in the first 128 B of each 256-B row, V
+    // in the second -- so that a byte permute forms a whole K address and one
+    // mask-or a whole V address.  The small regions and `g` stages sit below
+    // the block, the other `na` stages above it.
+    bool tblock;
+    int small, g, na;
 };
 
+// Shared address where the dynamic shared memory starts on this GPU (the
+// first 1 KB of a CTA's window is reserved by the system); the table-block
+// layout is sized for it and every kernel checks it at run time.
+constexpr int kSmemBase = 1024;
+constexpr int kTBlock = 65536;
+
+constexpr Layout make_layout(int D, int KB, int VB);
+
+constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
+    Layout L{};
+    L.tblock = true;
+    L.nwc = nwc_for(KB);
+    L.krows = 256;
+    L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
+    L.ktab = 0;
+    L.vtab = 0;
+    L.kw = L.krows;
+    L.vw = L.vrows;
+    L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
+    L.bqb = (D > 128) ? (D / 8) * 2 * 256 : 0;
+    L.small = kGP * D * 4 + 1024 + L.pro + L.bqb;
+    L.fixed = L.small;
+    L.mt = mt;
+    L.ts = L.nwc * 16 * mt;
+    L.stage = stage_bytes(D, KB, VB, L.ts);
+    const int below = kTBlock - kSmemBase - L.small;
+    L.g = below > 0 ? below / L.stage : 0;
+    L.na = (kSmemBase + kSmemLimit - 2 * kTBlock) / L.stage;
+    if (L.g > 4) L.g = 4;
+    if (L.g + L.na > 4) L.na = 4 - L.g;
+    // the warp merge uses the stages above the block as one contiguous area
+    while (L.na * L.stage < L.nwc * kGP * D * 4 && L.g > 0 && L.na < (kSmemBase + kSmemLimit - 2 * kTBlock) / L.stage) {
+        --L.g;
+        ++L.na;
+    }
+    L.nstage = (L.na * L.stage >= L.nwc * kGP * D * 4) ? L.g + L.na : 0;
+    L.smem = 2 * kTBlock + L.na * L.stage - kSmemBase;
+    return L;
+}
+
 constexpr Layout make_layout(int D, int KB, int VB) {
+    if (KB == 8) {
+        // the table block, when it holds at least as many stages as the linear layout would
+        const Layout t2 = make_tblock_layout(D, KB, VB, 2), t1 = make_tblock_layout(D, KB, VB, 1);
+        const Layout t = (D <= 128 && t2.nstage >= 3) ? t2 : t1;
+        if (t.nstage >= 3) return t;
+    }
     Layout L{};
     L.nwc = nwc_for(KB);
     L.krows = (KB == 16) ? 0 : (KB <= 4) ? (1 << (2 * KB)) : 256;
@@ -216,6 +269,10 @@ constexpr Layout make_layout(int D, int KB, int VB) {
     const int ns = (kSmemLimit - L.fixed) / L.stage;
     L.nstage = ns > cap ? cap : ns;
     L.smem = L.fixed + L.nstage * L.stage;
+    L.tblock = false;
+    L.small = 0;
+    L.g = 0;
+    L.na = L.nstage;
     return L;
 }
 
@@ -273,11 +330,13 @@ struct Cfg {
     static constexpr int FIXED = L.fixed;
     static constexpr int NSTAGE = L.nstage;
     static constexpr int SMEM = L.smem;
+    static constexpr bool TBLOCK = L.tblock;
+    static constexpr int SMALL = L.small, G_BELOW = L.g, N_ABOVE = L.na;
     static_assert(STAGE >= KBUF + VBUF + 2 * NBUF, "stage size");
     static_assert(NSTAGE >= 2 && NSTAGE <= 8, "stage count");
     static_assert(!KRAW || D % 64 == 0, "raw K needs 64-column blocks");
     // epilogue scratch (per-warp O slices, combine weights) lives in the stage ring
-    static_assert(NSTAGE * STAGE >= NWC * kGP * D * 4, "stage ring too small for the warp merge");
+    static_assert(N_ABOVE * STAGE >= NWC * kGP * D * 4, "stage ring too small for the warp merge");
 };
 
 // ---------------------------------------------------------------------------
@@ -297,20 +356,23 @@ __device__ __forceinline__ void k_role(const uint32_t (&w)[KCW], int kt, uint32_
 // ---------------------------------------------------------------------------
 // Dequant: V role (one dim of two tokens a, b)
 // ---------------------------------------------------------------------------
-template <int VB, int VCW>
+// TB: table-block layout (256-B rows, lane4 already holds the table address
+// bits and the lane offset, so an address is one shift and one or).
+template <int VB, int VCW, bool TB>
 __device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint32_t (&wb)[VCW], int j,
                                            uint32_t tab, uint32_t lane4) {
     const int s = VB * j;
     const uint32_t m = (1u << VB) - 1u;
+    constexpr int RS = TB ? 8 : 7;
     if constexpr (VB <= 4) {
         const uint32_t ca = bits_at<VCW>(wa, s) & m;
         const uint32_t cb = bits_at<VCW>(wb, s) & m;
-        return lds32(tab + (((ca | (cb << VB)) << 7) | lane4));
+        return lds32((TB ? 0u : tab) + (((ca | (cb << VB)) << RS) | lane4));
     } else {
         const uint32_t ca = bits_at<VCW>(wa, s) & m;
         const uint32_t cb = bits_at<VCW>(wb, s) & m;
-        const uint32_t va = lds32(tab + ((ca << 7) | lane4));
-        const uint32_t vb = lds32(tab + ((cb << 7) | lane4));
+        const uint32_t va = lds32((TB ? 0u : tab) + ((ca << RS) | lane4));
+        const uint32_t vb = lds32((TB ? 0u : tab) + ((cb << RS) | lane4));
         return __byte_perm(va, vb, 0x7610);
     }
 }
@@ -319,7 +381,7 @@ __device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint
 // 64-bit values) are interleaved once into z_even / z_odd whose field i
 // (2*VB bits) is code_a | code_b << VB of dim 2i / 2i+1; each pair is then one
 // shift and one mask.
-template <int VB>
+template <int VB, bool TB>
 struct VPairs {
     static constexpr uint64_t even_mask() {
         uint64_t m = 0;
@@ -333,11 +395,14 @@ struct VPairs {
         zo = ((a >> VB) & me) | (b & ~me);
     }
     // shared-memory address of the pair-table slot for dim j (0..15) of the chunk
+    // (TB: 256-B rows and lane4 carrying the table address, so no add)
     __device__ __forceinline__ uint32_t addr(int j, uint32_t tab, uint32_t lane4) const {
+        constexpr int RS = TB ? 8 : 7;
         const uint64_t z = (j & 1) ? zo : ze;
         const int s = VB * (j & ~1);
-        const uint32_t x = (s >= 7) ? static_cast<uint32_t>(z >> (s - 7)) : static_cast<uint32_t>(z << (7 - s));
-        return tab + ((x & (((1u << (2 * VB)) - 1u) << 7)) | lane4);
+        const uint32_t x = (s >= RS) ? static_cast<uint32_t>(z >> (s - RS)) : static_cast<uint32_t>(z << (RS - s));
+        const uint32_t f = (x & (((1u << (2 * VB)) - 1u) << RS)) | lane4;
+        return TB ? f : tab + f;
     }
 };
 
@@ -429,7 +494,7 @@ template <typename C>
 __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const uint32_t* vcompact, uint8_t* ktab_s,
                                                  uint8_t* vtab_s, int ctid) {
     if constexpr (C::KROWS > 0) replicate_one<C, C::KROWS, 1, C::KPAIR ? 128 : 256>(kcompact, ktab_s, ctid);
-    replicate_one<C, C::VROWS, 1, 128>(vcompact, vtab_s, ctid);
+    replicate_one<C, C::VROWS, 1, C::TBLOCK ? 256 : 128>(vcompact, vtab_s, ctid);
 }
 
 // q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
@@ -537,9 +602,11 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* ktab_s = smem;
-    uint8_t* vtab_s = ktab_s + C::KTAB;
-    float* qs = reinterpret_cast<float*>(vtab_s + C::VTAB);              // [kGP][D]
+    const uint32_t sbase = smem_addr(smem);
+    // table block (8-bit K): the tables at shared address kTBlock, the rest around them
+    uint8_t* ktab_s = C::TBLOCK ? smem + (static_cast<uint32_t>(kTBlock) - sbase) : smem;
+    uint8_t* vtab_s = C::TBLOCK ? ktab_s + 128 : ktab_s + C::KTAB;
+    float* qs = reinterpret_cast<float*>(C::TBLOCK ? smem : vtab_s + C::VTAB);  // [kGP][D]
     uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE <= 8]
     uint64_t* empty = full + 8;                                          // [NSTAGE <= 8]
@@ -550,9 +617,22 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
     int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
     uint8_t* bq_s = pro + C::PRO;                                    // q' fragments (D > 128)
-    uint8_t* ring = bq_s + C::BQB;
+    uint8_t* below = bq_s + C::BQB;                                      // stages 0 .. G_BELOW-1
     if constexpr (C::KRAW)  // the swizzled K blocks need 1024-byte aligned shared addresses
-        ring += (1024u - (smem_addr(ring) & 1023u)) & 1023u;
+        below += (1024u - (smem_addr(below) & 1023u)) & 1023u;
+    // stages G_BELOW .. NSTAGE-1, contiguous (also the warp-merge area)
+    uint8_t* ring = C::TBLOCK ? smem + (static_cast<uint32_t>(2 * kTBlock) - sbase) : below;
+    auto stage_ptr = [&](int s) -> uint8_t* {
+        return (C::TBLOCK && s < C::G_BELOW) ? below + s * C::STAGE : ring + (s - C::G_BELOW) * C::STAGE;
+    };
+    if constexpr (C::TBLOCK) {
+        // the layout was sized for the dynamic shared memory starting at kSmemBase
+        if (sbase + C::SMALL + C::G_BELOW * C::STAGE > static_cast<uint32_t>(kTBlock) ||
+            static_cast<uint32_t>(2 * kTBlock + C::N_ABOVE * C::STAGE) > sbase + C::SMEM) {
+            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_LAYOUT);
+            return;
+        }
+    }
 
     allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -613,7 +693,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                 const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
                 const int64_t nv = min(static_cast<int64_t>(C::TS), t1 - ts);
                 const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
-                uint8_t* st = ring + s * C::STAGE;
+                uint8_t* st = stage_ptr(s);
                 const uint32_t vbytes = n8 * C::BPV, nbytes = n8 * 2;
                 if constexpr (C::KRAW) {
                     // whole boxes of TS rows per 64-column block (rows past the tensor read as zero)
@@ -717,8 +797,10 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             l_run[j] = 0.0f;
         }
         const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
-        const uint32_t koff = uint32_t(lane * 4);
-        const uint32_t lane4 = uint32_t(lane * 4);
+        // table block: the table address bits ride in the lane offsets (kTBlock is
+        // 64 KB aligned, the V half of a row starts at +128)
+        const uint32_t koff = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) : 0u);
+        const uint32_t lane4 = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) + 128u : 0u);
 
         // ------------------------------------------------------------ main loop
         for (int it = 0; it < ntiles; ++it) {
@@ -732,7 +814,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                 }
                 break;
             }
-            const uint8_t* st = ring + s * C::STAGE;
+            const uint8_t* st = stage_ptr(s);
             const uint8_t* kbuf = st;
             const uint8_t* vbuf = st + C::KBUF;
             const __half* knrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF);
@@ -776,12 +858,15 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                         for (int kt = 0; kt < C::KTS; ++kt) {
                             // bytes 2(kt&1), 2(kt&1)+1 of word kt/2 are dims d0, d1 of this k-tile
                             const uint32_t wA = wa[kt >> 1], wB = wb[kt >> 1];
-                            const uint32_t sel0 = 0x5504u + ((2u * (kt & 1)) << 4);
+                            // address = [koff byte 3][koff byte 2 / 0][code][koff byte 0]: with the
+                            // table block the permute alone forms it, else it is added to ktab_a
+                            const uint32_t sel0 = (C::TBLOCK ? 0x7604u : 0x5504u) + ((2u * (kt & 1)) << 4);
                             const uint32_t sel1 = sel0 + 0x10u;
-                            const uint32_t r0v = lds32(ktab_a + __byte_perm(wA, koff, sel0));
-                            const uint32_t r1v = lds32(ktab_a + __byte_perm(wB, koff, sel0));
-                            const uint32_t r2v = lds32(ktab_a + __byte_perm(wA, koff, sel1));
-                            const uint32_t r3v = lds32(ktab_a + __byte_perm(wB, koff, sel1));
+                            const uint32_t kb = C::TBLOCK ? 0u : ktab_a;
+                            const uint32_t r0v = lds32(kb + __byte_perm(wA, koff, sel0));
+                            const uint32_t r1v = lds32(kb + __byte_perm(wB, koff, sel0));
+                            const uint32_t r2v = lds32(kb + __byte_perm(wA, koff, sel1));
+                            const uint32_t r3v = lds32(kb + __byte_perm(wB, koff, sel1));
                             uint32_t q00, q01, q10 = 0u, q11 = 0u;
                             q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
                             mma16816(sc[mt][0], r0v, r1v, r2v, r3v, q00, q01);
@@ -889,9 +974,9 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
 #pragma unroll
                         for (int sub = 0; sub < NSUB; ++sub) {
                             const int vbit = g * C::VCB + 16 * VB * sub;
-                            const VPairs<VB> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
+                            const VPairs<VB, C::TBLOCK> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
                                                  load_bits64(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
-                            const VPairs<VB> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
+                            const VPairs<VB, C::TBLOCK> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
                                                  load_bits64(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
                             constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
 #pragma unroll
@@ -915,10 +1000,10 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                         load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
 #pragma unroll
                         for (int dm = 0; dm < C::KT; ++dm) {
-                            const uint32_t a0 = v_role<VB, C::VCW>(v0, v1, 2 * dm, vtab_a, lane4);
-                            const uint32_t a1 = v_role<VB, C::VCW>(v0, v1, 2 * dm + 1, vtab_a, lane4);
-                            const uint32_t a2 = v_role<VB, C::VCW>(v2, v3, 2 * dm, vtab_a, lane4);
-                            const uint32_t a3 = v_role<VB, C::VCW>(v2, v3, 2 * dm + 1, vtab_a, lane4);
+                            const uint32_t a0 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm, vtab_a, lane4);
+                            const uint32_t a1 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm + 1, vtab_a, lane4);
+                            const uint32_t a2 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm, vtab_a, lane4);
+                            const uint32_t a3 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm + 1, vtab_a, lane4);
                             mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
                         }
                     }
