@@ -70,11 +70,14 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the V codec's sign word of this lane's dims (codec data, written by no kernel)
+    uint32_t sw = 0;
+    if ((VPL & (VPL - 1)) == 0 && a.cv.is_wht) sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
     // let the next decode kernel on the stream start its table set-up, then
     // wait for this call's decode grid (and the visibility of its records)
     allow_dependent_launch();
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int pair = blockIdx.x;
     const int u = pair / p.G, hl = pair - (pair / p.G) * p.G;  // unit, head within its group
     const int qc = hl / kGP, g = hl - qc * kGP;
@@ -154,7 +157,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
                 }
             }
             const float f = 1.0f / static_cast<float>(D);
-            const uint32_t sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
             const int sb = (lane * VPL) & 31;
 #pragma unroll
             for (int v = 0; v < VPL; ++v) {

@@ -100,6 +100,19 @@ __device__ __forceinline__ void tma_g2s_2d(void* dst, const CUtensorMap* map, in
         : "memory");
 }
 
+// L2 prefetch of a byte range (16-byte aligned, size a multiple of 16); a hint
+// with no effect on what any load returns.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_l2_2d(const CUtensorMap* map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 __device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -677,11 +690,36 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             bulk_g2s(pro + C::PRO_V, a.cv.vtab, C::VW * 4, setup);
             if (sbytes) bulk_g2s(pro + C::PRO_S, a.ck.sign_bits, sbytes, setup);
             if (vsbytes) bulk_g2s(pro + C::PRO_S + 64, a.cv.sign_bits, vsbytes, setup);
+            {
+                // While the previous kernel finishes, pull the first NSTAGE tiles of this
+                // split (by max_seq: the lengths are not read yet) into L2.  A prefetch
+                // changes no value any load returns, so it may precede the wait; the
+                // copies into shared memory come after it.
+                const int64_t pf_end = min(min(t0 + p.chunk, a.max_seq), t0 + static_cast<int64_t>(C::NSTAGE) * C::TS);
+                if (pf_end > t0) {
+                    const uint32_t ntok = static_cast<uint32_t>(pf_end - t0);  // a multiple of 8
+                    if constexpr (C::KRAW) {
+                        for (int it = 0; it * C::TS < static_cast<int>(ntok); ++it)
+#pragma unroll
+                            for (int cb = 0; cb < D / 64; ++cb)
+                                prefetch_l2_2d(&kmap, 64 * cb, static_cast<int>(row0 + t0 + it * C::TS));
+                    } else {
+                        prefetch_l2(static_cast<const uint8_t*>(a.k) + (row0 + t0) * C::BPK, ntok * C::BPK);
+                        prefetch_l2(a.k_norms + row0 + t0, ntok * 2);
+                    }
+                    prefetch_l2(a.v_codes + (row0 + t0) * C::BPV, ntok * C::BPV);
+                    prefetch_l2(a.v_norms + row0 + t0, ntok * 2);
+                }
+                // the query block and the 16-byte granule holding seq_lens[b] (allocations
+                // are 256-byte aligned, so the granule lies inside the caller's buffer)
+                prefetch_l2(a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes);
+                prefetch_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(a.seq_lens + b) & ~uintptr_t(15)), 16);
+            }
             asm volatile("griddepcontrol.wait;" ::: "memory");
-            t1 = min(clamped_len(a, b), t0 + p.chunk);
-            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
             mbar_arrive_expect_tx(setup_q, qbytes);
             bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup_q);
+            t1 = min(clamped_len(a, b), t0 + p.chunk);
+            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
             const uint8_t* kg = static_cast<const uint8_t*>(a.k);
             for (int it = 0; it < ntiles; ++it) {
                 const int s = it % C::NSTAGE;
