@@ -184,10 +184,14 @@ constexpr int al16(int x) { return (x + 15) / 16 * 16; }
 constexpr int al128(int x) { return (x + 127) / 128 * 128; }
 constexpr int al1024(int x) { return (x + 1023) / 1024 * 1024; }
 
-// Consumer warps per CTA (+ one TMA producer warp).  Coded K: 11, three warps
-// per SM sub-partition at a 168-register budget.  Raw fp16 K: 4, whose stages
-// are 4x larger per token, so that four stages of 64 tokens fit.
-constexpr int nwc_for(int KB) { return KB == 16 ? 4 : 11; }
+// Consumer warps per CTA (+ one TMA producer warp), measured per kind:
+//   raw fp16 K: 4, whose stages are 4x larger per token, so that four stages
+//     of 64 tokens fit;
+//   8-bit K, d <= 128: 8 with two m-tiles per warp per stage (more independent
+//     work per warp beats more warps here: 18.7 vs 19.9 us on the 32K workload);
+//   other coded K: 11 with one m-tile, three warps per SM sub-partition at the
+//     168-register budget.
+constexpr int nwc_for(int D, int KB) { return KB == 16 ? 4 : (KB == 8 && D <= 128) ? 8 : 11; }
 
 // Bytes of one stage of ts tokens: K codes (raw K: D/64 swizzled column blocks
 // of ts rows x 128 B, each 1024-byte aligned), V codes, K norms, V norms.
@@ -220,7 +224,7 @@ constexpr Layout make_layout(int D, int KB, int VB);
 constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
     Layout L{};
     L.tblock = true;
-    L.nwc = nwc_for(KB);
+    L.nwc = nwc_for(D, KB);
     L.krows = 256;
     L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
     L.ktab = 0;
@@ -257,7 +261,7 @@ constexpr Layout make_layout(int D, int KB, int VB) {
         if (t.nstage >= 3) return t;
     }
     Layout L{};
-    L.nwc = nwc_for(KB);
+    L.nwc = nwc_for(D, KB);
     L.krows = (KB == 16) ? 0 : (KB <= 4) ? (1 << (2 * KB)) : 256;
     L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
     // 32 lanes x 4 B: 128-B rows for pair entries, 256-B rows for 8-bit codes
