@@ -9,9 +9,9 @@
 //   other dims: z_j = fp64 fma chain of Q[j][i] k_i over ascending i,
 //   code_j = #{ i : z_j > RN64(m_i * RN64(D / RN64(sqrt(d)))) };
 //   codes packed LSB-first into 32-bit words.
-// One warp per vector: lane l owns elements [l*E, (l+1)*E), E = d / 32.  The
-// 2^b - 1 thresholds of a vector are computed once per warp (spread over its
-// lanes) into shared memory and each coordinate finds its code by a b-step
+// One warp per vector at a time: lane l owns elements [l*E, (l+1)*E), E = d / 32.
+// The 2^b - 1 thresholds of a vector are computed once per warp (spread over
+// its lanes) into shared memory and each coordinate finds its code by a b-step
 // binary search over them ("number of boundaries exceeded").
 #include <cuda_fp16.h>
 #include <math_constants.h>
@@ -64,6 +64,32 @@ __device__ __forceinline__ double u128_to_f64_rn(uint64_t hi, uint64_t lo) {
     }
     top |= (rest != 0) ? 1ull : 0ull;  // sticky bit below the rounding position
     return ldexp(__ull2double_rn(top), 64 - nz);
+}
+
+// Exact 128-bit sum of squares of the warp's values (hi:lo on all lanes).
+template <int E>
+__device__ __forceinline__ void warp_sumsq(const int64_t (&k)[E], int E_rt, uint64_t& hi_out, uint64_t& lo_out) {
+    uint64_t lo = 0, hi = 0;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        if (e < E_rt) {
+            const uint64_t a = static_cast<uint64_t>(k[e] < 0 ? -k[e] : k[e]);
+            const uint64_t plo = a * a, phi = __umul64hi(a, a);
+            const uint64_t nlo = lo + plo;
+            hi += phi + (nlo < lo ? 1ull : 0ull);
+            lo = nlo;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const uint64_t olo = __shfl_xor_sync(kFull, lo, off);
+        const uint64_t ohi = __shfl_xor_sync(kFull, hi, off);
+        const uint64_t nlo = lo + olo;
+        hi += ohi + (nlo < lo ? 1ull : 0ull);
+        lo = nlo;
+    }
+    hi_out = hi;
+    lo_out = lo;
 }
 
 // Exact sum of squares of the warp's values, returned as RN64 on all lanes.
@@ -156,16 +182,54 @@ __device__ __forceinline__ void pack_store(const int (&code)[E], int E_rt, int l
 }
 
 constexpr int kWarps = 8;
+constexpr float kNearTie = 2e-6f;  // relative margin of the fp32 boundary test (see below)
+
+// |w| rounded to fp32 from its two 32-bit halves (relative error <= 2^-23).
+__device__ __forceinline__ float abs_to_f32(int64_t w) {
+    const uint64_t a = static_cast<uint64_t>(w < 0 ? -w : w);
+    return fmaf(static_cast<float>(static_cast<uint32_t>(a >> 32)), 4294967296.0f,
+                static_cast<float>(static_cast<uint32_t>(a)));
+}
+
+// Exact code of an integer coordinate: #{ i : w > RN64(m_i * D) }, by a
+// binary search with the thresholds computed in fp64 on the fly.
+__device__ __noinline__ int exact_code(int64_t w, double D, const double* mid, int L) {
+    int pos = 0;
+    for (int s = L >> 1; s > 0; s >>= 1)
+        if (__double2ll_rd(__dmul_rn(__ldg(mid + pos + s - 1), D)) < w) pos += s;
+    return pos;
+}
 
 // Power-of-two dims: E = dim / 32 in {1, 2, 4, 8, 16}.
+//
+// A warp takes 32 vectors at a time.  Pass 1 forms each vector's exact 128-bit
+// sum of squares (all lanes), lane j keeping vector j's; the fp64 work of the
+// norm (rounding S, the square root, the fp16 norm) then runs once for all 32
+// vectors, one per lane -- the GPU's fp64 rate is a small fraction of its
+// fp32 and integer rates.  For 2-4 bit codes the 2^b - 1 exact integer
+// thresholds floor(RN64(m_i D)) (w > RN64(m_i D) <=> w > floor(...), w an
+// integer) of the 32 vectors are formed in the same lane-parallel step.  Pass
+// 2 re-reads each vector, applies the exact int64 butterfly and finds each
+// code by a binary search: over those integer thresholds for 2-4 bits; for 8
+// bits (255 thresholds per vector) over fp32 thresholds m_i * D, a coordinate
+// within 2e-6 (relative) of its fp32 boundaries -- further than the fp32
+// rounding of w, m_i, D and the product can move it -- being decided exactly
+// instead (exact_code).  Outside that margin the fp32 comparison agrees with
+// w > RN64(m_i D), so the codes are bit-exact either way.
 template <int E>
 __global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams p) {
-    __shared__ int64_t s_thr[kWarps][256];
+    __shared__ float s_thr[kWarps][256];         // 8-bit codes: fp32 thresholds of one vector
+    __shared__ int64_t s_ithr[kWarps][32 * 15];  // 2-4 bit codes: integer thresholds of 32 vectors
     __shared__ uint32_t s_pack[kWarps][128];
+    __shared__ float s_mid[256];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int L = 1 << p.bits;
-    int64_t* thr = s_thr[warp];
+    for (int i = threadIdx.x; i < L - 1; i += blockDim.x) s_mid[i] = __double2float_rn(__ldg(p.mid + i));
+    __syncthreads();
+    float* thr = s_thr[warp];
+    int64_t* ithr = s_ithr[warp];
     uint32_t* pk = s_pack[warp];
+    const bool small_book = p.bits <= 4;
     // signs of this lane's elements as a bit mask
     uint32_t smask = 0;
 #pragma unroll
@@ -174,58 +238,120 @@ __global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams
         smask |= ((__ldg(p.sign_bits + (j >> 5)) >> (j & 31)) & 1u) << e;
     }
     const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kWarps + warp; v < total;
-         v += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const uint16_t* src;
-        int64_t dst;
-        if (!map_row(p, v, src, dst)) {
-            if (lane == 0 && p.dev_error) atomicOr(p.dev_error, TQ_DEVERR_POSITION);
-            continue;
+    const int64_t nbatch = (total + 31) / 32;
+    for (int64_t bt = static_cast<int64_t>(blockIdx.x) * kWarps + warp; bt < nbatch;
+         bt += static_cast<int64_t>(gridDim.x) * kWarps) {
+        const int64_t v0 = bt * 32;
+        const int nb = static_cast<int>(min(static_cast<int64_t>(32), total - v0));
+        // ---- pass 1: exact sums of squares; lane j keeps vector j's
+        uint64_t my_hi = 0, my_lo = 0;
+        for (int jv = 0; jv < nb; ++jv) {
+            const uint16_t* src;
+            int64_t dst;
+            if (!map_row(p, v0 + jv, src, dst)) continue;
+            uint32_t hv[E];
+            load_row<E>(src, lane, E, hv);
+            int64_t k[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) k[e] = f16_exact(hv[e]);
+            uint64_t hi, lo;
+            warp_sumsq<E>(k, E, hi, lo);
+            if (lane == jv) {
+                my_hi = hi;
+                my_lo = lo;
+            }
         }
-        uint32_t hv[E];
-        load_row<E>(src, lane, E, hv);
-        int64_t k[E];
+        // ---- fp64 per vector, one vector per lane: D = RN64(sqrt(RN64(S))), the norm
+        double myD = 0.0;
+        float myDf = 0.0f;
+        int64_t mydst = -1;
+        if (lane < nb) {
+            const uint16_t* src;
+            if (map_row(p, v0 + lane, src, mydst)) {
+                myD = __dsqrt_rn(u128_to_f64_rn(my_hi, my_lo));
+                myDf = __double2float_rn(myD);
+                p.norms[mydst] = __half_as_ushort(__double2half(ldexp(myD, -24)));
+                if (small_book)
+                    for (int i = 0; i < L - 1; ++i) ithr[lane * 15 + i] = __double2ll_rd(__dmul_rn(__ldg(p.mid + i), myD));
+            } else {
+                mydst = -1;
+                if (p.dev_error) atomicOr(p.dev_error, TQ_DEVERR_POSITION);
+            }
+        }
+        __syncwarp();  // the batch's integer thresholds are visible to the warp
+        // ---- pass 2: rotate and quantise
+        for (int jv = 0; jv < nb; ++jv) {
+            const int64_t dst = __shfl_sync(kFull, mydst, jv);
+            if (dst < 0) continue;
+            const double D = __shfl_sync(kFull, myD, jv);
+            const float Df = __shfl_sync(kFull, myDf, jv);
+            const uint16_t* src = p.B > 0 ? p.x + (v0 + jv) * p.dim : p.x + (v0 + jv) * p.xstride;
+            uint32_t hv[E];
+            load_row<E>(src, lane, E, hv);
+            int64_t k[E];
 #pragma unroll
-        for (int e = 0; e < E; ++e) k[e] = f16_exact(hv[e]);
-        const double D = __dsqrt_rn(warp_sumsq_rn<E>(k, E));
-        // thresholds F_i = floor(RN64(m_i * D)); w > F_i  <=>  w > RN64(m_i * D)
-        for (int i = lane; i < L; i += 32)
-            thr[i] = (i < L - 1) ? __double2ll_rd(__dmul_rn(__ldg(p.mid + i), D)) : INT64_MAX;
-        // w = H (s . k): in-lane stages, then cross-lane stages
+            for (int e = 0; e < E; ++e) k[e] = f16_exact(hv[e]);
+            if (!small_book)
+                for (int i = lane; i < L - 1; i += 32) thr[i] = s_mid[i] * Df;
+            // w = H (s . k): in-lane stages, then cross-lane stages
 #pragma unroll
-        for (int e = 0; e < E; ++e)
-            if ((smask >> e) & 1u) k[e] = -k[e];
+            for (int e = 0; e < E; ++e)
+                if ((smask >> e) & 1u) k[e] = -k[e];
 #pragma unroll
-        for (int h = 1; h < E; h <<= 1) {
+            for (int h = 1; h < E; h <<= 1) {
 #pragma unroll
-            for (int e = 0; e < E; ++e) {
-                if ((e & h) == 0) {
-                    const int64_t a = k[e], b = k[e + h];
-                    k[e] = a + b;
-                    k[e + h] = a - b;
+                for (int e = 0; e < E; ++e) {
+                    if ((e & h) == 0) {
+                        const int64_t a = k[e], b = k[e + h];
+                        k[e] = a + b;
+                        k[e + h] = a - b;
+                    }
                 }
             }
-        }
 #pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const bool upper = (lane & m) != 0;
+            for (int m = 1; m < 32; m <<= 1) {
+                const bool upper = (lane & m) != 0;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int64_t o = __shfl_xor_sync(kFull, k[e], m);
+                    k[e] = upper ? (o - k[e]) : (k[e] + o);
+                }
+            }
+            __syncwarp();
+            int code[E];
+            if (small_book) {
+                const int64_t* it = ithr + jv * 15;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    int pos = 0;
+                    for (int st = L >> 1; st > 0; st >>= 1)
+                        if (it[pos + st - 1] < k[e]) pos += st;
+                    code[e] = pos;
+                }
+            } else {
 #pragma unroll
             for (int e = 0; e < E; ++e) {
-                const int64_t o = __shfl_xor_sync(kFull, k[e], m);
-                k[e] = upper ? (o - k[e]) : (k[e] + o);
+                const float af = abs_to_f32(k[e]);
+                const float wf = k[e] < 0 ? -af : af;
+                int pos = 0;
+                for (int st = L >> 1; st > 0; st >>= 1)
+                    if (thr[pos + st - 1] < wf) pos += st;
+                // the boundaries next to the fp32 result decide it; any within the margin -> exact
+                bool near = false;
+                if (pos > 0) {
+                    const float t = thr[pos - 1];
+                    near |= fabsf(wf - t) <= kNearTie * fabsf(t);
+                }
+                if (pos < L - 1) {
+                    const float t = thr[pos];
+                    near |= fabsf(wf - t) <= kNearTie * fabsf(t);
+                }
+                if (near) pos = exact_code(k[e], D, p.mid, L);
+                code[e] = pos;
             }
+            }
+            pack_store<E>(code, E, lane, p.bits, p.dim, pk, p.codes + dst * p.cstride);
         }
-        __syncwarp();
-        int code[E];
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            int pos = 0;
-            for (int s = L >> 1; s > 0; s >>= 1)
-                if (thr[pos + s - 1] < k[e]) pos += s;
-            code[e] = pos;
-        }
-        pack_store<E>(code, E, lane, p.bits, p.dim, pk, p.codes + dst * p.cstride);
-        if (lane == 0) p.norms[dst] = __half_as_ushort(__double2half(ldexp(D, -24)));
     }
 }
 
@@ -316,7 +442,7 @@ cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64
     if (total <= 0) return cudaSuccess;
     const int sms = num_sms(c->device);
     if (c->is_wht) {
-        const int64_t want = (total + kWarps - 1) / kWarps;
+        const int64_t want = ((total + 31) / 32 + kWarps - 1) / kWarps;  // one batch of 32 vectors per warp
         const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
         const int E = c->dim / 32;
         switch (E) {
