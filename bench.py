@@ -68,8 +68,10 @@ def _peaks():
 
 
 def _source_sha():
+    """Hash of the sources that define the decode kernels (the ncu counters' validity key)."""
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "quantized_kv_cache_10_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "quantized_kv_cache_10_gb300", "csrc")
+    for f in sorted(glob.glob(os.path.join(csrc, "tq_decode_*")) + [os.path.join(csrc, "tq_internal.h")]):
         with open(f, "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
