@@ -82,6 +82,8 @@ def lib():
             L.orc_dequant.restype = i32
             L.orc_attention_unit.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i64, dp, vp]
             L.orc_attention_unit.restype = i32
+            L.orc_attention_unit_tail.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i64, vp, vp, i64, dp, vp, vp]
+            L.orc_attention_unit_tail.restype = i32
             _lib = L
     return _lib
 
@@ -228,11 +230,13 @@ class Codec:
 
 
 def attention_unit(ck: Codec, cv: Codec, q_f16: np.ndarray, k, k_norms, v_codes, v_norms,
-                   length: int, scale: float) -> np.ndarray:
-    """Attention of G query heads [G, d] over one KV head's first `length` tokens.
+                   length: int, scale: float, k_tail=None, v_tail=None, return_lse: bool = False):
+    """Attention of G query heads [G, d] over one KV head's first `length` tokens,
+    followed by the raw fp16 tail tokens k_tail / v_tail [n_tail, d] when given.
 
     k is packed K codes [>=length, bpv] (with k_norms) or raw fp16 K [>=length, d]
-    when ck.bits == 16.  Returns [G, d] float64.
+    when ck.bits == 16.  Returns [G, d] float64 (and the [G] log-sum-exp of the
+    scaled scores when return_lse).
     """
     q = np.ascontiguousarray(q_f16, dtype=np.float16)
     G = q.shape[0]
@@ -246,11 +250,21 @@ def attention_unit(ck: Codec, cv: Codec, q_f16: np.ndarray, k, k_norms, v_codes,
         kn = np.ascontiguousarray(k_norms, dtype=np.float16).view(np.uint16)
     vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
     vn = np.ascontiguousarray(v_norms, dtype=np.float16).view(np.uint16)
-    rc = lib().orc_attention_unit(ck._h, cv._h, _p(q.view(np.uint16)), G, _p(kk), _p(kn), _p(vc),
-                                  _p(vn), int(length), float(scale), _p(out))
+    if k_tail is None:
+        kt = vt = np.zeros((1, d), dtype=np.uint16)
+        nt = 0
+    else:
+        kt = np.ascontiguousarray(k_tail, dtype=np.float16).reshape(-1, d).view(np.uint16)
+        vt = np.ascontiguousarray(v_tail, dtype=np.float16).reshape(-1, d).view(np.uint16)
+        nt = kt.shape[0]
+        assert vt.shape[0] == nt
+    lse = np.zeros(G, dtype=np.float64)
+    rc = lib().orc_attention_unit_tail(ck._h, cv._h, _p(q.view(np.uint16)), G, _p(kk), _p(kn), _p(vc),
+                                       _p(vn), int(length), _p(kt), _p(vt), int(nt), float(scale),
+                                       _p(out), _p(lse))
     if rc != 0:
         raise RuntimeError("oracle attention failed")
-    return out
+    return (out, lse) if return_lse else out
 
 
 def attention(ck: Codec, cv: Codec, q, k, k_norms, v_codes, v_norms, seq_lens, scale,

@@ -549,40 +549,73 @@ int orc_dequant(const orc_codec *c, const uint8_t *codes, int64_t code_stride, c
  * codec has bits == 16; v: packed V codes + norms.  q: [G, d] fp16.
  * s_n = scale <q, K^_n>; p = softmax (max-subtracted, two passes);
  * out[g] = sum p_n V^_n / sum p_n; len == 0 gives zeros.  fp64 throughout. */
-int orc_attention_unit(const orc_codec *ck, const orc_codec *cv, const uint16_t *q, int G,
-                       const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
-                       const uint16_t *v_norms, int64_t len, double scale, double *out)
+/* Decode attention of G query heads over the first `len` cached tokens of one
+ * (batch, KV head) unit followed by `n_tail` raw fp16 tokens (k_tail, v_tail,
+ * [n_tail][d]): tokens kept unencoded -- the pending tokens that wait in fp16
+ * for a full batch ("add TurboQuant KV cache compression", Design) and fp16
+ * sink tokens (turboquant-mlx guide "KV cache compression") -- read in the
+ * same softmax as the packed cache.  The definition written out:
+ * dequantise the cache, append the tail, naive two-pass softmax in fp64.
+ * lse (optional, [G]) receives log(sum_t exp(s_t)) of the scaled scores.
+ * With no token at all the output is zero and lse is -inf. */
+int orc_attention_unit_tail(const orc_codec *ck, const orc_codec *cv, const uint16_t *q, int G,
+                            const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                            const uint16_t *v_norms, int64_t len, const uint16_t *k_tail,
+                            const uint16_t *v_tail, int64_t n_tail, double scale, double *out,
+                            double *lse)
 {
     int d = cv->d;
-    if (len <= 0) { memset(out, 0, sizeof(double) * (size_t)G * d); return 0; }
-    int bpk = d * ck->bits / 8, bpv = d * cv->bits / 8;
-    double *Kh = (double *)malloc(sizeof(double) * (size_t)len * d);
-    double *Vh = (double *)malloc(sizeof(double) * (size_t)len * d);
-    double *s = (double *)malloc(sizeof(double) * (size_t)len);
-    if (!Kh || !Vh || !s) { free(Kh); free(Vh); free(s); return -1; }
-    if (ck->bits == 16) {
-        const uint16_t *kr = (const uint16_t *)k;
-        for (int64_t i = 0; i < len * d; ++i) Kh[i] = orc_f16_to_f64(kr[i]);
-    } else {
-        orc_dequant(ck, (const uint8_t *)k, bpk, k_norms, len, Kh);
+    if (len < 0) len = 0;
+    if (n_tail < 0) n_tail = 0;
+    int64_t n = len + n_tail;
+    if (n <= 0) {
+        memset(out, 0, sizeof(double) * (size_t)G * d);
+        if (lse) for (int g = 0; g < G; ++g) lse[g] = -INFINITY;
+        return 0;
     }
-    orc_dequant(cv, v_codes, bpv, v_norms, len, Vh);
+    int bpk = d * ck->bits / 8, bpv = d * cv->bits / 8;
+    double *Kh = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *Vh = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *s = (double *)malloc(sizeof(double) * (size_t)n);
+    if (!Kh || !Vh || !s) { free(Kh); free(Vh); free(s); return -1; }
+    if (len > 0) {
+        if (ck->bits == 16) {
+            const uint16_t *kr = (const uint16_t *)k;
+            for (int64_t i = 0; i < len * d; ++i) Kh[i] = orc_f16_to_f64(kr[i]);
+        } else {
+            orc_dequant(ck, (const uint8_t *)k, bpk, k_norms, len, Kh);
+        }
+        orc_dequant(cv, v_codes, bpv, v_norms, len, Vh);
+    }
+    for (int64_t i = 0; i < n_tail * d; ++i) {
+        Kh[len * d + i] = orc_f16_to_f64(k_tail[i]);
+        Vh[len * d + i] = orc_f16_to_f64(v_tail[i]);
+    }
     for (int g = 0; g < G; ++g) {
         double mx = -INFINITY;
-        for (int64_t t = 0; t < len; ++t) {
+        for (int64_t t = 0; t < n; ++t) {
             double acc = 0.0;
             for (int i = 0; i < d; ++i) acc += orc_f16_to_f64(q[(int64_t)g * d + i]) * Kh[t * d + i];
             s[t] = scale * acc;
             if (s[t] > mx) mx = s[t];
         }
         double l = 0.0;
-        for (int64_t t = 0; t < len; ++t) { s[t] = exp(s[t] - mx); l += s[t]; }
+        for (int64_t t = 0; t < n; ++t) { s[t] = exp(s[t] - mx); l += s[t]; }
         for (int i = 0; i < d; ++i) {
             double acc = 0.0;
-            for (int64_t t = 0; t < len; ++t) acc += s[t] * Vh[t * d + i];
+            for (int64_t t = 0; t < n; ++t) acc += s[t] * Vh[t * d + i];
             out[(int64_t)g * d + i] = acc / l;
         }
+        if (lse) lse[g] = mx + log(l);
     }
     free(Kh); free(Vh); free(s);
     return 0;
+}
+
+int orc_attention_unit(const orc_codec *ck, const orc_codec *cv, const uint16_t *q, int G,
+                       const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                       const uint16_t *v_norms, int64_t len, double scale, double *out)
+{
+    return orc_attention_unit_tail(ck, cv, q, G, k, k_norms, v_codes, v_norms, len, NULL, NULL, 0, scale,
+                                   out, NULL);
 }

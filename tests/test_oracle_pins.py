@@ -370,3 +370,37 @@ def test_attention_large_scale_selects_best_key():
     o = oracle.attention_unit(ck, cv, q, kc, kn, vc, vn, 20, 1e4)
     best = int(np.argmax(kh @ q[0].astype(np.float64)))
     np.testing.assert_allclose(o[0], cv.dequant(vc, vn)[best], atol=1e-9)
+
+
+# --------------------------------------------------------------------------- raw fp16 tail tokens
+def test_attention_tail_only_is_plain_softmax_attention():
+    # No cached token: the result is ordinary softmax attention over the fp16 tail.
+    d = 64
+    ck, cv = oracle.Codec(d, 4, 42), oracle.Codec(d, 4, 43)
+    q = tq_inputs.fp16_normal(11, (3, d))
+    kt, vt = tq_inputs.fp16_normal(12, (9, d)), tq_inputs.fp16_normal(13, (9, d))
+    empty = np.zeros((1, ck.bytes_per_vec), np.uint8)
+    o, lse = oracle.attention_unit(ck, cv, q, empty, np.zeros(1, np.float16), empty, np.zeros(1, np.float16), 0,
+                                   0.2, kt, vt, return_lse=True)
+    s = 0.2 * (q.astype(np.float64) @ kt.astype(np.float64).T)
+    p = np.exp(s - s.max(1, keepdims=True))
+    np.testing.assert_allclose(o, (p @ vt.astype(np.float64)) / p.sum(1, keepdims=True), rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, np.log(np.exp(s).sum(1)), rtol=1e-14)
+
+
+def test_attention_cache_plus_tail_is_the_lse_merge_of_the_parts():
+    # Softmax over two disjoint token sets: out = (e^lse_a out_a + e^lse_b out_b) / (e^lse_a + e^lse_b).
+    ck, cv, q, K, kc, kn, vc, vn = _unit(n=70)
+    d = q.shape[1]
+    kt, vt = tq_inputs.fp16_normal(21, (13, d)), tq_inputs.fp16_normal(22, (13, d))
+    sc = 1 / math.sqrt(d)
+    both, lse = oracle.attention_unit(ck, cv, q, kc, kn, vc, vn, 70, sc, kt, vt, return_lse=True)
+    cache, lse_c = oracle.attention_unit(ck, cv, q, kc, kn, vc, vn, 70, sc, return_lse=True)
+    tail, lse_t = oracle.attention_unit(ck, cv, q, kc, kn, vc, vn, 0, sc, kt, vt, return_lse=True)
+    m = np.maximum(lse_c, lse_t)
+    wc, wt = np.exp(lse_c - m)[:, None], np.exp(lse_t - m)[:, None]
+    np.testing.assert_allclose(both, (wc * cache + wt * tail) / (wc + wt), rtol=0, atol=1e-13)
+    np.testing.assert_allclose(lse, m + np.log(wc + wt)[:, 0], rtol=1e-13)
+    # no cache and a single tail token: the output is that token's value
+    big, _ = oracle.attention_unit(ck, cv, q[:1], kc, kn, vc, vn, 0, 1.0, kt[:1], vt[:1], return_lse=True)
+    np.testing.assert_allclose(big[0], vt[0].astype(np.float64), rtol=0, atol=1e-15)
