@@ -204,6 +204,29 @@ tq_status tq_decode_attend(const tq_codec *ck, const tq_codec *cv, const uint16_
                            void *workspace, size_t ws_bytes, void *stream);
 
 /*
+ * tq_decode_attend with unencoded fp16 tail tokens read in the same softmax:
+ * for sequence b the attention runs over its seq_lens[b] packed tokens and then
+ * tail_lens[b] raw tokens of k_tail / v_tail -- the pending tokens that wait
+ * in fp16 until a batch of 64 is encoded ("add TurboQuant KV cache
+ * compression", Design) or fp16 sink tokens (turboquant-mlx guide "KV cache
+ * compression") -- with no separate pass over them.  The tail is scored
+ * against the unrotated query and merged with the cache's softmax state in
+ * the original basis (the combine kernel does it).
+ *   k_tail, v_tail  device fp16 [B, n_kv_heads, max_tail, dim], 16-byte aligned
+ *   tail_lens       device int32 [B]; values outside [0, max_tail] are clamped
+ *                   and flagged with TQ_DEVERR_SEQ_LEN; 0 = no tail token
+ *   max_tail        > 0
+ * Every other argument, the workspace and the errors as tq_decode_attend.
+ */
+tq_status tq_decode_attend_tail(const tq_codec *ck, const tq_codec *cv, const uint16_t *q,
+                                const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                                const uint16_t *v_norms, const int32_t *seq_lens, int B, int n_q_heads,
+                                int n_kv_heads, int64_t max_seq, const uint16_t *k_tail,
+                                const uint16_t *v_tail, const int32_t *tail_lens, int max_tail,
+                                float scale, uint16_t *out, void *workspace, size_t ws_bytes,
+                                void *stream);
+
+/*
  * Decode attention for callers that cannot allocate device memory.  The
  * pages have no counterpart of this entry point; it exists for code that must
  * not call cudaMalloc where it attends -- work recorded into a CUDA graph it

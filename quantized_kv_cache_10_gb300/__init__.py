@@ -18,8 +18,8 @@ __all__ = [
     "TQError", "Codec", "tq_version", "tq_codec_create", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
-    "tq_get_device_error", "tq_decode_attend_noalloc", "parse_scheme", "bytes_per_vec", "LIB_PATH",
-    "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION",
+    "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail", "parse_scheme", "bytes_per_vec",
+    "LIB_PATH", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtq.so")
@@ -30,6 +30,8 @@ _lib = C.CDLL(LIB_PATH)
 
 TQ_DEVERR_SEQ_LEN = 1
 TQ_DEVERR_POSITION = 2
+TQ_DEVERR_TIMEOUT = 4
+TQ_DEVERR_LAYOUT = 8
 
 _vp, _i32, _i64, _u64, _sz = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_size_t
 _sig = {
@@ -47,6 +49,8 @@ _sig = {
     "tq_decode_attend": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, C.c_float,
                                 _vp, _vp, _sz, _vp]),
     "tq_get_device_error": (_i32, [_vp, _vp, C.POINTER(_i32)]),
+    "tq_decode_attend_tail": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp,
+                                     _i32, C.c_float, _vp, _vp, C.c_size_t, _vp]),
     "tq_decode_attend_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, C.c_float,
                                         _vp, _vp]),
 }
@@ -239,6 +243,39 @@ def tq_decode_attend(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor, k_n
                                  _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, S, float(scale),
                                  _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"),
                                  workspace.numel(), _stream(stream)), "tq_decode_attend")
+
+
+def tq_decode_attend_tail(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor, k_norms: torch.Tensor | None,
+                          v_codes: torch.Tensor, v_norms: torch.Tensor, seq_lens: torch.Tensor, k_tail: torch.Tensor,
+                          v_tail: torch.Tensor, tail_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                          scale: float | None = None, stream=None):
+    """tq_decode_attend plus unencoded fp16 tail tokens in the same softmax: k_tail / v_tail
+    [B, Hkv, max_tail, dim] fp16, tail_lens [B] int32 (tokens of the tail used per sequence)."""
+    B, Hq, d = q.shape
+    Hkv, S = v_codes.shape[1], v_codes.shape[2]
+    max_tail = k_tail.shape[2]
+    for t, nm in ((q, "q"), (k, "k"), (v_codes, "v_codes"), (v_norms, "v_norms"), (seq_lens, "seq_lens"),
+                  (k_tail, "k_tail"), (v_tail, "v_tail"), (tail_lens, "tail_lens"), (out, "out"),
+                  (workspace, "workspace")):
+        _contig(t, nm)
+    if tuple(k_tail.shape) != (B, Hkv, max_tail, d) or tuple(v_tail.shape) != (B, Hkv, max_tail, d):
+        raise ValueError("k_tail / v_tail must be [B, Hkv, max_tail, dim]")
+    if ck.bits == 16:
+        kp = _dev(k, torch.float16, "k")
+        kn = None
+    else:
+        kp = _dev(k, torch.uint8, "k")
+        _contig(k_norms, "k_norms")
+        kn = _dev(k_norms, torch.float16, "k_norms")
+    if scale is None:
+        scale = d ** -0.5
+    _check(_lib.tq_decode_attend_tail(ck.handle, cv.handle, _dev(q, torch.float16, "q"), kp, kn,
+                                      _dev(v_codes, torch.uint8, "v_codes"), _dev(v_norms, torch.float16, "v_norms"),
+                                      _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, S,
+                                      _dev(k_tail, torch.float16, "k_tail"), _dev(v_tail, torch.float16, "v_tail"),
+                                      _dev(tail_lens, torch.int32, "tail_lens"), max_tail, float(scale),
+                                      _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"),
+                                      workspace.numel(), _stream(stream)), "tq_decode_attend_tail")
 
 
 def tq_get_device_error(error_word: torch.Tensor, stream=None) -> int:

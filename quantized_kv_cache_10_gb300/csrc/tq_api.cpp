@@ -22,6 +22,51 @@ bool on_codec_device(const tq_codec* c) {
 
 }  // namespace
 
+namespace {
+
+tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, const void* k,
+                             const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
+                             const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
+                             const uint16_t* k_tail, const uint16_t* v_tail, const int32_t* tail_lens,
+                             int max_tail, float scale, uint16_t* out, void* workspace, size_t ws_bytes,
+                             void* stream) {
+    if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
+    if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
+    if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
+    if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
+    if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
+    if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
+        return TQ_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
+    if (tail_lens) {
+        if (!k_tail || !v_tail || max_tail <= 0 || !aligned(tail_lens, 4) || !aligned(k_tail, 16) ||
+            !aligned(v_tail, 16))
+            return TQ_ERR_INVALID_ARG;
+    }
+    if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
+    tq::DecodePlan p;
+    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;
+    if (!workspace || !aligned(workspace, 256) || ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
+    tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
+                     B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace,
+                     tail_lens ? k_tail : nullptr, tail_lens ? v_tail : nullptr, tail_lens,
+                     tail_lens ? max_tail : 0};
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaErrorNotSupported;
+    if (tq::decode_mma_supported(ck, cv, p.G)) {
+        p.kernel = 1;
+        e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
+    }
+    if (e == cudaErrorNotSupported) {
+        p.kernel = 0;
+        e = tq::launch_decode_simt(a, p, st);
+    }
+    if (e != cudaSuccess) return from_cuda(e);
+    return from_cuda(tq::launch_decode_combine(a, p, st));
+}
+
+}  // namespace
+
 extern "C" {
 
 tq_status tq_encode(const tq_codec* c, const uint16_t* x, int64_t n_vec, int64_t x_row_stride, uint8_t* codes,
@@ -79,32 +124,20 @@ tq_status tq_decode_attend(const tq_codec* ck, const tq_codec* cv, const uint16_
                            const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
                            const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
                            float scale, uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
-    if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
-    if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
-    if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
-    if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-    if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
-    if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
-        return TQ_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
-    if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
-    tq::DecodePlan p;
-    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;
-    if (!workspace || !aligned(workspace, 256) || ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
-    tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
-                     B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace};
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaErrorNotSupported;
-    if (tq::decode_mma_supported(ck, cv, p.G)) {
-        p.kernel = 1;
-        e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
-    }
-    if (e == cudaErrorNotSupported) {
-        p.kernel = 0;
-        e = tq::launch_decode_simt(a, p, st);
-    }
-    if (e != cudaSuccess) return from_cuda(e);
-    return from_cuda(tq::launch_decode_combine(a, p, st));
+    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads,
+                              max_seq, nullptr, nullptr, nullptr, 0, scale, out, workspace, ws_bytes, stream);
+}
+
+tq_status tq_decode_attend_tail(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, const void* k,
+                                const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
+                                const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
+                                const uint16_t* k_tail, const uint16_t* v_tail, const int32_t* tail_lens,
+                                int max_tail, float scale, uint16_t* out, void* workspace, size_t ws_bytes,
+                                void* stream) {
+    if (!tail_lens) return TQ_ERR_INVALID_ARG;
+    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads,
+                              max_seq, k_tail, v_tail, tail_lens, max_tail, scale, out, workspace, ws_bytes,
+                              stream);
 }
 
 tq_status tq_get_device_error(void* error_word, void* stream, int* code) {

@@ -70,6 +70,8 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
+    __shared__ __align__(16) float s_ot[kCombineWarps][D];     // raw fp16 tail, original basis
+    __shared__ float s_mt[kCombineWarps], s_lt[kCombineWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // the V codec's sign word of this lane's dims (codec data, written by no kernel)
     uint32_t sw = 0;
@@ -115,6 +117,53 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     if (lane == 0) {
         s_m[warp] = m;
         s_l[warp] = l;
+    }
+    // Unencoded fp16 tail tokens of the sequence (pending tokens, sink tokens) in the
+    // same softmax: warp w scores tokens w, w + 4, ... against the unrotated query in
+    // the original basis (log2 units, like the cache) and keeps its own online state.
+    int nt = 0;
+    if (a.tail_lens) {
+        nt = __ldg(a.tail_lens + b);
+        if (nt < 0 || nt > a.max_tail) {
+            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+            nt = nt < 0 ? 0 : a.max_tail;
+        }
+    }
+    if (nt > 0) {
+        float qv[VPL], mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
+        const float f = kLog2e * a.scale;
+        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            qv[v] = __half2float(__ushort_as_half(qh[v])) * f;
+            ot[v] = 0.0f;
+        }
+        const int64_t row0 = (static_cast<int64_t>(b) * a.Hkv + (h / p.G)) * a.max_tail;
+        for (int n = warp; n < nt; n += kCombineWarps) {
+            const uint16_t* kr = a.k_tail + (row0 + n) * D + lane * VPL;
+            const uint16_t* vr = a.v_tail + (row0 + n) * D + lane * VPL;
+            float part = 0.0f, vv[VPL];
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) {
+                part = fmaf(qv[v], __half2float(__ushort_as_half(kr[v])), part);
+                vv[v] = __half2float(__ushort_as_half(vr[v]));
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
+            const float mn = fmaxf(mt, part);
+            const float al = exp2f(mt - mn);  // 0 while mt is -inf
+            const float pw = exp2f(part - mn);
+            lt = fmaf(lt, al, pw);
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) ot[v] = fmaf(ot[v], al, pw * vv[v]);
+            mt = mn;
+        }
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) s_ot[warp][lane * VPL + v] = ot[v];
+        if (lane == 0) {
+            s_mt[warp] = mt;
+            s_lt[warp] = lt;
+        }
     }
     __syncthreads();
     if (warp != 0) return;
@@ -183,6 +232,29 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         }
 #pragma unroll
         for (int v = 0; v < VPL; ++v) res[v] *= f;
+    }
+    if (nt > 0) {
+        // merge the tail's state (original basis) with the cache's normalised output res:
+        // out = (W_c res + W_t o_t / l_t) / (W_c + W_t), W = sum of weights relative to one max
+        float mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) ot[v] = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kCombineWarps; ++w) {
+            if (w < nt) {  // warps beyond the tail length hold no state
+                float os[VPL];
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) os[v] = s_ot[w][lane * VPL + v];
+                merge_state<VPL>(mt, lt, ot, s_mt[w], s_lt[w], os);
+            }
+        }
+        const float mm = fmaxf(m, mt);
+        const float wc = (m == -CUDART_INF_F) ? 0.0f : l * exp2f(m - mm);
+        const float wt = lt * exp2f(mt - mm);
+        const float den = wc + wt;
+        const float ic = den > 0.0f ? wc / den : 0.0f, it = den > 0.0f ? exp2f(mt - mm) / den : 0.0f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) res[v] = fmaf(res[v], ic, ot[v] * it);
     }
     uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
     if constexpr (VPL % 2 == 0) {

@@ -111,6 +111,11 @@ struct DecodeArgs {
     float scale;
     uint16_t* out;
     void* ws;
+    // unencoded fp16 tail tokens read in the same softmax (none when tail_lens is null)
+    const uint16_t* k_tail;
+    const uint16_t* v_tail;
+    const int32_t* tail_lens;
+    int max_tail;
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
