@@ -397,6 +397,32 @@ def gpu_arm(args):
     peak, peak_kind = _peaks()
     achieved = bytes_step / dec_mean / 1e9
 
+    # the same decode-attention call with a 63-token unencoded fp16 tail (the most a
+    # pending batch holds before it is encoded), read in the same softmax
+    tail_us = None
+    if replica_mode and graphs:
+        TT = 63
+        k_tail = torch.from_numpy(np.ascontiguousarray(K[:, :, :PB])).to(dev)
+        v_tail = torch.from_numpy(np.ascontiguousarray(V[:, :, :PB])).to(dev)
+        tlens = torch.full((w.B,), TT, dtype=torch.int32, device=dev)
+
+        def attend_tail(i):
+            r = i % R
+            tq.tq_decode_attend_tail(ck, cv, q, kc[r], None if kn is None else kn[r], vc[r], vn[r], lens, k_tail,
+                                     v_tail, tlens, out, wsb)
+
+        gt = capture(attend_tail, PB)
+        gt.replay()
+        torch.cuda.synchronize()
+        reps = max(8, args.steps // PB)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(reps):
+            gt.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        tail_us = e0.elapsed_time(e1) * 1e3 / (reps * PB)
+
     # one call on its own after an L2 flush (latency of an isolated decode step)
     iso = []
     for i in range(16):
@@ -485,6 +511,7 @@ def gpu_arm(args):
                      "kernel": kname, "decode_us": dec_mean * 1e6,
                      "note": "one decode-attention call (decode kernel + split-K combine kernel) per launch"},
         "isolated_call_us": statistics.median(iso),
+        "with_fp16_tail": {"tail_tokens": 63, "call_us": tail_us},
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

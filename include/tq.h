@@ -227,6 +227,39 @@ tq_status tq_decode_attend_tail(const tq_codec *ck, const tq_codec *cv, const ui
                                 void *stream);
 
 /*
+ * Two-phase KV cache of one layer for B sequences of equal length ("add
+ * TurboQuant KV cache compression", Design; the update / attend / memory
+ * interface of "How I built VeloxQuant-MLX"): prefill tokens are kept as raw
+ * fp16 and compressed in one batch on the first decode step; after that every
+ * decode step attends over the packed tokens, the pending fp16 tokens and the
+ * step's new token, and appends the new token to the pending buffer in the same
+ * launch; when 64 tokens are pending they are encoded into the packed cache.
+ * The cache owns its device memory (allocated by tq_cache_create and
+ * tq_cache_prefill, released by tq_cache_destroy); it keeps host-side counters,
+ * so calls on one cache must come from one host thread in order, on one stream
+ * (or streams the caller orders).  Codecs must outlive the cache.
+ *   tq_cache_create   ck, cv as for tq_decode_attend; max_seq % 8 == 0.
+ *   tq_cache_prefill  k, v: device fp16 [B, n_kv_heads, T, dim]; only before the
+ *                     first decode step, once.
+ *   tq_cache_decode   q: device fp16 [B, n_q_heads, dim]; k_new, v_new: device
+ *                     fp16 [B, n_kv_heads, dim]; out: device fp16 [B, n_q_heads,
+ *                     dim].  TQ_ERR_INVALID_ARG once max_seq tokens are held.
+ *   tq_cache_info     tokens held, packed, pending; bytes in use (packed bytes of
+ *                     the packed tokens, 4*dim bytes per fp16 token, per KV head).
+ *   tq_cache_device_error  reads and clears the device error words (syncs).
+ */
+typedef struct tq_cache tq_cache;
+tq_status tq_cache_create(const tq_codec *ck, const tq_codec *cv, int B, int n_q_heads, int n_kv_heads,
+                          int64_t max_seq, tq_cache **out);
+void tq_cache_destroy(tq_cache *cache);
+tq_status tq_cache_prefill(tq_cache *cache, const uint16_t *k, const uint16_t *v, int T, void *stream);
+tq_status tq_cache_decode(tq_cache *cache, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,
+                          float scale, uint16_t *out, void *stream);
+tq_status tq_cache_info(const tq_cache *cache, int64_t *tokens, int64_t *encoded, int *pending,
+                        size_t *bytes_in_use);
+tq_status tq_cache_device_error(tq_cache *cache, void *stream, int *code);
+
+/*
  * Decode attention for callers that cannot allocate device memory.  The
  * pages have no counterpart of this entry point; it exists for code that must
  * not call cudaMalloc where it attends -- work recorded into a CUDA graph it

@@ -19,7 +19,7 @@ __all__ = [
     "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
     "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail", "parse_scheme", "bytes_per_vec",
-    "LIB_PATH", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
+    "LIB_PATH", "KVCache", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtq.so")
@@ -51,6 +51,12 @@ _sig = {
     "tq_get_device_error": (_i32, [_vp, _vp, C.POINTER(_i32)]),
     "tq_decode_attend_tail": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp,
                                      _i32, C.c_float, _vp, _vp, C.c_size_t, _vp]),
+    "tq_cache_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, C.POINTER(_vp)]),
+    "tq_cache_destroy": (None, [_vp]),
+    "tq_cache_prefill": (_i32, [_vp, _vp, _vp, _i32, _vp]),
+    "tq_cache_decode": (_i32, [_vp, _vp, _vp, _vp, C.c_float, _vp, _vp]),
+    "tq_cache_info": (_i32, [_vp, C.POINTER(_i64), C.POINTER(_i64), C.POINTER(_i32), C.POINTER(_sz)]),
+    "tq_cache_device_error": (_i32, [_vp, _vp, C.POINTER(_i32)]),
     "tq_decode_attend_noalloc": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, C.c_float,
                                         _vp, _vp]),
 }
@@ -276,6 +282,64 @@ def tq_decode_attend_tail(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor
                                       _dev(tail_lens, torch.int32, "tail_lens"), max_tail, float(scale),
                                       _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"),
                                       workspace.numel(), _stream(stream)), "tq_decode_attend_tail")
+
+
+class KVCache:
+    """The two-phase KV cache of one layer (tq_cache_*): raw fp16 prefill compressed on the
+    first decode step, then per step attend + append with pending tokens kept in fp16 and
+    encoded 64 at a time.  Owns its device memory."""
+
+    def __init__(self, ck: Codec, cv: Codec, B: int, n_q_heads: int, n_kv_heads: int, max_seq: int):
+        h = _vp()
+        _check(_lib.tq_cache_create(ck.handle, cv.handle, B, n_q_heads, n_kv_heads, max_seq, C.byref(h)),
+               "tq_cache_create")
+        self._h, self._codecs = h.value, (ck, cv)   # the codecs must outlive the cache
+        self.B, self.Hq, self.Hkv, self.dim = B, n_q_heads, n_kv_heads, cv.dim
+
+    def prefill(self, k: torch.Tensor, v: torch.Tensor, stream=None):
+        """k, v: fp16 [B, Hkv, T, dim] on the device."""
+        T = k.shape[2]
+        for t, nm in ((k, "k"), (v, "v")):
+            _contig(t, nm)
+            if tuple(t.shape) != (self.B, self.Hkv, T, self.dim):
+                raise ValueError(f"{nm} must be [B, Hkv, T, dim]")
+        _check(_lib.tq_cache_prefill(self._h, _dev(k, torch.float16, "k"), _dev(v, torch.float16, "v"), T,
+                                     _stream(stream)), "tq_cache_prefill")
+
+    def decode(self, q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, out: torch.Tensor,
+               scale: float | None = None, stream=None):
+        """q, out: fp16 [B, Hq, dim]; k_new, v_new: fp16 [B, Hkv, dim]."""
+        for t, nm in ((q, "q"), (k_new, "k_new"), (v_new, "v_new"), (out, "out")):
+            _contig(t, nm)
+        if scale is None:
+            scale = self.dim ** -0.5
+        _check(_lib.tq_cache_decode(self._h, _dev(q, torch.float16, "q"), _dev(k_new, torch.float16, "k_new"),
+                                    _dev(v_new, torch.float16, "v_new"), float(scale),
+                                    _dev(out, torch.float16, "out"), _stream(stream)), "tq_cache_decode")
+
+    def info(self):
+        """(tokens held, packed tokens, pending fp16 tokens, bytes in use)."""
+        t, e, p, b = _i64(), _i64(), _i32(), _sz()
+        _check(_lib.tq_cache_info(self._h, C.byref(t), C.byref(e), C.byref(p), C.byref(b)), "tq_cache_info")
+        return t.value, e.value, p.value, b.value
+
+    def device_error(self, stream=None) -> int:
+        code = _i32()
+        st = _lib.tq_cache_device_error(self._h, _stream(stream), C.byref(code))
+        if st not in (0, 6):
+            raise TQError(st, "tq_cache_device_error")
+        return code.value
+
+    def close(self):
+        if self._h:
+            _lib.tq_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def tq_get_device_error(error_word: torch.Tensor, stream=None) -> int:

@@ -50,7 +50,7 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
     tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
                      B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace,
                      tail_lens ? k_tail : nullptr, tail_lens ? v_tail : nullptr, tail_lens,
-                     tail_lens ? max_tail : 0};
+                     tail_lens ? max_tail : 0, 0, nullptr, nullptr};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
     if (tq::decode_mma_supported(ck, cv, p.G)) {

@@ -61,6 +61,59 @@ __device__ __forceinline__ void merge_state(float& m, float& l, float (&acc)[VPL
     m = mn;
 }
 
+// x (lane owns dims [VPL lane, VPL (lane + 1)), original basis) -> sqrt(d) R x, the units
+// of the decode kernels' rotated accumulators: H (s . x) for the Walsh-Hadamard
+// rotation R = H diag(s) / sqrt(d), sqrt(d) Q x for the dense one.
+template <int VPL>
+__device__ __forceinline__ void to_rotated_units(const DecodeArgs& a, float (&x)[VPL], int lane) {
+    constexpr int D = 32 * VPL;
+    if constexpr ((VPL & (VPL - 1)) == 0) {
+        if (a.cv.is_wht) {
+            const uint32_t sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
+            const int sb = (lane * VPL) & 31;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v)
+                if ((sw >> (sb + v)) & 1u) x[v] = -x[v];
+#pragma unroll
+            for (int hh = 1; hh < VPL; hh <<= 1)
+#pragma unroll
+                for (int v = 0; v < VPL; ++v)
+                    if (!(v & hh)) {
+                        const float p = x[v], q = x[v + hh];
+                        x[v] = p + q;
+                        x[v + hh] = p - q;
+                    }
+#pragma unroll
+            for (int lm = 1; lm < 32; lm <<= 1) {
+                const bool upper = (lane & lm) != 0;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                    const float y = __shfl_xor_sync(kFullMask, x[v], lm);
+                    x[v] = upper ? (y - x[v]) : (x[v] + y);
+                }
+            }
+            return;
+        }
+    }
+    // (Q x)_i = sum_j Q^T[j][i] x_j, j ascending
+    float r[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) r[v] = 0.0f;
+    const float* qcol = a.cv.qt + lane * VPL;
+    for (int src = 0; src < 32; ++src) {
+#pragma unroll
+        for (int w = 0; w < VPL; ++w) {
+            const float xj = __shfl_sync(kFullMask, x[w], src);
+            const float* qrow = qcol + static_cast<int64_t>(src * VPL + w) * D;
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) r[v] = fmaf(__ldg(qrow + v), xj, r[v]);
+        }
+    }
+    const float sd = sqrtf(static_cast<float>(D));
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) x[v] = r[v] * sd;
+}
+
 // One CTA per (batch, query head); VPL = d / 32 dims per lane: lane owns dims
 // [VPL lane, VPL (lane + 1)).  Warp w merges splits w, w + 4, ... in one pass
 // (every load of a batch in flight at once, no separate max pass), then warp 0
@@ -70,22 +123,113 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
-    __shared__ __align__(16) float s_ot[kCombineWarps][D];     // raw fp16 tail, original basis
-    __shared__ float s_mt[kCombineWarps], s_lt[kCombineWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     // the V codec's sign word of this lane's dims (codec data, written by no kernel)
     uint32_t sw = 0;
     if ((VPL & (VPL - 1)) == 0 && a.cv.is_wht) sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
-    // let the next decode kernel on the stream start its table set-up, then
-    // wait for this call's decode grid (and the visibility of its records)
-    allow_dependent_launch();
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int pair = blockIdx.x;
     const int u = pair / p.G, hl = pair - (pair / p.G) * p.G;  // unit, head within its group
     const int qc = hl / kGP, g = hl - qc * kGP;
     const int vu = u * p.q_chunks + qc;
     const int b = u / a.Hkv;
     const int h = (u - b * a.Hkv) * p.G + hl;
+    // let the next decode kernel on the stream start its table set-up
+    allow_dependent_launch();
+    // Unencoded fp16 tail tokens of the sequence (pending tokens, sink tokens) in the
+    // same softmax: warp w scores tokens w, w + 4, ... against the unrotated query in
+    // the original basis (log2 units, like the cache) and keeps its own online state.
+    // The decode kernel triggers this grid only after its own dependency wait, so the
+    // call's inputs (q, the tail, the new token) are complete here, before this
+    // grid's wait: the tail overlaps the decode kernel.  (Loads bypass L1.)
+    float tail_m = -CUDART_INF_F, tail_l = 0.0f, tail_o[VPL];
+#pragma unroll
+    for (int v = 0; v < VPL; ++v) tail_o[v] = 0.0f;
+    int nt = 0;  // tail tokens in the buffer
+    if (a.tail_lens) {
+        nt = __ldcg(a.tail_lens + b);
+        if (nt < 0 || nt > a.max_tail) {
+            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+            nt = nt < 0 ? 0 : a.max_tail;
+        }
+    } else if (a.k_tail) {
+        nt = a.tail_n > 0 ? a.tail_n : 0;
+    }
+    const int kvh = h / p.G;
+    const int64_t tail_row0 = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.max_tail;
+    const int64_t new_row = static_cast<int64_t>(b) * a.Hkv + kvh;
+    const int ntot = nt + (a.k_new ? 1 : 0);  // the new token is scored after the buffer's
+    if (a.k_new && hl == 0 && warp == 0) {
+        // append the new token to the tail buffer (one CTA per KV head writes it; the
+        // other CTAs of the head read only tokens below nt)
+        if (nt < a.max_tail) {
+            const uint16_t* ks = a.k_new + new_row * D;
+            const uint16_t* vs = a.v_new + new_row * D;
+            uint16_t* kd = const_cast<uint16_t*>(a.k_tail) + (tail_row0 + nt) * D;
+            uint16_t* vd = const_cast<uint16_t*>(a.v_tail) + (tail_row0 + nt) * D;
+            for (int i = lane; i < D; i += 32) {
+                kd[i] = __ldcg(ks + i);
+                vd[i] = __ldcg(vs + i);
+            }
+        } else if (lane == 0) {
+            atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+        }
+    }
+    if (ntot > 0) {
+        float qv[VPL], mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
+        const float f = kLog2e * a.scale;
+        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+            qv[v] = __half2float(__ushort_as_half(__ldcg(qh + v))) * f;
+            ot[v] = 0.0f;
+        }
+        // TCH tokens per round with all their loads in flight (one memory latency per round)
+        constexpr int TCH = VPL <= 4 ? 4 : 2;
+        for (int n0 = warp; n0 < ntot; n0 += kCombineWarps * TCH) {
+            float kv[TCH][VPL], vv[TCH][VPL];
+#pragma unroll
+            for (int j = 0; j < TCH; ++j) {
+                const int n = n0 + j * kCombineWarps;
+                if (n < ntot) {
+                    const int64_t row = (n < nt) ? (tail_row0 + n) : new_row;
+                    const uint16_t* kr = ((n < nt) ? a.k_tail : a.k_new) + row * D + lane * VPL;
+                    const uint16_t* vr = ((n < nt) ? a.v_tail : a.v_new) + row * D + lane * VPL;
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v) {
+                        kv[j][v] = __half2float(__ushort_as_half(__ldcg(kr + v)));
+                        vv[j][v] = __half2float(__ushort_as_half(__ldcg(vr + v)));
+                    }
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < TCH; ++j) {
+                if (n0 + j * kCombineWarps < ntot) {
+                    float part = 0.0f;
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v) part = fmaf(qv[v], kv[j][v], part);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
+                    const float mn = fmaxf(mt, part);
+                    const float al = exp2f(mt - mn);  // 0 while mt is -inf
+                    const float pw = exp2f(part - mn);
+                    lt = fmaf(lt, al, pw);
+#pragma unroll
+                    for (int v = 0; v < VPL; ++v) ot[v] = fmaf(ot[v], al, pw * vv[j][v]);
+                    mt = mn;
+                }
+            }
+        }
+        // into the units of the cache's accumulator, sqrt(d) R o_t (= H (s . o_t) for the
+        // Walsh-Hadamard rotation, sqrt(d) Q o_t for the dense one), so that the tail merges
+        // with the cache partials like one more partial
+        to_rotated_units<VPL>(a, ot, lane);
+        tail_m = mt;
+        tail_l = lt;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) tail_o[v] = ot[v];
+    }
+    // wait for this call's decode grid (and the visibility of its records)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int ns = p.n_split;
     const int rec = kGP * (D + 2);
     const float* base = partial_ptr(a.ws, p, vu, 0, D);
@@ -112,58 +256,12 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 #pragma unroll
         for (int j = 0; j < CH; ++j) merge_state<VPL>(m, l, acc, mv[j], lv[j], ov[j]);
     }
+    merge_state<VPL>(m, l, acc, tail_m, tail_l, tail_o);  // (a no-op without tail tokens)
 #pragma unroll
     for (int v = 0; v < VPL; ++v) s_o[warp][lane * VPL + v] = acc[v];
     if (lane == 0) {
         s_m[warp] = m;
         s_l[warp] = l;
-    }
-    // Unencoded fp16 tail tokens of the sequence (pending tokens, sink tokens) in the
-    // same softmax: warp w scores tokens w, w + 4, ... against the unrotated query in
-    // the original basis (log2 units, like the cache) and keeps its own online state.
-    int nt = 0;
-    if (a.tail_lens) {
-        nt = __ldg(a.tail_lens + b);
-        if (nt < 0 || nt > a.max_tail) {
-            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
-            nt = nt < 0 ? 0 : a.max_tail;
-        }
-    }
-    if (nt > 0) {
-        float qv[VPL], mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
-        const float f = kLog2e * a.scale;
-        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-            qv[v] = __half2float(__ushort_as_half(qh[v])) * f;
-            ot[v] = 0.0f;
-        }
-        const int64_t row0 = (static_cast<int64_t>(b) * a.Hkv + (h / p.G)) * a.max_tail;
-        for (int n = warp; n < nt; n += kCombineWarps) {
-            const uint16_t* kr = a.k_tail + (row0 + n) * D + lane * VPL;
-            const uint16_t* vr = a.v_tail + (row0 + n) * D + lane * VPL;
-            float part = 0.0f, vv[VPL];
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) {
-                part = fmaf(qv[v], __half2float(__ushort_as_half(kr[v])), part);
-                vv[v] = __half2float(__ushort_as_half(vr[v]));
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
-            const float mn = fmaxf(mt, part);
-            const float al = exp2f(mt - mn);  // 0 while mt is -inf
-            const float pw = exp2f(part - mn);
-            lt = fmaf(lt, al, pw);
-#pragma unroll
-            for (int v = 0; v < VPL; ++v) ot[v] = fmaf(ot[v], al, pw * vv[v]);
-            mt = mn;
-        }
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) s_ot[warp][lane * VPL + v] = ot[v];
-        if (lane == 0) {
-            s_mt[warp] = mt;
-            s_lt[warp] = lt;
-        }
     }
     __syncthreads();
     if (warp != 0) return;
@@ -232,29 +330,6 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
         }
 #pragma unroll
         for (int v = 0; v < VPL; ++v) res[v] *= f;
-    }
-    if (nt > 0) {
-        // merge the tail's state (original basis) with the cache's normalised output res:
-        // out = (W_c res + W_t o_t / l_t) / (W_c + W_t), W = sum of weights relative to one max
-        float mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) ot[v] = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kCombineWarps; ++w) {
-            if (w < nt) {  // warps beyond the tail length hold no state
-                float os[VPL];
-#pragma unroll
-                for (int v = 0; v < VPL; ++v) os[v] = s_ot[w][lane * VPL + v];
-                merge_state<VPL>(mt, lt, ot, s_mt[w], s_lt[w], os);
-            }
-        }
-        const float mm = fmaxf(m, mt);
-        const float wc = (m == -CUDART_INF_F) ? 0.0f : l * exp2f(m - mm);
-        const float wt = lt * exp2f(mt - mm);
-        const float den = wc + wt;
-        const float ic = den > 0.0f ? wc / den : 0.0f, it = den > 0.0f ? exp2f(mt - mm) / den : 0.0f;
-#pragma unroll
-        for (int v = 0; v < VPL; ++v) res[v] = fmaf(res[v], ic, ot[v] * it);
     }
     uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
     if constexpr (VPL % 2 == 0) {

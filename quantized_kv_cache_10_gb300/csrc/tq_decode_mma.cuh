@@ -651,7 +651,6 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
         }
     }
 
-    allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int u = blockIdx.y, split = blockIdx.x;
     const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
@@ -683,6 +682,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
     int issued = 0;  // tiles whose copies the producer has started (producer lane 0)
     if (warp == C::NWC) {
         // ------------------------------------------------------------ producer
+        if (lane != 0) allow_dependent_launch();  // these lanes read nothing
         if (lane == 0) {
             // prologue data first: compact tables, this unit's query block, sign words
             const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
@@ -720,6 +720,7 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
                 prefetch_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(a.seq_lens + b) & ~uintptr_t(15)), 16);
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            allow_dependent_launch();
             mbar_arrive_expect_tx(setup_q, qbytes);
             bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup_q);
             t1 = min(clamped_len(a, b), t0 + p.chunk);
@@ -765,6 +766,10 @@ __global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
             replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
                                 reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            // Past the wait, everything stream-ordered before this kernel is complete: the
+            // combine kernel that follows may start (and read the call's inputs) once every
+            // thread of every CTA has said so.
+            allow_dependent_launch();
             t1 = min(clamped_len(a, b), t0 + p.chunk);
             ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
             ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));

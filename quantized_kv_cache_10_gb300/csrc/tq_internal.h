@@ -111,11 +111,17 @@ struct DecodeArgs {
     float scale;
     uint16_t* out;
     void* ws;
-    // unencoded fp16 tail tokens read in the same softmax (none when tail_lens is null)
+    // unencoded fp16 tail tokens read in the same softmax: tail_lens[b] of them, or
+    // tail_n for every sequence when tail_lens is null (no tail when tail_n <= 0)
     const uint16_t* k_tail;
     const uint16_t* v_tail;
     const int32_t* tail_lens;
     int max_tail;
+    int tail_n;
+    // optional new token [B, Hkv, dim] fp16: attended after the tail and appended to it
+    // (written at tail index tail_n into k_tail / v_tail) in the same launch
+    const uint16_t* k_new;
+    const uint16_t* v_new;
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
