@@ -303,6 +303,10 @@ struct Cfg {
     static constexpr Layout L = make_layout(D, KB, VB);
     static constexpr int NWC = L.nwc;               // consumer warps
     static constexpr int NTHREADS = (NWC + 1) * 32;
+    // register budget per thread: 8-bit K at d <= 128 measured fastest at 144 (17.3 vs 18.3 us
+    // per call at 168 on the 32K workload; 128: 19.4, 136: 17.6, 152: 18.5, 160: 18.5); others
+    // take what three warps per SM sub-partition allow (raw K: two warps)
+    static constexpr int MAXREG = (KB == 16) ? 232 : (KB == 8 && D <= 128) ? 144 : 168;
     static constexpr int MT = L.mt;                 // m-tiles of 16 tokens per warp per stage
     static constexpr int TS = L.ts;                 // tokens per stage
     static constexpr bool KRAW = (KB == 16);        // raw fp16 K rows (no codebook)
@@ -615,7 +619,7 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, int KB, int VB, int NT>
-__global__ void __launch_bounds__(Cfg<D, KB, VB, NT>::NTHREADS, 1)
+__global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT>;
     extern __shared__ __align__(1024) uint8_t smem[];

@@ -41,6 +41,7 @@ struct EncParams {
     const float* qt;  // Q^T row-major (dense)
     int bits;
     int dim;
+    int vb;           // vectors per warp batch (power-of-two dims), 1..32
 };
 
 __device__ __forceinline__ int64_t f16_exact(uint32_t h) {
@@ -238,11 +239,11 @@ __global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams
         smask |= ((__ldg(p.sign_bits + (j >> 5)) >> (j & 31)) & 1u) << e;
     }
     const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
-    const int64_t nbatch = (total + 31) / 32;
+    const int64_t nbatch = (total + p.vb - 1) / p.vb;
     for (int64_t bt = static_cast<int64_t>(blockIdx.x) * kWarps + warp; bt < nbatch;
          bt += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const int64_t v0 = bt * 32;
-        const int nb = static_cast<int>(min(static_cast<int64_t>(32), total - v0));
+        const int64_t v0 = bt * p.vb;
+        const int nb = static_cast<int>(min(static_cast<int64_t>(p.vb), total - v0));
         // ---- pass 1: exact sums of squares; lane j keeps vector j's
         uint64_t my_hi = 0, my_lo = 0;
         for (int jv = 0; jv < nb; ++jv) {
@@ -442,7 +443,11 @@ cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64
     if (total <= 0) return cudaSuccess;
     const int sms = num_sms(c->device);
     if (c->is_wht) {
-        const int64_t want = ((total + 31) / 32 + kWarps - 1) / kWarps;  // one batch of 32 vectors per warp
+        // batches of up to 32 vectors per warp, smaller when there are too few vectors to
+        // give every warp of the GPU one (pending-batch encodes of a few thousand vectors)
+        const int64_t per_warp = total / (static_cast<int64_t>(sms) * kWarps * 4);
+        p.vb = static_cast<int>(per_warp < 1 ? 1 : (per_warp > 32 ? 32 : per_warp));
+        const int64_t want = ((total + p.vb - 1) / p.vb + kWarps - 1) / kWarps;
         const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
         const int E = c->dim / 32;
         switch (E) {
