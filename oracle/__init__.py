@@ -84,6 +84,9 @@ def lib():
             L.orc_attention_unit.restype = i32
             L.orc_attention_unit_tail.argtypes = [vp, vp, vp, i32, vp, vp, vp, vp, i64, vp, vp, i64, dp, vp, vp]
             L.orc_attention_unit_tail.restype = i32
+            L.orc_attention_multi_unit.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, vp, i64,
+                                                   dp, vp]
+            L.orc_attention_multi_unit.restype = i32
             _lib = L
     return _lib
 
@@ -265,6 +268,43 @@ def attention_unit(ck: Codec, cv: Codec, q_f16: np.ndarray, k, k_norms, v_codes,
     if rc != 0:
         raise RuntimeError("oracle attention failed")
     return (out, lse) if return_lse else out
+
+
+def attention_multi_unit(ck: Codec, cv: Codec, q_f16: np.ndarray, k, k_norms, v_codes, v_norms,
+                         length: int, scale: float, k_tail=None, v_tail=None):
+    """Causal attention of the last L positions of one (batch, KV head) unit.
+
+    q_f16 [G, L, d]: the L query rows of each of the G query heads sharing the
+    KV head.  The sequence is the first `length` cached tokens followed by the
+    raw fp16 tail tokens k_tail / v_tail [n_tail, d]; query l sits at position
+    length + n_tail - L + l and sees the tokens up to it.  Returns [G, L, d]
+    float64.
+    """
+    q = np.ascontiguousarray(q_f16, dtype=np.float16)
+    G, L, d = q.shape
+    assert d == cv.dim
+    out = np.zeros((G, L, d), dtype=np.float64)
+    if ck.bits == 16:
+        kk = np.ascontiguousarray(k, dtype=np.float16).view(np.uint16)
+        kn = np.zeros(1, dtype=np.uint16)
+    else:
+        kk = np.ascontiguousarray(k, dtype=np.uint8)
+        kn = np.ascontiguousarray(k_norms, dtype=np.float16).view(np.uint16)
+    vc = np.ascontiguousarray(v_codes, dtype=np.uint8)
+    vn = np.ascontiguousarray(v_norms, dtype=np.float16).view(np.uint16)
+    if k_tail is None:
+        kt = vt = np.zeros((1, d), dtype=np.uint16)
+        nt = 0
+    else:
+        kt = np.ascontiguousarray(k_tail, dtype=np.float16).reshape(-1, d).view(np.uint16)
+        vt = np.ascontiguousarray(v_tail, dtype=np.float16).reshape(-1, d).view(np.uint16)
+        nt = kt.shape[0]
+        assert vt.shape[0] == nt
+    rc = lib().orc_attention_multi_unit(ck._h, cv._h, _p(q.view(np.uint16)), G, L, _p(kk), _p(kn), _p(vc),
+                                        _p(vn), int(length), _p(kt), _p(vt), int(nt), float(scale), _p(out))
+    if rc != 0:
+        raise RuntimeError("oracle multi-query attention failed")
+    return out
 
 
 def attention(ck: Codec, cv: Codec, q, k, k_norms, v_codes, v_norms, seq_lens, scale,

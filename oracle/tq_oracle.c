@@ -544,11 +544,6 @@ int orc_dequant(const orc_codec *c, const uint8_t *codes, int64_t code_stride, c
     return 0;
 }
 
-/* Decode attention for one (batch b, KV head) unit and its G query heads.
- * k: packed K codes [len, bpv_k] + norms, or raw fp16 [len, d] when the K
- * codec has bits == 16; v: packed V codes + norms.  q: [G, d] fp16.
- * s_n = scale <q, K^_n>; p = softmax (max-subtracted, two passes);
- * out[g] = sum p_n V^_n / sum p_n; len == 0 gives zeros.  fp64 throughout. */
 /* Decode attention of G query heads over the first `len` cached tokens of one
  * (batch, KV head) unit followed by `n_tail` raw fp16 tokens (k_tail, v_tail,
  * [n_tail][d]): tokens kept unencoded -- the pending tokens that wait in fp16
@@ -609,6 +604,74 @@ int orc_attention_unit_tail(const orc_codec *ck, const orc_codec *cv, const uint
         if (lse) lse[g] = mx + log(l);
     }
     free(Kh); free(Vh); free(s);
+    return 0;
+}
+
+/* Attention of L consecutive query positions per query head over one (batch,
+ * KV head) unit: the L query rows of each of the G heads sharing the KV head
+ * ("add TurboQuant KV cache compression", review of the NR0 path: a query
+ * chunk holds L rows per head, and a row's KV head follows from its query head).
+ * The sequence is the first `len` cached tokens followed by `n_tail` raw fp16
+ * tokens, P = len + n_tail tokens at positions 0 .. P-1; the queries are the
+ * last L positions, query l at position P - L + l, and each attends to the
+ * tokens at positions up to its own (causal).  The definition written out: the
+ * full score matrix of every query against every token, an additive mask of
+ * -inf above each query's position, a naive two-pass softmax per row, fp64.
+ * q, out: [G][L][d] (head-major rows).  A row with no visible token gives 0. */
+int orc_attention_multi_unit(const orc_codec *ck, const orc_codec *cv, const uint16_t *q, int G, int L,
+                             const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                             const uint16_t *v_norms, int64_t len, const uint16_t *k_tail,
+                             const uint16_t *v_tail, int64_t n_tail, double scale, double *out)
+{
+    int d = cv->d;
+    if (len < 0) len = 0;
+    if (n_tail < 0) n_tail = 0;
+    if (G <= 0 || L <= 0) return -1;
+    int64_t n = len + n_tail;
+    int64_t rows = (int64_t)G * L;
+    memset(out, 0, sizeof(double) * (size_t)rows * d);
+    if (n <= 0) return 0;
+    int bpk = d * ck->bits / 8, bpv = d * cv->bits / 8;
+    double *Kh = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *Vh = (double *)malloc(sizeof(double) * (size_t)n * d);
+    double *S = (double *)malloc(sizeof(double) * (size_t)rows * n);
+    if (!Kh || !Vh || !S) { free(Kh); free(Vh); free(S); return -1; }
+    if (len > 0) {
+        if (ck->bits == 16) {
+            const uint16_t *kr = (const uint16_t *)k;
+            for (int64_t i = 0; i < len * d; ++i) Kh[i] = orc_f16_to_f64(kr[i]);
+        } else {
+            orc_dequant(ck, (const uint8_t *)k, bpk, k_norms, len, Kh);
+        }
+        orc_dequant(cv, v_codes, bpv, v_norms, len, Vh);
+    }
+    for (int64_t i = 0; i < n_tail * d; ++i) {
+        Kh[len * d + i] = orc_f16_to_f64(k_tail[i]);
+        Vh[len * d + i] = orc_f16_to_f64(v_tail[i]);
+    }
+    /* scores with the causal mask: row r = g * L + l sits at position n - L + l */
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t pos = n - L + (r % L);
+        for (int64_t t = 0; t < n; ++t) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += orc_f16_to_f64(q[r * d + i]) * Kh[t * d + i];
+            S[r * n + t] = (t <= pos) ? scale * acc : -INFINITY;
+        }
+    }
+    for (int64_t r = 0; r < rows; ++r) {
+        double *s = S + r * n;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < n; ++t) if (s[t] > mx) mx = s[t];
+        if (mx == -INFINITY) continue;  /* no visible token: the row stays 0 */
+        double l = 0.0;
+        for (int64_t t = 0; t < n; ++t) { s[t] = exp(s[t] - mx); l += s[t]; }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < n; ++t) acc += s[t] * Vh[t * d + i];
+            out[r * d + i] = acc / l;
+        }
+    }
+    free(Kh); free(Vh); free(S);
     return 0;
 }
 

@@ -404,3 +404,64 @@ def test_attention_cache_plus_tail_is_the_lse_merge_of_the_parts():
     # no cache and a single tail token: the output is that token's value
     big, _ = oracle.attention_unit(ck, cv, q[:1], kc, kn, vc, vn, 0, 1.0, kt[:1], vt[:1], return_lse=True)
     np.testing.assert_allclose(big[0], vt[0].astype(np.float64), rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- several query positions
+def _multi_case(n=40, n_tail=6, G=2, L=5, d=64, bits_k=4, bits_v=3):
+    ck, cv = oracle.Codec(d, bits_k, 42), oracle.Codec(d, bits_v, 43)
+    K = tq_inputs.fp16_normal(31, (n, d))
+    V = tq_inputs.fp16_normal(32, (n, d))
+    kc, kn, _, _ = ck.encode(K)
+    vc, vn, _, _ = cv.encode(V)
+    kt, vt = tq_inputs.fp16_normal(33, (n_tail, d)), tq_inputs.fp16_normal(34, (n_tail, d))
+    q = tq_inputs.fp16_normal(35, (G, L, d))
+    return ck, cv, q, kc, kn, vc, vn, kt, vt
+
+
+def test_multi_query_is_textbook_causal_attention():
+    # Masked softmax written with numpy over the explicit token matrix: scores
+    # above each query's position get -inf (np.triu of the last L rows).
+    ck, cv, q, kc, kn, vc, vn, kt, vt = _multi_case()
+    n, L, sc = 46, 5, 0.15
+    o = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 40, sc, kt, vt)
+    kh = np.concatenate([ck.dequant(kc, kn), kt.astype(np.float64)])
+    vh = np.concatenate([cv.dequant(vc, vn), vt.astype(np.float64)])
+    mask = np.triu(np.ones((n, n), bool), 1)[n - L:]          # row l: tokens after position n-L+l
+    for g in range(2):
+        s = sc * q[g].astype(np.float64) @ kh.T
+        s[mask] = -np.inf
+        p = np.exp(s - s.max(1, keepdims=True))
+        np.testing.assert_allclose(o[g], (p @ vh) / p.sum(1, keepdims=True), rtol=1e-12, atol=1e-14)
+
+
+def test_multi_query_rows_are_single_queries_over_their_prefix():
+    # Row l equals one decode query over the tokens up to its position, computed
+    # by the single-query function on the truncated cache and tail.
+    ck, cv, q, kc, kn, vc, vn, kt, vt = _multi_case(n_tail=3, L=7)   # rows 0-3 reach into the cache
+    o = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 40, 0.125, kt, vt)
+    for ell in range(7):
+        vis = 40 + 3 - 7 + ell + 1
+        nc, ntl = min(40, vis), max(0, vis - 40)
+        one = oracle.attention_unit(ck, cv, q[:, ell], kc[:max(nc, 1)], kn[:max(nc, 1)], vc[:max(nc, 1)],
+                                    vn[:max(nc, 1)], nc, 0.125, kt[:ntl] if ntl else None,
+                                    vt[:ntl] if ntl else None)
+        np.testing.assert_allclose(o[:, ell], one, rtol=0, atol=1e-14)
+
+
+def test_multi_query_ignores_future_tokens_and_reduces_to_decode():
+    ck, cv, q, kc, kn, vc, vn, kt, vt = _multi_case(L=4)
+    o = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 40, 0.2, kt, vt)
+    # changing the last tail token changes only the last query row
+    kt2, vt2 = kt.copy(), vt.copy()
+    kt2[-1], vt2[-1] = -kt2[-1], vt2[-1] * np.float16(3)
+    o2 = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 40, 0.2, kt2, vt2)
+    np.testing.assert_array_equal(o2[:, :3], o[:, :3])
+    assert np.abs(o2[:, 3] - o[:, 3]).max() > 1e-3
+    # L = 1 is the decode query over everything
+    o1 = oracle.attention_multi_unit(ck, cv, q[:, 3:4], kc, kn, vc, vn, 40, 0.2, kt, vt)
+    dec = oracle.attention_unit(ck, cv, q[:, 3], kc, kn, vc, vn, 40, 0.2, kt, vt)
+    np.testing.assert_allclose(o1[:, 0], dec, rtol=0, atol=1e-15)
+    # more query positions than tokens: the rows before the first token are zero
+    ov = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 2, 0.2)
+    np.testing.assert_array_equal(ov[:, :2], 0.0)
+    np.testing.assert_allclose(ov[:, 2], np.repeat(cv.dequant(vc[:1], vn[:1]), 2, 0), rtol=0, atol=1e-15)
