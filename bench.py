@@ -423,6 +423,40 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         tail_us = e0.elapsed_time(e1) * 1e3 / (reps * PB)
 
+    # speculative verification: the same cache attended by L = 4 query positions per head
+    # (4 drafted tokens held as the fp16 tail), causal, one decode + combine launch pair
+    multi = None
+    if replica_mode and graphs:
+        LQ = 4
+        mq = torch.from_numpy(tq_inputs.fp16_normal(tq_inputs.stream_seed(w.seed, tq_inputs.Q_ID, 1),
+                                                    (w.B, w.Hq, LQ, w.d))).to(dev)
+        mout = torch.empty((w.B, w.Hq, LQ, w.d), dtype=torch.float16, device=dev)
+        mws = torch.empty(tq.tq_decode_attend_multi_workspace_bytes(w.B, w.Hq, w.Hkv, LQ, w.S, w.d),
+                          dtype=torch.uint8, device=dev)
+        tq.tq_workspace_init(mws)
+        mk = torch.from_numpy(np.ascontiguousarray(K[:, :, :LQ])).to(dev)
+        mv = torch.from_numpy(np.ascontiguousarray(V[:, :, :LQ])).to(dev)
+        mlens = torch.full((w.B,), LQ, dtype=torch.int32, device=dev)
+
+        def attend_multi(i):
+            r = i % R
+            tq.tq_decode_attend_multi(ck, cv, mq, kc[r], None if kn is None else kn[r], vc[r], vn[r], lens, mout,
+                                      mws, k_tail=mk, v_tail=mv, tail_lens=mlens)
+
+        gm = capture(attend_multi, PB)
+        gm.replay()
+        torch.cuda.synchronize()
+        reps = max(8, args.steps // PB)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(reps):
+            gm.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        m_us = e0.elapsed_time(e1) * 1e3 / (reps * PB)
+        multi = {"query_positions": LQ, "fp16_tail_tokens": LQ, "call_us": m_us,
+                 "packed_GBps": bytes_step / (m_us * 1e-6) / 1e9}
+
     # one call on its own after an L2 flush (latency of an isolated decode step)
     iso = []
     for i in range(16):
@@ -512,6 +546,7 @@ def gpu_arm(args):
                      "note": "one decode-attention call (decode kernel + split-K combine kernel) per launch"},
         "isolated_call_us": statistics.median(iso),
         "with_fp16_tail": {"tail_tokens": 63, "call_us": tail_us},
+        "multi_query": multi,
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

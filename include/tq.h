@@ -227,6 +227,37 @@ tq_status tq_decode_attend_tail(const tq_codec *ck, const tq_codec *cv, const ui
                                 void *stream);
 
 /*
+ * Attention of several query positions per sequence over the packed cache
+ * (and optional fp16 tail), for chunked prefill and speculative verification
+ * ("add TurboQuant KV cache compression", review of the NR0 path: a query chunk
+ * holds L rows per query head, and every row reads the KV head of its query
+ * head).  The sequence b is its seq_lens[b] packed tokens followed by its
+ * tail_lens[b] tail tokens (none when tail_lens is NULL); the L queries of a
+ * head are its last L positions, query l at position
+ * seq_lens[b] + tail_lens[b] - L + l, and each attends to the tokens at
+ * positions up to its own (causal).  A query before the first token gives a
+ * zero row.  L == 1 is tq_decode_attend / tq_decode_attend_tail.
+ * Every KV tile is dequantised once per group of up to 8 query rows (rows are
+ * head-major: the G heads of a KV head times L positions).
+ *   q, out    device fp16 [B, n_q_heads, L, dim] (q 16-byte aligned)
+ *   L         1 .. 4096
+ *   k_tail, v_tail, tail_lens, max_tail   as tq_decode_attend_tail, or all
+ *             NULL / 0 for no tail
+ *   workspace device, >= tq_decode_attend_multi_workspace_bytes(...) bytes,
+ *             otherwise as tq_decode_attend
+ * Every other argument and the errors as tq_decode_attend.
+ */
+size_t tq_decode_attend_multi_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int L, int64_t max_seq,
+                                              int dim);
+tq_status tq_decode_attend_multi(const tq_codec *ck, const tq_codec *cv, const uint16_t *q, int L,
+                                 const void *k, const uint16_t *k_norms, const uint8_t *v_codes,
+                                 const uint16_t *v_norms, const int32_t *seq_lens, int B, int n_q_heads,
+                                 int n_kv_heads, int64_t max_seq, const uint16_t *k_tail,
+                                 const uint16_t *v_tail, const int32_t *tail_lens, int max_tail,
+                                 float scale, uint16_t *out, void *workspace, size_t ws_bytes,
+                                 void *stream);
+
+/*
  * Two-phase KV cache of one layer for B sequences of equal length ("add
  * TurboQuant KV cache compression", Design; the update / attend / memory
  * interface of "How I built VeloxQuant-MLX"): prefill tokens are kept as raw

@@ -18,7 +18,8 @@ __all__ = [
     "TQError", "Codec", "tq_version", "tq_codec_create", "tq_codec_destroy", "tq_codec_info",
     "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
-    "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail", "parse_scheme", "bytes_per_vec",
+    "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail",
+    "tq_decode_attend_multi", "tq_decode_attend_multi_workspace_bytes", "parse_scheme", "bytes_per_vec",
     "LIB_PATH", "KVCache", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
 ]
 
@@ -51,6 +52,9 @@ _sig = {
     "tq_get_device_error": (_i32, [_vp, _vp, C.POINTER(_i32)]),
     "tq_decode_attend_tail": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp, _vp,
                                      _i32, C.c_float, _vp, _vp, C.c_size_t, _vp]),
+    "tq_decode_attend_multi_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64, _i32]),
+    "tq_decode_attend_multi": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp,
+                                      _vp, _i32, C.c_float, _vp, _vp, C.c_size_t, _vp]),
     "tq_cache_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, C.POINTER(_vp)]),
     "tq_cache_destroy": (None, [_vp]),
     "tq_cache_prefill": (_i32, [_vp, _vp, _vp, _i32, _vp]),
@@ -282,6 +286,56 @@ def tq_decode_attend_tail(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor
                                       _dev(tail_lens, torch.int32, "tail_lens"), max_tail, float(scale),
                                       _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"),
                                       workspace.numel(), _stream(stream)), "tq_decode_attend_tail")
+
+
+def tq_decode_attend_multi_workspace_bytes(B: int, n_q_heads: int, n_kv_heads: int, L: int, max_seq: int,
+                                           dim: int) -> int:
+    return int(_lib.tq_decode_attend_multi_workspace_bytes(B, n_q_heads, n_kv_heads, L, max_seq, dim))
+
+
+def tq_decode_attend_multi(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tensor, k_norms: torch.Tensor | None,
+                           v_codes: torch.Tensor, v_norms: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor,
+                           workspace: torch.Tensor, k_tail: torch.Tensor | None = None,
+                           v_tail: torch.Tensor | None = None, tail_lens: torch.Tensor | None = None,
+                           scale: float | None = None, stream=None):
+    """Causal attention of the last L positions of every sequence: q, out [B, Hq, L, dim] fp16;
+    the sequence is its packed tokens then (optionally) its fp16 tail tokens k_tail / v_tail
+    [B, Hkv, max_tail, dim] with tail_lens [B] int32 of them in use."""
+    B, Hq, L, d = q.shape
+    Hkv, S = v_codes.shape[1], v_codes.shape[2]
+    for t, nm in ((q, "q"), (k, "k"), (v_codes, "v_codes"), (v_norms, "v_norms"), (seq_lens, "seq_lens"),
+                  (out, "out"), (workspace, "workspace")):
+        _contig(t, nm)
+    if tuple(out.shape) != (B, Hq, L, d):
+        raise ValueError("out must be [B, Hq, L, dim]")
+    if tail_lens is None:
+        if k_tail is not None or v_tail is not None:
+            raise ValueError("k_tail / v_tail need tail_lens")
+        kt = vt = tl = None
+        max_tail = 0
+    else:
+        for t, nm in ((k_tail, "k_tail"), (v_tail, "v_tail"), (tail_lens, "tail_lens")):
+            _contig(t, nm)
+        max_tail = k_tail.shape[2]
+        if tuple(k_tail.shape) != (B, Hkv, max_tail, d) or tuple(v_tail.shape) != (B, Hkv, max_tail, d):
+            raise ValueError("k_tail / v_tail must be [B, Hkv, max_tail, dim]")
+        kt, vt = _dev(k_tail, torch.float16, "k_tail"), _dev(v_tail, torch.float16, "v_tail")
+        tl = _dev(tail_lens, torch.int32, "tail_lens")
+    if ck.bits == 16:
+        kp = _dev(k, torch.float16, "k")
+        kn = None
+    else:
+        kp = _dev(k, torch.uint8, "k")
+        _contig(k_norms, "k_norms")
+        kn = _dev(k_norms, torch.float16, "k_norms")
+    if scale is None:
+        scale = d ** -0.5
+    _check(_lib.tq_decode_attend_multi(ck.handle, cv.handle, _dev(q, torch.float16, "q"), L, kp, kn,
+                                       _dev(v_codes, torch.uint8, "v_codes"), _dev(v_norms, torch.float16, "v_norms"),
+                                       _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, S, kt, vt, tl, max_tail,
+                                       float(scale), _dev(out, torch.float16, "out"),
+                                       _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+                                       _stream(stream)), "tq_decode_attend_multi")
 
 
 class KVCache:

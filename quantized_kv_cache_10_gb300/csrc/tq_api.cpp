@@ -15,6 +15,8 @@ tq_status from_cuda(cudaError_t e) {
     return TQ_ERR_CUDA;
 }
 
+constexpr int kMaxQueryPositions = 4096;  // tq_decode_attend_multi: L
+
 bool on_codec_device(const tq_codec* c) {
     int d = -1;
     return cudaGetDevice(&d) == cudaSuccess && d == c->device;
@@ -26,15 +28,15 @@ namespace {
 
 tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, const void* k,
                              const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
-                             const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
-                             const uint16_t* k_tail, const uint16_t* v_tail, const int32_t* tail_lens,
-                             int max_tail, float scale, uint16_t* out, void* workspace, size_t ws_bytes,
-                             void* stream) {
+                             const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int L,
+                             int64_t max_seq, const uint16_t* k_tail, const uint16_t* v_tail,
+                             const int32_t* tail_lens, int max_tail, float scale, uint16_t* out, void* workspace,
+                             size_t ws_bytes, void* stream) {
     if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
     if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
     if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
     if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
-    if (max_seq <= 0 || max_seq % 8 != 0) return TQ_ERR_INVALID_ARG;
+    if (max_seq <= 0 || max_seq % 8 != 0 || L <= 0 || L > kMaxQueryPositions) return TQ_ERR_INVALID_ARG;
     if (!aligned(k, 16) || !aligned(v_codes, 16) || !aligned(v_norms, 16) || (k_norms && !aligned(k_norms, 16)))
         return TQ_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(out, 4) || !aligned(seq_lens, 4)) return TQ_ERR_INVALID_ARG;
@@ -45,15 +47,16 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
     }
     if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
     tq::DecodePlan p;
-    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;
+    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, L, max_seq, p))
+        return TQ_ERR_INVALID_ARG;
     if (!workspace || !aligned(workspace, 256) || ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
     tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
                      B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace,
                      tail_lens ? k_tail : nullptr, tail_lens ? v_tail : nullptr, tail_lens,
-                     tail_lens ? max_tail : 0, 0, nullptr, nullptr};
+                     tail_lens ? max_tail : 0, 0, nullptr, nullptr, L};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
-    if (tq::decode_mma_supported(ck, cv, p.G)) {
+    if (tq::decode_mma_supported(ck, cv)) {
         p.kernel = 1;
         e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
     }
@@ -111,7 +114,17 @@ size_t tq_decode_attend_workspace_bytes(int B, int n_q_heads, int n_kv_heads, in
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
     if (dim < 32 || dim > 512 || dim % 32) return 0;
     tq::DecodePlan p;
-    if (!tq::make_decode_plan(dim, dev, B, n_q_heads, n_kv_heads, max_seq, p)) return 0;
+    if (!tq::make_decode_plan(dim, dev, B, n_q_heads, n_kv_heads, 1, max_seq, p)) return 0;
+    return p.ws_bytes;
+}
+
+size_t tq_decode_attend_multi_workspace_bytes(int B, int n_q_heads, int n_kv_heads, int L, int64_t max_seq,
+                                              int dim) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dim < 32 || dim > 512 || dim % 32 || L <= 0 || L > kMaxQueryPositions) return 0;
+    tq::DecodePlan p;
+    if (!tq::make_decode_plan(dim, dev, B, n_q_heads, n_kv_heads, L, max_seq, p)) return 0;
     return p.ws_bytes;
 }
 
@@ -124,7 +137,7 @@ tq_status tq_decode_attend(const tq_codec* ck, const tq_codec* cv, const uint16_
                            const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
                            const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
                            float scale, uint16_t* out, void* workspace, size_t ws_bytes, void* stream) {
-    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads,
+    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, 1,
                               max_seq, nullptr, nullptr, nullptr, 0, scale, out, workspace, ws_bytes, stream);
 }
 
@@ -135,7 +148,18 @@ tq_status tq_decode_attend_tail(const tq_codec* ck, const tq_codec* cv, const ui
                                 int max_tail, float scale, uint16_t* out, void* workspace, size_t ws_bytes,
                                 void* stream) {
     if (!tail_lens) return TQ_ERR_INVALID_ARG;
-    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads,
+    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, 1,
+                              max_seq, k_tail, v_tail, tail_lens, max_tail, scale, out, workspace, ws_bytes,
+                              stream);
+}
+
+tq_status tq_decode_attend_multi(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, int L, const void* k,
+                                 const uint16_t* k_norms, const uint8_t* v_codes, const uint16_t* v_norms,
+                                 const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int64_t max_seq,
+                                 const uint16_t* k_tail, const uint16_t* v_tail, const int32_t* tail_lens,
+                                 int max_tail, float scale, uint16_t* out, void* workspace, size_t ws_bytes,
+                                 void* stream) {
+    return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, L,
                               max_seq, k_tail, v_tail, tail_lens, max_tail, scale, out, workspace, ws_bytes,
                               stream);
 }

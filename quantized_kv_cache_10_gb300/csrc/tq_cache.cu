@@ -190,13 +190,13 @@ tq_status tq_cache_decode(tq_cache* c, const uint16_t* q, const uint16_t* k_new,
     }
     // attend over the packed tokens, the pending ones and the new one; append the new one
     tq::DecodePlan p;
-    if (!tq::make_decode_plan(c->dim, c->device, c->B, c->Hq, c->Hkv, c->max_seq, p)) return TQ_ERR_INVALID_ARG;
+    if (!tq::make_decode_plan(c->dim, c->device, c->B, c->Hq, c->Hkv, 1, c->max_seq, p)) return TQ_ERR_INVALID_ARG;
     if (c->ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
     tq::DecodeArgs a{tq::dev_view(c->ck), tq::dev_view(c->cv), q, c->kc, c->kn, c->vc, c->vn, c->d_count,
                      c->B, c->Hq, c->Hkv, c->max_seq, scale, out, c->ws,
-                     c->pk, c->pv, nullptr, kPending, c->pending, k_new, v_new};
+                     c->pk, c->pv, nullptr, kPending, c->pending, k_new, v_new, 1};
     e = cudaErrorNotSupported;
-    if (tq::decode_mma_supported(c->ck, c->cv, p.G)) {
+    if (tq::decode_mma_supported(c->ck, c->cv)) {
         p.kernel = 1;
         e = tq::launch_decode_mma(a, p, st);
     }

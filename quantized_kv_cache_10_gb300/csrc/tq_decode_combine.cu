@@ -11,11 +11,12 @@
 // every cached vector): diag(s) H acc / d for the Walsh-Hadamard rotation,
 // Q^T acc / sqrt(d) for the dense one.
 //
-// One CTA per (batch, query head).  It is launched with programmatic stream
-// serialization: its CTAs may be resident before the decode grid finishes,
-// and griddepcontrol.wait holds them until that grid has completed and its
-// partial records are visible.  Every head is merged in parallel, each in one
-// round of loads, instead of all heads of a unit by one last-arriving CTA.
+// One CTA per query row (batch, query head, query position).  It is launched
+// with programmatic stream serialization: its CTAs may be resident before the
+// decode grid finishes, and griddepcontrol.wait holds them until that grid has
+// completed and its partial records are visible.  Every row is merged in
+// parallel, each in one round of loads, instead of all rows of a unit by one
+// last-arriving CTA.
 #include "tq_decode_common.cuh"
 
 namespace tq {
@@ -114,7 +115,8 @@ __device__ __forceinline__ void to_rotated_units(const DecodeArgs& a, float (&x)
     for (int v = 0; v < VPL; ++v) x[v] = r[v] * sd;
 }
 
-// One CTA per (batch, query head); VPL = d / 32 dims per lane: lane owns dims
+// One CTA per query row (batch, query head, query position); VPL = d / 32 dims per
+// lane: lane owns dims
 // [VPL lane, VPL (lane + 1)).  Warp w merges splits w, w + 4, ... in one pass
 // (every load of a batch in flight at once, no separate max pass), then warp 0
 // merges the four warp states in a fixed order and writes the head's output.
@@ -128,11 +130,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     uint32_t sw = 0;
     if ((VPL & (VPL - 1)) == 0 && a.cv.is_wht) sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
     const int pair = blockIdx.x;
-    const int u = pair / p.G, hl = pair - (pair / p.G) * p.G;  // unit, head within its group
+    const int u = pair / p.S, hl = pair - (pair / p.S) * p.S;  // unit, row within the unit
     const int qc = hl / kGP, g = hl - qc * kGP;
     const int vu = u * p.q_chunks + qc;
     const int b = u / a.Hkv;
-    const int h = (u - b * a.Hkv) * p.G + hl;
+    const int kvh = u - b * a.Hkv;
+    const int ell = hl % p.L;  // query position (the unit's rows are head-major)
+    const int64_t qrow = (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + hl;
     // let the next decode kernel on the stream start its table set-up
     allow_dependent_launch();
     // Unencoded fp16 tail tokens of the sequence (pending tokens, sink tokens) in the
@@ -144,20 +148,11 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     float tail_m = -CUDART_INF_F, tail_l = 0.0f, tail_o[VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) tail_o[v] = 0.0f;
-    int nt = 0;  // tail tokens in the buffer
-    if (a.tail_lens) {
-        nt = __ldcg(a.tail_lens + b);
-        if (nt < 0 || nt > a.max_tail) {
-            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
-            nt = nt < 0 ? 0 : a.max_tail;
-        }
-    } else if (a.k_tail) {
-        nt = a.tail_n > 0 ? a.tail_n : 0;
-    }
-    const int kvh = h / p.G;
+    const int nt = tail_count(a, b);  // tail tokens in the buffer
+    const int nvis = p.L > 1 ? tail_visible(nt, p.L, ell) : nt;  // of them before this row's position
     const int64_t tail_row0 = (static_cast<int64_t>(b) * a.Hkv + kvh) * a.max_tail;
     const int64_t new_row = static_cast<int64_t>(b) * a.Hkv + kvh;
-    const int ntot = nt + (a.k_new ? 1 : 0);  // the new token is scored after the buffer's
+    const int ntot = nvis + (a.k_new ? 1 : 0);  // the new token is scored after the buffer's
     if (a.k_new && hl == 0 && warp == 0) {
         // append the new token to the tail buffer (one CTA per KV head writes it; the
         // other CTAs of the head read only tokens below nt)
@@ -177,7 +172,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     if (ntot > 0) {
         float qv[VPL], mt = -CUDART_INF_F, lt = 0.0f, ot[VPL];
         const float f = kLog2e * a.scale;
-        const uint16_t* qh = a.q + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
+        const uint16_t* qh = a.q + qrow * D + lane * VPL;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
             qv[v] = __half2float(__ushort_as_half(__ldcg(qh + v))) * f;
@@ -191,9 +186,9 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
             for (int j = 0; j < TCH; ++j) {
                 const int n = n0 + j * kCombineWarps;
                 if (n < ntot) {
-                    const int64_t row = (n < nt) ? (tail_row0 + n) : new_row;
-                    const uint16_t* kr = ((n < nt) ? a.k_tail : a.k_new) + row * D + lane * VPL;
-                    const uint16_t* vr = ((n < nt) ? a.v_tail : a.v_new) + row * D + lane * VPL;
+                    const int64_t row = (n < nvis) ? (tail_row0 + n) : new_row;
+                    const uint16_t* kr = ((n < nvis) ? a.k_tail : a.k_new) + row * D + lane * VPL;
+                    const uint16_t* vr = ((n < nvis) ? a.v_tail : a.v_new) + row * D + lane * VPL;
 #pragma unroll
                     for (int v = 0; v < VPL; ++v) {
                         kv[j][v] = __half2float(__ushort_as_half(__ldcg(kr + v)));
@@ -331,7 +326,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 #pragma unroll
         for (int v = 0; v < VPL; ++v) res[v] *= f;
     }
-    uint16_t* o = a.out + (static_cast<int64_t>(b) * a.Hq + h) * D + lane * VPL;
+    uint16_t* o = a.out + qrow * D + lane * VPL;
     if constexpr (VPL % 2 == 0) {
         // out is 4-byte aligned and VPL lane offsets are even: 32-bit stores
         uint32_t* o32 = reinterpret_cast<uint32_t*>(o);
@@ -348,7 +343,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 template <int VPL>
 cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_units * p.G);
+    cfg.gridDim = dim3(p.n_units * p.S);
     cfg.blockDim = dim3(kCombineWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;

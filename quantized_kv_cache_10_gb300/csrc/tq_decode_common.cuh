@@ -41,13 +41,42 @@ __device__ __forceinline__ int64_t clamped_len(const DecodeArgs& a, int b) {
     return L;
 }
 
-// q' for query head h into dst[0..d): the K rotation applied to q, scaled by
-// log2(e) * scale / sqrt(d) (raw K: q * log2(e) * scale, no rotation).
-// Executed by one full warp.
-__device__ inline void rotate_query_warp(const DecodeArgs& a, int b, int h, float* dst) {
+// Unencoded tail tokens of sequence b: tail_lens[b] (clamped to [0, max_tail],
+// out-of-range values flagged), else tail_n for every sequence, else 0.  The
+// new token of the cache manager is not counted.
+__device__ __forceinline__ int tail_count(const DecodeArgs& a, int b) {
+    if (a.tail_lens) {
+        int nt = __ldcg(a.tail_lens + b);
+        if (nt < 0 || nt > a.max_tail) {
+            if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+            nt = nt < 0 ? 0 : a.max_tail;
+        }
+        return nt;
+    }
+    return (a.k_tail && a.tail_n > 0) ? a.tail_n : 0;
+}
+
+// Causal visibility for query position ell of L: the queries are the last L of
+// the sequence's len + tail tokens (packed first, then tail), and each attends
+// to the tokens up to its own position.  Packed tokens visible: all of them
+// unless the query sits before the end of the packed part.
+__device__ __forceinline__ int64_t packed_visible(int64_t len, int tail, int L, int ell) {
+    const int64_t hidden = static_cast<int64_t>(L - 1 - ell) - tail;  // packed tokens after the query
+    return hidden > 0 ? (len > hidden ? len - hidden : 0) : len;
+}
+// ... and tail tokens visible to it.
+__device__ __forceinline__ int tail_visible(int tail, int L, int ell) {
+    const int v = tail - (L - 1 - ell);
+    return v > 0 ? v : 0;
+}
+
+// q' for query row `row` of q ([B, Hq, L, d] as rows of d) into dst[0..d): the K
+// rotation applied to q, scaled by log2(e) * scale / sqrt(d) (raw K:
+// q * log2(e) * scale, no rotation).  Executed by one full warp.
+__device__ inline void rotate_query_warp(const DecodeArgs& a, int64_t row, float* dst) {
     const int lane = threadIdx.x & 31;
     const int d = a.cv.dim;
-    const uint16_t* q = a.q + (static_cast<int64_t>(b) * a.Hq + h) * d;
+    const uint16_t* q = a.q + row * d;
     const DevCodec& ck = a.ck;
     if (ck.bits == 16) {
         const float f = kLog2e * a.scale;

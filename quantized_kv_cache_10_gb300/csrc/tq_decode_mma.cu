@@ -161,8 +161,8 @@ cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t r
 
 }  // namespace mma_detail
 
-bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G) {
-    if (G < 1 || G > 8 || cv->bits == 16 || ck->dim != cv->dim) return false;
+bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv) {
+    if (cv->bits == 16 || ck->dim != cv->dim) return false;
     const int d = cv->dim;
     if (d != 64 && d != 96 && d != 128 && d != 256) return false;
     for (const auto& s : mma_detail::kSchemes)
@@ -188,7 +188,11 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t sms = num_sms(dev);
-    int64_t ns = (sms + p.n_units - 1) / p.n_units;
+    const int64_t ctas = int64_t(p.n_units) * p.q_chunks;  // CTAs per split
+    int64_t ns = (sms + ctas - 1) / ctas;
+    // several row groups per unit (each re-reads the unit's tiles, mostly from L2):
+    // keep the grid to one wave
+    if (p.q_chunks > 1 && ns * ctas > sms) ns = sms / ctas;
     const int64_t cap = (a.max_seq + 255) / 256;
     if (ns > cap) ns = cap;
     if (ns < 1) ns = 1;
@@ -199,7 +203,10 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
         p.n_split = static_cast<int>(ns);
         p.chunk = chunk;
     }
-    const int nt = p.G > 4 ? 2 : 1;
+    // query rows per CTA, min(S, 8): up to 4 (one n-tile, hi/lo columns of q) or 5..8;
+    // codes 3 and 4 are the same for the instantiation with several query positions or
+    // row groups per unit (causal masks, fp16 hi/lo split of P)
+    const int nt = (p.S > 4 ? 2 : 1) + ((p.L > 1 || p.q_chunks > 1) ? 2 : 0);
     switch (a.cv.dim) {
         case 64: return launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st);
         case 96: return launch_mma_d_extern<96>(a, p, a.ck.bits, a.cv.bits, nt, st);

@@ -139,6 +139,16 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// fp16 (hi, lo) split of two fp32 values: hi = fp16(x), lo = fp16(x - hi), so hi + lo
+// carries x to ~2^-22 relative (packed pairs: a in the low half).
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -618,7 +628,7 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, int KB, int VB, int NT>
+template <int D, int KB, int VB, int NT, bool MULTI>
 __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT>;
@@ -633,6 +643,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     uint64_t* empty = full + 8;                                          // [NSTAGE <= 8]
     uint64_t* setup = full + 16;                                         // codec tables, sign words
     uint64_t* setup_q = full + 17;                                       // the query block
+    int* s_erel = reinterpret_cast<int*>(misc + 160);                    // [kGP] causal ends
     float* wm = reinterpret_cast<float*>(misc + 256);                    // [C::NWC][kGP]
     float* wl = wm + C::NWC * kGP;                                         // [C::NWC][kGP]
     int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
@@ -656,10 +667,17 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     }
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int u = blockIdx.y, split = blockIdx.x;
+    // blockIdx.y: (unit, group of <= kGP query rows); the unit's rows are its G query
+    // heads times L query positions, head-major, contiguous in q and out
+    // (the MULTI instantiation serves several query positions or more than kGP rows per
+    // unit; the other one is the decode case: one CTA per unit along y, rows = heads)
+    const int vu = blockIdx.y, split = blockIdx.x;
+    const int u = MULTI ? vu / p.q_chunks : vu;
+    const int s0 = MULTI ? (vu - u * p.q_chunks) * kGP : 0;
     const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
-    const int G = p.G;
-    const int h0 = kvh * G;
+    const int G = MULTI ? min(kGP, p.S - s0) : p.G;  // query rows of this CTA
+    const int64_t qrow0 = MULTI ? (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + s0
+                                : static_cast<int64_t>(b) * a.Hq + kvh * G;
     const int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
     const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
     // This kernel is launched with programmatic stream serialization: it may
@@ -720,13 +738,13 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                 }
                 // the query block and the 16-byte granule holding seq_lens[b] (allocations
                 // are 256-byte aligned, so the granule lies inside the caller's buffer)
-                prefetch_l2(a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes);
+                prefetch_l2(a.q + qrow0 * D, qbytes);
                 prefetch_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(a.seq_lens + b) & ~uintptr_t(15)), 16);
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             allow_dependent_launch();
             mbar_arrive_expect_tx(setup_q, qbytes);
-            bulk_g2s(pro + C::PRO_Q, a.q + (static_cast<int64_t>(b) * a.Hq + h0) * D, qbytes, setup_q);
+            bulk_g2s(pro + C::PRO_Q, a.q + qrow0 * D, qbytes, setup_q);
             t1 = min(clamped_len(a, b), t0 + p.chunk);
             ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
             const uint8_t* kg = static_cast<const uint8_t*>(a.k);
@@ -763,6 +781,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     } else {
         // ------------------------------------------------------------ consumers: prologue
         const int ctid = tid;  // 0 .. C::NWC * 32 - 1
+        int64_t len = 0;
         {
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
@@ -774,7 +793,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
             // combine kernel that follows may start (and read the call's inputs) once every
             // thread of every CTA has said so.
             allow_dependent_launch();
-            t1 = min(clamped_len(a, b), t0 + p.chunk);
+            len = clamped_len(a, b);
+            t1 = min(len, t0 + p.chunk);
             ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
             ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
             if (!ok && lane == 0) {
@@ -783,6 +803,15 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
             }
             rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
                               reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp, lane, ctid);
+            if (MULTI && ctid < kGP) {
+                // Causal end of each query row, as tokens past t0: the rows' positions are the
+                // last L of the sequence (packed tokens, then tail), so every packed token is
+                // visible when L == 1 or the tail is long enough.  Clamped to t1, it also marks
+                // the split's end.
+                const int tail = p.L > 1 ? tail_count(a, b) : 0;
+                const int64_t e = min(packed_visible(len, tail, p.L, (s0 + ctid) % p.L), t1);
+                s_erel[ctid] = e > t0 ? static_cast<int>(e - t0) : 0;
+            }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
@@ -938,17 +967,21 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                     }
                     }
                 }
-                // ---- scale by K norms, mask, tile max ----
+                // ---- scale by K norms, mask (tile end, causal limit), tile max ----
                 float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
                 float tmax[NT];
 #pragma unroll
                 for (int j = 0; j < NT; ++j) tmax[j] = -CUDART_INF_F;
+                // this thread's query rows (2t + j, or t when NT == 1): causal ends in the tile
+                // (decode: the tile's end)
+                int lim[NT];
+#pragma unroll
+                for (int j = 0; j < NT; ++j) lim[j] = MULTI ? s_erel[(NT == 2) ? 2 * t + j : t] - it * C::TS : nvalid;
 #pragma unroll
                 for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
                     for (int hr = 0; hr < 2; ++hr) {
                         const int r = r0 + 16 * mt + g + 8 * hr;
-                        const bool ok = r < nvalid;
                         const float nk = C::KRAW ? 1.0f : __half2float(knrm[r]);
 #pragma unroll
                         for (int j = 0; j < NT; ++j) {
@@ -959,7 +992,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                                 x = sc[mt][0][2 * hr + j];
                             else
                                 x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
-                            x = ok ? x * nk : -CUDART_INF_F;
+                            // lim <= t1 - ts, so this also masks the rows past the tile's end
+                            x = (r < lim[j]) ? x * nk : -CUDART_INF_F;
                             sv[mt][hr][j] = x;
                             tmax[j] = fmaxf(tmax[j], x);
                         }
@@ -983,7 +1017,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                     l_run[j] *= alpha[j];
                 }
                 if (__any_sync(kFullMask, rescale)) {
-                    const float a1 = (NT == 2) ? alpha[NT - 1] : 1.0f;
+                    // (MULTI, NT == 1: columns 2t and 2t + 1 both hold row t, hi and lo of P)
+                    const float a1 = (NT == 2 || MULTI) ? alpha[NT - 1] : 1.0f;
 #pragma unroll
                     for (int i = 0; i < C::KT; ++i) {
                         O[i][0] *= alpha[0];
@@ -1010,16 +1045,36 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                             pv[hr][j] = ok ? pp * nvv : 0.0f;
                         }
                     }
-                    uint32_t x0, x1;
+                    // With several query positions (MULTI), P' is fp16 hi + lo, so the weights
+                    // keep ~2^-22 of their precision: the first rows of a chunk see only a few
+                    // tokens, and one fp16 P would carry their weights' 2^-11 rounding into
+                    // the output.  NT == 1 puts the lo part in the free column 2t + 1, NT == 2
+                    // multiplies V by it in a second mma.  Decode keeps one fp16 P, as fp16
+                    // attention does.
+                    uint32_t x0, x1, pl0 = 0u, pl1 = 0u;
                     if constexpr (NT == 2) {
-                        x0 = pack_f16(pv[0][0], pv[0][1]);
-                        x1 = pack_f16(pv[1][0], pv[1][1]);
+                        if constexpr (MULTI) {
+                            uint32_t y0, y1;
+                            split_f16x2(pv[0][0], pv[0][1], x0, y0);
+                            split_f16x2(pv[1][0], pv[1][1], x1, y1);
+                            pl0 = movmatrix_t(y0);
+                            pl1 = movmatrix_t(y1);
+                        } else {
+                            x0 = pack_f16(pv[0][0], pv[0][1]);
+                            x1 = pack_f16(pv[1][0], pv[1][1]);
+                        }
+                    } else if constexpr (MULTI) {
+                        uint32_t h0, l0;  // (row g, row g + 8) pairs
+                        split_f16x2(pv[0][0], pv[1][0], h0, l0);
+                        x0 = (h0 & 0xffffu) | (l0 << 16);
+                        x1 = (h0 >> 16) | (l0 & 0xffff0000u);
                     } else {
                         x0 = pack_f16(pv[0][0], 0.0f);
                         x1 = pack_f16(pv[1][0], 0.0f);
                     }
                     const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
                     // V of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile, thread g's dims
+                    constexpr bool SPLIT = MULTI && NT == 2;
                     if constexpr (C::VPAIR) {
                         constexpr int NSUB = (D / 8 + 15) / 16;  // chunks of up to 16 dims
 #pragma unroll
@@ -1039,6 +1094,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                                     const uint32_t a2 = lds32(p89.addr(2 * k, vtab_a, lane4));
                                     const uint32_t a3 = lds32(p89.addr(2 * k + 1, vtab_a, lane4));
                                     mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                                    if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
                                 }
                             }
                         }
@@ -1056,6 +1112,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                             const uint32_t a2 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm, vtab_a, lane4);
                             const uint32_t a3 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm + 1, vtab_a, lane4);
                             mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                            if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
                         }
                     }
                 }
@@ -1102,6 +1159,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                 slice[(2 * t + 1) * D + d0] = f[1] * O[dm][1];
                 slice[(2 * t) * D + d0 + 1] = f[0] * O[dm][2];
                 slice[(2 * t + 1) * D + d0 + 1] = f[1] * O[dm][3];
+            } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
+                slice[t * D + d0] = f[0] * (O[dm][0] + O[dm][1]);
+                slice[t * D + d0 + 1] = f[0] * (O[dm][2] + O[dm][3]);
+                slice[(4 + t) * D + d0] = 0.0f;
+                slice[(4 + t) * D + d0 + 1] = 0.0f;
             } else {
                 slice[t * D + d0] = f[0] * O[dm][0];
                 slice[t * D + d0 + 1] = f[0] * O[dm][2];
@@ -1111,7 +1173,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
         // fixed-order sum of the warp slices, straight into this CTA's partial record
-        float* part = partial_ptr(a.ws, p, u, split, D);
+        float* part = partial_ptr(a.ws, p, vu, split, D);
         const float4* all4 = reinterpret_cast<const float4*>(ring);
         float4* part4 = reinterpret_cast<float4*>(part);
         for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
@@ -1155,7 +1217,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
 cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows);
 
 // Launch of one instantiation; split plan for one CTA per SM.
-template <int D, int KB, int VB, int NT>
+template <int D, int KB, int VB, int NT, bool MULTI>
 cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
     using C = Cfg<D, KB, VB, NT>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
@@ -1163,7 +1225,7 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
@@ -1175,7 +1237,7 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_split, p.n_units);
+    cfg.gridDim = dim3(p.n_split, p.n_units * p.q_chunks);
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
@@ -1184,13 +1246,18 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT>, a, p, kmap);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI>, a, p, kmap);
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
     if constexpr (mma_fits(D, KB_, VB_)) {                                                    \
         if (kb == KB_ && vb == VB_)                                                           \
-            return nt == 2 ? launch_inst<D, KB_, VB_, 2>(a, p, st) : launch_inst<D, KB_, VB_, 1>(a, p, st); \
+            switch (nt) {                                                                     \
+                case 1: return launch_inst<D, KB_, VB_, 1, false>(a, p, st);                      \
+                case 2: return launch_inst<D, KB_, VB_, 2, false>(a, p, st);                      \
+                case 3: return launch_inst<D, KB_, VB_, 1, true>(a, p, st);                       \
+                default: return launch_inst<D, KB_, VB_, 2, true>(a, p, st);                      \
+            }                                                                                 \
     }
 
 // The (K bits, V bits) schemes with a tensor-core instantiation.

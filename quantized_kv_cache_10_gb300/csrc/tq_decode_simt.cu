@@ -1,11 +1,14 @@
 // tq_decode_simt.cu -- general fused decode attention (any supported dim,
 // bit width and GQA ratio) on the fp32 SIMT pipes.
 //
-// One CTA per (batch, KV head, query group of <= 8 heads, sequence split);
-// each warp walks every 8th token of the split: it unpacks the token's K
-// codes, looks the centroids up in shared memory, scores all query heads of
-// the group at once (GQA without expanding K/V: "add TurboQuant KV cache
-// compression", review of the NR0 head mapping), updates an online softmax
+// One CTA per (batch, KV head, group of <= 8 query rows, sequence split); the
+// rows of a KV head are its G query heads times the L query positions of each,
+// head-major.  Each warp walks every 8th token of the split: it unpacks the
+// token's K codes, looks the centroids up in shared memory, scores all query
+// rows of the group at once (GQA without expanding K/V: "add TurboQuant KV
+// cache compression", review of the NR0 head mapping: a row's KV head follows
+// from its query head), masks the tokens after each row's position, updates an
+// online softmax
 // and accumulates P . dequant(V) in the rotated basis ("anyone still talking
 // about mlx-swift-lm?").  Warp states merge in shared memory and the CTA
 // writes its split-K partial; the combine kernel (tq_decode_combine.cu)
@@ -50,13 +53,21 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     const int u = vu / p.q_chunks, qc = vu - (vu / p.q_chunks) * p.q_chunks;
     const int b = u / a.Hkv;
     const int kvh = u - b * a.Hkv;
-    const int h0 = kvh * p.G + qc * kGP;
-    const int Gc = min(kGP, p.G - qc * kGP);
+    const int s0 = qc * kGP;                      // first row of this group within the unit
+    const int Gc = min(kGP, p.S - s0);
+    const int64_t row0q = (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + s0;
     const int64_t len = clamped_len(a, b);
     const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
     const int64_t t1 = min(len, t0 + p.chunk);
+    // end of the packed tokens each row sees (causal; every token when L == 1)
+    int64_t vis[kGP];
+    {
+        const int tail = p.L > 1 ? tail_count(a, b) : 0;
+#pragma unroll
+        for (int g = 0; g < kGP; ++g) vis[g] = packed_visible(len, tail, p.L, (s0 + g) % p.L);
+    }
 
-    if (warp < Gc) rotate_query_warp(a, b, h0 + warp, qs + warp * d);
+    if (warp < Gc) rotate_query_warp(a, row0q + warp, qs + warp * d);
     const bool rawk = a.ck.bits == 16;
     if (!rawk)
         for (int i = tid; i < (1 << a.ck.bits); i += kThreads) ctk[i] = __ldg(a.ck.centroids + i);
@@ -99,6 +110,9 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
             }
             s[g] = part * nk;
         }
+        bool seen[kGP];
+#pragma unroll
+        for (int g = 0; g < kGP; ++g) seen[g] = g < Gc && t < vis[g];
         const uint8_t* vr = a.v_codes + (row0 + t) * a.cv.bpv;
         float vv[E];
 #pragma unroll
@@ -106,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
         const float nv = __half2float(__ushort_as_half(a.v_norms[row0 + t]));
 #pragma unroll
         for (int g = 0; g < kGP; ++g) {
-            if (g < Gc) {
+            if (seen[g]) {
                 const float mn = fmaxf(m[g], s[g]);
                 const float alpha = exp2f(m[g] - mn);
                 const float pp = exp2f(s[g] - mn);
@@ -195,12 +209,16 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStr
     }
 }
 
-bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int64_t max_seq, DecodePlan& plan) {
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seq <= 0 || d <= 0) return false;
+bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int L, int64_t max_seq, DecodePlan& plan) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Hq % Hkv != 0 || max_seq <= 0 || d <= 0 || L <= 0) return false;
     plan = DecodePlan{};
     plan.G = Hq / Hkv;
+    plan.L = L;
+    if (int64_t(plan.G) * L > (1 << 20)) return false;
+    plan.S = plan.G * L;
     plan.kernel = 0;
-    plan.q_chunks = (plan.G + kGP - 1) / kGP;
+    plan.q_chunks = (plan.S + kGP - 1) / kGP;
+    if (int64_t(B) * Hkv * plan.q_chunks > 65535) return false;  // grid y
     plan.n_units = B * Hkv;
     const int64_t vunits = int64_t(plan.n_units) * plan.q_chunks;
     const int64_t target = 2 * int64_t(num_sms(device));

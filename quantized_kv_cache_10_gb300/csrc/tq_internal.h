@@ -68,7 +68,9 @@ struct DecodePlan {
     int kernel;          // 0 = SIMT (general), 1 = tensor-core (mma.sync) kernel
     int n_units;         // B * n_kv_heads
     int G;               // query heads per KV head
-    int q_chunks;        // SIMT: query groups of at most 8 per unit
+    int L;               // query positions per query head (1 for decode)
+    int S;               // query rows per unit: G * L, head-major (row = head * L + position)
+    int q_chunks;        // CTAs per (unit, split) along the rows: groups of at most 8 rows
     int n_split;         // CTAs per unit along the sequence
     int64_t chunk;       // tokens per split (multiple of 8 / tile)
     size_t ws_bytes;     // total workspace bytes
@@ -77,7 +79,7 @@ struct DecodePlan {
 
 // Split-K plan (independent of the kernel chosen, so the workspace size only
 // depends on the shape and the device).  plan.kernel is set by the caller.
-bool make_decode_plan(int dim, int device, int B, int Hq, int Hkv, int64_t max_seq, DecodePlan& plan);
+bool make_decode_plan(int dim, int device, int B, int Hq, int Hkv, int L, int64_t max_seq, DecodePlan& plan);
 
 // By-value view of a codec for kernels (host structs are not visible on the
 // device).
@@ -122,6 +124,10 @@ struct DecodeArgs {
     // (written at tail index tail_n into k_tail / v_tail) in the same launch
     const uint16_t* k_new;
     const uint16_t* v_new;
+    // query positions per query head: q and out are [B, Hq, L, dim]; the queries are the
+    // last L positions of each sequence (packed tokens, then tail tokens) and each attends
+    // to the tokens up to its own position (L == 1: every token)
+    int L;
 };
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
@@ -129,7 +135,7 @@ cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStr
 // May lower p.n_split / raise p.chunk (one CTA per SM); p is then the plan the
 // kernel ran with, which the combine kernel needs.
 cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st);
-bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv, int G);
+bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv);
 // Combine of the split-K partials, inverse V rotation and fp16 store
 // (tq_decode_combine.cu).  Launched right after a decode kernel on the same
 // stream; p must be the plan that kernel ran with.

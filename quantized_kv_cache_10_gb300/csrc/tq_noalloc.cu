@@ -66,7 +66,7 @@ tq_status tq_decode_attend_noalloc(const tq_codec* ck, const tq_codec* cv, const
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev != ck->device || dev != cv->device) return TQ_ERR_INVALID_ARG;
     tq::DecodePlan p;
-    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, max_seq, p)) return TQ_ERR_INVALID_ARG;
+    if (!tq::make_decode_plan(cv->dim, cv->device, B, n_q_heads, n_kv_heads, 1, max_seq, p)) return TQ_ERR_INVALID_ARG;
     if (p.ws_bytes > kScratchBytes) return TQ_ERR_WORKSPACE;  // shape too large for the fixed scratch
     void* ws = nullptr;
     if (scratch_address(&ws) != cudaSuccess) return TQ_ERR_CUDA;
