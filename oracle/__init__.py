@@ -87,6 +87,13 @@ def lib():
             L.orc_attention_multi_unit.argtypes = [vp, vp, vp, i32, i32, vp, vp, vp, vp, i64, vp, vp, i64,
                                                    dp, vp]
             L.orc_attention_multi_unit.restype = i32
+            L.orc_qjl_sketch_copy.argtypes = [i32, u64, vp]
+            L.orc_encode_qjl.argtypes = [vp, u64, vp, i64, i64, vp, i64, vp, vp, i64, vp]
+            L.orc_encode_qjl.restype = i32
+            L.orc_qjl_scores.argtypes = [vp, u64, vp, i32, vp, vp, vp, vp, i64, vp]
+            L.orc_qjl_scores.restype = i32
+            L.orc_attention_qjl_unit.argtypes = [vp, u64, vp, vp, i32, vp, vp, vp, vp, vp, vp, i64, dp, vp]
+            L.orc_attention_qjl_unit.restype = i32
             _lib = L
     return _lib
 
@@ -222,6 +229,41 @@ class Codec:
         lib().orc_encode_codes(self._h, _p(x), _p(codes), _p(w), _p(D))
         return codes, w, float(D[0])
 
+    # ---- QJL residual sketch (TurboQuantProd): this codec's MSE codes + sign bits ----
+    def qjl_sketch(self) -> np.ndarray:
+        """The fp32 sketch matrix S [d, d] (rows j) of this codec's seed."""
+        S = np.zeros((self.dim, self.dim), dtype=np.float32)
+        lib().orc_qjl_sketch_copy(self.dim, C.c_uint64(self.seed), _p(S))
+        return S
+
+    def encode_qjl(self, x_f16: np.ndarray):
+        """x [n, d] fp16 -> (codes, norms fp16, signs [n, d/8] uint8, residual norms fp16)."""
+        x = np.ascontiguousarray(x_f16, dtype=np.float16).reshape(-1, self.dim)
+        n, d = x.shape[0], self.dim
+        codes = np.zeros((n, self.bytes_per_vec), dtype=np.uint8)
+        norms = np.zeros(n, dtype=np.uint16)
+        signs = np.zeros((n, d // 8), dtype=np.uint8)
+        rn = np.zeros(n, dtype=np.uint16)
+        rc = lib().orc_encode_qjl(self._h, C.c_uint64(self.seed), _p(x.view(np.uint16)), n, d, _p(codes),
+                                  self.bytes_per_vec, _p(norms), _p(signs), d // 8, _p(rn))
+        if rc != 0:
+            raise RuntimeError("oracle QJL encode failed")
+        return codes, norms.view(np.float16), signs, rn.view(np.float16)
+
+    def qjl_scores(self, q_f16, codes, norms, signs, rnorms) -> np.ndarray:
+        """Estimated <q_g, k_n> [G, n] (unscaled) from the stored MSE + QJL fields."""
+        q = np.ascontiguousarray(q_f16, dtype=np.float16).reshape(-1, self.dim)
+        G, n = q.shape[0], np.asarray(codes).reshape(-1, self.bytes_per_vec).shape[0]
+        out = np.zeros((G, n), dtype=np.float64)
+        rc = lib().orc_qjl_scores(self._h, C.c_uint64(self.seed), _p(q.view(np.uint16)), G,
+                                  _p(np.ascontiguousarray(codes, dtype=np.uint8)),
+                                  _p(np.ascontiguousarray(norms, dtype=np.float16).view(np.uint16)),
+                                  _p(np.ascontiguousarray(signs, dtype=np.uint8)),
+                                  _p(np.ascontiguousarray(rnorms, dtype=np.float16).view(np.uint16)), n, _p(out))
+        if rc != 0:
+            raise RuntimeError("oracle QJL scores failed")
+        return out
+
     def dequant(self, codes: np.ndarray, norms_f16: np.ndarray) -> np.ndarray:
         c = np.ascontiguousarray(codes, dtype=np.uint8).reshape(-1, self.bytes_per_vec)
         nr = np.ascontiguousarray(norms_f16, dtype=np.float16).reshape(-1).view(np.uint16)
@@ -304,6 +346,27 @@ def attention_multi_unit(ck: Codec, cv: Codec, q_f16: np.ndarray, k, k_norms, v_
                                         _p(vn), int(length), _p(kt), _p(vt), int(nt), float(scale), _p(out))
     if rc != 0:
         raise RuntimeError("oracle multi-query attention failed")
+    return out
+
+
+def attention_qjl_unit(ck: Codec, cv: Codec, q_f16, k_codes, k_norms, k_signs, k_rnorms, v_codes, v_norms,
+                       length: int, scale: float) -> np.ndarray:
+    """Decode attention of G query heads [G, d] over `length` keys stored as MSE codes
+    + QJL sign sketch + residual norms (scores by the QJL estimator) and MSE-coded
+    values.  Returns [G, d] float64."""
+    q = np.ascontiguousarray(q_f16, dtype=np.float16)
+    G, d = q.shape
+    out = np.zeros((G, d), dtype=np.float64)
+    rc = lib().orc_attention_qjl_unit(
+        ck._h, C.c_uint64(ck.seed), cv._h, _p(q.view(np.uint16)), G,
+        _p(np.ascontiguousarray(k_codes, dtype=np.uint8)),
+        _p(np.ascontiguousarray(k_norms, dtype=np.float16).view(np.uint16)),
+        _p(np.ascontiguousarray(k_signs, dtype=np.uint8)),
+        _p(np.ascontiguousarray(k_rnorms, dtype=np.float16).view(np.uint16)),
+        _p(np.ascontiguousarray(v_codes, dtype=np.uint8)),
+        _p(np.ascontiguousarray(v_norms, dtype=np.float16).view(np.uint16)), int(length), float(scale), _p(out))
+    if rc != 0:
+        raise RuntimeError("oracle QJL attention failed")
     return out
 
 

@@ -544,6 +544,160 @@ int orc_dequant(const orc_codec *c, const uint8_t *codes, int64_t code_stride, c
     return 0;
 }
 
+/* ---------------------------------------------------------------------------
+ * QJL residual sketch (TurboQuantProd: "How I built VeloxQuant-MLX", Stage 3:
+ * QJL Residual Correction).  A key keeps its b-bit MSE codes and norm (the
+ * codec above, b = its bits) plus one sign bit per sketch row of its residual
+ * and the residual's norm.  Readings fixed here (listed in the design notes):
+ *  - sketch S: m = d rows of iid N(0,1), the Gaussian stream of seed + 2
+ *    (orc_gaussian), rounded to fp32, row-major S[j][i];
+ *  - residual, in the rotated basis and scaled by sqrt(d) (power-of-two d):
+ *    rho_i = RN64(w_i 2^-24 - n16 c[code_i]) (one fma), rounded to fp32;
+ *  - sign bit j = 1 when t_j < 0, t_j = fp32 fma chain over i ascending of
+ *    S[j][i] rho_i (the decision is taken in fp32, in this order), packed
+ *    LSB-first, d / 8 bytes per vector;
+ *  - residual norm gamma = RN16(RN64(sqrt(G2 / d))), G2 = fp64 chain over i
+ *    ascending of rho_i^2 (exact products), so gamma = |k - k^_MSE|;
+ *  - estimator (unbiased, the QJL form): <q, k> ~ <q, k^_MSE>
+ *    + gamma sqrt(pi/2) / m sum_j z_j <S_j, R q>, z_j = +1 / -1 for bit 0 / 1.
+ *    (The page prints the correction with sign(<S_j, q>) and pi/(2m); that
+ *    product of two signs estimates an angle, not the inner product, and is
+ *    not unbiased as the page says the correction is: the unbiased QJL form is
+ *    taken.) */
+float *orc_qjl_sketch(int d, uint64_t seed)
+{
+    double *g = (double *)malloc(sizeof(double) * (size_t)d * d);
+    float *S = (float *)malloc(sizeof(float) * (size_t)d * d);
+    if (!g || !S) { free(g); free(S); return NULL; }
+    orc_gaussian((int64_t)d * d, seed + 2, g);
+    for (int64_t i = 0; i < (int64_t)d * d; ++i) S[i] = (float)g[i];
+    free(g);
+    return S;
+}
+
+void orc_qjl_sketch_copy(int d, uint64_t seed, float *out)
+{
+    float *S = orc_qjl_sketch(d, seed);
+    if (S) { memcpy(out, S, sizeof(float) * (size_t)d * d); free(S); }
+}
+
+/* Encode n vectors with the MSE codec c (power-of-two d) plus the QJL sketch of
+ * their residuals: codes / norms as orc_encode, signs [n][d/8] (row stride
+ * sign_stride bytes), rnorms [n] fp16. */
+int orc_encode_qjl(const orc_codec *c, uint64_t seed, const uint16_t *x, int64_t n, int64_t x_stride,
+                   uint8_t *codes, int64_t code_stride, uint16_t *norms, uint8_t *signs, int64_t sign_stride,
+                   uint16_t *rnorms)
+{
+    int d = c->d;
+    if (!c->is_wht || c->bits == 16) return -1;
+    if (orc_encode(c, x, n, x_stride, codes, code_stride, norms, NULL, NULL) != 0) return -1;
+    float *S = orc_qjl_sketch(d, seed);
+    double *w = (double *)malloc(sizeof(double) * d);
+    int32_t *cd = (int32_t *)malloc(sizeof(int32_t) * d);
+    float *rho = (float *)malloc(sizeof(float) * d);
+    if (!S || !w || !cd || !rho) { free(S); free(w); free(cd); free(rho); return -1; }
+    for (int64_t v = 0; v < n; ++v) {
+        double D, sc;
+        orc_rotate(c, x + v * x_stride, w, &D, &sc);
+        orc_unpack(codes + v * code_stride, d, c->bits, cd);
+        double n16 = orc_f16_to_f64(norms[v]);
+        double G2 = 0.0;
+        for (int i = 0; i < d; ++i) {
+            double r64 = fma(-n16, (double)c->c32[cd[i]], ldexp(w[i], -24));
+            rho[i] = (float)r64;
+            G2 = fma((double)rho[i], (double)rho[i], G2);
+        }
+        rnorms[v] = orc_f64_to_f16(sqrt(G2 / (double)d));
+        uint8_t *sg = signs + v * sign_stride;
+        memset(sg, 0, (size_t)d / 8);
+        for (int j = 0; j < d; ++j) {
+            float t = 0.0f;
+            for (int i = 0; i < d; ++i) t = fmaf(S[(int64_t)j * d + i], rho[i], t);
+            if (t < 0.0f) sg[j >> 3] |= (uint8_t)(1u << (j & 7));
+        }
+    }
+    free(S); free(w); free(cd); free(rho);
+    return 0;
+}
+
+/* Estimated inner products <q_g, k_n> (unscaled) of G queries [G][d] with len
+ * keys stored as MSE codes + norms + QJL signs + residual norms, fp64:
+ * <q, k^_MSE> + gamma sqrt(pi/2) / d sum_j z_j (S R q)_j. */
+int orc_qjl_scores(const orc_codec *ck, uint64_t seed, const uint16_t *q, int G, const uint8_t *k_codes,
+                   const uint16_t *k_norms, const uint8_t *k_signs, const uint16_t *k_rnorms, int64_t len,
+                   double *out)
+{
+    int d = ck->d;
+    if (!ck->is_wht || ck->bits == 16) return -1;
+    if (len <= 0) return 0;
+    int bpk = d * ck->bits / 8;
+    float *S = orc_qjl_sketch(d, seed);
+    double *Kh = (double *)malloc(sizeof(double) * (size_t)len * d);
+    double *rq = (double *)malloc(sizeof(double) * d);
+    double *u = (double *)malloc(sizeof(double) * d);
+    if (!S || !Kh || !rq || !u) { free(S); free(Kh); free(rq); free(u); return -1; }
+    orc_dequant(ck, k_codes, bpk, k_norms, len, Kh);
+    const double coef = sqrt(acos(-1.0) / 2.0) / (double)d;
+    for (int g = 0; g < G; ++g) {
+        const uint16_t *qg = q + (int64_t)g * d;
+        /* R q = H diag(s) q / sqrt(d), explicit matrix */
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i)
+                acc += (double)ck->H[(int64_t)j * d + i] * (double)ck->s[i] * orc_f16_to_f64(qg[i]);
+            rq[j] = acc / sqrt((double)d);
+        }
+        for (int j = 0; j < d; ++j) {
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += (double)S[(int64_t)j * d + i] * rq[i];
+            u[j] = acc;
+        }
+        for (int64_t t = 0; t < len; ++t) {
+            double mse = 0.0, corr = 0.0;
+            for (int i = 0; i < d; ++i) mse += orc_f16_to_f64(qg[i]) * Kh[t * d + i];
+            const uint8_t *sg = k_signs + t * (d / 8);
+            for (int j = 0; j < d; ++j) corr += ((sg[j >> 3] >> (j & 7)) & 1u) ? -u[j] : u[j];
+            out[(int64_t)g * len + t] = mse + orc_f16_to_f64(k_rnorms[t]) * coef * corr;
+        }
+    }
+    free(S); free(Kh); free(rq); free(u);
+    return 0;
+}
+
+/* Decode attention of G query heads over len keys stored with the QJL sketch
+ * (scores from orc_qjl_scores, times scale) and MSE-coded values: naive
+ * two-pass softmax, fp64.  len == 0 gives zeros. */
+int orc_attention_qjl_unit(const orc_codec *ck, uint64_t seed, const orc_codec *cv, const uint16_t *q, int G,
+                           const uint8_t *k_codes, const uint16_t *k_norms, const uint8_t *k_signs,
+                           const uint16_t *k_rnorms, const uint8_t *v_codes, const uint16_t *v_norms, int64_t len,
+                           double scale, double *out)
+{
+    int d = cv->d;
+    memset(out, 0, sizeof(double) * (size_t)G * d);
+    if (len <= 0) return 0;
+    double *sc = (double *)malloc(sizeof(double) * (size_t)G * len);
+    double *Vh = (double *)malloc(sizeof(double) * (size_t)len * d);
+    if (!sc || !Vh) { free(sc); free(Vh); return -1; }
+    if (orc_qjl_scores(ck, seed, q, G, k_codes, k_norms, k_signs, k_rnorms, len, sc) != 0 ||
+        orc_dequant(cv, v_codes, d * cv->bits / 8, v_norms, len, Vh) != 0) {
+        free(sc); free(Vh); return -1;
+    }
+    for (int g = 0; g < G; ++g) {
+        double *s = sc + (int64_t)g * len;
+        double mx = -INFINITY;
+        for (int64_t t = 0; t < len; ++t) { s[t] *= scale; if (s[t] > mx) mx = s[t]; }
+        double l = 0.0;
+        for (int64_t t = 0; t < len; ++t) { s[t] = exp(s[t] - mx); l += s[t]; }
+        for (int i = 0; i < d; ++i) {
+            double acc = 0.0;
+            for (int64_t t = 0; t < len; ++t) acc += s[t] * Vh[t * d + i];
+            out[(int64_t)g * d + i] = acc / l;
+        }
+    }
+    free(sc); free(Vh);
+    return 0;
+}
+
 /* Decode attention of G query heads over the first `len` cached tokens of one
  * (batch, KV head) unit followed by `n_tail` raw fp16 tokens (k_tail, v_tail,
  * [n_tail][d]): tokens kept unencoded -- the pending tokens that wait in fp16

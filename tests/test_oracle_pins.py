@@ -465,3 +465,75 @@ def test_multi_query_ignores_future_tokens_and_reduces_to_decode():
     ov = oracle.attention_multi_unit(ck, cv, q, kc, kn, vc, vn, 2, 0.2)
     np.testing.assert_array_equal(ov[:, :2], 0.0)
     np.testing.assert_allclose(ov[:, 2], np.repeat(cv.dequant(vc[:1], vn[:1]), 2, 0), rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------- QJL residual sketch
+def _rotation(ck):
+    # R = H diag(s) / sqrt(d) from scipy's Hadamard matrix and the oracle's signs
+    d = ck.dim
+    return scipy.linalg.hadamard(d).astype(np.float64) * ck.tables()["signs"].astype(np.float64)[None, :] / math.sqrt(d)
+
+
+def test_qjl_signs_and_residual_norm_match_an_independent_computation():
+    # Residual in the rotated basis from numpy (x - dequant(x), rotated by scipy's H) and the
+    # sketch product in float64: the fp32 sign decisions agree outside the fp32 rounding band,
+    # and the residual norm is the fp16 of |x - x^|.
+    d = 128
+    ck = oracle.Codec(d, 3, 42)
+    x = tq_inputs.fp16_normal(51, (64, d), tq_inputs.outlier_channels(d, 0))
+    codes, norms, signs, rn = ck.encode_qjl(x)
+    r = x.astype(np.float64) - ck.dequant(codes, norms)            # original basis
+    np.testing.assert_allclose(rn.astype(np.float64), np.linalg.norm(r, axis=1), rtol=2 ** -10, atol=0)
+    S = ck.qjl_sketch().astype(np.float64)
+    t = (r @ _rotation(ck).T) @ S.T * math.sqrt(d)                 # = S rho
+    band = 1e-5 * (np.abs(r @ _rotation(ck).T) @ np.abs(S).T) * math.sqrt(d)
+    bits = np.unpackbits(signs, axis=1, bitorder="little").astype(bool)
+    decided = np.abs(t) > band
+    assert decided.mean() > 0.999
+    np.testing.assert_array_equal(bits[decided], (t < 0)[decided])
+    # the sketch is the seed's Gaussian stream (seed + 2) rounded to fp32
+    np.testing.assert_array_equal(ck.qjl_sketch().ravel(), oracle.gaussian(d * d, 44).astype(np.float32))
+
+
+def test_qjl_estimator_is_unbiased_with_the_qjl_variance():
+    # Over rotation/sketch seeds, the estimate of <q, k> averages to the true inner product,
+    # and its spread matches the QJL variance |r|^2 / m ((pi/2) |q|^2 - <q, r^>^2): a wrong
+    # constant (pi/2m, 1/m), a sign flip or a missing |r| fails one of the two.
+    d = 64
+    x = tq_inputs.fp16_normal(61, (1, d))
+    q = tq_inputs.fp16_normal(62, (1, d))
+    true = float((q.astype(np.float64) @ x.astype(np.float64).T)[0, 0])
+    est, var = [], []
+    for seed in range(400):
+        ck = oracle.Codec(d, 2, 1000 + seed)
+        codes, norms, signs, rn = ck.encode_qjl(x)
+        est.append(ck.qjl_scores(q, codes, norms, signs, rn)[0, 0])
+        r = (x.astype(np.float64) - ck.dequant(codes, norms))[0]
+        qn = q.astype(np.float64)[0]
+        rh = r / np.linalg.norm(r)
+        var.append(float(r @ r) / d * (math.pi / 2 * float(qn @ qn) - float(qn @ rh) ** 2))
+    est = np.array(est)
+    sd = math.sqrt(np.mean(var))
+    assert abs(est.mean() - true) < 4 * sd / math.sqrt(len(est)), (est.mean(), true, sd)
+    assert 0.8 < est.var() / np.mean(var) < 1.25, (est.var(), np.mean(var))
+
+
+def test_qjl_correction_tracks_the_residual_inner_product():
+    # The correction term (estimate minus <q, k^_MSE>) of many keys follows the residual's
+    # inner product <q, k - k^_MSE> with slope 1 (least squares; averaged over sketch seeds,
+    # since one sketch's errors are shared by all keys) and positive correlation: a flipped
+    # sign-bit convention or a wrong scale fails it.
+    d = 64
+    x = tq_inputs.fp16_normal(71, (1000, d))
+    q = tq_inputs.fp16_normal(72, (1, d)).astype(np.float64)
+    slopes, cors = [], []
+    for seed in range(24):
+        ck = oracle.Codec(d, 2, 500 + seed)
+        codes, norms, signs, rn = ck.encode_qjl(x)
+        kh = ck.dequant(codes, norms)
+        corr = ck.qjl_scores(q.astype(np.float16), codes, norms, signs, rn)[0] - (kh @ q.T)[:, 0]
+        resid = ((x.astype(np.float64) - kh) @ q.T)[:, 0]
+        slopes.append(float(resid @ corr / (resid @ resid)))
+        cors.append(np.corrcoef(corr, resid)[0, 1])
+    assert min(cors) > 0.2
+    assert 0.88 < np.mean(slopes) < 1.12, (np.mean(slopes), np.std(slopes))
