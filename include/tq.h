@@ -258,6 +258,47 @@ tq_status tq_decode_attend_multi(const tq_codec *ck, const tq_codec *cv, const u
                                  void *stream);
 
 /*
+ * Keys with a QJL residual sketch (the TurboQuantProd variant, "How I built
+ * VeloxQuant-MLX", Stage 3: QJL Residual Correction): a key keeps its
+ * `bits`-bit MSE codes and norm, plus the sign bits of a Gaussian sketch of
+ * its quantisation residual (m = dim sketch rows, 1 bit each) and the
+ * residual's norm, and attention estimates <q, k> as
+ *   <q, k^_MSE> + |r| sqrt(pi/2) / m * sum_j z_j <S_j, R q>
+ * (unbiased; z_j = +1 / -1 for sign bit 0 / 1, R the codec's rotation).
+ *
+ * tq_codec_create_qjl: as tq_codec_create with bits in {2, 3, 4} (the MSE part)
+ *   and a power-of-two dim; S is the Gaussian stream of seed + 2 (Box-Muller on
+ *   SplitMix64, the dense rotation's generator) rounded to fp32, S[j][i].
+ *   tq_codec_export_sketch copies S (host, dim * dim floats).
+ * tq_encode_qjl: tq_encode of the MSE part, then per vector
+ *   rho_i = RN64(w_i 2^-24 - n16 c[code_i]) rounded to fp32 (w = H (s . k),
+ *   k = x 2^24 exact), sign bit j = [fp32 fma chain over i ascending of
+ *   S[j][i] rho_i < 0] (LSB-first, dim / 8 bytes per vector), and
+ *   rnorms = RN16(sqrt(G2 / dim)), G2 = fp64 chain over i ascending of rho_i^2.
+ *     signs   device [n_vec] rows of sign_row_stride bytes (a multiple of 4,
+ *             >= dim / 8), 4-byte aligned
+ *     rnorms  device fp16 [n_vec]
+ *   Other arguments and rules as tq_encode.
+ * tq_decode_attend_qjl: tq_decode_attend with the QJL estimator for the scores;
+ *   k_signs [B, n_kv_heads, max_seq, dim / 8], k_rnorms [B, n_kv_heads,
+ *   max_seq] fp16 beside the MSE codes and norms.  Runs on the SIMT kernel.
+ * A QJL codec passed to the other decode calls or to tq_cache_create is
+ * rejected (their keys carry no sketch); tq_encode / tq_encode_append with it
+ * write the MSE part only.
+ */
+tq_status tq_codec_create_qjl(int dim, int bits, uint64_t seed, tq_codec **out);
+tq_status tq_codec_export_sketch(const tq_codec *codec, float *sketch);
+tq_status tq_encode_qjl(const tq_codec *codec, const uint16_t *x, int64_t n_vec, int64_t x_row_stride,
+                        uint8_t *codes, int64_t code_row_stride, uint16_t *norms, uint8_t *signs,
+                        int64_t sign_row_stride, uint16_t *rnorms, void *stream);
+tq_status tq_decode_attend_qjl(const tq_codec *ck, const tq_codec *cv, const uint16_t *q,
+                               const uint8_t *k_codes, const uint16_t *k_norms, const uint8_t *k_signs,
+                               const uint16_t *k_rnorms, const uint8_t *v_codes, const uint16_t *v_norms,
+                               const int32_t *seq_lens, int B, int n_q_heads, int n_kv_heads,
+                               int64_t max_seq, float scale, uint16_t *out, void *workspace,
+                               size_t ws_bytes, void *stream);
+
+/*
  * Two-phase KV cache of one layer for B sequences of equal length ("add
  * TurboQuant KV cache compression", Design; the update / attend / memory
  * interface of "How I built VeloxQuant-MLX"): prefill tokens are kept as raw

@@ -19,7 +19,8 @@ __all__ = [
     "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
     "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail",
-    "tq_decode_attend_multi", "tq_decode_attend_multi_workspace_bytes", "parse_scheme", "bytes_per_vec",
+    "tq_decode_attend_multi", "tq_decode_attend_multi_workspace_bytes", "tq_codec_create_qjl",
+    "tq_codec_export_sketch", "tq_encode_qjl", "tq_decode_attend_qjl", "parse_scheme", "bytes_per_vec",
     "LIB_PATH", "KVCache", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
 ]
 
@@ -55,6 +56,11 @@ _sig = {
     "tq_decode_attend_multi_workspace_bytes": (_sz, [_i32, _i32, _i32, _i32, _i64, _i32]),
     "tq_decode_attend_multi": (_i32, [_vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64, _vp, _vp,
                                       _vp, _i32, C.c_float, _vp, _vp, C.c_size_t, _vp]),
+    "tq_codec_create_qjl": (_i32, [_i32, _i32, _u64, C.POINTER(_vp)]),
+    "tq_codec_export_sketch": (_i32, [_vp, _vp]),
+    "tq_encode_qjl": (_i32, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
+    "tq_decode_attend_qjl": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64,
+                                    C.c_float, _vp, _vp, _sz, _vp]),
     "tq_cache_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, C.POINTER(_vp)]),
     "tq_cache_destroy": (None, [_vp]),
     "tq_cache_prefill": (_i32, [_vp, _vp, _vp, _i32, _vp]),
@@ -153,6 +159,22 @@ def tq_codec_create(dim: int, bits: int, seed: int) -> Codec:
     return Codec(h.value)
 
 
+def tq_codec_create_qjl(dim: int, bits: int, seed: int) -> Codec:
+    """Key codec of the QJL-residual variant: `bits`-bit MSE codes + a dim-row sign sketch."""
+    h = _vp()
+    _check(_lib.tq_codec_create_qjl(dim, bits, C.c_uint64(seed), C.byref(h)), "tq_codec_create_qjl")
+    c = Codec(h.value)
+    c.qjl = True
+    return c
+
+
+def tq_codec_export_sketch(codec: Codec):
+    import numpy as np
+    S = np.zeros((codec.dim, codec.dim), dtype=np.float32)
+    _check(_lib.tq_codec_export_sketch(codec.handle, S.ctypes.data), "tq_codec_export_sketch")
+    return S
+
+
 def tq_codec_destroy(codec: Codec):
     codec.close()
 
@@ -188,6 +210,24 @@ def tq_encode(codec: Codec, x: torch.Tensor, codes: torch.Tensor, norms: torch.T
     _check(_lib.tq_encode(codec.handle, _dev(x, torch.float16, "x"), n, x.stride(0),
                           _dev(codes, torch.uint8, "codes"), codes.stride(0), _dev(norms, torch.float16, "norms"),
                           _stream(stream)), "tq_encode")
+
+
+def tq_encode_qjl(codec: Codec, x: torch.Tensor, codes: torch.Tensor, norms: torch.Tensor, signs: torch.Tensor,
+                  rnorms: torch.Tensor, stream=None):
+    """tq_encode plus the QJL residual sketch: signs [n, >=dim/8] uint8 (row stride a multiple
+    of 4), rnorms [n] fp16."""
+    n = x.shape[0]
+    if x.dim() != 2 or x.shape[1] != codec.dim or x.stride(1) != 1:
+        raise ValueError("x must be [n, dim] with unit inner stride")
+    for t, nm in ((codes, "codes"), (signs, "signs")):
+        if t.dim() != 2 or t.shape[0] != n or t.stride(1) != 1:
+            raise ValueError(f"{nm} must be [n, bytes] with unit inner stride")
+    if norms.numel() != n or rnorms.numel() != n:
+        raise ValueError("norms / rnorms must have n elements")
+    _check(_lib.tq_encode_qjl(codec.handle, _dev(x, torch.float16, "x"), n, x.stride(0),
+                              _dev(codes, torch.uint8, "codes"), codes.stride(0), _dev(norms, torch.float16, "norms"),
+                              _dev(signs, torch.uint8, "signs"), signs.stride(0),
+                              _dev(rnorms, torch.float16, "rnorms"), _stream(stream)), "tq_encode_qjl")
 
 
 def tq_encode_append(codec: Codec, x: torch.Tensor, start_pos: torch.Tensor, codes: torch.Tensor,
@@ -336,6 +376,31 @@ def tq_decode_attend_multi(ck: Codec, cv: Codec, q: torch.Tensor, k: torch.Tenso
                                        float(scale), _dev(out, torch.float16, "out"),
                                        _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
                                        _stream(stream)), "tq_decode_attend_multi")
+
+
+def tq_decode_attend_qjl(ck: Codec, cv: Codec, q: torch.Tensor, k_codes: torch.Tensor, k_norms: torch.Tensor,
+                         k_signs: torch.Tensor, k_rnorms: torch.Tensor, v_codes: torch.Tensor,
+                         v_norms: torch.Tensor, seq_lens: torch.Tensor, out: torch.Tensor, workspace: torch.Tensor,
+                         scale: float | None = None, stream=None):
+    """tq_decode_attend with QJL-sketched keys: k_signs [B, Hkv, S, dim/8] uint8 and
+    k_rnorms [B, Hkv, S] fp16 beside the MSE codes and norms."""
+    B, Hq, d = q.shape
+    Hkv, S = v_codes.shape[1], v_codes.shape[2]
+    for t, nm in ((q, "q"), (k_codes, "k_codes"), (k_norms, "k_norms"), (k_signs, "k_signs"),
+                  (k_rnorms, "k_rnorms"), (v_codes, "v_codes"), (v_norms, "v_norms"), (seq_lens, "seq_lens"),
+                  (out, "out"), (workspace, "workspace")):
+        _contig(t, nm)
+    if tuple(k_signs.shape) != (B, Hkv, S, d // 8):
+        raise ValueError("k_signs must be [B, Hkv, max_seq, dim/8]")
+    if scale is None:
+        scale = d ** -0.5
+    _check(_lib.tq_decode_attend_qjl(ck.handle, cv.handle, _dev(q, torch.float16, "q"),
+                                     _dev(k_codes, torch.uint8, "k_codes"), _dev(k_norms, torch.float16, "k_norms"),
+                                     _dev(k_signs, torch.uint8, "k_signs"), _dev(k_rnorms, torch.float16, "k_rnorms"),
+                                     _dev(v_codes, torch.uint8, "v_codes"), _dev(v_norms, torch.float16, "v_norms"),
+                                     _dev(seq_lens, torch.int32, "seq_lens"), B, Hq, Hkv, S, float(scale),
+                                     _dev(out, torch.float16, "out"), _dev(workspace, torch.uint8, "workspace"),
+                                     workspace.numel(), _stream(stream)), "tq_decode_attend_qjl")
 
 
 class KVCache:

@@ -31,8 +31,12 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
                              const int32_t* seq_lens, int B, int n_q_heads, int n_kv_heads, int L,
                              int64_t max_seq, const uint16_t* k_tail, const uint16_t* v_tail,
                              const int32_t* tail_lens, int max_tail, float scale, uint16_t* out, void* workspace,
-                             size_t ws_bytes, void* stream) {
-    if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
+                             size_t ws_bytes, void* stream, const uint8_t* k_signs = nullptr,
+                             const uint16_t* k_rnorms = nullptr) {
+    if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim || cv->qjl) return TQ_ERR_INVALID_ARG;
+    // keys with the QJL sketch come with their sign bits and residual norms, others without
+    if (bool(ck->qjl) != (k_signs != nullptr) || bool(ck->qjl) != (k_rnorms != nullptr)) return TQ_ERR_INVALID_ARG;
+    if (k_signs && (!aligned(k_signs, 4) || !aligned(k_rnorms, 2))) return TQ_ERR_INVALID_ARG;
     if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
     if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
     if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
@@ -53,10 +57,10 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
     tq::DecodeArgs a{tq::dev_view(ck), tq::dev_view(cv), q, k, k_norms, v_codes, v_norms, seq_lens,
                      B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace,
                      tail_lens ? k_tail : nullptr, tail_lens ? v_tail : nullptr, tail_lens,
-                     tail_lens ? max_tail : 0, 0, nullptr, nullptr, L};
+                     tail_lens ? max_tail : 0, 0, nullptr, nullptr, k_signs, k_rnorms, L};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
-    if (tq::decode_mma_supported(ck, cv)) {
+    if (!ck->qjl && tq::decode_mma_supported(ck, cv)) {
         p.kernel = 1;
         e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
     }
@@ -83,6 +87,20 @@ tq_status tq_encode(const tq_codec* c, const uint16_t* x, int64_t n_vec, int64_t
     if (!aligned(norms, 2) || !on_codec_device(c)) return TQ_ERR_INVALID_ARG;
     return from_cuda(tq::launch_encode(c, x, n_vec, x_row_stride, codes, code_row_stride, norms, 0, 0, 0, nullptr,
                                        0, nullptr, static_cast<cudaStream_t>(stream)));
+}
+
+tq_status tq_encode_qjl(const tq_codec* c, const uint16_t* x, int64_t n_vec, int64_t x_row_stride, uint8_t* codes,
+                        int64_t code_row_stride, uint16_t* norms, uint8_t* signs, int64_t sign_row_stride,
+                        uint16_t* rnorms, void* stream) {
+    if (!c || !c->qjl || n_vec < 0) return TQ_ERR_INVALID_ARG;
+    if (n_vec == 0) return TQ_OK;
+    if (!signs || !rnorms || !aligned(signs, 4) || (sign_row_stride & 3) || sign_row_stride < c->dim / 8 ||
+        !aligned(rnorms, 2))
+        return TQ_ERR_INVALID_ARG;
+    tq_status s = tq_encode(c, x, n_vec, x_row_stride, codes, code_row_stride, norms, stream);
+    if (s != TQ_OK) return s;
+    return from_cuda(tq::launch_qjl_sketch(c, x, n_vec, x_row_stride, codes, code_row_stride, norms, signs,
+                                           sign_row_stride, rnorms, static_cast<cudaStream_t>(stream)));
 }
 
 tq_status tq_encode_append(const tq_codec* c, const uint16_t* x, int B, int n_kv_heads, int T,
@@ -162,6 +180,17 @@ tq_status tq_decode_attend_multi(const tq_codec* ck, const tq_codec* cv, const u
     return decode_attend_impl(ck, cv, q, k, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, L,
                               max_seq, k_tail, v_tail, tail_lens, max_tail, scale, out, workspace, ws_bytes,
                               stream);
+}
+
+tq_status tq_decode_attend_qjl(const tq_codec* ck, const tq_codec* cv, const uint16_t* q, const uint8_t* k_codes,
+                               const uint16_t* k_norms, const uint8_t* k_signs, const uint16_t* k_rnorms,
+                               const uint8_t* v_codes, const uint16_t* v_norms, const int32_t* seq_lens, int B,
+                               int n_q_heads, int n_kv_heads, int64_t max_seq, float scale, uint16_t* out,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    if (!ck || !ck->qjl || !k_signs || !k_rnorms) return TQ_ERR_INVALID_ARG;
+    return decode_attend_impl(ck, cv, q, k_codes, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, 1,
+                              max_seq, nullptr, nullptr, nullptr, 0, scale, out, workspace, ws_bytes, stream,
+                              k_signs, k_rnorms);
 }
 
 tq_status tq_get_device_error(void* error_word, void* stream, int* code) {

@@ -107,6 +107,7 @@ tq_status tq_cache_create(const tq_codec* ck, const tq_codec* cv, int B, int n_q
     if (!out) return TQ_ERR_INVALID_ARG;
     *out = nullptr;
     if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
+    if (ck->qjl || cv->qjl) return TQ_ERR_UNSUPPORTED;  // the cache keeps MSE-coded keys only
     if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;
     if (max_seq <= 0 || max_seq % 8 != 0 || max_seq > (int64_t(1) << 30)) return TQ_ERR_INVALID_ARG;
     int dev = -1;
@@ -194,7 +195,7 @@ tq_status tq_cache_decode(tq_cache* c, const uint16_t* q, const uint16_t* k_new,
     if (c->ws_bytes < p.ws_bytes) return TQ_ERR_WORKSPACE;
     tq::DecodeArgs a{tq::dev_view(c->ck), tq::dev_view(c->cv), q, c->kc, c->kn, c->vc, c->vn, c->d_count,
                      c->B, c->Hq, c->Hkv, c->max_seq, scale, out, c->ws,
-                     c->pk, c->pv, nullptr, kPending, c->pending, k_new, v_new, 1};
+                     c->pk, c->pv, nullptr, kPending, c->pending, k_new, v_new, nullptr, nullptr, 1};
     e = cudaErrorNotSupported;
     if (tq::decode_mma_supported(c->ck, c->cv)) {
         p.kernel = 1;

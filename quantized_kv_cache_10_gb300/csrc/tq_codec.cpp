@@ -62,19 +62,24 @@ void rademacher_signs(int dim, uint64_t seed, std::vector<int8_t>& s) {
 // Gaussian matrix from Box-Muller on 53-bit uniforms u1 in (0,1], u2 in [0,1),
 // filled row-major; then Q from Householder QR with diag(R) > 0 (the unique
 // QR factor).  z = Q k.  Returns 0 on success.
-int dense_rotation(int dim, uint64_t seed, std::vector<float>& qout) {
-    const int d = dim;
-    const size_t dd = size_t(d) * d;
-    std::vector<double> A(dd);
+void gaussian_stream(size_t n, uint64_t seed, std::vector<double>& A) {
+    A.resize(n);
     SplitMix64 g(seed);
     const double two_pi = 6.283185307179586476925286766559;
-    for (size_t i = 0; i < dd; i += 2) {
+    for (size_t i = 0; i < n; i += 2) {
         double u1 = double((g.next() >> 11) + 1) * 0x1.0p-53;
         double u2 = double(g.next() >> 11) * 0x1.0p-53;
         double r = std::sqrt(-2.0 * std::log(u1));
         A[i] = r * std::cos(two_pi * u2);
-        if (i + 1 < dd) A[i + 1] = r * std::sin(two_pi * u2);
+        if (i + 1 < n) A[i + 1] = r * std::sin(two_pi * u2);
     }
+}
+
+int dense_rotation(int dim, uint64_t seed, std::vector<float>& qout) {
+    const int d = dim;
+    const size_t dd = size_t(d) * d;
+    std::vector<double> A;
+    gaussian_stream(dd, seed, A);
     // Householder: A (row-major, A[i*d + j]) -> R in the upper triangle.
     std::vector<double> V(dd, 0.0);  // reflector k stored in V[k*d + i], i >= k
     for (int k = 0; k < d; ++k) {
@@ -214,6 +219,8 @@ void free_device(tq_codec* c) {
     cudaFree(c->d_qt);
     cudaFree(c->d_ktab);
     cudaFree(c->d_vtab);
+    cudaFree(c->d_sketch);
+    cudaFree(c->d_sketch_t);
 }
 
 }  // namespace
@@ -299,6 +306,39 @@ tq_status tq_codec_create(int dim, int bits, uint64_t seed, tq_codec** out) {
         return e == cudaErrorMemoryAllocation ? TQ_ERR_OOM : TQ_ERR_CUDA;
     }
     *out = c;
+    return TQ_OK;
+}
+
+tq_status tq_codec_create_qjl(int dim, int bits, uint64_t seed, tq_codec** out) {
+    if (!out) return TQ_ERR_INVALID_ARG;
+    *out = nullptr;
+    if ((dim & (dim - 1)) != 0 || !(bits == 2 || bits == 3 || bits == 4)) return TQ_ERR_INVALID_ARG;
+    tq_codec* c = nullptr;
+    tq_status s = tq_codec_create(dim, bits, seed, &c);
+    if (s != TQ_OK) return s;
+    // S: the Gaussian stream of seed + 2 ("How I built VeloxQuant-MLX", Stage 3: a random
+    // Johnson-Lindenstrauss projection of the residual), rounded to fp32
+    std::vector<double> g;
+    tq::gaussian_stream(size_t(dim) * dim, seed + 2, g);
+    c->sketch.resize(g.size());
+    for (size_t i = 0; i < g.size(); ++i) c->sketch[i] = float(g[i]);
+    std::vector<float> st(c->sketch.size());
+    for (int j = 0; j < dim; ++j)
+        for (int i = 0; i < dim; ++i) st[size_t(i) * dim + j] = c->sketch[size_t(j) * dim + i];
+    cudaError_t e = upload(&c->d_sketch, c->sketch.data(), c->sketch.size());
+    if (e == cudaSuccess) e = upload(&c->d_sketch_t, st.data(), st.size());
+    if (e != cudaSuccess) {
+        tq_codec_destroy(c);
+        return e == cudaErrorMemoryAllocation ? TQ_ERR_OOM : TQ_ERR_CUDA;
+    }
+    c->qjl = 1;
+    *out = c;
+    return TQ_OK;
+}
+
+tq_status tq_codec_export_sketch(const tq_codec* c, float* sketch) {
+    if (!c || !sketch || !c->qjl) return TQ_ERR_INVALID_ARG;
+    std::memcpy(sketch, c->sketch.data(), c->sketch.size() * sizeof(float));
     return TQ_OK;
 }
 

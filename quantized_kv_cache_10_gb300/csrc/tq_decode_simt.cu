@@ -46,6 +46,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     float* wl = wm + kWarps * kGP;       // [kWarps][kGP]
     float* cm = wl + kWarps * kGP;       // [kGP]
     float* cl = cm + kGP;                // [kGP]
+    float* uq = cl + kGP;                // [kGP][d] S q' (keys with the QJL sketch)
 
     allow_dependent_launch();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -74,6 +75,22 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     for (int i = tid; i < (1 << a.cv.bits); i += kThreads) ctv[i] = __ldg(a.cv.centroids + i);
     for (int i = tid; i < kGP * d; i += kThreads) so[i] = 0.0f;
     __syncthreads();
+    const bool qjl = a.ck.sketch != nullptr;
+    if (qjl) {
+        // u = S q' per query row: the sketch of the rotated, scaled query ("How I built
+        // VeloxQuant-MLX", Stage 3: the correction reads <S_j, q> for every sketch row j)
+        for (int idx = tid; idx < Gc * d; idx += kThreads) {
+            const int g = idx / d, j = idx - (idx / d) * d;
+            const float* srow = a.ck.sketch + static_cast<int64_t>(j) * d;
+            float acc = 0.0f;
+            for (int i = 0; i < d; ++i) acc = fmaf(__ldg(srow + i), qs[g * d + i], acc);
+            uq[idx] = acc;
+        }
+        __syncthreads();
+    }
+    // QJL correction in score units: gamma sqrt(pi/2) / m * sqrt(d) with m = d sketch rows
+    // (q' carries 1 / sqrt(d) of the rotation's scale)
+    const float qjl_coef = 1.2533141373155003f * rsqrtf(static_cast<float>(d));
 
     float m[kGP], l[kGP], o[kGP][E];
 #pragma unroll
@@ -99,16 +116,38 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
             nk = __half2float(__ushort_as_half(a.k_norms[row0 + t]));
         }
         float s[kGP];
+        if (qjl) {
+            // <q, k^_MSE> + gamma sqrt(pi/2) / m sum_j z_j <S_j, R q>, this lane's E dims
+            const uint32_t zb = static_cast<uint32_t>(code_at(a.k_signs + (row0 + t) * (d / 8), lane, E));
+            const float gk = __half2float(__ushort_as_half(a.k_rnorms[row0 + t])) * qjl_coef;
 #pragma unroll
-        for (int g = 0; g < kGP; ++g) {
-            float part = 0.0f;
-            if (g < Gc) {
+            for (int g = 0; g < kGP; ++g) {
+                float part = 0.0f, zq = 0.0f;
+                if (g < Gc) {
 #pragma unroll
-                for (int e = 0; e < E; ++e) part = fmaf(qs[g * d + lane * E + e], kv[e], part);
+                    for (int e = 0; e < E; ++e) {
+                        part = fmaf(qs[g * d + lane * E + e], kv[e], part);
+                        const float u = uq[g * d + lane * E + e];
+                        zq += ((zb >> e) & 1u) ? -u : u;
+                    }
+                    part = fmaf(gk, zq, part * nk);
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
+                    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
+                }
+                s[g] = part;
             }
-            s[g] = part * nk;
+        } else {
+#pragma unroll
+            for (int g = 0; g < kGP; ++g) {
+                float part = 0.0f;
+                if (g < Gc) {
+#pragma unroll
+                    for (int e = 0; e < E; ++e) part = fmaf(qs[g * d + lane * E + e], kv[e], part);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
+                }
+                s[g] = part * nk;
+            }
         }
         bool seen[kGP];
 #pragma unroll
@@ -172,7 +211,7 @@ __global__ void __launch_bounds__(kThreads) decode_simt_kernel(const DecodeArgs 
     write_partial(a, p, vu, split, so, cm, cl, tid, kThreads);
 }
 
-size_t simt_smem_bytes(int d) { return sizeof(float) * (size_t(kGP) * d * 2 + 512 + 2 * kWarps * kGP + 2 * kGP); }
+size_t simt_smem_bytes(int d) { return sizeof(float) * (size_t(kGP) * d * 3 + 512 + 2 * kWarps * kGP + 2 * kGP); }
 
 template <int E>
 cudaError_t launch_simt_e(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {

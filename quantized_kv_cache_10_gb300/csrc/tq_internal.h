@@ -40,6 +40,12 @@ struct tq_codec {
     int vtab_words = 0;
     float k_alpha = 1.0f;   // d_ktab holds fp16(k_alpha * c): the kernel scales q' by 1 / k_alpha
     float v_alpha = 1.0f;   // d_vtab holds fp16(v_alpha * c): the kernel scales its output by 1 / v_alpha
+    // QJL residual sketch (keys of the TurboQuantProd variant, power-of-two dim): m = dim
+    // rows of iid N(0,1) from the Gaussian stream of seed + 2, rounded to fp32
+    int qjl = 0;
+    std::vector<float> sketch;        // [dim*dim] S row-major, S[j][i]
+    float* d_sketch = nullptr;        // S
+    float* d_sketch_t = nullptr;      // S^T row-major: S^T[i][j] = S[j][i]
 };
 
 namespace tq {
@@ -47,6 +53,7 @@ namespace tq {
 // Host-side codebook / rotation construction (tq_codec.cpp).
 void lloyd_max_gaussian(int bits, std::vector<double>& c64);
 int dense_rotation(int dim, uint64_t seed, std::vector<float>& q);
+void gaussian_stream(size_t n, uint64_t seed, std::vector<double>& out);
 void rademacher_signs(int dim, uint64_t seed, std::vector<int8_t>& s);
 
 int num_sms(int device);
@@ -61,6 +68,12 @@ cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64
 
 cudaError_t launch_dequant(const tq_codec* c, const uint8_t* codes, const uint16_t* norms,
                            int64_t n, float* out, cudaStream_t st);
+
+// QJL residual sketch of n vectors already encoded (codes, norms) with the codec's
+// MSE part: sign bits [n][sign_stride bytes] and residual norms [n] (tq_qjl.cu).
+cudaError_t launch_qjl_sketch(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride,
+                              const uint8_t* codes, int64_t cstride, const uint16_t* norms, uint8_t* signs,
+                              int64_t sstride, uint16_t* rnorms, cudaStream_t st);
 
 // Split-K plan for decode attention, shared by the workspace-size query and
 // the launcher so both agree for a given device and shape.
@@ -92,11 +105,12 @@ struct DevCodec {
     const uint32_t* ktab;
     const uint32_t* vtab;
     float k_alpha, v_alpha;
+    const float* sketch;  // QJL sketch S [dim][dim] (keys of the TurboQuantProd variant), else null
 };
 
 inline DevCodec dev_view(const tq_codec* c) {
     return DevCodec{c->dim, c->bits, c->is_wht, c->bytes_per_vec, c->d_centroids, c->d_sign_bits, c->d_q,
-                    c->d_qt, c->d_ktab, c->d_vtab, c->k_alpha, c->v_alpha};
+                    c->d_qt, c->d_ktab, c->d_vtab, c->k_alpha, c->v_alpha, c->qjl ? c->d_sketch : nullptr};
 }
 
 struct DecodeArgs {
@@ -124,6 +138,10 @@ struct DecodeArgs {
     // (written at tail index tail_n into k_tail / v_tail) in the same launch
     const uint16_t* k_new;
     const uint16_t* v_new;
+    // keys of the TurboQuantProd variant (ck.sketch set): sign bits of the residual's
+    // sketch [B, Hkv, max_seq, dim/8] and residual norms [B, Hkv, max_seq] fp16
+    const uint8_t* k_signs;
+    const uint16_t* k_rnorms;
     // query positions per query head: q and out are [B, Hq, L, dim]; the queries are the
     // last L positions of each sequence (packed tokens, then tail tokens) and each attends
     // to the tokens up to its own position (L == 1: every token)
