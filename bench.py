@@ -457,6 +457,56 @@ def gpu_arm(args):
         multi = {"query_positions": LQ, "fp16_tail_tokens": LQ, "call_us": m_us,
                  "packed_GBps": bytes_step / (m_us * 1e-6) / 1e9}
 
+    # keys with the QJL residual sketch (TurboQuantProd: 3-bit MSE codes + 1 sign bit per
+    # sketch row + residual norm) on the same shape, values as above
+    qjl = None
+    if replica_mode and graphs and (w.d & (w.d - 1)) == 0:
+        qb = 3
+        cq = tq.tq_codec_create_qjl(w.d, qb, w.rot_seed)
+        qkc = torch.empty((R, w.B, w.Hkv, w.S, cq.bytes_per_vec), dtype=torch.uint8, device=dev)
+        qkn = torch.empty((R, w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
+        qks = torch.empty((R, w.B, w.Hkv, w.S, w.d // 8), dtype=torch.uint8, device=dev)
+        qkr = torch.empty((R, w.B, w.Hkv, w.S), dtype=torch.float16, device=dev)
+        Kd = torch.from_numpy(K).to(dev)
+        qenc = []
+        for i in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            tq.tq_encode_qjl(cq, Kd.view(n, w.d), qkc[0].view(n, -1), qkn[0].view(-1), qks[0].view(n, -1),
+                             qkr[0].view(-1))
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if i > 0:
+                qenc.append(e0.elapsed_time(e1) * 1e-3)
+        del Kd
+        for r in range(1, R):
+            qkc[r].copy_(qkc[0])
+            qkn[r].copy_(qkn[0])
+            qks[r].copy_(qks[0])
+            qkr[r].copy_(qkr[0])
+
+        def attend_qjl(i):
+            r = i % R
+            tq.tq_decode_attend_qjl(cq, cv, q, qkc[r], qkn[r], qks[r], qkr[r], vc[r], vn[r], lens, out, wsb)
+
+        gq = capture(attend_qjl, PB)
+        gq.replay()
+        torch.cuda.synchronize()
+        reps = max(4, args.steps // (4 * PB))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for j in range(reps):
+            gq.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        q_us = e0.elapsed_time(e1) * 1e3 / (reps * PB)
+        qbytes = int(w.lengths().astype(np.int64).sum()) * w.Hkv * (
+            cq.bytes_per_vec + 2 + w.d // 8 + 2 + cv.bytes_per_vec + 2)
+        qjl = {"k_mse_bits": qb, "sketch_rows": w.d, "packed_bytes": qbytes, "call_us": q_us,
+               "GBps": qbytes / (q_us * 1e-6) / 1e9, "kernel": "tensor-core (mma.sync)",
+               "encode_Mvec_s": n / statistics.median(qenc) / 1e6}
+        del qkc, qkn, qks, qkr
+
     # one call on its own after an L2 flush (latency of an isolated decode step)
     iso = []
     for i in range(16):
@@ -547,6 +597,7 @@ def gpu_arm(args):
         "isolated_call_us": statistics.median(iso),
         "with_fp16_tail": {"tail_tokens": 63, "call_us": tail_us},
         "multi_query": multi,
+        "qjl": qjl,
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,

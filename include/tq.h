@@ -281,7 +281,9 @@ tq_status tq_decode_attend_multi(const tq_codec *ck, const tq_codec *cv, const u
  *   Other arguments and rules as tq_encode.
  * tq_decode_attend_qjl: tq_decode_attend with the QJL estimator for the scores;
  *   k_signs [B, n_kv_heads, max_seq, dim / 8], k_rnorms [B, n_kv_heads,
- *   max_seq] fp16 beside the MSE codes and norms.  Runs on the SIMT kernel.
+ *   max_seq] fp16 beside the MSE codes and norms (16-byte aligned for the
+ *   tensor-core kernel; other alignments, and more than 8 query heads per KV
+ *   head, run on the SIMT kernel).
  * A QJL codec passed to the other decode calls or to tq_cache_create is
  * rejected (their keys carry no sketch); tq_encode / tq_encode_append with it
  * write the MSE part only.

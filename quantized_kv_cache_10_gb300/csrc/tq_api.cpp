@@ -60,7 +60,7 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
                      tail_lens ? max_tail : 0, 0, nullptr, nullptr, k_signs, k_rnorms, L};
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
-    if (!ck->qjl && tq::decode_mma_supported(ck, cv)) {
+    if (tq::decode_mma_supported(ck, cv)) {
         p.kernel = 1;
         e = tq::launch_decode_mma(a, p, st);  // may shrink the split plan
     }

@@ -183,6 +183,17 @@ template <>
 cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
+    // query rows per CTA, min(S, 8): up to 4 (one n-tile, hi/lo columns of q) or 5..8;
+    // codes 3 and 4 are the same for the instantiation with several query positions or
+    // row groups per unit (causal masks, fp16 hi/lo split of P), 5 and 6 for keys with
+    // the QJL sketch (one row group, one query position, 16-byte aligned sketch fields)
+    const bool multi = p.L > 1 || p.q_chunks > 1;
+    int nt = (p.S > 4 ? 2 : 1) + (multi ? 2 : 0);
+    if (a.k_signs) {
+        const auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
+        if (multi || !al16(a.k_signs) || !al16(a.k_rnorms)) return cudaErrorNotSupported;  // SIMT
+        nt = (p.S > 4 ? 2 : 1) + 4;
+    }
     // one CTA per SM: as many splits per (batch, KV head) as fill the SMs once
     const DecodePlan p0 = p;
     int dev = 0;
@@ -203,17 +214,16 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
         p.n_split = static_cast<int>(ns);
         p.chunk = chunk;
     }
-    // query rows per CTA, min(S, 8): up to 4 (one n-tile, hi/lo columns of q) or 5..8;
-    // codes 3 and 4 are the same for the instantiation with several query positions or
-    // row groups per unit (causal masks, fp16 hi/lo split of P)
-    const int nt = (p.S > 4 ? 2 : 1) + ((p.L > 1 || p.q_chunks > 1) ? 2 : 0);
+    cudaError_t e = cudaErrorNotSupported;
     switch (a.cv.dim) {
-        case 64: return launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st);
-        case 96: return launch_mma_d_extern<96>(a, p, a.ck.bits, a.cv.bits, nt, st);
-        case 128: return launch_mma_d_extern<128>(a, p, a.ck.bits, a.cv.bits, nt, st);
-        case 256: return launch_mma_d_extern<256>(a, p, a.ck.bits, a.cv.bits, nt, st);
-        default: return cudaErrorNotSupported;
+        case 64: e = launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+        case 96: e = launch_mma_d_extern<96>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+        case 128: e = launch_mma_d_extern<128>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+        case 256: e = launch_mma_d_extern<256>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+        default: break;
     }
+    if (e == cudaErrorNotSupported) p = p0;  // the caller falls back with its own plan
+    return e;
 }
 
 }  // namespace tq

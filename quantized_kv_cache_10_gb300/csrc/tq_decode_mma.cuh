@@ -204,16 +204,18 @@ constexpr int al1024(int x) { return (x + 1023) / 1024 * 1024; }
 constexpr int nwc_for(int D, int KB) { return KB == 16 ? 4 : (KB == 8 && D <= 128) ? 8 : 11; }
 
 // Bytes of one stage of ts tokens: K codes (raw K: D/64 swizzled column blocks
-// of ts rows x 128 B, each 1024-byte aligned), V codes, K norms, V norms.
-constexpr int stage_bytes(int D, int KB, int VB, int ts) {
+// of ts rows x 128 B, each 1024-byte aligned), V codes, K norms, V norms, and
+// for keys with the QJL sketch their sign bits and residual norms.
+constexpr int stage_bytes(int D, int KB, int VB, int ts, bool qjl = false) {
     return KB == 16 ? al1024((D / 64) * al1024(ts * 128) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2))
-                    : al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2);
+                    : al128(ts * D * KB / 8 + 16) + al128(ts * D * VB / 8 + 16) + 2 * al128(ts * 2) +
+                          (qjl ? al128(ts * D / 8) + al128(ts * 2) : 0);
 }
 
 // Shared-memory layout of one (D, K bits, V bits) instantiation; the same
 // function serves the kernel (constexpr) and the host's support test.
 struct Layout {
-    int nwc, krows, vrows, ktab, vtab, kw, vw, pro, bqb, fixed, mt, ts, stage, nstage, smem;
+    int nwc, krows, vrows, ktab, vtab, kw, vw, pro, bqb, ubq, fixed, mt, ts, stage, nstage, smem;
     // 8-bit K ("table block"): both lookup tables share one 64 KB block at the
     // fixed shared address kTBlock -- K in the first 128 B of each 256-B row, V
     // in the second -- so that a byte permute forms a whole K address and one
@@ -229,7 +231,7 @@ struct Layout {
 constexpr int kSmemBase = 1024;
 constexpr int kTBlock = 65536;
 
-constexpr Layout make_layout(int D, int KB, int VB);
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false);
 
 constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
     Layout L{};
@@ -263,7 +265,7 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
     return L;
 }
 
-constexpr Layout make_layout(int D, int KB, int VB) {
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl) {
     if (KB == 8) {
         // the table block, when it holds at least as many stages as the linear layout would
         const Layout t2 = make_tblock_layout(D, KB, VB, 2), t1 = make_tblock_layout(D, KB, VB, 1);
@@ -284,14 +286,17 @@ constexpr Layout make_layout(int D, int KB, int VB) {
     L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
     // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
     // per (k-tile, n-tile)) instead of registers
-    L.bqb = (D > 128) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    // (also with the QJL sketch, whose own fragments and per-row values need the registers)
+    L.bqb = (D > 128 || qjl) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    // keys with the QJL sketch: the B fragments of u = S q' (D / 16 k-tiles, up to two n-tiles)
+    L.ubq = qjl ? (D / 16) * 2 * 256 : 0;
     // (+1024 for raw K: the ring is aligned to 1024 B at run time)
-    L.fixed = L.ktab + L.vtab + kGP * D * 4 + 1024 + L.pro + L.bqb + (KB == 16 ? 1024 : 0);
+    L.fixed = L.ktab + L.vtab + kGP * D * 4 + 1024 + L.pro + L.bqb + L.ubq + (KB == 16 ? 1024 : 0);
     // two m-tiles per warp per stage when three such stages fit (so two are in
     // flight while one is consumed), else one
-    L.mt = (KB != 16 && D <= 128 && L.fixed + 3 * stage_bytes(D, KB, VB, L.nwc * 32) <= kSmemLimit) ? 2 : 1;
+    L.mt = (KB != 16 && D <= 128 && L.fixed + 3 * stage_bytes(D, KB, VB, L.nwc * 32, qjl) <= kSmemLimit) ? 2 : 1;
     L.ts = L.nwc * 16 * L.mt;
-    L.stage = stage_bytes(D, KB, VB, L.ts);
+    L.stage = stage_bytes(D, KB, VB, L.ts, qjl);
     const int cap = (KB == 16) ? 6 : 4;
     const int ns = (kSmemLimit - L.fixed) / L.stage;
     L.nstage = ns > cap ? cap : ns;
@@ -304,13 +309,13 @@ constexpr Layout make_layout(int D, int KB, int VB) {
 }
 
 // Whether an instantiation fits (two stages at least); host and device.
-constexpr bool mma_fits(int D, int KB, int VB) {
-    return (KB != 16 || D % 64 == 0) && make_layout(D, KB, VB).nstage >= 2;
+constexpr bool mma_fits(int D, int KB, int VB, bool qjl = false) {
+    return (KB != 16 || D % 64 == 0) && (!qjl || KB <= 4) && make_layout(D, KB, VB, qjl).nstage >= 2;
 }
 
-template <int D, int KB, int VB, int NT>
+template <int D, int KB, int VB, int NT, bool QJL = false>
 struct Cfg {
-    static constexpr Layout L = make_layout(D, KB, VB);
+    static constexpr Layout L = make_layout(D, KB, VB, QJL);
     static constexpr int NWC = L.nwc;               // consumer warps
     static constexpr int NTHREADS = (NWC + 1) * 32;
     // register budget per thread: 8-bit K at d <= 128 measured fastest at 144 (17.3 vs 18.3 us
@@ -349,6 +354,10 @@ struct Cfg {
     static constexpr int KBUF = KRAW ? (D / 64) * KREG : al128(TS * BPK + 16);
     static constexpr int VBUF = al128(TS * BPV + 16);
     static constexpr int NBUF = al128(TS * 2);
+    // keys with the QJL sketch: sign bits (D / 8 bytes per token) and residual norms
+    static constexpr int SBUF = QJL ? al128(TS * D / 8) : 0;
+    static constexpr int RBUF = QJL ? al128(TS * 2) : 0;
+    static constexpr int UBQ = L.ubq;
     static constexpr int STAGE = L.stage;
     static constexpr int QBYTES = kGP * D * 4;      // q' fp32, later the merged O
     static constexpr int KW = L.kw, VW = L.vw;
@@ -363,7 +372,8 @@ struct Cfg {
     static constexpr int SMEM = L.smem;
     static constexpr bool TBLOCK = L.tblock;
     static constexpr int SMALL = L.small, G_BELOW = L.g, N_ABOVE = L.na;
-    static_assert(STAGE >= KBUF + VBUF + 2 * NBUF, "stage size");
+    static_assert(STAGE >= KBUF + VBUF + 2 * NBUF + SBUF + RBUF, "stage size");
+    static_assert(!QJL || (KB <= 4 && D % 32 == 0), "the QJL sketch rides on 2-4 bit keys");
     static_assert(NSTAGE >= 2 && NSTAGE <= 8, "stage count");
     static_assert(!KRAW || D % 64 == 0, "raw K needs 64-column blocks");
     // epilogue scratch (per-warp O slices, combine weights) lives in the stage ring
@@ -628,10 +638,10 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, int KB, int VB, int NT, bool MULTI>
-__global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL>
+__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
-    using C = Cfg<D, KB, VB, NT>;
+    using C = Cfg<D, KB, VB, NT, QJL>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
@@ -649,7 +659,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
     int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
     uint8_t* bq_s = pro + C::PRO;                                    // q' fragments (D > 128)
-    uint8_t* below = bq_s + C::BQB;                                      // stages 0 .. G_BELOW-1
+    uint8_t* ubq_s = bq_s + C::BQB;                                      // u = S q' fragments (QJL)
+    uint8_t* below = ubq_s + C::UBQ;                                     // stages 0 .. G_BELOW-1
     if constexpr (C::KRAW)  // the swizzled K blocks need 1024-byte aligned shared addresses
         below += (1024u - (smem_addr(below) & 1023u)) & 1023u;
     // stages G_BELOW .. NSTAGE-1, contiguous (also the warp-merge area)
@@ -768,9 +779,16 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                         tma_g2s_2d(st + cb * C::KREG, &kmap, 64 * cb, static_cast<int>(row0 + ts), full + s);
                 } else {
                     const uint32_t kbytes = n8 * C::BPK;
-                    mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes);
+                    const uint32_t sgbytes = QJL ? n8 * (D / 8) : 0u;
+                    mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes + (QJL ? sgbytes + nbytes : 0u));
                     bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
                     bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
+                    if constexpr (QJL) {
+                        bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF, a.k_signs + (row0 + ts) * (D / 8), sgbytes,
+                                 full + s);
+                        bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF + C::SBUF, a.k_rnorms + row0 + ts, nbytes,
+                                 full + s);
+                    }
                 }
                 bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
                 bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
@@ -865,7 +883,48 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                 }
             }
         }
-        if constexpr (C::BQ_SMEM) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+        if constexpr (QJL) {
+            // u = S q' for this CTA's query rows, as B fragments of the sketch k-tiles ("How I
+            // built VeloxQuant-MLX", Stage 3: the correction reads <S_j, q> for every sketch
+            // row j).  Sketch k-tile kk, thread (g, t): k = 2t, 2t+1, 2t+8, 2t+9 are sketch rows
+            // j0 .. j0 + 3, j0 = 32 (kk / 2) + 16 (kk % 2) + 4t -- nibble t of the half kk % 2
+            // of the keys' sign word kk / 2.  q' is split into fp16 hi and lo as for the scores.
+            const uint32_t ubq_a = smem_addr(ubq_s);
+            for (int item = ctid; item < (D / 16) * 32; item += C::NWC * 32) {
+                const int kk = item >> 5, ln = item & 31, gg = ln >> 2, tt = ln & 3;
+                const int qh = (NT == 2) ? gg : (gg >> 1);
+                const int j0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tt;
+                float u[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4* srow = reinterpret_cast<const float4*>(a.ck.sketch + static_cast<int64_t>(j0 + e) * D);
+                    const float* qrow = qs + qh * D;
+                    float acc = 0.0f;
+                    for (int i4 = 0; i4 < D / 4; ++i4) {
+                        const float4 sv4 = __ldg(srow + i4);
+                        acc = fmaf(sv4.x, qrow[4 * i4], acc);
+                        acc = fmaf(sv4.y, qrow[4 * i4 + 1], acc);
+                        acc = fmaf(sv4.z, qrow[4 * i4 + 2], acc);
+                        acc = fmaf(sv4.w, qrow[4 * i4 + 3], acc);
+                    }
+                    u[e] = acc;
+                }
+                float hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    hi[e] = __half2float(__float2half_rn(u[e]));
+                    lo[e] = u[e] - hi[e];
+                }
+                if constexpr (NT == 2) {
+                    sts64(ubq_a + ((kk * 2) * 32 + ln) * 8, pack_f16(hi[0], hi[1]), pack_f16(hi[2], hi[3]));
+                    sts64(ubq_a + ((kk * 2 + 1) * 32 + ln) * 8, pack_f16(lo[0], lo[1]), pack_f16(lo[2], lo[3]));
+                } else {
+                    const float* v = (gg & 1) ? lo : hi;  // interleaved hi / lo columns
+                    sts64(ubq_a + (kk * 32 + ln) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
+                }
+            }
+        }
+        if constexpr (C::BQ_SMEM || QJL) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
         float O[C::KT][4];
 #pragma unroll
@@ -963,6 +1022,43 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
                             q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
                             mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
                             if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
+                        }
+                        if constexpr (QJL) {
+                            // QJL correction into the same accumulators: row r's A entries are
+                            // +-v_r, v_r = gamma_r sqrt(pi/2) k_alpha / (sqrt(D) n16_K[r]) (the
+                            // accumulator is scaled by n16_K[r] afterwards), sign from bit j
+                            const uint8_t* sg = st + C::KBUF + C::VBUF + 2 * C::NBUF;
+                            const __half* rnm = reinterpret_cast<const __half*>(sg + C::SBUF);
+                            const float kap = 1.2533141373155003f * a.ck.k_alpha * rsqrtf(static_cast<float>(D));
+                            const float nka = __half2float(knrm[ra]), nkb = __half2float(knrm[rb]);
+                            const float fva = nka > 0.0f ? __half2float(rnm[ra]) * kap / nka : 0.0f;
+                            const float fvb = nkb > 0.0f ? __half2float(rnm[rb]) * kap / nkb : 0.0f;
+                            const uint32_t hva = pack_f16(fva, fva), hvb = pack_f16(fvb, fvb);
+                            const uint32_t sga = smem_addr(sg) + static_cast<uint32_t>(ra * (D / 8));
+                            const uint32_t sgb = smem_addr(sg) + static_cast<uint32_t>(rb * (D / 8));
+                            const uint32_t ubq_a = smem_addr(ubq_s);
+#pragma unroll
+                            for (int w4 = 0; w4 < D / 32; ++w4) {
+                                const uint32_t wsa = lds32(sga + 4 * w4), wsb = lds32(sgb + 4 * w4);
+#pragma unroll
+                                for (int h = 0; h < 2; ++h) {
+                                    const int kk = 2 * w4 + h;
+                                    const uint32_t na = wsa >> (16 * h + 4 * t), nb = wsb >> (16 * h + 4 * t);
+                                    // bit b of the nibble -> sign bit of half b (k = 2t + b, 2t + 8 + b)
+                                    const uint32_t a0 = hva ^ (((na & 1u) << 15) | ((na & 2u) << 30));
+                                    const uint32_t a2 = hva ^ (((na & 4u) << 13) | ((na & 8u) << 28));
+                                    const uint32_t a1 = hvb ^ (((nb & 1u) << 15) | ((nb & 2u) << 30));
+                                    const uint32_t a3 = hvb ^ (((nb & 4u) << 13) | ((nb & 8u) << 28));
+                                    uint32_t u00, u01;
+                                    lds64(ubq_a + ((kk * C::NTS) * 32 + lane) * 8, u00, u01);
+                                    mma16816(sc[mt][0], a0, a1, a2, a3, u00, u01);
+                                    if constexpr (C::NTS == 2) {
+                                        uint32_t u10, u11;
+                                        lds64(ubq_a + ((kk * C::NTS + 1) * 32 + lane) * 8, u10, u11);
+                                        mma16816(sc[mt][1], a0, a1, a2, a3, u10, u11);
+                                    }
+                                }
+                            }
                         }
                     }
                     }
@@ -1217,15 +1313,15 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT>::MAXREG))
 cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows);
 
 // Launch of one instantiation; split plan for one CTA per SM.
-template <int D, int KB, int VB, int NT, bool MULTI>
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false>
 cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    using C = Cfg<D, KB, VB, NT>;
+    using C = Cfg<D, KB, VB, NT, QJL>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
@@ -1246,7 +1342,7 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI>, a, p, kmap);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI, QJL>, a, p, kmap);
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
@@ -1256,7 +1352,12 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
                 case 1: return launch_inst<D, KB_, VB_, 1, false>(a, p, st);                      \
                 case 2: return launch_inst<D, KB_, VB_, 2, false>(a, p, st);                      \
                 case 3: return launch_inst<D, KB_, VB_, 1, true>(a, p, st);                       \
-                default: return launch_inst<D, KB_, VB_, 2, true>(a, p, st);                      \
+                case 4: return launch_inst<D, KB_, VB_, 2, true>(a, p, st);                       \
+                default:                                                                      \
+                    if constexpr (KB_ <= 4 && (D & (D - 1)) == 0 && mma_fits(D, KB_, VB_, true)) \
+                        return nt == 5 ? launch_inst<D, KB_, VB_, 1, false, true>(a, p, st)       \
+                                       : launch_inst<D, KB_, VB_, 2, false, true>(a, p, st);      \
+                    return cudaErrorNotSupported;                                             \
             }                                                                                 \
     }
 

@@ -108,9 +108,10 @@ def _decode_case(G, lens, d=128, kbits=3, vbits=3, S=520, B=None, seed=0):
     return got, ref
 
 
-@pytest.mark.parametrize("G", [1, 4, 8])
+@pytest.mark.parametrize("G", [1, 4, 8, 16])
 @pytest.mark.parametrize("kbits", [2, 3])
 def test_qjl_decode_parity(G, kbits):
+    # G <= 8: tensor-core kernel; G = 16 (two row groups per KV head): the SIMT kernel
     got, ref = _decode_case(G, lens=[517, 0, 64], kbits=kbits)
     check_close(got, ref, f"qjl G={G} K{kbits}+1")
 
