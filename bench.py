@@ -58,6 +58,25 @@ def _dist():
     return ws, rank, local
 
 
+def max_over_ranks(value, device="cpu"):
+    """The largest of every rank's value (the slowest rank's time); the value itself when
+    no process group of more than one rank is running.  device: where the reduction's
+    tensor lives (the rank's GPU for NCCL, the host for gloo)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank, world_size, slowest_seconds):
+    """Whole-job throughput: the units every rank processed (replicas: the same count on each)
+    over the slowest rank's time."""
+    return world_size * units_per_rank / slowest_seconds
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -388,12 +407,10 @@ def gpu_arm(args):
             dec_mean = statistics.mean(dec_t)
     torch.cuda.synchronize()
     assert tq.tq_get_device_error(wsb) == 0
+    tot = max_over_ranks(tot, dev)
     if ws_ > 1:
-        t = torch.tensor([tot], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        tot = float(t.item())
         torch.distributed.barrier()
-    value = ws_ * bytes_step * args.steps / tot / 1e9
+    value = job_throughput(bytes_step * args.steps, ws_, tot) / 1e9
     peak, peak_kind = _peaks()
     achieved = bytes_step / dec_mean / 1e9
 
@@ -563,7 +580,7 @@ def gpu_arm(args):
             e2e_tot += e0.elapsed_time(e1) * 1e-3
     h2d = h2d_tot / args.steps
     d2h = h_out.numel() * 2
-    e2e_v = ws_ * bytes_step * args.steps / e2e_tot / 1e9
+    e2e_v = job_throughput(bytes_step * args.steps, ws_, max_over_ranks(e2e_tot, dev)) / 1e9
 
     if rank != 0:
         if ws_ > 1:
