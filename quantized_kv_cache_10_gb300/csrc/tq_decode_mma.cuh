@@ -889,38 +889,46 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
             // row j).  Sketch k-tile kk, thread (g, t): k = 2t, 2t+1, 2t+8, 2t+9 are sketch rows
             // j0 .. j0 + 3, j0 = 32 (kk / 2) + 16 (kk % 2) + 4t -- nibble t of the half kk % 2
             // of the keys' sign word kk / 2.  q' is split into fp16 hi and lo as for the scores.
+            // Warp w takes sketch rows j = 32 w + lane for all rows of q' (S^T rows read
+            // across the lanes, coalesced; q' broadcast from shared memory), then forms the
+            // fragments of k-tiles 2w and 2w + 1 from its lanes by shuffles.
             const uint32_t ubq_a = smem_addr(ubq_s);
-            for (int item = ctid; item < (D / 16) * 32; item += C::NWC * 32) {
-                const int kk = item >> 5, ln = item & 31, gg = ln >> 2, tt = ln & 3;
+            for (int w = warp; w < D / 32; w += C::NWC) {
+                float uq[kGP];
+#pragma unroll
+                for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = 0.0f;
+                const float* col = a.ck.sketch_t + 32 * w + lane;
+#pragma unroll 4
+                for (int i = 0; i < D; ++i) {
+                    const float sv = __ldg(col + static_cast<int64_t>(i) * D);
+#pragma unroll
+                    for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv, qs[g2 * D + i], uq[g2]);
+                }
+                const int gg = lane >> 2, tt = lane & 3;
                 const int qh = (NT == 2) ? gg : (gg >> 1);
-                const int j0 = 32 * (kk >> 1) + 16 * (kk & 1) + 4 * tt;
-                float u[4];
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float4* srow = reinterpret_cast<const float4*>(a.ck.sketch + static_cast<int64_t>(j0 + e) * D);
-                    const float* qrow = qs + qh * D;
-                    float acc = 0.0f;
-                    for (int i4 = 0; i4 < D / 4; ++i4) {
-                        const float4 sv4 = __ldg(srow + i4);
-                        acc = fmaf(sv4.x, qrow[4 * i4], acc);
-                        acc = fmaf(sv4.y, qrow[4 * i4 + 1], acc);
-                        acc = fmaf(sv4.z, qrow[4 * i4 + 2], acc);
-                        acc = fmaf(sv4.w, qrow[4 * i4 + 3], acc);
+                for (int h = 0; h < 2; ++h) {
+                    const int kk = 2 * w + h;
+                    float hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // sketch row 32 w + 16 h + 4 tt + e of query row qh, from lane 16 h + 4 tt + e
+                        float x = 0.0f;
+#pragma unroll
+                        for (int g2 = 0; g2 < kGP; ++g2) {
+                            const float y = __shfl_sync(kFullMask, uq[g2], 16 * h + 4 * tt + e);
+                            if (g2 == qh) x = y;
+                        }
+                        hi[e] = __half2float(__float2half_rn(x));
+                        lo[e] = x - hi[e];
                     }
-                    u[e] = acc;
-                }
-                float hi[4], lo[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    hi[e] = __half2float(__float2half_rn(u[e]));
-                    lo[e] = u[e] - hi[e];
-                }
-                if constexpr (NT == 2) {
-                    sts64(ubq_a + ((kk * 2) * 32 + ln) * 8, pack_f16(hi[0], hi[1]), pack_f16(hi[2], hi[3]));
-                    sts64(ubq_a + ((kk * 2 + 1) * 32 + ln) * 8, pack_f16(lo[0], lo[1]), pack_f16(lo[2], lo[3]));
-                } else {
-                    const float* v = (gg & 1) ? lo : hi;  // interleaved hi / lo columns
-                    sts64(ubq_a + (kk * 32 + ln) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
+                    if constexpr (NT == 2) {
+                        sts64(ubq_a + ((kk * 2) * 32 + lane) * 8, pack_f16(hi[0], hi[1]), pack_f16(hi[2], hi[3]));
+                        sts64(ubq_a + ((kk * 2 + 1) * 32 + lane) * 8, pack_f16(lo[0], lo[1]), pack_f16(lo[2], lo[3]));
+                    } else {
+                        const float* v = (gg & 1) ? lo : hi;  // interleaved hi / lo columns
+                        sts64(ubq_a + (kk * 32 + lane) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
+                    }
                 }
             }
         }

@@ -105,12 +105,14 @@ struct DevCodec {
     const uint32_t* ktab;
     const uint32_t* vtab;
     float k_alpha, v_alpha;
-    const float* sketch;  // QJL sketch S [dim][dim] (keys of the TurboQuantProd variant), else null
+    const float* sketch;    // QJL sketch S [dim][dim] (keys of the TurboQuantProd variant), else null
+    const float* sketch_t;  // its transpose S^T [dim][dim]
 };
 
 inline DevCodec dev_view(const tq_codec* c) {
     return DevCodec{c->dim, c->bits, c->is_wht, c->bytes_per_vec, c->d_centroids, c->d_sign_bits, c->d_q,
-                    c->d_qt, c->d_ktab, c->d_vtab, c->k_alpha, c->v_alpha, c->qjl ? c->d_sketch : nullptr};
+                    c->d_qt, c->d_ktab, c->d_vtab, c->k_alpha, c->v_alpha, c->qjl ? c->d_sketch : nullptr,
+                    c->qjl ? c->d_sketch_t : nullptr};
 }
 
 struct DecodeArgs {
