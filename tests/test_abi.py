@@ -58,3 +58,31 @@ def test_package_binding_loads_and_parses_schemes():
     with pytest.raises(ValueError):
         tq.parse_scheme("kivi4")
     assert tq.bytes_per_vec(128, 3) == 48 and tq.bytes_per_vec(96, 3) == 36 and tq.bytes_per_vec(128, 16) == 256
+
+
+def test_host_side_checks_of_the_newer_entry_points(lib):
+    vp, i32, i64, u64, sz = C.c_void_p, C.c_int, C.c_int64, C.c_uint64, C.c_size_t
+    h = C.c_void_p()
+    # QJL codecs: power-of-two dims and 2-4 MSE bits only (checked before any device work)
+    lib.tq_codec_create_qjl.argtypes = [i32, i32, u64, C.POINTER(vp)]
+    for dim, bits in [(96, 3), (160, 3), (128, 8), (128, 16), (128, 1)]:
+        assert lib.tq_codec_create_qjl(dim, bits, 42, C.byref(h)) == 1
+    assert lib.tq_codec_create_qjl(128, 3, 42, None) == 1
+    lib.tq_codec_export_sketch.argtypes = [vp, vp]
+    assert lib.tq_codec_export_sketch(None, None) == 1
+    lib.tq_encode_qjl.argtypes = [vp, vp, i64, i64, vp, i64, vp, vp, i64, vp, vp]
+    assert lib.tq_encode_qjl(None, None, 4, 128, None, 48, None, None, 16, None, None) == 1
+    lib.tq_decode_attend_qjl.argtypes = [vp] * 10 + [i32, i32, i32, i64, C.c_float, vp, vp, sz, vp]
+    assert lib.tq_decode_attend_qjl(*([None] * 10), 1, 8, 1, 64, 0.1, None, None, 0, None) == 1
+    # several query positions: L outside [1, 4096] is refused by the workspace query and the call
+    lib.tq_decode_attend_multi_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32]
+    lib.tq_decode_attend_multi_workspace_bytes.restype = sz
+    for L in (0, -1, 4097):
+        assert lib.tq_decode_attend_multi_workspace_bytes(1, 8, 1, L, 64, 128) == 0
+    lib.tq_decode_attend_multi.argtypes = [vp, vp, vp, i32] + [vp] * 5 + [i32, i32, i32, i64, vp, vp, vp, i32,
+                                                                        C.c_float, vp, vp, sz, vp]
+    assert lib.tq_decode_attend_multi(None, None, None, 0, *([None] * 5), 1, 8, 1, 64, None, None, None, 0,
+                                      0.1, None, None, 0, None) == 1
+    # the cache refuses missing codecs
+    lib.tq_cache_create.argtypes = [vp, vp, i32, i32, i32, i64, C.POINTER(vp)]
+    assert lib.tq_cache_create(None, None, 1, 8, 1, 64, C.byref(h)) == 1
