@@ -18,7 +18,7 @@
  *  [TW]   "anyone still talking about mlx-swift-lm?" post: fused decode
  *         (score, softmax, inline dequant, K read in its rotated basis).
  *
- * Arithmetic (the reading this oracle fixes; every choice is listed in the design doc):
+ * Arithmetic (the reading this oracle fixes where the pages leave a choice open):
  *  - fp16 inputs are turned into exact integers k = x * 2^24 (|k| < 2^40).
  *  - Power-of-two d: w = H * (s (.) k) with the explicit Sylvester matrix
  *    H[i][j] = (-1)^popcount(i & j), in exact int64 ([VQ] Stage 1: random +-1
@@ -548,7 +548,7 @@ int orc_dequant(const orc_codec *c, const uint8_t *codes, int64_t code_stride, c
  * QJL residual sketch (TurboQuantProd: "How I built VeloxQuant-MLX", Stage 3:
  * QJL Residual Correction).  A key keeps its b-bit MSE codes and norm (the
  * codec above, b = its bits) plus one sign bit per sketch row of its residual
- * and the residual's norm.  Readings fixed here (listed in the design notes):
+ * and the residual's norm.  Readings fixed here, where the page leaves them open:
  *  - sketch S: m = d rows of iid N(0,1), the Gaussian stream of seed + 2
  *    (orc_gaussian), rounded to fp32, row-major S[j][i];
  *  - residual, in the rotated basis and scaled by sqrt(d) (power-of-two d):

@@ -3,7 +3,7 @@
 This module holds none of the method's arithmetic: it only draws the fp16
 K/V/q tensors, the outlier channels and the ragged lengths that stand in for
 the pages' model workloads (Llama-3.2-3B / Qwen3-8B / Mistral-7B style
-attention layers: 24/8 or 32/8 or 64/8 heads, head_dim 128; see DESIGN.md).
+attention layers: 24/8 or 32/8 or 64/8 heads, head_dim 128).
 
 Generator: SplitMix64 (Steele, Lea, Flood 2014) in counter form, output i of
 a stream with seed s is mix(s + (i + 1) * 0x9E3779B97F4A7C15); standard
