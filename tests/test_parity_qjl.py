@@ -144,3 +144,45 @@ def test_qjl_codecs_are_refused_where_keys_carry_no_sketch():
                          torch.zeros(4, dtype=torch.float16, device=dev),
                          torch.zeros((4, 16), dtype=torch.uint8, device=dev),
                          torch.zeros(4, dtype=torch.float16, device=dev))
+
+
+def test_qjl_full_size_long_context_sampled():
+    # the 32K-token shape (64/8 heads, d 128) with 3-bit MSE + QJL keys and 3-bit values,
+    # the bench's launch configuration; two (batch, KV head) units compared
+    torch, tq = torch_mods()
+    dev = torch.device("cuda")
+    w = tq_inputs.WORKLOADS["c4_long_k8v3"]
+    d, S, Hkv = w.d, w.S, w.Hkv
+    ck, cv = tq.tq_codec_create_qjl(d, 3, w.rot_seed), tq.tq_codec_create(d, 3, w.rot_seed)
+    ok, ov = oracle.Codec(d, 3, w.rot_seed), oracle.Codec(d, 3, w.rot_seed)
+    K, V, q = w.kv("k", 8), w.kv("v", 8), w.q()
+    n = w.B * Hkv * S
+    kc = torch.empty((w.B, Hkv, S, ck.bytes_per_vec), dtype=torch.uint8, device=dev)
+    kn = torch.empty((w.B, Hkv, S), dtype=torch.float16, device=dev)
+    ks = torch.empty((w.B, Hkv, S, d // 8), dtype=torch.uint8, device=dev)
+    kr = torch.empty((w.B, Hkv, S), dtype=torch.float16, device=dev)
+    vc = torch.empty((w.B, Hkv, S, cv.bytes_per_vec), dtype=torch.uint8, device=dev)
+    vn = torch.empty((w.B, Hkv, S), dtype=torch.float16, device=dev)
+    tq.tq_encode_qjl(ck, torch.from_numpy(K).to(dev).view(n, d), kc.view(n, -1), kn.view(-1), ks.view(n, -1),
+                     kr.view(-1))
+    tq.tq_encode(cv, torch.from_numpy(V).to(dev).view(n, d), vc.view(n, -1), vn.view(-1))
+    out = torch.empty((w.B, w.Hq, d), dtype=torch.float16, device=dev)
+    ws = torch.empty(tq.tq_decode_attend_workspace_bytes(w.B, w.Hq, Hkv, S, d), dtype=torch.uint8, device=dev)
+    tq.tq_workspace_init(ws)
+    lens = w.lengths()
+    tq.tq_decode_attend_qjl(ck, cv, torch.from_numpy(q).to(dev), kc, kn, ks, kr, vc, vn,
+                            torch.from_numpy(lens).to(dev), out, ws)
+    torch.cuda.synchronize()
+    assert tq.tq_get_device_error(ws) == 0
+    got = out.float().cpu().numpy().astype(np.float64)
+    kcc, knn, kss, krr = kc.cpu().numpy(), kn.cpu().numpy(), ks.cpu().numpy(), kr.cpu().numpy()
+    vcc, vnn = vc.cpu().numpy(), vn.cpu().numpy()
+    G = w.G
+    for b, h in [(0, 1), (0, 6)]:
+        L = int(lens[b])
+        # the GPU's sketch fields of this unit are the oracle's, bit for bit
+        c_, n_, s_, r_ = ok.encode_qjl(K[b, h, :L])
+        assert np.array_equal(kss[b, h, :L], s_) and np.array_equal(krr[b, h, :L].view(np.uint16), r_.view(np.uint16))
+        ref = oracle.attention_qjl_unit(ok, ov, q[b, h * G:(h + 1) * G], kcc[b, h, :L], knn[b, h, :L], kss[b, h, :L],
+                                        krr[b, h, :L], vcc[b, h, :L], vnn[b, h, :L], L, 1 / math.sqrt(d))
+        check_close(got[b, h * G:(h + 1) * G], ref, f"c4-shape qjl unit {b},{h}")
