@@ -537,3 +537,22 @@ def test_qjl_correction_tracks_the_residual_inner_product():
         cors.append(np.corrcoef(corr, resid)[0, 1])
     assert min(cors) > 0.2
     assert 0.88 < np.mean(slopes) < 1.12, (np.mean(slopes), np.std(slopes))
+
+
+def test_qjl_attention_is_softmax_over_the_estimated_scores():
+    # the QJL attention oracle = explicit softmax of scale x the estimator's scores, applied to
+    # the dequantised values (numpy), and with a zero residual it is the plain MSE attention
+    d = 64
+    ck, cv = oracle.Codec(d, 3, 42), oracle.Codec(d, 3, 43)
+    K = tq_inputs.fp16_normal(91, (57, d))
+    V = tq_inputs.fp16_normal(92, (57, d))
+    q = tq_inputs.fp16_normal(93, (4, d))
+    kc, kn, ks, kr = ck.encode_qjl(K)
+    vc, vn, _, _ = cv.encode(V)
+    o = oracle.attention_qjl_unit(ck, cv, q, kc, kn, ks, kr, vc, vn, 57, 0.2)
+    s = 0.2 * ck.qjl_scores(q, kc, kn, ks, kr)
+    p = np.exp(s - s.max(1, keepdims=True))
+    np.testing.assert_allclose(o, (p @ cv.dequant(vc, vn)) / p.sum(1, keepdims=True), rtol=1e-12, atol=1e-14)
+    plain = oracle.attention_unit(ck, cv, q, kc, kn, vc, vn, 57, 0.2)
+    zero = oracle.attention_qjl_unit(ck, cv, q, kc, kn, ks, np.zeros_like(kr), vc, vn, 57, 0.2)
+    np.testing.assert_allclose(zero, plain, rtol=0, atol=1e-13)
