@@ -109,6 +109,22 @@ def _traffic(kernel_name):
     return e.get("dram_bytes_per_launch")
 
 
+def _lead(us=30.0):
+    """Keeps the GPU busy for ~us microseconds on the current stream before a start event,
+    so that the timed launches are already queued when the event fires: device time
+    without the host's submission latency."""
+    import torch
+    torch.cuda._sleep(int(us * _sm_mhz()))
+
+
+def _sm_mhz():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f).get("sm_max_mhz", 2070.0))
+    return 2070.0
+
+
 class Clocks:
     """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -246,6 +262,65 @@ def reference_arm(args):
 
 
 # --------------------------------------------------------------------------- GPU arm
+# integer-equivalent instructions per encoded vector (lane operations), the bound the
+# exact encode is held to: the int64 butterfly (d log2 d add/subs, two 32-bit
+# operations each), the exact 128-bit square sum (~5 per element), the b-step
+# binary search (compare + select per step) and the packing (~3 per element)
+def encode_lane_ops(d, bits):
+    return 2 * d * int(math.log2(d)) + 5 * d + (2 * bits + 3) * d
+
+
+def encode_sweep(tq, dev, stream, peak_gbs, sm_mhz, sizes=None, d=256, bits_list=(3, 4), seed=0, rot_seed=42):
+    """Encode throughput over batch sizes (the head-dim-256 workload's codecs: 3-bit K/V and
+    the 4-bit V of the raw-key scheme).  Each size runs back-to-back calls replayed from a
+    CUDA graph; call r reads vectors [(r N) mod 2^20, +N) of a 2^20-vector input (512 MB),
+    so sizes >= 2^18 stream from HBM and smaller ones are latency-bound and L2-resident."""
+    import torch
+    sizes = sizes or tq_inputs.ENCODE_SWEEP
+    NMAX = max(sizes)
+    base = 1 << 16
+    blk = torch.from_numpy(tq_inputs.fp16_normal(tq_inputs.stream_seed(seed, 7, 0), (base, d))).to(dev)
+    x = blk.repeat((NMAX + base - 1) // base, 1)[:NMAX].contiguous()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    lane_rate = sms * 128 * sm_mhz * 1e6                     # 32-bit lane operations per second
+    out = []
+    for bits in bits_list:
+        c = tq.tq_codec_create(d, bits, rot_seed)
+        codes = torch.empty((NMAX, c.bytes_per_vec), dtype=torch.uint8, device=dev)
+        norms = torch.empty(NMAX, dtype=torch.float16, device=dev)
+        for N in sizes:
+            calls = max(4, min(256, (1 << 22) // N))
+            offs = [(r * N) % NMAX for r in range(calls)]
+
+            def run():
+                for o in offs:
+                    tq.tq_encode(c, x[o:o + N], codes[o:o + N], norms[o:o + N])
+            run()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                run()
+            g.replay()
+            torch.cuda.synchronize()
+            ts = []
+            for _ in range(3):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                _lead()
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e-3 / calls)
+            t = statistics.median(ts)
+            bpv = 2 * d + c.bytes_per_vec + 2
+            out.append({"n_vec": N, "dim": d, "bits": bits, "us_per_call": t * 1e6, "Mvec_s": N / t / 1e6,
+                        "hbm_frac": N * bpv / t / 1e9 / peak_gbs,
+                        "intop_frac": N * encode_lane_ops(d, bits) / t / lane_rate})
+        del codes, norms
+    return {"points": out, "bytes_per_vec": "2d + d*b/8 + 2",
+            "intop_bound": f"lane ops per vector 2 d log2 d + 5 d + (2 b + 3) d at {sms} SMs x 128 lanes x "
+                           f"{sm_mhz:.0f} MHz"}
+
+
 def gpu_arm(args):
     import torch
     ws_, rank, local = _dist()
@@ -318,9 +393,9 @@ def gpu_arm(args):
     def encode_batch(r):
         if w.k_bits == 16:
             kc[r, :, :, -PB:].copy_(k_new)                   # raw fp16 keys are stored as they are
+            tq.tq_encode_append(cv, v_new, pos, vc[r], vn[r])
         else:
-            tq.tq_encode_append(ck, k_new, pos, kc[r], kn[r])
-        tq.tq_encode_append(cv, v_new, pos, vc[r], vn[r])
+            tq.tq_encode_append_kv(ck, cv, k_new, v_new, pos, kc[r], kn[r], vc[r], vn[r])   # one launch
 
     def attend(r):
         tq.tq_decode_attend(ck, cv, q, kc[r], None if kn is None else kn[r], vc[r], vn[r], lens, out, wsb)
@@ -330,7 +405,7 @@ def gpu_arm(args):
             encode_batch(i % R)
         attend(i % R)
 
-    enc_launches = 1 if w.k_bits == 16 else 2               # our kernels per pending-batch encode
+    enc_launches = 1                                         # our kernels per pending-batch encode
     launches = 2 * args.steps + enc_launches * ((args.steps + PB - 1) // PB)
 
     def capture(fn, count):
@@ -364,6 +439,7 @@ def gpu_arm(args):
     with Clocks(local) as clk:
         if replica_mode:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            _lead()
             e0.record(stream)
             if graphs:
                 for _ in range(args.steps // PB):
@@ -379,6 +455,7 @@ def gpu_arm(args):
             # the decode-attention call alone (no pending-batch encodes), same replicas
             reps = max(8, args.steps // PB)
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            _lead()
             e0.record(stream)
             for j in range(reps):
                 if graphs:
@@ -394,6 +471,7 @@ def gpu_arm(args):
             for i in range(args.steps):
                 flush.zero_()
                 e0, e1, e2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+                _lead()
                 e0.record(stream)
                 if i % PB == 0:
                     encode_batch(0)
@@ -433,6 +511,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         reps = max(8, args.steps // PB)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _lead()
         e0.record(stream)
         for j in range(reps):
             gt.replay()
@@ -465,6 +544,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         reps = max(8, args.steps // PB)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _lead()
         e0.record(stream)
         for j in range(reps):
             gm.replay()
@@ -488,6 +568,7 @@ def gpu_arm(args):
         qenc = []
         for i in range(3):
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            _lead()
             e0.record(stream)
             tq.tq_encode_qjl(cq, Kd.view(n, w.d), qkc[0].view(n, -1), qkn[0].view(-1), qks[0].view(n, -1),
                              qkr[0].view(-1))
@@ -511,6 +592,7 @@ def gpu_arm(args):
         torch.cuda.synchronize()
         reps = max(4, args.steps // (4 * PB))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _lead()
         e0.record(stream)
         for j in range(reps):
             gq.replay()
@@ -529,11 +611,17 @@ def gpu_arm(args):
     for i in range(16):
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        _lead()
         e0.record(stream)
         attend(0)
         e1.record(stream)
         torch.cuda.synchronize()
         iso.append(e0.elapsed_time(e1) * 1e3)
+
+    # encode throughput sweep over batch sizes (1 .. 2^20 vectors, head dim 256, 3 and 4 bits)
+    sweep = None
+    if not args.no_encode_sweep:
+        sweep = encode_sweep(tq, dev, stream, peak, _sm_mhz())
 
     # ---- end to end through the public API: pinned host inputs in, output back ----
     h_q = torch.from_numpy(w.q()).pin_memory()
@@ -616,6 +704,7 @@ def gpu_arm(args):
         "multi_query": multi,
         "qjl": qjl,
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
+        "encode_sweep": sweep,
         "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches,
         "clocks": clk.summary(),
@@ -635,6 +724,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(tq_inputs.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
+    ap.add_argument("--no-encode-sweep", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
         reference_arm(args)

@@ -144,6 +144,25 @@ tq_status tq_encode_append(const tq_codec *codec, const uint16_t *x, int B, int 
                            uint16_t *norms, int32_t *dev_error, void *stream);
 
 /*
+ * The K and the V pending-token batch of one layer encoded in one launch
+ * ([PR] Design, "Batch recompression": the pending K and V tokens are
+ * recompressed together), each with its own codec; otherwise exactly two
+ * tq_encode_append calls (same arguments, same results, bit for bit).
+ *   ck, cv           coded codecs of the same dim (bits != 16, no QJL sketch)
+ *   k, v             device fp16 [B, n_kv_heads, T, dim] contiguous
+ *   start_pos        device int32 [B], shared by K and V
+ *   k_codes, k_norms K cache [B, n_kv_heads, max_seq, ck bytes_per_vec] / [.., max_seq] fp16
+ *   v_codes, v_norms V cache, likewise with cv
+ *   dev_error        optional, as for tq_encode_append
+ * Errors: TQ_ERR_INVALID_ARG on a null pointer, misalignment, different dims,
+ * raw or sketched codecs, or codecs of another device; nothing is enqueued then.
+ */
+tq_status tq_encode_append_kv(const tq_codec *ck, const tq_codec *cv, const uint16_t *k, const uint16_t *v,
+                              int B, int n_kv_heads, int T, const int32_t *start_pos, int64_t max_seq,
+                              uint8_t *k_codes, uint16_t *k_norms, uint8_t *v_codes, uint16_t *v_norms,
+                              int32_t *dev_error, void *stream);
+
+/*
  * Dequantise (debugging aid): out[v] = n16_v * R^T (c[codes_v] / sqrt(dim)),
  * fp32, computed with a fp32 butterfly (WHT) or fp32 Q^T product (dense).
  *   codes device [n_vec, bytes_per_vec] contiguous; norms device fp16

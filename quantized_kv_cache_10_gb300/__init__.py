@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "TQError", "Codec", "tq_version", "tq_codec_create", "tq_codec_destroy", "tq_codec_info",
-    "tq_codec_export", "tq_encode", "tq_encode_append", "tq_dequant",
+    "tq_codec_export", "tq_encode", "tq_encode_append", "tq_encode_append_kv", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
     "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail",
     "tq_decode_attend_multi", "tq_decode_attend_multi_workspace_bytes", "tq_codec_create_qjl",
@@ -45,6 +45,7 @@ _sig = {
     "tq_codec_export": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "tq_encode": (_i32, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "tq_encode_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "tq_encode_append_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tq_dequant": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "tq_decode_attend_workspace_bytes": (_sz, [_i32, _i32, _i32, _i64, _i32]),
     "tq_workspace_init": (_i32, [_vp, _sz, _vp]),
@@ -247,6 +248,29 @@ def tq_encode_append(codec: Codec, x: torch.Tensor, start_pos: torch.Tensor, cod
                                  _dev(start_pos, torch.int32, "start_pos"), max_seq,
                                  _dev(codes, torch.uint8, "codes"), _dev(norms, torch.float16, "norms"), err,
                                  _stream(stream)), "tq_encode_append")
+
+
+def tq_encode_append_kv(ck: Codec, cv: Codec, k: torch.Tensor, v: torch.Tensor, start_pos: torch.Tensor,
+                        k_codes: torch.Tensor, k_norms: torch.Tensor, v_codes: torch.Tensor, v_norms: torch.Tensor,
+                        dev_error: torch.Tensor | None = None, stream=None):
+    """The K and V pending batches [B, Hkv, T, dim] fp16 into their caches in one launch (codes
+    [B, Hkv, max_seq, bpv], norms [B, Hkv, max_seq]) at positions start_pos[b] + t."""
+    B, H, T, d = k.shape
+    if tuple(v.shape) != (B, H, T, d) or d != ck.dim or d != cv.dim:
+        raise ValueError("k and v must be [B, Hkv, T, dim] with the codecs' dim")
+    for t, nm in ((k, "k"), (v, "v"), (k_codes, "k_codes"), (k_norms, "k_norms"), (v_codes, "v_codes"),
+                  (v_norms, "v_norms"), (start_pos, "start_pos")):
+        _contig(t, nm)
+    max_seq = k_codes.shape[2]
+    if (tuple(k_codes.shape) != (B, H, max_seq, ck.bytes_per_vec) or tuple(k_norms.shape) != (B, H, max_seq) or
+            tuple(v_codes.shape) != (B, H, max_seq, cv.bytes_per_vec) or tuple(v_norms.shape) != (B, H, max_seq)):
+        raise ValueError("cache shapes do not match")
+    err = _dev(dev_error, torch.int32, "dev_error") if dev_error is not None else None
+    _check(_lib.tq_encode_append_kv(ck.handle, cv.handle, _dev(k, torch.float16, "k"), _dev(v, torch.float16, "v"),
+                                    B, H, T, _dev(start_pos, torch.int32, "start_pos"), max_seq,
+                                    _dev(k_codes, torch.uint8, "k_codes"), _dev(k_norms, torch.float16, "k_norms"),
+                                    _dev(v_codes, torch.uint8, "v_codes"), _dev(v_norms, torch.float16, "v_norms"),
+                                    err, _stream(stream)), "tq_encode_append_kv")
 
 
 def tq_dequant(codec: Codec, codes: torch.Tensor, norms: torch.Tensor, out: torch.Tensor, stream=None):

@@ -117,6 +117,26 @@ tq_status tq_encode_append(const tq_codec* c, const uint16_t* x, int B, int n_kv
                                        start_pos, max_seq, dev_error, static_cast<cudaStream_t>(stream)));
 }
 
+tq_status tq_encode_append_kv(const tq_codec* ck, const tq_codec* cv, const uint16_t* k, const uint16_t* v, int B,
+                              int n_kv_heads, int T, const int32_t* start_pos, int64_t max_seq, uint8_t* k_codes,
+                              uint16_t* k_norms, uint8_t* v_codes, uint16_t* v_norms, int32_t* dev_error,
+                              void* stream) {
+    if (!ck || !cv || ck->bits == 16 || cv->bits == 16 || ck->qjl || cv->qjl || ck->dim != cv->dim)
+        return TQ_ERR_INVALID_ARG;
+    if (B < 0 || n_kv_heads < 0 || T < 0 || max_seq <= 0) return TQ_ERR_INVALID_ARG;
+    if (B == 0 || n_kv_heads == 0 || T == 0) return TQ_OK;
+    if (!k || !v || !start_pos || !k_codes || !k_norms || !v_codes || !v_norms) return TQ_ERR_INVALID_ARG;
+    if (!aligned(k, 4) || !aligned(v, 4) || !aligned(k_codes, 4) || !aligned(v_codes, 4) || !aligned(k_norms, 2) ||
+        !aligned(v_norms, 2) || !aligned(start_pos, 4))
+        return TQ_ERR_INVALID_ARG;
+    if (dev_error && !aligned(dev_error, 4)) return TQ_ERR_INVALID_ARG;
+    if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
+    const tq::EncodeJob jobs[2] = {
+        {ck, k, 0, ck->dim, k_codes, ck->bytes_per_vec, k_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error},
+        {cv, v, 0, cv->dim, v_codes, cv->bytes_per_vec, v_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error}};
+    return from_cuda(tq::launch_encode_jobs(jobs, 2, static_cast<cudaStream_t>(stream)));
+}
+
 tq_status tq_dequant(const tq_codec* c, const uint8_t* codes, const uint16_t* norms, int64_t n_vec, float* out,
                      void* stream) {
     if (!c || c->bits == 16 || n_vec < 0) return TQ_ERR_INVALID_ARG;

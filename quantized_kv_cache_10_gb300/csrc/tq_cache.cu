@@ -83,7 +83,6 @@ tq_status encode_tokens(tq_cache* c, const uint16_t* k, const uint16_t* v, int T
     c->count_stale = true;
     cudaError_t e = set_count(c, pos, st);
     if (e != cudaSuccess) return from_cuda(e);
-    tq_status s = TQ_OK;
     if (c->ck->bits == 16) {
         // raw K rows are stored as they are: one strided copy per (sequence, KV head) plane
         const size_t rb = static_cast<size_t>(c->dim) * 2;
@@ -92,8 +91,9 @@ tq_status encode_tokens(tq_cache* c, const uint16_t* k, const uint16_t* v, int T
                               cudaMemcpyDeviceToDevice, st);
         if (e != cudaSuccess) return from_cuda(e);
     } else {
-        s = tq_encode_append(c->ck, k, c->B, c->Hkv, T, c->d_count, c->max_seq, c->kc, c->kn, c->d_err, st);
-        if (s != TQ_OK) return s;
+        // K and V in one launch
+        return tq_encode_append_kv(c->ck, c->cv, k, v, c->B, c->Hkv, T, c->d_count, c->max_seq, c->kc, c->kn, c->vc,
+                                   c->vn, c->d_err, st);
     }
     return tq_encode_append(c->cv, v, c->B, c->Hkv, T, c->d_count, c->max_seq, c->vc, c->vn, c->d_err, st);
 }

@@ -117,9 +117,13 @@ __device__ inline void rotate_query_warp(const DecodeArgs& a, int64_t row, float
     }
 }
 
-// Lets the combine kernel that follows on the stream (launched with
-// programmatic stream serialization) be scheduled while this grid still runs;
-// the combine kernel waits for this grid's completion before it reads.
+// Lets the kernel that follows on the stream (launched with programmatic
+// stream serialization) be scheduled while this grid still runs.  A CTA counts
+// as triggered at the first execution by any of its threads, and the combine
+// kernel reads the call's inputs before its own dependency wait, so a decode
+// kernel executes this only in threads that have passed griddepcontrol.wait
+// (or, launched without programmatic serialization, anywhere: everything
+// before it on the stream has then completed before it starts).
 __device__ __forceinline__ void allow_dependent_launch() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }

@@ -231,9 +231,9 @@ struct Layout {
 constexpr int kSmemBase = 1024;
 constexpr int kTBlock = 65536;
 
-constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false);
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false, bool multi = false);
 
-constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
+constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
     Layout L{};
     L.tblock = true;
     L.nwc = nwc_for(D, KB);
@@ -244,7 +244,9 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
     L.kw = L.krows;
     L.vw = L.vrows;
     L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
-    L.bqb = (D > 128) ? (D / 8) * 2 * 256 : 0;
+    // q' B fragments in shared memory: D > 128, or several query positions (q_hi and q_lo
+    // n-tiles, which registers would not hold beside the rest)
+    L.bqb = (D > 128 || multi) ? (D / 8) * 2 * 256 : 0;
     L.small = kGP * D * 4 + 1024 + L.pro + L.bqb;
     L.fixed = L.small;
     L.mt = mt;
@@ -265,10 +267,10 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt) {
     return L;
 }
 
-constexpr Layout make_layout(int D, int KB, int VB, bool qjl) {
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
     if (KB == 8) {
         // the table block, when it holds at least as many stages as the linear layout would
-        const Layout t2 = make_tblock_layout(D, KB, VB, 2), t1 = make_tblock_layout(D, KB, VB, 1);
+        const Layout t2 = make_tblock_layout(D, KB, VB, 2, multi), t1 = make_tblock_layout(D, KB, VB, 1, multi);
         const Layout t = (D <= 128 && t2.nstage >= 3) ? t2 : t1;
         if (t.nstage >= 3) return t;
     }
@@ -287,7 +289,8 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl) {
     // D > 128: the q' B fragments live in shared memory (one copy, 8 B per lane
     // per (k-tile, n-tile)) instead of registers
     // (also with the QJL sketch, whose own fragments and per-row values need the registers)
-    L.bqb = (D > 128 || qjl) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    // (and for 8-bit K with several query positions: q_hi and q_lo n-tiles)
+    L.bqb = (D > 128 || qjl || (multi && KB == 8)) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
     // keys with the QJL sketch: the B fragments of u = S q' (D / 16 k-tiles, up to two n-tiles)
     L.ubq = qjl ? (D / 16) * 2 * 256 : 0;
     // (+1024 for raw K: the ring is aligned to 1024 B at run time)
@@ -309,19 +312,20 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl) {
 }
 
 // Whether an instantiation fits (two stages at least); host and device.
-constexpr bool mma_fits(int D, int KB, int VB, bool qjl = false) {
-    return (KB != 16 || D % 64 == 0) && (!qjl || KB <= 4) && make_layout(D, KB, VB, qjl).nstage >= 2;
+constexpr bool mma_fits(int D, int KB, int VB, bool qjl = false, bool multi = false) {
+    return (KB != 16 || D % 64 == 0) && (!qjl || KB <= 4) && make_layout(D, KB, VB, qjl, multi).nstage >= 2;
 }
 
-template <int D, int KB, int VB, int NT, bool QJL = false>
+template <int D, int KB, int VB, int NT, bool QJL = false, bool MULTI = false>
 struct Cfg {
-    static constexpr Layout L = make_layout(D, KB, VB, QJL);
+    static constexpr Layout L = make_layout(D, KB, VB, QJL, MULTI);
     static constexpr int NWC = L.nwc;               // consumer warps
     static constexpr int NTHREADS = (NWC + 1) * 32;
     // register budget per thread: 8-bit K at d <= 128 measured fastest at 144 (17.3 vs 18.3 us
     // per call at 168 on the 32K workload; 128: 19.4, 136: 17.6, 152: 18.5, 160: 18.5); others
     // take what three warps per SM sub-partition allow (raw K: two warps)
-    static constexpr int MAXREG = (KB == 16) ? 232 : (KB == 8 && D <= 128) ? 144 : 168;
+    // (the instantiation for several query positions, whose 8-bit K scores keep q_lo, takes 168)
+    static constexpr int MAXREG = (KB == 16) ? 232 : (KB == 8 && D <= 128 && !MULTI) ? 144 : 168;
     static constexpr int MT = L.mt;                 // m-tiles of 16 tokens per warp per stage
     static constexpr int TS = L.ts;                 // tokens per stage
     static constexpr bool KRAW = (KB == 16);        // raw fp16 K rows (no codebook)
@@ -334,8 +338,11 @@ struct Cfg {
     static constexpr int KTS = KEXP ? D / 8 : D / 16;  // score k-tiles
     // score n-tiles: 8-bit K with 5..8 query heads scores against q_hi only --
     // (K_hi, K_lo) x q_hi keeps K exact to ~2^-22 and leaves only q's fp16
-    // rounding (~2^-12 relative), for 1.5 instead of 2.5 mma per token.
-    static constexpr int NTS = (KEXP && NT == 2) ? 1 : NT;
+    // rounding (~2^-12 relative), for 1.5 instead of 2.5 mma per token.  With
+    // several query positions the first rows of a chunk see one or a few tokens,
+    // where a score's rounding is not averaged over many tokens but moves the
+    // output directly: they keep q_lo too.
+    static constexpr int NTS = (KEXP && NT == 2 && !MULTI) ? 1 : NT;
     static constexpr int BQB = L.bqb;
     static constexpr bool BQ_SMEM = BQB > 0;
     static constexpr bool KPAIR = KB <= 4;
@@ -639,9 +646,9 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, int KB, int VB, int NT, bool MULTI, bool QJL>
-__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
+__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
-    using C = Cfg<D, KB, VB, NT, QJL>;
+    using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
@@ -697,6 +704,13 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
     // griddepcontrol.wait it touches only the codec's tables and sign words,
     // which no kernel writes; q, the cache, the lengths and the workspace come
     // after the wait.
+    //
+    // The dependent combine launch counts a CTA as triggered at the first
+    // griddepcontrol.launch_dependents any of its threads executes, so no
+    // thread executes it before it has itself passed griddepcontrol.wait: the
+    // combine reads the call's inputs (q, the tail, the new token) and writes
+    // the tail buffer before its own wait, which is only safe once everything
+    // stream-ordered before this kernel has completed.
     int64_t t1 = t0;
     int ntiles = 0;
 
@@ -715,7 +729,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
     int issued = 0;  // tiles whose copies the producer has started (producer lane 0)
     if (warp == C::NWC) {
         // ------------------------------------------------------------ producer
-        if (lane != 0) allow_dependent_launch();  // these lanes read nothing
+        // (lanes 1-31 issue nothing and never trigger the dependent launch: the
+        // CTA's trigger must follow a dependency wait)
         if (lane == 0) {
             // prologue data first: compact tables, this unit's query block, sign words
             const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
@@ -809,7 +824,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL>::MAXREG))
             asm volatile("griddepcontrol.wait;" ::: "memory");
             // Past the wait, everything stream-ordered before this kernel is complete: the
             // combine kernel that follows may start (and read the call's inputs) once every
-            // thread of every CTA has said so.
+            // CTA has triggered, which each CTA does only after one of its threads has
+            // passed this wait.
             allow_dependent_launch();
             len = clamped_len(a, b);
             t1 = min(len, t0 + p.chunk);
@@ -1323,7 +1339,7 @@ cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t r
 // Launch of one instantiation; split plan for one CTA per SM.
 template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false>
 cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    using C = Cfg<D, KB, VB, NT, QJL>;
+    using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
@@ -1359,8 +1375,12 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
             switch (nt) {                                                                     \
                 case 1: return launch_inst<D, KB_, VB_, 1, false>(a, p, st);                      \
                 case 2: return launch_inst<D, KB_, VB_, 2, false>(a, p, st);                      \
-                case 3: return launch_inst<D, KB_, VB_, 1, true>(a, p, st);                       \
-                case 4: return launch_inst<D, KB_, VB_, 2, true>(a, p, st);                       \
+                case 3:                                                                       \
+                case 4:                                                                       \
+                    if constexpr (mma_fits(D, KB_, VB_, false, true))                         \
+                        return nt == 3 ? launch_inst<D, KB_, VB_, 1, true>(a, p, st)              \
+                                       : launch_inst<D, KB_, VB_, 2, true>(a, p, st);             \
+                    return cudaErrorNotSupported;                                             \
                 default:                                                                      \
                     if constexpr (KB_ <= 4 && (D & (D - 1)) == 0 && mma_fits(D, KB_, VB_, true)) \
                         return nt == 5 ? launch_inst<D, KB_, VB_, 1, false, true>(a, p, st)       \

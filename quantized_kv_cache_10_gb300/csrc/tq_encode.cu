@@ -182,6 +182,17 @@ __device__ __forceinline__ void pack_store(const int (&code)[E], int E_rt, int l
     __syncwarp();
 }
 
+// Launched with programmatic stream serialization: the kernel may start while
+// the previous kernel on the stream still runs.  Its inputs (the vectors, the
+// positions) and its outputs are touched only after this wait, which returns
+// once everything stream-ordered before it has completed; right after it the
+// next kernel (e.g. the decode attention that reads the cache) may begin its
+// own set-up.
+__device__ __forceinline__ void grid_dependency_sync() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 constexpr int kWarps = 8;
 constexpr float kNearTie = 2e-6f;  // relative margin of the fp32 boundary test (see below)
 
@@ -217,15 +228,24 @@ __device__ __noinline__ int exact_code(int64_t w, double D, const double* mid, i
 // rounding of w, m_i, D and the product can move it -- being decided exactly
 // instead (exact_code).  Outside that margin the fp32 comparison agrees with
 // w > RN64(m_i D), so the codes are bit-exact either way.
+//
+// Two jobs (e.g. the K and the V pending batch, each with its own codec) may
+// share one launch: blocks [0, grid0) take job 0, the rest job 1.
 template <int E>
-__global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams p) {
+__global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams p0, const EncParams p1, int grid0) {
     __shared__ float s_thr[kWarps][256];         // 8-bit codes: fp32 thresholds of one vector
     __shared__ int64_t s_ithr[kWarps][32 * 15];  // 2-4 bit codes: integer thresholds of 32 vectors
     __shared__ uint32_t s_pack[kWarps][128];
     __shared__ float s_mid[256];
+    const bool job1 = static_cast<int>(blockIdx.x) >= grid0;
+    const EncParams& p = job1 ? p1 : p0;
+    const int64_t blk = job1 ? blockIdx.x - grid0 : blockIdx.x;
+    const int64_t nblk = job1 ? gridDim.x - grid0 : grid0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int L = 1 << p.bits;
+    // codec data (written by no kernel) before the dependency wait
     for (int i = threadIdx.x; i < L - 1; i += blockDim.x) s_mid[i] = __double2float_rn(__ldg(p.mid + i));
+    grid_dependency_sync();
     __syncthreads();
     float* thr = s_thr[warp];
     int64_t* ithr = s_ithr[warp];
@@ -240,8 +260,7 @@ __global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams
     }
     const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
     const int64_t nbatch = (total + p.vb - 1) / p.vb;
-    for (int64_t bt = static_cast<int64_t>(blockIdx.x) * kWarps + warp; bt < nbatch;
-         bt += static_cast<int64_t>(gridDim.x) * kWarps) {
+    for (int64_t bt = blk * kWarps + warp; bt < nbatch; bt += nblk * kWarps) {
         const int64_t v0 = bt * p.vb;
         const int nb = static_cast<int>(min(static_cast<int64_t>(p.vb), total - v0));
         // ---- pass 1: exact sums of squares; lane j keeps vector j's
@@ -360,7 +379,12 @@ constexpr int kDenseWarps = 4;
 constexpr int kDenseMaxE = 15;
 
 // Other dims (multiple of 32, not a power of two): E = dim / 32 at run time.
-__global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const EncParams p) {
+__global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const EncParams p0, const EncParams p1,
+                                                                         int grid0) {
+    const bool job1 = static_cast<int>(blockIdx.x) >= grid0;
+    const EncParams& p = job1 ? p1 : p0;
+    const int64_t blk = job1 ? blockIdx.x - grid0 : blockIdx.x;
+    const int64_t nblk = job1 ? gridDim.x - grid0 : grid0;
     __shared__ double s_thr[kDenseWarps][256];
     __shared__ uint32_t s_pack[kDenseWarps][128];
     __shared__ double s_k[kDenseWarps][kDenseMaxE * 32];
@@ -372,8 +396,8 @@ __global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const En
     double* kk = s_k[warp];
     const double sqrt_d = __dsqrt_rn(static_cast<double>(p.dim));
     const int64_t total = (p.B > 0) ? static_cast<int64_t>(p.B) * p.H * p.T : p.n;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kDenseWarps + warp; v < total;
-         v += static_cast<int64_t>(gridDim.x) * kDenseWarps) {
+    grid_dependency_sync();
+    for (int64_t v = blk * kDenseWarps + warp; v < total; v += nblk * kDenseWarps) {
         const uint16_t* src;
         int64_t dst;
         if (!map_row(p, v, src, dst)) {
@@ -415,56 +439,91 @@ __global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const En
     }
 }
 
-}  // namespace
-
-cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride,
-                          uint8_t* codes, int64_t cstride, uint16_t* norms, int B, int H, int T,
-                          const int32_t* start_pos, int64_t max_seq, int32_t* dev_error,
-                          cudaStream_t st) {
+// Parameters and grid of one encode job (vb and the grid depend on the vector count).
+static EncParams make_params(const EncodeJob& j, int sms, int& grid) {
+    const tq_codec* c = j.c;
     EncParams p{};
-    p.x = x;
-    p.n = n;
-    p.xstride = xstride;
-    p.codes = codes;
-    p.cstride = cstride;
-    p.norms = norms;
-    p.B = B;
-    p.H = H;
-    p.T = T;
-    p.start_pos = start_pos;
-    p.max_seq = max_seq;
-    p.dev_error = dev_error;
+    p.x = j.x;
+    p.n = j.n;
+    p.xstride = j.xstride;
+    p.codes = j.codes;
+    p.cstride = j.cstride;
+    p.norms = j.norms;
+    p.B = j.B;
+    p.H = j.H;
+    p.T = j.T;
+    p.start_pos = j.start_pos;
+    p.max_seq = j.max_seq;
+    p.dev_error = j.dev_error;
     p.mid = c->d_midpoints;
     p.sign_bits = c->d_sign_bits;
     p.qt = c->d_qt;
     p.bits = c->bits;
     p.dim = c->dim;
-    const int64_t total = (B > 0) ? static_cast<int64_t>(B) * H * T : n;
-    if (total <= 0) return cudaSuccess;
-    const int sms = num_sms(c->device);
+    const int64_t total = (j.B > 0) ? static_cast<int64_t>(j.B) * j.H * j.T : j.n;
     if (c->is_wht) {
         // batches of up to 32 vectors per warp, smaller when there are too few vectors to
         // give every warp of the GPU one (pending-batch encodes of a few thousand vectors)
         const int64_t per_warp = total / (static_cast<int64_t>(sms) * kWarps * 4);
         p.vb = static_cast<int>(per_warp < 1 ? 1 : (per_warp > 32 ? 32 : per_warp));
         const int64_t want = ((total + p.vb - 1) / p.vb + kWarps - 1) / kWarps;
-        const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
-        const int E = c->dim / 32;
-        switch (E) {
-            case 1: encode_wht_kernel<1><<<grid, kWarps * 32, 0, st>>>(p); break;
-            case 2: encode_wht_kernel<2><<<grid, kWarps * 32, 0, st>>>(p); break;
-            case 4: encode_wht_kernel<4><<<grid, kWarps * 32, 0, st>>>(p); break;
-            case 8: encode_wht_kernel<8><<<grid, kWarps * 32, 0, st>>>(p); break;
-            case 16: encode_wht_kernel<16><<<grid, kWarps * 32, 0, st>>>(p); break;
+        grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+    } else {
+        const int64_t want = (total + kDenseWarps - 1) / kDenseWarps;
+        grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
+    }
+    return p;
+}
+
+template <typename K>
+static cudaError_t launch_pdl(K kernel, int grid, int threads, cudaStream_t st, const EncParams& p0,
+                              const EncParams& p1, int grid0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, p0, p1, grid0);
+}
+
+}  // namespace
+
+cudaError_t launch_encode_jobs(const EncodeJob* jobs, int njobs, cudaStream_t st) {
+    if (njobs < 1 || njobs > 2) return cudaErrorInvalidValue;
+    const tq_codec* c = jobs[0].c;
+    if (njobs == 2 && (jobs[1].c->dim != c->dim || jobs[1].c->is_wht != c->is_wht)) return cudaErrorInvalidValue;
+    const int sms = num_sms(c->device);
+    int g[2] = {0, 0};
+    EncParams p[2];
+    for (int i = 0; i < njobs; ++i) p[i] = make_params(jobs[i], sms, g[i]);
+    if (njobs == 1) p[1] = p[0];
+    const int grid = g[0] + g[1];
+    if (grid <= 0) return cudaSuccess;   // nothing to encode
+    if (c->is_wht) {
+        switch (c->dim / 32) {
+            case 1: return launch_pdl(encode_wht_kernel<1>, grid, kWarps * 32, st, p[0], p[1], g[0]);
+            case 2: return launch_pdl(encode_wht_kernel<2>, grid, kWarps * 32, st, p[0], p[1], g[0]);
+            case 4: return launch_pdl(encode_wht_kernel<4>, grid, kWarps * 32, st, p[0], p[1], g[0]);
+            case 8: return launch_pdl(encode_wht_kernel<8>, grid, kWarps * 32, st, p[0], p[1], g[0]);
+            case 16: return launch_pdl(encode_wht_kernel<16>, grid, kWarps * 32, st, p[0], p[1], g[0]);
             default: return cudaErrorInvalidValue;
         }
-    } else {
-        if (c->dim / 32 > kDenseMaxE) return cudaErrorInvalidValue;
-        const int64_t want = (total + kDenseWarps - 1) / kDenseWarps;
-        const int grid = static_cast<int>(want < int64_t(sms) * 16 ? want : int64_t(sms) * 16);
-        encode_dense_kernel<<<grid, kDenseWarps * 32, 0, st>>>(p);
     }
-    return cudaGetLastError();
+    if (c->dim / 32 > kDenseMaxE) return cudaErrorInvalidValue;
+    return launch_pdl(encode_dense_kernel, grid, kDenseWarps * 32, st, p[0], p[1], g[0]);
+}
+
+cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride,
+                          uint8_t* codes, int64_t cstride, uint16_t* norms, int B, int H, int T,
+                          const int32_t* start_pos, int64_t max_seq, int32_t* dev_error,
+                          cudaStream_t st) {
+    const EncodeJob j{c, x, n, xstride, codes, cstride, norms, B, H, T, start_pos, max_seq, dev_error};
+    return launch_encode_jobs(&j, 1, st);
 }
 
 }  // namespace tq

@@ -66,6 +66,24 @@ cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64
                           int B, int H, int T, const int32_t* start_pos, int64_t max_seq,
                           int32_t* dev_error, cudaStream_t st);
 
+// One encode job: n vectors of x (row stride xstride) into codes / norms, or, in
+// append mode (B > 0), x [B, H, T, dim] into cache rows from start_pos[b].
+struct EncodeJob {
+    const tq_codec* c;
+    const uint16_t* x;
+    int64_t n, xstride;
+    uint8_t* codes;
+    int64_t cstride;
+    uint16_t* norms;
+    int B, H, T;
+    const int32_t* start_pos;
+    int64_t max_seq;
+    int32_t* dev_error;
+};
+// One or two jobs (same dim and rotation kind, e.g. the K and the V pending batch)
+// in one launch.
+cudaError_t launch_encode_jobs(const EncodeJob* jobs, int njobs, cudaStream_t st);
+
 cudaError_t launch_dequant(const tq_codec* c, const uint8_t* codes, const uint16_t* norms,
                            int64_t n, float* out, cudaStream_t st);
 

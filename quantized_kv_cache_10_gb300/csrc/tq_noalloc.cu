@@ -56,6 +56,7 @@ tq_status tq_decode_attend_noalloc(const tq_codec* ck, const tq_codec* cv, const
                                    float scale, uint16_t* out, void* stream) {
     // The same argument checks as tq_decode_attend, made before anything is enqueued.
     if (!ck || !cv || cv->bits == 16 || ck->dim != cv->dim) return TQ_ERR_INVALID_ARG;
+    if (ck->qjl || cv->qjl) return TQ_ERR_INVALID_ARG;  // sketched keys have their own entry point
     if (!q || !k || !v_codes || !v_norms || !seq_lens || !out) return TQ_ERR_INVALID_ARG;
     if ((ck->bits == 16) != (k_norms == nullptr)) return TQ_ERR_INVALID_ARG;
     if (B <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return TQ_ERR_INVALID_ARG;

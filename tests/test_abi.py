@@ -83,6 +83,10 @@ def test_host_side_checks_of_the_newer_entry_points(lib):
                                                                         C.c_float, vp, vp, sz, vp]
     assert lib.tq_decode_attend_multi(None, None, None, 0, *([None] * 5), 1, 8, 1, 64, None, None, None, 0,
                                       0.1, None, None, 0, None) == 1
+    # the K+V pending-batch encode refuses missing codecs before touching a device
+    lib.tq_encode_append_kv.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, i64, vp, vp, vp, vp, vp, vp]
+    assert lib.tq_encode_append_kv(None, None, None, None, 1, 8, 64, None, 128, None, None, None, None, None,
+                                   None) == 1
     # the cache refuses missing codecs
     lib.tq_cache_create.argtypes = [vp, vp, i32, i32, i32, i64, C.POINTER(vp)]
     assert lib.tq_cache_create(None, None, 1, 8, 1, 64, C.byref(h)) == 1

@@ -83,6 +83,38 @@ def test_dense_rotation_is_qr_factor_of_seeded_gaussian(d):
     np.testing.assert_allclose(Q, Qn * sg, atol=1e-6)
 
 
+@pytest.mark.parametrize("d", [96, 160])
+def test_dense_rotation_application_and_threshold_scale(d):
+    # The oracle's dense (non-power-of-two) rotation as applied in encode: z = Q k on the
+    # exact integers k = x * 2^24 (an fma chain over i ascending), D = RN64(sqrt(RN64(S)))
+    # and the threshold scale D' = D / sqrt(d) of the orthonormal Q.  Pinned to an
+    # independent fp64 product (numpy, another summation order) within the rounding bound
+    # of either order, to the norm from exact Python integers, and to nearest-centroid
+    # codes of t = z / D' formed from those independent values.  A transposed Q, a
+    # dropped or shifted term, or D in place of D' fails here.
+    bits = 3
+    c = oracle.Codec(d, bits, 42)
+    Q = c.tables()["Q"].astype(np.float64)
+    _, c32, mid = oracle.lloyd_max(bits)[:3]
+    x = tq_inputs.fp16_normal(21, (40, d), tq_inputs.outlier_channels(d))
+    for v in range(len(x)):
+        k = x[v].astype(np.float64) * 2.0**24            # exact integers (|k| < 2^40)
+        codes, z, D = c.encode_codes(x[v])
+        zr = Q @ k
+        bound = 2 * d * 2.0**-53 * (np.abs(Q) @ np.abs(k))
+        assert np.all(np.abs(z - zr) <= bound)
+        assert np.max(np.abs(z - Q.T @ k)) > 1e3 * bound.max()
+        S = sum(int(i) ** 2 for i in k.astype(np.int64))
+        assert D == math.sqrt(float(S))                   # both roundings correct, bit for bit
+        Dp = D / math.sqrt(d)
+        want = _brute_codes(zr, Dp, c32)
+        near = np.min(np.abs(zr[:, None] - mid[None, :] * Dp), axis=1) <= 2 * bound
+        assert near.sum() <= 1
+        np.testing.assert_array_equal(codes[~near], want[~near])
+        # the rotation preserves the norm: |Q k| = |k| to Q's fp32 rounding
+        assert abs(math.sqrt(float(zr @ zr)) / D - 1.0) < 1e-6
+
+
 # --------------------------------------------------------------------------- codebook
 def test_lloyd_max_classical_values():
     for row in _golden_lines("lloyd_max_gaussian.txt"):

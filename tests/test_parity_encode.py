@@ -126,6 +126,68 @@ def test_encode_append_pending_batch_and_bad_positions():
             assert np.all(cc[b, h, untouched] == 0)
 
 
+@pytest.mark.parametrize("d,kb,vb", [(128, 8, 3), (128, 4, 2), (96, 8, 3), (256, 3, 3)])
+def test_encode_append_kv_is_two_appends_in_one_launch(d, kb, vb):
+    # The K and V pending batches encoded in one launch ("add TurboQuant KV cache
+    # compression", Design: batch recompression): bit for bit the two single-codec
+    # appends, and the oracle's encoding of every written row.
+    torch, tq = torch_mods()
+    dev = torch.device("cuda")
+    B, H, T, S = 2, 3, 64, 320
+    ck, cv = tq.tq_codec_create(d, kb, 42), tq.tq_codec_create(d, vb, 42)
+    k = tq_inputs.fp16_normal(51, (B, H, T, d), tq_inputs.outlier_channels(d))
+    v = tq_inputs.fp16_normal(52, (B, H, T, d))
+    start = torch.tensor([7, 256], dtype=torch.int32, device=dev)
+    kd, vd = torch.from_numpy(k).to(dev), torch.from_numpy(v).to(dev)
+
+    def caches():
+        return (torch.zeros((B, H, S, ck.bytes_per_vec), dtype=torch.uint8, device=dev),
+                torch.zeros((B, H, S), dtype=torch.float16, device=dev),
+                torch.zeros((B, H, S, cv.bytes_per_vec), dtype=torch.uint8, device=dev),
+                torch.zeros((B, H, S), dtype=torch.float16, device=dev))
+    a = caches()
+    tq.tq_encode_append_kv(ck, cv, kd, vd, start, *a)
+    b = caches()
+    tq.tq_encode_append(ck, kd, start, b[0], b[1])
+    tq.tq_encode_append(cv, vd, start, b[2], b[3])
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    ok, ov = oracle.Codec(d, kb, 42), oracle.Codec(d, vb, 42)
+    kc, kn, vc, vn = (t.cpu().numpy() for t in a)
+    st = start.cpu().numpy()
+    for bb in range(B):
+        for h in range(H):
+            rkc, rkn, _, m1 = ok.encode(k[bb, h])
+            rvc, rvn, _, m2 = ov.encode(v[bb, h])
+            assert m1 == 0 and m2 == 0
+            sl = slice(st[bb], st[bb] + T)
+            np.testing.assert_array_equal(kc[bb, h, sl], rkc)
+            np.testing.assert_array_equal(vc[bb, h, sl], rvc)
+            np.testing.assert_array_equal(kn[bb, h, sl].view(np.uint16), rkn.view(np.uint16))
+            np.testing.assert_array_equal(vn[bb, h, sl].view(np.uint16), rvn.view(np.uint16))
+
+
+def test_encode_append_kv_argument_checks():
+    torch, tq = torch_mods()
+    dev = torch.device("cuda")
+    c128, c96 = tq.tq_codec_create(128, 4, 42), tq.tq_codec_create(96, 4, 42)
+    raw = tq.tq_codec_create(128, 16, 42)
+    x = torch.zeros((1, 1, 4, 128), dtype=torch.float16, device=dev)
+    pos = torch.zeros(1, dtype=torch.int32, device=dev)
+    kc = torch.zeros((1, 1, 8, 64), dtype=torch.uint8, device=dev)
+    kn = torch.zeros((1, 1, 8), dtype=torch.float16, device=dev)
+    lib = tq._lib
+    st = torch.cuda.current_stream().cuda_stream
+    args = (x.data_ptr(), x.data_ptr(), 1, 1, 4, pos.data_ptr(), 8, kc.data_ptr(), kn.data_ptr(), kc.data_ptr(),
+            kn.data_ptr(), None, st)
+    assert lib.tq_encode_append_kv(c128.handle, c96.handle, *args) == 1      # different dims
+    assert lib.tq_encode_append_kv(raw.handle, c128.handle, *args) == 1      # raw keys are not encoded
+    assert lib.tq_encode_append_kv(c128.handle, c128.handle, *args[:7], None, *args[8:]) == 1
+    assert lib.tq_encode_append_kv(c128.handle, c128.handle, *args) == 0
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("name", ["c2_llama3b", "c4_long_k8v3", "c4_long_k8v3_d96"])
 def test_encode_full_size_sampled(name):
     # Full-size K/V of the workload encoded in one launch each; a sample of rows

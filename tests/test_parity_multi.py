@@ -9,9 +9,14 @@ import pytest
 
 import oracle
 import tq_inputs
-from tq_helpers import check_close, codecs, encode_cache, oracle_codecs, torch_mods
+from tq_helpers import ATOL, check_close, codecs, encode_cache, oracle_codecs, torch_mods
 
 pytestmark = pytest.mark.gpu
+
+# The first rows of a chunk attend to one or a few tokens, so their outputs are
+# dequantised values (up to ~4 in magnitude) whose fp16 store alone is off by up to
+# ~1e-3; the kernel's own error (beyond that rounding) keeps a 2x margin to the bound.
+MARGIN = ATOL / 2
 
 
 def _run(w, L, lens, tail_lens=None, max_tail=0, seed=700):
@@ -61,7 +66,7 @@ def test_multi_small_all_outputs(G, L, kb, vb):
     # lengths: a long sequence, an empty one, one shorter than L, one ending inside a tile
     w = tq_inputs.Workload("m", B=4, Hq=2 * G, Hkv=2, d=128, S=520, k_bits=kb, v_bits=vb, k_outliers=True)
     got, ref, ws = _run(w, L, lens=[517, 0, 3, 64], tail_lens=[1, 4, 0, 20], max_tail=32)
-    check_close(got, ref, f"multi G={G} L={L} K{kb}V{vb}")
+    check_close(got, ref, f"multi G={G} L={L} K{kb}V{vb}", beyond_store_max=MARGIN)
     _, tq = torch_mods()
     assert tq.tq_get_device_error(ws) == 0
 
@@ -71,7 +76,7 @@ def test_multi_without_tail_masks_inside_the_cache(L):
     # no tail: the causal mask falls on the last L packed tokens
     w = tq_inputs.Workload("m", B=2, Hq=8, Hkv=2, d=128, S=384, k_bits=8, v_bits=3, k_outliers=True)
     got, ref, _ = _run(w, L, lens=[384, 130])
-    check_close(got, ref, f"multi no tail L={L}")
+    check_close(got, ref, f"multi no tail L={L}", beyond_store_max=MARGIN)
 
 
 @pytest.mark.parametrize("d,kb", [(64, 4), (96, 8), (256, 3), (256, 16), (160, 4)])
@@ -79,7 +84,7 @@ def test_multi_head_dims(d, kb):
     # d 160 has no tensor-core instantiation: the SIMT kernel runs
     w = tq_inputs.Workload("m", B=2, Hq=8, Hkv=2, d=d, S=256, k_bits=kb, v_bits=3, k_outliers=True)
     got, ref, _ = _run(w, 3, lens=[255, 77], tail_lens=[1, 9], max_tail=16)
-    check_close(got, ref, f"multi d={d} K{kb}")
+    check_close(got, ref, f"multi d={d} K{kb}", beyond_store_max=MARGIN)
 
 
 def test_multi_l1_is_the_decode_call():
@@ -136,7 +141,14 @@ def test_multi_full_size_long_context_sampled():
     G = w.G
     for b, h in [(0, 2), (0, 7)]:
         n = int(lens[b])
+        # the GPU-written codes and norms of this unit are the oracle's encoding, bit for bit
+        rkc, rkn, _, mk = ok_k.encode(K[b, h, :n])
+        rvc, rvn, _, mv = ok_v.encode(V[b, h, :n])
+        assert mk == 0 and mv == 0
+        assert np.array_equal(kcc[b, h, :n], rkc) and np.array_equal(vcc[b, h, :n], rvc)
+        assert np.array_equal(knn[b, h, :n].view(np.uint16), rkn.view(np.uint16))
+        assert np.array_equal(vnn[b, h, :n].view(np.uint16), rvn.view(np.uint16))
         ref = oracle.attention_multi_unit(ok_k, ok_v, q[b, h * G:(h + 1) * G], kcc[b, h, :n], knn[b, h, :n],
                                           vcc[b, h, :n], vnn[b, h, :n], n, 1 / math.sqrt(w.d), kt[b, h, :T],
                                           vt[b, h, :T])
-        check_close(got[b, h * G:(h + 1) * G], ref, f"c4 multi unit {b},{h}")
+        check_close(got[b, h * G:(h + 1) * G], ref, f"c4 multi unit {b},{h}", beyond_store_max=MARGIN)

@@ -97,6 +97,14 @@ def test_tail_full_size_long_context_sampled():
     G = w.G
     for b, h in [(0, 0), (0, 5)]:
         L = int(lens[b])
+        # the GPU-written codes and norms of this unit are the oracle's encoding, bit for bit
+        # (so the comparison below is against the oracle's attention over its own cache)
+        rkc, rkn, _, mk = ok_k.encode(K[b, h, :L])
+        rvc, rvn, _, mv = ok_v.encode(V[b, h, :L])
+        assert mk == 0 and mv == 0
+        assert np.array_equal(kcc[b, h, :L], rkc) and np.array_equal(vcc[b, h, :L], rvc)
+        assert np.array_equal(knn[b, h, :L].view(np.uint16), rkn.view(np.uint16))
+        assert np.array_equal(vnn[b, h, :L].view(np.uint16), rvn.view(np.uint16))
         ref = oracle.attention_unit(ok_k, ok_v, q[b, h * G:(h + 1) * G], kcc[b, h, :L], knn[b, h, :L],
                                     vcc[b, h, :L], vnn[b, h, :L], L, 1 / math.sqrt(w.d), kt[b, h, :T], vt[b, h, :T])
         check_close(got[b, h * G:(h + 1) * G], ref, f"c4 tail unit {b},{h}")

@@ -60,25 +60,29 @@ def decode(w, ck, cv, q, kc, kn, vc, vn, lens=None, scale=None):
     return out.float().cpu().numpy().astype(np.float64), ws
 
 
-def check_close(got, ref, what=""):
+def check_close(got, ref, what="", beyond_store_max=None):
     """got: the CUDA path's fp16 attention output (as float64); ref: the oracle's fp64 value.
 
-    The output is stored as fp16, so even an exact kernel is off by up to half an fp16
-    ulp of the value (1.95e-3 for values in [4, 8), which a row attending to a single
-    token can reach); the max-abs bound applies to the error beyond that rounding."""
+    Asserts the raw max-abs error <= ATOL and the relative L2 error <= RTOL_L2.  Beside
+    the raw error it reports the error beyond the fp16 output store's own rounding
+    (half an fp16 ulp of the reference value: the part an exactly computed result
+    would still show), which isolates the kernel's arithmetic; beyond_store_max, when
+    given, bounds that part too.  Returns (raw max-abs, beyond-store max, rel-L2)."""
     err = got - ref
     half_ulp = np.spacing(np.abs(ref).astype(np.float16)).astype(np.float64) / 2
     raw = float(np.abs(err).max()) if err.size else 0.0
-    mx = float((np.abs(err) - half_ulp).max()) if err.size else 0.0
+    beyond = float(np.maximum(np.abs(err) - half_ulp, 0.0).max()) if err.size else 0.0
     nrm = float(np.linalg.norm(ref))
     rel = float(np.linalg.norm(err) / nrm) if nrm > 0 else float(np.linalg.norm(err))
     log = os.environ.get("TQ_PARITY_LOG")      # optional record of the measured errors
     if log:
         with open(log, "a") as f:
-            f.write(f"{what}\tmax_abs {raw:.3e}\tbeyond_fp16_store {mx:.3e}\trel_l2 {rel:.3e}\n")
-    assert mx <= ATOL and rel <= RTOL_L2, (f"{what}: max-abs {raw:.3e}, {mx:.3e} beyond the fp16 store's rounding "
-                                           f"(<= {ATOL}), rel-L2 {rel:.3e} (<= {RTOL_L2})")
-    return mx, rel
+            f.write(f"{what}\tmax_abs {raw:.3e}\tbeyond_fp16_store {beyond:.3e}\trel_l2 {rel:.3e}\n")
+    msg = f"{what}: max-abs {raw:.3e} (<= {ATOL}), {beyond:.3e} beyond the fp16 store, rel-L2 {rel:.3e} (<= {RTOL_L2})"
+    assert raw <= ATOL and rel <= RTOL_L2, msg
+    if beyond_store_max is not None:
+        assert beyond <= beyond_store_max, msg + f"; beyond-store bound {beyond_store_max}"
+    return raw, beyond, rel
 
 
 def oracle_unit_reference(w, ok_k, ok_v, q, K, V, b, h, lens):
