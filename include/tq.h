@@ -383,6 +383,17 @@ tq_status tq_decode_attend_noalloc(const tq_codec *ck, const tq_codec *cv, const
                                    uint16_t *out, void *stream);
 
 /*
+ * Profiling builds only (libtq_timeline.so, compiled with -DTQ_TIMELINE): registers
+ * a zeroed device buffer of at least 4 * 4096 * 8 * 8 bytes, 8-byte aligned, into
+ * which every later decode-attention call records globaltimer stamps of its decode
+ * and combine CTAs' phases, calls of even and odd index since the registration in
+ * alternate halves (NULL unregisters).  The default library
+ * returns TQ_ERR_UNSUPPORTED and records nothing.  No counterpart on the pages: a
+ * measurement aid.
+ */
+tq_status tq_debug_set_timeline(void *buffer, size_t bytes);
+
+/*
  * Reads and clears the device error word of a decode workspace (or of any
  * int32 word passed as dev_error to tq_encode_append).  Synchronises
  * `stream`.  *code receives the OR of TQ_DEVERR_* flags seen since the last

@@ -24,7 +24,9 @@ __all__ = [
     "LIB_PATH", "KVCache", "TQ_DEVERR_SEQ_LEN", "TQ_DEVERR_POSITION", "TQ_DEVERR_TIMEOUT", "TQ_DEVERR_LAYOUT",
 ]
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtq.so")
+# TQ_LIB_VARIANT=timeline loads the profiling build (libtq_timeline.so, see timeline.py)
+_LIBNAME = "libtq_timeline.so" if os.environ.get("TQ_LIB_VARIANT") == "timeline" else "libtq.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), _LIBNAME)
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
                       "(the CUDA library is required; there is no CPU fallback)")
@@ -45,6 +47,7 @@ _sig = {
     "tq_codec_export": (_i32, [_vp, _vp, _vp, _vp, _vp]),
     "tq_encode": (_i32, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "tq_encode_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp]),
+    "tq_debug_set_timeline": (_i32, [_vp, _sz]),
     "tq_encode_append_kv": (_i32, [_vp, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tq_dequant": (_i32, [_vp, _vp, _vp, _i64, _vp, _vp]),
     "tq_decode_attend_workspace_bytes": (_sz, [_i32, _i32, _i32, _i64, _i32]),

@@ -24,6 +24,10 @@ LIB = os.path.join(PKG, "libtq.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
+# Build variants: the library (default) and the profiling build that records the decode
+# and combine kernels' phase timeline (-DTQ_TIMELINE, libtq_timeline.so).
+VARIANTS = {None: ([], "", "libtq.so"), "timeline": (["-DTQ_TIMELINE"], "-timeline", "libtq_timeline.so")}
+
 
 def _cuda_home() -> str:
     home = os.environ.get("CUDA_HOME") or "/usr/local/cuda"
@@ -46,12 +50,12 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(f) > t for f in [src] + _headers())
 
 
-def _compile(src: str, cuda: str) -> tuple[str, str]:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, cuda: str, build_dir: str, defs: list) -> tuple[str, str]:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     if not _stale(obj, src):
         return obj, ""
     nvcc = os.path.join(cuda, "bin", "nvcc")
-    common = ["-O3", "-std=c++17", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    common = ["-O3", "-std=c++17", "-I", INC, "-I", CSRC, "-Xcompiler", "-fPIC", *defs]
     if src.endswith(".cu"):
         cmd = [nvcc, *ARCH, "-lineinfo", "--expt-relaxed-constexpr", "-Xptxas", "-v", *common,
                "-c", src, "-o", obj]
@@ -63,35 +67,39 @@ def _compile(src: str, cuda: str) -> tuple[str, str]:
     return obj, r.stderr
 
 
-def build(verbose: bool = False) -> str:
-    """Compile every csrc/*.cu and *.cpp and link libtq.so; returns its path."""
+def build(verbose: bool = False, variant: str | None = None) -> str:
+    """Compile every csrc/*.cu and *.cpp and link the library of `variant` (None: libtq.so);
+    returns its path."""
     cuda = _cuda_home()
-    os.makedirs(BUILD, exist_ok=True)
+    defs, suffix, libname = VARIANTS[variant]
+    build_dir = BUILD + suffix
+    lib_path = os.path.join(PKG, libname)
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
-        results = list(ex.map(lambda s: _compile(s, cuda), srcs))
+        results = list(ex.map(lambda s: _compile(s, cuda, build_dir, defs), srcs))
     objs = [o for o, _ in results]
     logs = [log for _, log in results if log]
     if logs:
-        with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        with open(os.path.join(build_dir, "ptxas.log"), "w") as f:
             f.write("\n".join(logs))
-    stamp = os.path.join(BUILD, "libtq.stamp")     # the library was linked from this architecture's objects
-    fresh = os.path.exists(LIB) and os.path.exists(stamp) and \
-        all(os.path.getmtime(o) <= os.path.getmtime(LIB) for o in objs)
+    stamp = os.path.join(build_dir, "libtq.stamp")     # the library was linked from this architecture's objects
+    fresh = os.path.exists(lib_path) and os.path.exists(stamp) and \
+        all(os.path.getmtime(o) <= os.path.getmtime(lib_path) for o in objs)
     if not fresh:
-        tmp = LIB + f".tmp{os.getpid()}"
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [os.path.join(cuda, "bin", "nvcc"), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
                "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib_path)
         with open(stamp, "w") as f:
-            f.write(LIB + "\n")
+            f.write(lib_path + "\n")
     if verbose:
-        print(LIB)
-    return LIB
+        print(lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    build(verbose="-v" in sys.argv)
+    build(verbose="-v" in sys.argv, variant="timeline" if "--timeline" in sys.argv else None)

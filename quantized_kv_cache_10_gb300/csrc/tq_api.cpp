@@ -1,6 +1,7 @@
 // tq_api.cpp -- argument checking and dispatch for the C ABI in include/tq.h.
 // Every check happens before anything is enqueued; a failed check returns a
 // status and leaves the stream untouched.
+#include <atomic>
 #include <cstdint>
 
 #include "tq_internal.h"
@@ -23,6 +24,23 @@ bool on_codec_device(const tq_codec* c) {
 }
 
 }  // namespace
+
+namespace {
+
+#ifdef TQ_TIMELINE
+std::atomic<unsigned long long*> g_timeline{nullptr};
+std::atomic<unsigned int> g_timeline_calls{0};  // decode-attention calls since registration
+#endif
+
+}  // namespace
+
+unsigned long long* tq::timeline_buffer() {
+#ifdef TQ_TIMELINE
+    return g_timeline.load();
+#else
+    return nullptr;
+#endif
+}
 
 namespace {
 
@@ -58,6 +76,10 @@ tq_status decode_attend_impl(const tq_codec* ck, const tq_codec* cv, const uint1
                      B, n_q_heads, n_kv_heads, max_seq, scale, out, workspace,
                      tail_lens ? k_tail : nullptr, tail_lens ? v_tail : nullptr, tail_lens,
                      tail_lens ? max_tail : 0, 0, nullptr, nullptr, k_signs, k_rnorms, L};
+    a.tl = tq::timeline_buffer();
+#ifdef TQ_TIMELINE
+    a.tl_seq = g_timeline_calls.fetch_add(1);
+#endif
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaErrorNotSupported;
     if (tq::decode_mma_supported(ck, cv)) {
@@ -211,6 +233,20 @@ tq_status tq_decode_attend_qjl(const tq_codec* ck, const tq_codec* cv, const uin
     return decode_attend_impl(ck, cv, q, k_codes, k_norms, v_codes, v_norms, seq_lens, B, n_q_heads, n_kv_heads, 1,
                               max_seq, nullptr, nullptr, nullptr, 0, scale, out, workspace, ws_bytes, stream,
                               k_signs, k_rnorms);
+}
+
+tq_status tq_debug_set_timeline(void* buffer, size_t bytes) {
+#ifdef TQ_TIMELINE
+    const size_t need = (2ull * 2 * tq::kTlSlotsHost * tq::kTlStampsHost) * sizeof(unsigned long long);
+    if (buffer && (bytes < need || !aligned(buffer, 8))) return TQ_ERR_INVALID_ARG;
+    g_timeline.store(static_cast<unsigned long long*>(buffer));
+    g_timeline_calls.store(0);
+    return TQ_OK;
+#else
+    (void)buffer;
+    (void)bytes;
+    return TQ_ERR_UNSUPPORTED;
+#endif
 }
 
 tq_status tq_get_device_error(void* error_word, void* stream, int* code) {

@@ -17,6 +17,8 @@
 // completed and its partial records are visible.  Every row is merged in
 // parallel, each in one round of loads, instead of all rows of a unit by one
 // last-arriving CTA.
+#include <atomic>
+
 #include "tq_decode_common.cuh"
 
 namespace tq {
@@ -120,12 +122,25 @@ __device__ __forceinline__ void to_rotated_units(const DecodeArgs& a, float (&x)
 // [VPL lane, VPL (lane + 1)).  Warp w merges splits w, w + 4, ... in one pass
 // (every load of a batch in flight at once, no separate max pass), then warp 0
 // merges the four warp states in a fixed order and writes the head's output.
+//
+// Residence beside the decode kernel: the combine grid becomes eligible while every
+// decode CTA is resident, and only if a combine CTA fits beside one does it start there
+// (scoring the tail during the decode); otherwise its CTAs wait for the first SMs the
+// decode grid frees and pile up there, several per SM, keeping the next call's decode
+// CTAs off those SMs.  So it uses at most 64 registers per thread up to d = 192 (one
+// warp per SM sub-partition fits beside three 144-register decode warps), the same
+// shared-memory split as the decode kernel, and a shared-memory pad sized at launch
+// so that exactly one combine CTA fits beside a decode CTA.
 template <int VPL>
-__global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
+__global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 6 ? 8 : 4)) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#ifdef TQ_TIMELINE
+    unsigned long long tl_t[kTlStamps] = {};  // entry, dependency wait passed, output stored, SM id
+#endif
+    TQ_TL(tl_t, 0);
     // the V codec's sign word of this lane's dims (codec data, written by no kernel)
     uint32_t sw = 0;
     if ((VPL & (VPL - 1)) == 0 && a.cv.is_wht) sw = __ldg(a.cv.sign_bits + ((lane * VPL) >> 5));
@@ -179,7 +194,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
             ot[v] = 0.0f;
         }
         // TCH tokens per round with all their loads in flight (one memory latency per round)
-        constexpr int TCH = VPL <= 4 ? 4 : 2;
+        constexpr int TCH = VPL <= 2 ? 4 : 2;
         for (int n0 = warp; n0 < ntot; n0 += kCombineWarps * TCH) {
             float kv[TCH][VPL], vv[TCH][VPL];
 #pragma unroll
@@ -225,12 +240,13 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
     }
     // wait for this call's decode grid (and the visibility of its records)
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    TQ_TL(tl_t, 1);
     const int ns = p.n_split;
     const int rec = kGP * (D + 2);
     const float* base = partial_ptr(a.ws, p, vu, 0, D);
     const float* ob = base + g * D + lane * VPL;
 
-    constexpr int CH = VPL <= 4 ? 8 : (VPL <= 8 ? 4 : 2);
+    constexpr int CH = VPL <= 4 ? 5 : (VPL <= 8 ? 4 : 2);
     float m = -CUDART_INF_F, l = 0.0f, acc[VPL];
 #pragma unroll
     for (int v = 0; v < VPL; ++v) acc[v] = 0.0f;
@@ -338,14 +354,73 @@ __global__ void __launch_bounds__(kCombineWarps * 32) decode_combine_kernel(cons
 #pragma unroll
         for (int v = 0; v < VPL; ++v) o[v] = __half_as_ushort(__float2half_rn(res[v]));
     }
+#ifdef TQ_TIMELINE
+    TQ_TL(tl_t, 2);
+    if (threadIdx.x == 0 && a.tl) {
+        unsigned sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        tl_t[3] = sm;  // the SM this CTA ran on
+        unsigned long long* r = tl_record(a, true, blockIdx.x);
+        if (r)
+            for (int i = 0; i < kTlStamps; ++i) r[i] = tl_t[i];
+    }
+#endif
+}
+
+// Shared memory per SM and reserved per CTA on the current device (cached per device).
+void smem_limits(int& per_sm, int& reserved) {
+    static std::atomic<int> cache_sm[64], cache_res[64];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int i = dev & 63;
+    per_sm = cache_sm[i].load();
+    reserved = cache_res[i].load();
+    if (per_sm == 0) {
+        if (cudaDeviceGetAttribute(&per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess) per_sm = 0;
+        if (cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess) reserved = 0;
+        cache_res[i].store(reserved);
+        cache_sm[i].store(per_sm);
+    }
+}
+
+// Dynamic shared memory that pads a combine CTA so that exactly one fits beside a
+// decode CTA of the kernel just launched (0 when that is not in reach).  The combine
+// grid becomes eligible while every decode CTA is resident; padded this way its CTAs
+// spread one per SM instead of several on the SMs that free up first, where they
+// would keep out the next call's decode CTA (a second one does not fit there either).
+int combine_pad_bytes(int decode_smem, int static_bytes) {
+    if (decode_smem <= 0) return 0;
+    int per_sm = 0, reserved = 0;
+    smem_limits(per_sm, reserved);
+    const int free_bytes = per_sm - (decode_smem + reserved);  // beside one decode CTA
+    const int own = static_bytes + reserved;                   // one combine CTA, unpadded
+    if (free_bytes < own || free_bytes > 96 * 1024) return 0;
+    // one padded CTA: own + pad <= free_bytes - 256; two: 2 (own + pad) > free_bytes
+    const int pad = free_bytes / 2 + 256 - own;
+    if (pad <= 0 || own + pad > free_bytes - 256 || pad > 48 * 1024) return 0;
+    return (pad + 127) / 128 * 128;
 }
 
 template <int VPL>
 cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    // The L1 / shared-memory split of an SM is set for the CTAs it holds, and a CTA whose
+    // kernel prefers another split waits for an idle SM: the combine asks for the same
+    // all-shared-memory split as the decode kernel, so that it can run beside it.
+    static std::atomic<uint64_t> configured{0};  // one bit per device
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const uint64_t bit = 1ull << (dev & 63);
+    if (!(configured.load() & bit)) {
+        const cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel<VPL>,
+                                                   cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(p.n_units * p.S);
     cfg.blockDim = dim3(kCombineWarps * 32);
-    cfg.dynamicSmemBytes = 0;
+    constexpr int kStatic = kCombineWarps * 32 * VPL * 4 + 2 * kCombineWarps * 4;  // s_o, s_m, s_l
+    cfg.dynamicSmemBytes = combine_pad_bytes(p.decode_smem, kStatic);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -117,6 +117,28 @@ __device__ inline void rotate_query_warp(const DecodeArgs& a, int64_t row, float
     }
 }
 
+// Phase timeline of the decode and combine kernels, for profiling builds only
+// (compiled with -DTQ_TIMELINE into libtq_timeline.so; the library built by
+// default contains none of it).  Buffer of 64-bit words: two halves (the calls
+// of even / odd index since the buffer was registered) of kTlSlots decode-CTA
+// records and kTlSlots combine-CTA records of kTlStamps globaltimer stamps (ns).
+#ifdef TQ_TIMELINE
+constexpr int kTlSlots = kTlSlotsHost, kTlStamps = kTlStampsHost;
+#define TQ_TL(arr, i) \
+    if (threadIdx.x == 0) (arr)[i] = tl_now()
+__device__ __forceinline__ unsigned long long tl_now() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ unsigned long long* tl_record(const DecodeArgs& a, bool combine, int slot) {
+    if (slot >= kTlSlots) return nullptr;
+    return a.tl + (a.tl_seq & 1u) * (2ull * kTlSlots * kTlStamps) + ((combine ? kTlSlots : 0) + slot) * kTlStamps;
+}
+#else
+#define TQ_TL(arr, i)
+#endif
+
 // Lets the kernel that follows on the stream (launched with programmatic
 // stream serialization) be scheduled while this grid still runs.  A CTA counts
 // as triggered at the first execution by any of its threads, and the combine

@@ -171,16 +171,16 @@ bool decode_mma_supported(const tq_codec* ck, const tq_codec* cv) {
 }
 
 template <int D>
-cudaError_t launch_mma_d_extern(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
+cudaError_t launch_mma_d_extern(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
 // defined in tq_decode_mma_d{64,96,128,256}.cu
 template <>
-cudaError_t launch_mma_d_extern<64>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+cudaError_t launch_mma_d_extern<64>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 template <>
-cudaError_t launch_mma_d_extern<96>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+cudaError_t launch_mma_d_extern<96>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 template <>
-cudaError_t launch_mma_d_extern<128>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+cudaError_t launch_mma_d_extern<128>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 template <>
-cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, const DecodePlan&, int, int, int, cudaStream_t);
+cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     // query rows per CTA, min(S, 8): up to 4 (one n-tile, hi/lo columns of q) or 5..8;

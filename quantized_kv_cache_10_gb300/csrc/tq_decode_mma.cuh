@@ -548,8 +548,8 @@ __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const
 // q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
 // qs[kGP][D] (rows >= G zero), with every global load in flight at once.
 template <int D, int NWC, bool RAW>
-__device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint32_t* signs, int G,
-                                               float* qs, int warp, int lane, int ctid) {
+__device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint16_t* qglob,
+                                               const uint32_t* signs, int G, float* qs, int warp, int lane, int ctid) {
     constexpr int NTH = NWC * 32;
     if constexpr (RAW) {
         // raw fp16 K is scored in the original basis: q' = q * log2(e) * scale
@@ -557,36 +557,56 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
         for (int i = ctid; i < kGP * D; i += NTH)
             qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) * f : 0.0f;
     } else if constexpr ((D & (D - 1)) == 0) {
-        // power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense one
+        // Power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense
+        // one.  Warp w < G rotates query row w in registers, straight from global memory
+        // (lane l holds dims [VPL l, VPL (l + 1))): H (s . q) by butterflies of stride < VPL
+        // inside the lane and the rest across lanes, natural (Sylvester) order.
+        constexpr int VPL = D / 32;
         if (warp < G) {
-            float* dst = qs + warp * D;
-            uint32_t hv[D / 32], sw[D / 32];
+            const uint16_t* src = qglob + warp * D + lane * VPL;
+            float x[VPL];
+            if constexpr (VPL == 8) {
+                const uint4 u = *reinterpret_cast<const uint4*>(src);
+                const uint32_t w4[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) {
-                hv[k] = qg[warp * D + lane + 32 * k];
-                sw[k] = signs[k];
+                for (int v = 0; v < 8; ++v)
+                    x[v] = __half2float(__ushort_as_half(static_cast<uint16_t>(w4[v / 2] >> (16 * (v & 1)))));
+            } else if constexpr (VPL == 4) {
+                const uint2 u = *reinterpret_cast<const uint2*>(src);
+                const uint32_t w2[2] = {u.x, u.y};
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    x[v] = __half2float(__ushort_as_half(static_cast<uint16_t>(w2[v / 2] >> (16 * (v & 1)))));
+            } else {
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) x[v] = __half2float(__ushort_as_half(src[v]));
             }
+            const uint32_t sw = signs[(lane * VPL) >> 5] >> ((lane * VPL) & 31);
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) {
-                const float v = __half2float(__ushort_as_half(static_cast<uint16_t>(hv[k])));
-                dst[lane + 32 * k] = ((sw[k] >> lane) & 1u) ? -v : v;
-            }
-            __syncwarp();
+            for (int v = 0; v < VPL; ++v)
+                if ((sw >> v) & 1u) x[v] = -x[v];
 #pragma unroll
-            for (int hh = 1; hh < D; hh <<= 1) {
+            for (int hh = 1; hh < VPL; hh <<= 1)
 #pragma unroll
-                for (int i0 = 0; i0 < D / 2; i0 += 32) {
-                    const int i = i0 + lane;
-                    const int lo = (i / hh) * (2 * hh) + (i % hh);
-                    const float x = dst[lo], y = dst[lo + hh];
-                    dst[lo] = x + y;
-                    dst[lo + hh] = x - y;
+                for (int v = 0; v < VPL; ++v)
+                    if (!(v & hh)) {
+                        const float p = x[v], q = x[v + hh];
+                        x[v] = p + q;
+                        x[v + hh] = p - q;
+                    }
+#pragma unroll
+            for (int lm = 1; lm < 32; lm <<= 1) {
+                const bool upper = (lane & lm) != 0;
+#pragma unroll
+                for (int v = 0; v < VPL; ++v) {
+                    const float y = __shfl_xor_sync(kFullMask, x[v], lm);
+                    x[v] = upper ? (y - x[v]) : (x[v] + y);
                 }
-                __syncwarp();
             }
             const float f = kLog2e * a.scale / (static_cast<float>(D) * a.ck.k_alpha);
+            float* dst = qs + warp * D + lane * VPL;
 #pragma unroll
-            for (int k = 0; k < D / 32; ++k) dst[lane + 32 * k] *= f;
+            for (int v = 0; v < VPL; ++v) dst[v] = x[v] * f;
         }
         for (int i = G * D + ctid; i < kGP * D; i += NTH) qs[i] = 0.0f;
     } else {
@@ -642,6 +662,18 @@ __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int 
     }
 }
 
+// float2 slot of (row, dims 2c and 2c + 1) in a warp's merge slice of kGP rows x D/2
+// units: row-major, with bits 0-1 of c XOR-ed by a Gray code of the row and, where the
+// lane's g does not already vary them, bits 2-3 by bits of c above bit 3.  In the
+// epilogue's stores (lane g, t: c = (D/16) g + dm, rows 2t / 2t + 1 or t) the 16 lanes
+// of a half-warp then hit 16 distinct 8-byte bank pairs.  Only bits 0-3 of c change and
+// the XOR depends on the row and on bits of c above bit 3 only: an involution per row.
+template <int D>
+__device__ __forceinline__ int merge_slot(int row, int c) {
+    const int fold = (D >= 256) ? ((c >> 4) & 3) << 2 : (D >= 128) ? ((c >> 4) & 1) << 2 : 0;
+    return row * (D / 2) + (c ^ (((row ^ (row >> 1)) & 3) | fold));
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -649,6 +681,9 @@ template <int D, int KB, int VB, int NT, bool MULTI, bool QJL>
 __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
+    // q is staged in shared memory by the producer for raw K and the dense rotation; with
+    // the Walsh-Hadamard rotation each consumer warp reads its query row itself
+    constexpr bool Q_STAGED = C::KRAW || (D & (D - 1)) != 0;
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
@@ -685,6 +720,15 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     }
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#ifdef TQ_TIMELINE
+    // stamps of consumer thread 0 (in spare bytes of the barrier area, not registers):
+    // entry, [the SM id], dependency wait passed, first tile consumed, own loop done, all
+    // warps' loops done, partial written, query ready
+    // (misc: barriers at 0..143, causal ends at 160..191, free 192..255, warp maxima from 256)
+    unsigned long long* tl_t = reinterpret_cast<unsigned long long*>(misc + 192);
+    static_assert(kTlStamps * 8 <= 64, "timeline stamps");
+#endif
+    TQ_TL(tl_t, 0);
     // blockIdx.y: (unit, group of <= kGP query rows); the unit's rows are its G query
     // heads times L query positions, head-major, contiguous in q and out
     // (the MULTI instantiation serves several query positions or more than kGP rows per
@@ -727,6 +771,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     __syncthreads();
 
     int issued = 0;  // tiles whose copies the producer has started (producer lane 0)
+    // tiles the producer issues before it reads the length: a ring-full, within max_seq
+    auto pre_tiles = [](int64_t t0_, int64_t chunk, int64_t max_seq) -> int {
+        const int64_t e = min(t0_ + chunk, max_seq);
+        const int64_t n = e > t0_ ? (e - t0_ + C::TS - 1) / C::TS : 0;
+        return static_cast<int>(min(n, static_cast<int64_t>(C::NSTAGE)));
+    };
     if (warp == C::NWC) {
         // ------------------------------------------------------------ producer
         // (lanes 1-31 issue nothing and never trigger the dependent launch: the
@@ -769,20 +819,16 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             }
             asm volatile("griddepcontrol.wait;" ::: "memory");
             allow_dependent_launch();
-            mbar_arrive_expect_tx(setup_q, qbytes);
-            bulk_g2s(pro + C::PRO_Q, a.q + qrow0 * D, qbytes, setup_q);
-            t1 = min(clamped_len(a, b), t0 + p.chunk);
-            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+            if constexpr (Q_STAGED) {
+                mbar_arrive_expect_tx(setup_q, qbytes);
+                bulk_g2s(pro + C::PRO_Q, a.q + qrow0 * D, qbytes, setup_q);
+            }
             const uint8_t* kg = static_cast<const uint8_t*>(a.k);
-            for (int it = 0; it < ntiles; ++it) {
+            // Tile `it` of the token range [t0, tend): its copies into stage it % NSTAGE.
+            auto issue = [&](int it, int64_t tend) {
                 const int s = it % C::NSTAGE;
-                if (it >= C::NSTAGE && !mbar_wait(empty + s, ((it / C::NSTAGE) - 1) & 1)) {
-                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
-                    *s_abort = 1;
-                    break;
-                }
                 const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
-                const int64_t nv = min(static_cast<int64_t>(C::TS), t1 - ts);
+                const int64_t nv = min(static_cast<int64_t>(C::TS), tend - ts);
                 const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
                 uint8_t* st = stage_ptr(s);
                 const uint32_t vbytes = n8 * C::BPV, nbytes = n8 * 2;
@@ -807,10 +853,37 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 }
                 bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
                 bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
+            };
+            // The first ring-full of tiles goes out before the sequence length is known, sized
+            // by max_seq (every copy stays inside the caller's cache); the consumers mask the
+            // tokens past the length, and tiles past it are drained unconsumed.
+            const int pre = pre_tiles(t0, p.chunk, a.max_seq);
+            for (int it = 0; it < pre; ++it) issue(it, min(t0 + p.chunk, a.max_seq));
+            t1 = min(clamped_len(a, b), t0 + p.chunk);
+            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+            issued = pre;
+            for (int it = pre; it < ntiles; ++it) {
+                const int s = it % C::NSTAGE;
+                if (it >= C::NSTAGE && !mbar_wait(empty + s, ((it / C::NSTAGE) - 1) & 1)) {
+                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                    break;
+                }
+                issue(it, t1);
                 issued = it + 1;
+            }
+            // Tiles issued before the length was known that lie past it are never consumed:
+            // their copies land before the consumers reuse the ring for the merge.
+            for (int it = ntiles; it < pre; ++it) {
+                if (!mbar_wait(full + (it % C::NSTAGE), (it / C::NSTAGE) & 1)) {
+                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                    *s_abort = 1;
+                    break;
+                }
             }
         }
         __syncwarp();  // reconverge the producer warp before the block-wide barriers
+        asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
     } else {
         // ------------------------------------------------------------ consumers: prologue
         const int ctid = tid;  // 0 .. C::NWC * 32 - 1
@@ -819,9 +892,17 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             // Every prologue read of global memory is issued at once (one memory
             // latency for the CTA, not one per loop iteration).
             bool ok = __all_sync(kFullMask, mbar_wait(setup, 0));
+#ifdef TQ_TIMELINE
+            if (threadIdx.x == 0) {  // slot 1: the SM this CTA runs on
+                unsigned sm;
+                asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+                tl_t[1] = sm;
+            }
+#endif
             replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
                                 reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
             asm volatile("griddepcontrol.wait;" ::: "memory");
+            TQ_TL(tl_t, 2);
             // Past the wait, everything stream-ordered before this kernel is complete: the
             // combine kernel that follows may start (and read the call's inputs) once every
             // CTA has triggered, which each CTA does only after one of its threads has
@@ -830,13 +911,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             len = clamped_len(a, b);
             t1 = min(len, t0 + p.chunk);
             ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
-            ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
+            if constexpr (Q_STAGED) ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
             if (!ok && lane == 0) {
                 atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
                 *s_abort = 1;
             }
-            rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
-                              reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp, lane, ctid);
+            rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q), a.q + qrow0 * D,
+                                               reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp,
+                                               lane, ctid);
             if (MULTI && ctid < kGP) {
                 // Causal end of each query row, as tokens past t0: the rows' positions are the
                 // last L of the sequence (packed tokens, then tail), so every packed token is
@@ -848,6 +930,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+        TQ_TL(tl_t, 7);
 
         const int g = lane >> 2, t = lane & 3;
         // q' B fragments: Bq[kt][nt][2] (in shared memory for D > 128)
@@ -977,6 +1060,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 }
                 break;
             }
+#ifdef TQ_TIMELINE
+            if (it == 0) TQ_TL(tl_t, 3);
+#endif
             const uint8_t* st = stage_ptr(s);
             const uint8_t* kbuf = st;
             const uint8_t* vbuf = st + C::KBUF;
@@ -1241,6 +1327,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             if (lane == 0) mbar_arrive(empty + s);
         }
         // ------------------------------------------------------------ warp totals
+        TQ_TL(tl_t, 4);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 4);
@@ -1259,8 +1346,10 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 wl[warp * kGP + 4 + t] = 0.0f;
             }
         }
-        // every consumer is done with the ring; wm / wl are visible
-        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+        // every consumer is done with the ring, wm / wl are visible, and the producer has no
+        // copy in flight (barrier 2 counts the producer warp's arrival)
+        asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+        TQ_TL(tl_t, 5);
         float f[NT];
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
@@ -1270,29 +1359,29 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             // the V table holds v_alpha * c: divide it out here, once per output
             f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M) / a.cv.v_alpha;
         }
-        float* slice = reinterpret_cast<float*>(ring) + warp * kGP * D;
+        // Each warp's O slice goes to shared memory as float2 units (dims 2c, 2c + 1 of one
+        // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
+        // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
+        // of a row parity on the same two banks).
+        float2* slice = reinterpret_cast<float2*>(ring) + warp * (kGP * D / 2);
 #pragma unroll
         for (int dm = 0; dm < C::KT; ++dm) {
-            const int d0 = (D / 8) * g + 2 * dm;
+            const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
             if constexpr (NT == 2) {
-                slice[(2 * t) * D + d0] = f[0] * O[dm][0];
-                slice[(2 * t + 1) * D + d0] = f[1] * O[dm][1];
-                slice[(2 * t) * D + d0 + 1] = f[0] * O[dm][2];
-                slice[(2 * t + 1) * D + d0 + 1] = f[1] * O[dm][3];
+                slice[merge_slot<D>(2 * t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
+                slice[merge_slot<D>(2 * t + 1, c)] = make_float2(f[1] * O[dm][1], f[1] * O[dm][3]);
             } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
-                slice[t * D + d0] = f[0] * (O[dm][0] + O[dm][1]);
-                slice[t * D + d0 + 1] = f[0] * (O[dm][2] + O[dm][3]);
-                slice[(4 + t) * D + d0] = 0.0f;
-                slice[(4 + t) * D + d0 + 1] = 0.0f;
+                slice[merge_slot<D>(t, c)] = make_float2(f[0] * (O[dm][0] + O[dm][1]), f[0] * (O[dm][2] + O[dm][3]));
+                slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
             } else {
-                slice[t * D + d0] = f[0] * O[dm][0];
-                slice[t * D + d0 + 1] = f[0] * O[dm][2];
-                slice[(4 + t) * D + d0] = 0.0f;
-                slice[(4 + t) * D + d0 + 1] = 0.0f;
+                slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
+                slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-        // fixed-order sum of the warp slices, straight into this CTA's partial record
+        // fixed-order sum of the warp slices, straight into this CTA's partial record: thread i
+        // sums the float4 at physical units 2i, 2i + 1 of every slice (the same swizzled place
+        // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
         float* part = partial_ptr(a.ws, p, vu, split, D);
         const float4* all4 = reinterpret_cast<const float4*>(ring);
         float4* part4 = reinterpret_cast<float4*>(part);
@@ -1306,7 +1395,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 acc.z += x.z;
                 acc.w += x.w;
             }
-            part4[i] = acc;
+            const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
+            const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
+            part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
         }
         if (tid < kGP) {
             const int q = tid;
@@ -1322,6 +1413,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
         }
     }
     __syncthreads();
+#ifdef TQ_TIMELINE
+    TQ_TL(tl_t, 6);
+    if (tid == 0 && a.tl) {
+        unsigned long long* r = tl_record(a, false, blockIdx.y * gridDim.x + blockIdx.x);
+        if (r)
+            for (int i = 0; i < kTlStamps; ++i) r[i] = tl_t[i];
+    }
+#endif
     if (warp == C::NWC && lane == 0 && *s_abort) {
         // a wait gave up: let every copy this CTA issued land before shared memory is released
         for (int it = (issued > C::NSTAGE ? issued - C::NSTAGE : 0); it < issued; ++it) {
@@ -1338,7 +1437,7 @@ cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t r
 
 // Launch of one instantiation; split plan for one CTA per SM.
 template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false>
-cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
@@ -1360,6 +1459,7 @@ cudaError_t launch_inst(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s
     cfg.gridDim = dim3(p.n_split, p.n_units * p.q_chunks);
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM;
+    p.decode_smem = C::SMEM;  // the combine kernel sizes its footprint against it
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1394,7 +1494,7 @@ constexpr int kSchemes[][2] = {{4, 4}, {3, 3}, {2, 2}, {4, 2}, {4, 3}, {8, 3}, {
                                {16, 4}, {16, 2}, {16, 3}};
 
 template <int D>
-cudaError_t launch_mma_d(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
+cudaError_t launch_mma_d(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
     TQ_MMA_CASE(4, 4)
     TQ_MMA_CASE(3, 3)
     TQ_MMA_CASE(2, 2)

@@ -5,10 +5,10 @@
 namespace tq {
 
 template <int D>
-cudaError_t launch_mma_d_extern(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
+cudaError_t launch_mma_d_extern(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
 
 template <>
-cudaError_t launch_mma_d_extern<96>(const DecodeArgs& a, const DecodePlan& p, int kb, int vb, int nt,
+cudaError_t launch_mma_d_extern<96>(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt,
                                      cudaStream_t st) {
     return mma_detail::launch_mma_d<96>(a, p, kb, vb, nt, st);
 }

@@ -270,6 +270,7 @@ bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int L, int64_t 
     plan.chunk = chunk;
     plan.n_split = int((max_seq + chunk - 1) / chunk);
     plan.part_offset = 256;  // after the device error word
+    plan.decode_smem = 0;    // set by the tensor-core launcher
     plan.ws_bytes = plan.part_offset + size_t(vunits) * plan.n_split * kGP * (d + 2) * sizeof(float);
     return true;
 }

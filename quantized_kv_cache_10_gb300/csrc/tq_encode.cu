@@ -232,15 +232,11 @@ __device__ __noinline__ int exact_code(int64_t w, double D, const double* mid, i
 // Two jobs (e.g. the K and the V pending batch, each with its own codec) may
 // share one launch: blocks [0, grid0) take job 0, the rest job 1.
 template <int E>
-__global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams p0, const EncParams p1, int grid0) {
+__device__ __forceinline__ void encode_wht_body(const EncParams& p, int64_t blk, int64_t nblk) {
     __shared__ float s_thr[kWarps][256];         // 8-bit codes: fp32 thresholds of one vector
     __shared__ int64_t s_ithr[kWarps][32 * 15];  // 2-4 bit codes: integer thresholds of 32 vectors
     __shared__ uint32_t s_pack[kWarps][128];
     __shared__ float s_mid[256];
-    const bool job1 = static_cast<int>(blockIdx.x) >= grid0;
-    const EncParams& p = job1 ? p1 : p0;
-    const int64_t blk = job1 ? blockIdx.x - grid0 : blockIdx.x;
-    const int64_t nblk = job1 ? gridDim.x - grid0 : grid0;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int L = 1 << p.bits;
     // codec data (written by no kernel) before the dependency wait
@@ -375,16 +371,20 @@ __global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const EncParams
     }
 }
 
+template <int E>
+__global__ void __launch_bounds__(kWarps * 32) encode_wht_kernel(const __grid_constant__ EncParams p0,
+                                                                 const __grid_constant__ EncParams p1, int grid0) {
+    if (static_cast<int>(blockIdx.x) < grid0)
+        encode_wht_body<E>(p0, blockIdx.x, grid0);
+    else
+        encode_wht_body<E>(p1, blockIdx.x - grid0, gridDim.x - grid0);
+}
+
 constexpr int kDenseWarps = 4;
 constexpr int kDenseMaxE = 15;
 
 // Other dims (multiple of 32, not a power of two): E = dim / 32 at run time.
-__global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const EncParams p0, const EncParams p1,
-                                                                         int grid0) {
-    const bool job1 = static_cast<int>(blockIdx.x) >= grid0;
-    const EncParams& p = job1 ? p1 : p0;
-    const int64_t blk = job1 ? blockIdx.x - grid0 : blockIdx.x;
-    const int64_t nblk = job1 ? gridDim.x - grid0 : grid0;
+__device__ __forceinline__ void encode_dense_body(const EncParams& p, int64_t blk, int64_t nblk) {
     __shared__ double s_thr[kDenseWarps][256];
     __shared__ uint32_t s_pack[kDenseWarps][128];
     __shared__ double s_k[kDenseWarps][kDenseMaxE * 32];
@@ -437,6 +437,15 @@ __global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const En
         if (lane == 0) p.norms[dst] = __half_as_ushort(__double2half(ldexp(D, -24)));
         __syncwarp();
     }
+}
+
+__global__ void __launch_bounds__(kDenseWarps * 32) encode_dense_kernel(const __grid_constant__ EncParams p0,
+                                                                         const __grid_constant__ EncParams p1,
+                                                                         int grid0) {
+    if (static_cast<int>(blockIdx.x) < grid0)
+        encode_dense_body(p0, blockIdx.x, grid0);
+    else
+        encode_dense_body(p1, blockIdx.x - grid0, gridDim.x - grid0);
 }
 
 // Parameters and grid of one encode job (vb and the grid depend on the vector count).

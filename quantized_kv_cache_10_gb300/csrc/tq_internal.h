@@ -106,6 +106,7 @@ struct DecodePlan {
     int64_t chunk;       // tokens per split (multiple of 8 / tile)
     size_t ws_bytes;     // total workspace bytes
     size_t part_offset;  // byte offset of the split-K partial records
+    int decode_smem;     // dynamic shared memory of the decode kernel launched (0: unknown)
 };
 
 // Split-K plan (independent of the kernel chosen, so the workspace size only
@@ -166,7 +167,16 @@ struct DecodeArgs {
     // last L positions of each sequence (packed tokens, then tail tokens) and each attends
     // to the tokens up to its own position (L == 1: every token)
     int L;
+    // phase-timeline buffer of a profiling build (tq_debug_set_timeline), else null, and
+    // the call's index (its parity selects the half of the buffer the call writes)
+    unsigned long long* tl;
+    unsigned int tl_seq;
 };
+
+// The timeline buffer registered with tq_debug_set_timeline (profiling builds), else null;
+// its layout (tq_decode_common.cuh): 2 + 2 * 2 * kTlSlotsHost * kTlStampsHost words.
+unsigned long long* timeline_buffer();
+constexpr int kTlSlotsHost = 4096, kTlStampsHost = 8;
 
 cudaError_t launch_decode_simt(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st);
 // Returns cudaErrorNotSupported when no tensor-core instantiation matches.
