@@ -321,6 +321,63 @@ def encode_sweep(tq, dev, stream, peak_gbs, sm_mhz, sizes=None, d=256, bits_list
                            f"{sm_mhz:.0f} MHz"}
 
 
+def e2e_from_c(tq, ck, cv, w, K, V, q, lens, pos, k_new, v_new, out, kc, kn, vc, vn, R, wsb, stream, steps,
+               warmup, PB, bytes_step, world, graph_steps=0):
+    """The same steps driven from a C loop over the C ABI (libtq_e2e.so): per step the
+    host->device copy of q and the lengths from pinned memory on a copy stream (every 64th
+    step also the pending K/V batch and its positions, then tq_encode_append_kv), one
+    tq_decode_attend, and the device->host copy of the output; CUDA events on the stream."""
+    import ctypes
+    import torch
+    path = os.path.join(ROOT, "quantized_kv_cache_10_gb300", "libtq_e2e.so")
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    f = lib.tq_e2e_decode_steps
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    f.argtypes = [vp, vp, i32, i32, i32, i64, i32, vp, sz, sz] + [vp] * 4 + [vp, vp, vp, vp, i32, vp, sz] + \
+        [vp] * 5 + \
+        [i32, i32, i32, vp] + [ctypes.POINTER(ctypes.c_double)] * 4
+    f.restype = i32
+    # the step's inputs in one staging buffer: the query block, then the lengths (16-byte aligned)
+    qb = w.B * w.Hq * w.d * 2
+    off = (qb + 15) // 16 * 16
+    h_in = torch.zeros(off + 4 * w.B, dtype=torch.uint8).pin_memory()
+    h_in[:qb].copy_(torch.from_numpy(w.q()).view(torch.uint8).reshape(-1))
+    h_in[off:].copy_(torch.from_numpy(w.lengths()).view(torch.uint8))
+    stride = (h_in.numel() + 255) // 256 * 256                 # two device input buffers (ping-pong)
+    d_in = torch.empty(2 * stride, dtype=torch.uint8, device=q.device)
+    h_pos = torch.from_numpy(w.lengths() - PB).pin_memory()
+    h_k = torch.from_numpy(np.ascontiguousarray(K[:, :, -PB:])).pin_memory()
+    h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -PB:])).pin_memory()
+    h_out = torch.empty((2, w.B, w.Hq, w.d), dtype=torch.float16).pin_memory()
+    d_out2 = torch.empty((2, w.B, w.Hq, w.d), dtype=torch.float16, device=q.device)
+    sec, hsec, h2d, d2h = ctypes.c_double(), ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    if graph_steps:                       # a stream that can be captured (not the legacy default stream)
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream()
+    rc = f(ck.handle, cv.handle, w.B, w.Hq, w.Hkv, w.S, PB, d_in.data_ptr(), off, stride, pos.data_ptr(),
+           k_new.data_ptr(), v_new.data_ptr(), d_out2.data_ptr(), kc.data_ptr(), kn.data_ptr(), vc.data_ptr(),
+           vn.data_ptr(), R, wsb.data_ptr(), wsb.numel(), h_in.data_ptr(), h_pos.data_ptr(),
+           h_k.data_ptr(), h_v.data_ptr(), h_out.data_ptr(), warmup, steps, graph_steps, stream.cuda_stream,
+           ctypes.byref(sec), ctypes.byref(hsec), ctypes.byref(h2d), ctypes.byref(d2h))
+    if rc != 0:
+        raise RuntimeError(f"end-to-end C loop failed with code {rc}")
+    v = job_throughput(bytes_step * steps, world, max_over_ranks(sec.value, q.device)) / 1e9
+    if graph_steps:
+        return {"value": v, "unit": "GB/s", "h2d_bytes_per_step": h2d.value, "d2h_bytes_per_step": d2h.value,
+                "host_us_per_step": hsec.value * 1e6,
+                "driver": f"the same C loop's steps captured once as CUDA graphs of {graph_steps} steps (copies, "
+                          "encode and decode-attention calls as recorded) and replayed"}
+    return {"value": v, "unit": "GB/s", "h2d_bytes_per_step": h2d.value, "d2h_bytes_per_step": d2h.value,
+            "host_us_per_step": hsec.value * 1e6,
+            "driver": "C loop over the C ABI (libtq_e2e.so): per step one cudaMemcpyAsync of the query block and "
+                      "lengths (pinned, double-buffered, on an input copy stream overlapping the previous step), one "
+                      "tq_decode_attend, one cudaMemcpyAsync of the output back (double-buffered, own stream); every 64th "
+                      "step the K/V batch "
+                      "copies and tq_encode_append_kv"}
+
+
 def gpu_arm(args):
     import torch
     ws_, rank, local = _dist()
@@ -623,7 +680,15 @@ def gpu_arm(args):
     if not args.no_encode_sweep:
         sweep = encode_sweep(tq, dev, stream, peak, _sm_mhz())
 
-    # ---- end to end through the public API: pinned host inputs in, output back ----
+    # ---- end to end through the C ABI, driven from C: pinned host inputs in, output back ----
+    e2e_c = e2e_g = None
+    if w.k_bits != 16 and replica_mode:
+        e2e_c = e2e_from_c(tq, ck, cv, w, K, V, q, lens, pos, k_new, v_new, out, kc, kn, vc, vn, R, wsb, stream,
+                           args.steps, args.warmup, PB, bytes_step, ws_)
+        e2e_g = e2e_from_c(tq, ck, cv, w, K, V, q, lens, pos, k_new, v_new, out, kc, kn, vc, vn, R, wsb, stream,
+                           max(args.steps, PB), args.warmup, PB, bytes_step, ws_, graph_steps=PB)
+
+    # ---- end to end through the Python binding: pinned host inputs in, output back ----
     h_q = torch.from_numpy(w.q()).pin_memory()
     h_k = torch.from_numpy(np.ascontiguousarray(K[:, :, -PB:])).pin_memory()
     h_v = torch.from_numpy(np.ascontiguousarray(V[:, :, -PB:])).pin_memory()
@@ -705,7 +770,11 @@ def gpu_arm(args):
         "qjl": qjl,
         "encode": {"value": enc_mvec, "unit": "Mvec/s", "n_vec": n_enc, "dim": w.d},
         "encode_sweep": sweep,
-        "e2e": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": e2e_c if e2e_c else {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                                    "d2h_bytes_per_step": d2h, "driver": "Python binding"},
+        "e2e_graph": e2e_g,
+        "e2e_python": {"value": e2e_v, "unit": "GB/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                       "driver": "Python binding (ctypes) per call"},
         "gpu_launches": launches,
         "clocks": clk.summary(),
         "cpu_baseline": cpu,

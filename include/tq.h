@@ -331,19 +331,25 @@ tq_status tq_decode_attend_qjl(const tq_codec *ck, const tq_codec *cv, const uin
  * tq_cache_prefill, released by tq_cache_destroy); it keeps host-side counters,
  * so calls on one cache must come from one host thread in order, on one stream
  * (or streams the caller orders).  Codecs must outlive the cache.
- *   tq_cache_create   ck, cv as for tq_decode_attend; max_seq % 8 == 0.
+ *   tq_cache_create   ck, cv as for tq_decode_attend; max_seq % 8 == 0 (tokens per
+ *                     sequence the cache holds); min_tokens in [0, 4096]: the first
+ *                     min_tokens tokens of every sequence stay fp16 for good (sink
+ *                     tokens, turboquant-mlx guide "KV cache compression",
+ *                     --kv-min-tokens), scored exactly in the same softmax; the
+ *                     rest are packed as above.
  *   tq_cache_prefill  k, v: device fp16 [B, n_kv_heads, T, dim]; only before the
  *                     first decode step, once.
  *   tq_cache_decode   q: device fp16 [B, n_q_heads, dim]; k_new, v_new: device
  *                     fp16 [B, n_kv_heads, dim]; out: device fp16 [B, n_q_heads,
  *                     dim].  TQ_ERR_INVALID_ARG once max_seq tokens are held.
- *   tq_cache_info     tokens held, packed, pending; bytes in use (packed bytes of
- *                     the packed tokens, 4*dim bytes per fp16 token, per KV head).
+ *   tq_cache_info     tokens held (sinks included), packed, pending; bytes in use
+ *                     (packed bytes of the packed tokens, 4*dim bytes per fp16
+ *                     token -- sink, pending or prefill -- per KV head).
  *   tq_cache_device_error  reads and clears the device error words (syncs).
  */
 typedef struct tq_cache tq_cache;
 tq_status tq_cache_create(const tq_codec *ck, const tq_codec *cv, int B, int n_q_heads, int n_kv_heads,
-                          int64_t max_seq, tq_cache **out);
+                          int64_t max_seq, int min_tokens, tq_cache **out);
 void tq_cache_destroy(tq_cache *cache);
 tq_status tq_cache_prefill(tq_cache *cache, const uint16_t *k, const uint16_t *v, int T, void *stream);
 tq_status tq_cache_decode(tq_cache *cache, const uint16_t *q, const uint16_t *k_new, const uint16_t *v_new,

@@ -65,7 +65,7 @@ _sig = {
     "tq_encode_qjl": (_i32, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp, _i64, _vp, _vp]),
     "tq_decode_attend_qjl": (_i32, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i64,
                                     C.c_float, _vp, _vp, _sz, _vp]),
-    "tq_cache_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, C.POINTER(_vp)]),
+    "tq_cache_create": (_i32, [_vp, _vp, _i32, _i32, _i32, _i64, _i32, C.POINTER(_vp)]),
     "tq_cache_destroy": (None, [_vp]),
     "tq_cache_prefill": (_i32, [_vp, _vp, _vp, _i32, _vp]),
     "tq_cache_decode": (_i32, [_vp, _vp, _vp, _vp, C.c_float, _vp, _vp]),
@@ -433,12 +433,14 @@ def tq_decode_attend_qjl(ck: Codec, cv: Codec, q: torch.Tensor, k_codes: torch.T
 class KVCache:
     """The two-phase KV cache of one layer (tq_cache_*): raw fp16 prefill compressed on the
     first decode step, then per step attend + append with pending tokens kept in fp16 and
-    encoded 64 at a time.  Owns its device memory."""
+    encoded 64 at a time; the first min_tokens tokens of every sequence stay fp16 (sink
+    tokens).  Owns its device memory."""
 
-    def __init__(self, ck: Codec, cv: Codec, B: int, n_q_heads: int, n_kv_heads: int, max_seq: int):
+    def __init__(self, ck: Codec, cv: Codec, B: int, n_q_heads: int, n_kv_heads: int, max_seq: int,
+                 min_tokens: int = 0):
         h = _vp()
-        _check(_lib.tq_cache_create(ck.handle, cv.handle, B, n_q_heads, n_kv_heads, max_seq, C.byref(h)),
-               "tq_cache_create")
+        _check(_lib.tq_cache_create(ck.handle, cv.handle, B, n_q_heads, n_kv_heads, max_seq, min_tokens,
+                                    C.byref(h)), "tq_cache_create")
         self._h, self._codecs = h.value, (ck, cv)   # the codecs must outlive the cache
         self.B, self.Hq, self.Hkv, self.dim = B, n_q_heads, n_kv_heads, cv.dim
 

@@ -101,5 +101,31 @@ def build(verbose: bool = False, variant: str | None = None) -> str:
     return lib_path
 
 
+E2E_SRC = os.path.join(CSRC, "e2e", "tq_e2e_loop.cpp")
+E2E_LIB = os.path.join(PKG, "libtq_e2e.so")
+
+
+def build_e2e(verbose: bool = False) -> str:
+    """The benchmark's end-to-end driver (libtq_e2e.so): a C loop over the public C ABI,
+    linked against libtq.so; returns its path."""
+    lib = build(verbose=verbose)
+    cuda = _cuda_home()
+    stamp = os.path.join(BUILD, "libtq_e2e.stamp")
+    if os.path.exists(E2E_LIB) and os.path.exists(stamp) and \
+            os.path.getmtime(E2E_LIB) >= max(os.path.getmtime(E2E_SRC), os.path.getmtime(lib)):
+        return E2E_LIB
+    tmp = E2E_LIB + f".tmp{os.getpid()}"
+    cmd = [os.path.join(cuda, "bin", "nvcc"), "-O2", "-std=c++17", "-shared", "-Xcompiler", "-fPIC", "-I", INC,
+           "-x", "c++", E2E_SRC, "-o", tmp, "-L", PKG, "-ltq", "-cudart", "shared",
+           "-Xlinker", "-rpath,$ORIGIN", "-Xlinker", "-rpath," + os.path.join(cuda, "lib64")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed: {' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, E2E_LIB)
+    with open(stamp, "w") as f:
+        f.write(E2E_LIB + "\n")
+    return E2E_LIB
+
+
 if __name__ == "__main__":
     build(verbose="-v" in sys.argv, variant="timeline" if "--timeline" in sys.argv else None)

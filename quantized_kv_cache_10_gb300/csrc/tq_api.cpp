@@ -154,8 +154,8 @@ tq_status tq_encode_append_kv(const tq_codec* ck, const tq_codec* cv, const uint
     if (dev_error && !aligned(dev_error, 4)) return TQ_ERR_INVALID_ARG;
     if (!on_codec_device(ck) || !on_codec_device(cv)) return TQ_ERR_INVALID_ARG;
     const tq::EncodeJob jobs[2] = {
-        {ck, k, 0, ck->dim, k_codes, ck->bytes_per_vec, k_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error},
-        {cv, v, 0, cv->dim, v_codes, cv->bytes_per_vec, v_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error}};
+        {ck, k, 0, ck->dim, k_codes, ck->bytes_per_vec, k_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error, T},
+        {cv, v, 0, cv->dim, v_codes, cv->bytes_per_vec, v_norms, B, n_kv_heads, T, start_pos, max_seq, dev_error, T}};
     return from_cuda(tq::launch_encode_jobs(jobs, 2, static_cast<cudaStream_t>(stream)));
 }
 

@@ -30,8 +30,9 @@ struct EncParams {
     uint8_t* codes;
     int64_t cstride;
     uint16_t* norms;
-    // append mode when B > 0
+    // append mode when B > 0: x is planes of xplane >= T rows per (sequence, head)
     int B, H, T;
+    int64_t xplane;
     const int32_t* start_pos;
     int64_t max_seq;
     int32_t* dev_error;
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool map_row(const EncParams& p, int64_t v, const uin
     const int64_t rem = v - b * per_b;
     const int64_t h = rem / p.T;
     const int64_t t = rem - h * p.T;
-    src = p.x + v * p.dim;
+    src = p.x + ((b * p.H + h) * p.xplane + t) * p.dim;
     const int64_t pos = static_cast<int64_t>(__ldg(p.start_pos + b)) + t;
     if (pos < 0 || pos >= p.max_seq) return false;
     dst = (b * p.H + h) * p.max_seq + pos;
@@ -301,7 +302,9 @@ __device__ __forceinline__ void encode_wht_body(const EncParams& p, int64_t blk,
             if (dst < 0) continue;
             const double D = __shfl_sync(kFull, myD, jv);
             const float Df = __shfl_sync(kFull, myDf, jv);
-            const uint16_t* src = p.B > 0 ? p.x + (v0 + jv) * p.dim : p.x + (v0 + jv) * p.xstride;
+            const uint16_t* src;
+            int64_t dst_unused;
+            map_row(p, v0 + jv, src, dst_unused);
             uint32_t hv[E];
             load_row<E>(src, lane, E, hv);
             int64_t k[E];
@@ -461,6 +464,7 @@ static EncParams make_params(const EncodeJob& j, int sms, int& grid) {
     p.B = j.B;
     p.H = j.H;
     p.T = j.T;
+    p.xplane = j.xplane > 0 ? j.xplane : j.T;
     p.start_pos = j.start_pos;
     p.max_seq = j.max_seq;
     p.dev_error = j.dev_error;
@@ -531,7 +535,7 @@ cudaError_t launch_encode(const tq_codec* c, const uint16_t* x, int64_t n, int64
                           uint8_t* codes, int64_t cstride, uint16_t* norms, int B, int H, int T,
                           const int32_t* start_pos, int64_t max_seq, int32_t* dev_error,
                           cudaStream_t st) {
-    const EncodeJob j{c, x, n, xstride, codes, cstride, norms, B, H, T, start_pos, max_seq, dev_error};
+    const EncodeJob j{c, x, n, xstride, codes, cstride, norms, B, H, T, start_pos, max_seq, dev_error, T};
     return launch_encode_jobs(&j, 1, st);
 }
 

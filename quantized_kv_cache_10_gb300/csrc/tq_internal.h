@@ -79,6 +79,7 @@ struct EncodeJob {
     const int32_t* start_pos;
     int64_t max_seq;
     int32_t* dev_error;
+    int64_t xplane;  // append mode: rows of x per (sequence, head) plane (>= T; 0: T, contiguous)
 };
 // One or two jobs (same dim and rotation kind, e.g. the K and the V pending batch)
 // in one launch.

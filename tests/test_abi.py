@@ -88,5 +88,5 @@ def test_host_side_checks_of_the_newer_entry_points(lib):
     assert lib.tq_encode_append_kv(None, None, None, None, 1, 8, 64, None, 128, None, None, None, None, None,
                                    None) == 1
     # the cache refuses missing codecs
-    lib.tq_cache_create.argtypes = [vp, vp, i32, i32, i32, i64, C.POINTER(vp)]
-    assert lib.tq_cache_create(None, None, 1, 8, 1, 64, C.byref(h)) == 1
+    lib.tq_cache_create.argtypes = [vp, vp, i32, i32, i32, i64, i32, C.POINTER(vp)]
+    assert lib.tq_cache_create(None, None, 1, 8, 1, 64, 0, C.byref(h)) == 1
