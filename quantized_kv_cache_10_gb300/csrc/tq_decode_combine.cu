@@ -241,9 +241,16 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 6 ? 8 : 4)) decode
     // wait for this call's decode grid (and the visibility of its records)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     TQ_TL(tl_t, 1);
-    const int ns = p.n_split;
+    // the unit's records: n_split of them, or, on the token-balanced schedule, the slots
+    // its index entry lists (none while the sequence is empty)
+    int ns = p.n_split;
     const int rec = kGP * (D + 2);
     const float* base = partial_ptr(a.ws, p, vu, 0, D);
+    if (p.stream) {
+        const int2 ix = __ldcg(unit_index_ptr(a.ws, p, u));
+        ns = (__ldg(a.seq_lens + b) > 0) ? ix.y : 0;
+        base = partial_slot_ptr(a.ws, p, ns > 0 ? ix.x : 0, D);
+    }
     const float* ob = base + g * D + lane * VPL;
 
     constexpr int CH = VPL <= 4 ? 5 : (VPL <= 8 ? 4 : 2);

@@ -29,6 +29,17 @@ __device__ __forceinline__ float* partial_ptr(void* ws, const DecodePlan& p, int
     return base + (static_cast<int64_t>(vu) * p.n_split + split) * (kGP * (d + 2));
 }
 
+// Partial record at slot `slot` of the token-balanced schedule (CTA c, unit u: slot c + u).
+__device__ __forceinline__ float* partial_slot_ptr(void* ws, const DecodePlan& p, int64_t slot, int d) {
+    float* base = reinterpret_cast<float*>(static_cast<char*>(ws) + p.part_offset);
+    return base + slot * (kGP * (d + 2));
+}
+
+// {first slot, count} of unit u's records under the token-balanced schedule.
+__device__ __forceinline__ int2* unit_index_ptr(void* ws, const DecodePlan& p, int u) {
+    return reinterpret_cast<int2*>(static_cast<char*>(ws) + p.idx_offset) + u;
+}
+
 __device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int32_t*>(ws); }
 
 // Clamped sequence length of batch b (flags out-of-range values).

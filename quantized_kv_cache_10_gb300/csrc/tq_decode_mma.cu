@@ -181,6 +181,15 @@ template <>
 cudaError_t launch_mma_d_extern<128>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 template <>
 cudaError_t launch_mma_d_extern<256>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
+template <int D>
+cudaError_t launch_mma_d_stream_extern(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st);
+// defined in tq_decode_mma_d{64,128,256}_stream.cu
+template <>
+cudaError_t launch_mma_d_stream_extern<64>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
+template <>
+cudaError_t launch_mma_d_stream_extern<128>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
+template <>
+cudaError_t launch_mma_d_stream_extern<256>(const DecodeArgs&, DecodePlan&, int, int, int, cudaStream_t);
 
 cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     // query rows per CTA, min(S, 8): up to 4 (one n-tile, hi/lo columns of q) or 5..8;
@@ -215,6 +224,24 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
         p.chunk = chunk;
     }
     cudaError_t e = cudaErrorNotSupported;
+    // Several sequences, one query position: the token-balanced schedule, one CTA per SM
+    // over all units' tokens (ragged lengths and unit counts that do not fill whole waves
+    // leave no SM idle).  It needs the power-of-two (Walsh-Hadamard) dims and coded keys.
+    const int d = a.cv.dim;
+    if (a.B > 1 && !multi && !a.k_signs && a.ck.bits != 16 && (d & (d - 1)) == 0 &&
+        sms + int64_t(p.n_units) <= p0.n_rec) {
+        p.stream = 1;
+        p.n_cta = static_cast<int>(sms);
+        switch (d) {
+            case 64: e = launch_mma_d_stream_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+            case 128: e = launch_mma_d_stream_extern<128>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+            case 256: e = launch_mma_d_stream_extern<256>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
+            default: break;
+        }
+        if (e != cudaErrorNotSupported) return e;
+        p.stream = 0;
+        p.n_cta = 0;
+    }
     switch (a.cv.dim) {
         case 64: e = launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
         case 96: e = launch_mma_d_extern<96>(a, p, a.ck.bits, a.cv.bits, nt, st); break;

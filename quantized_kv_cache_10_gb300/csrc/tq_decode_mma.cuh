@@ -675,15 +675,124 @@ __device__ __forceinline__ int merge_slot(int row, int c) {
 }
 
 // ---------------------------------------------------------------------------
+// Token-balanced schedule (several sequences, one query position)
+// ---------------------------------------------------------------------------
+// The units' tokens are laid end to end in unit order (u = b * Hkv + h), unit u
+// spanning len_b rounded up to a multiple of 8 positions, and CTA c takes positions
+// [c W, (c + 1) W), W = the total over the CTAs rounded up to 8 (at least kStreamMinW).
+// Every boundary is a multiple of 8, so each segment of a unit starts on an 8-token
+// boundary (16-byte aligned copies) and holds at least one real token.  Every warp that
+// needs the segments walks them itself (warp-collective, same result in each).
+constexpr int64_t kStreamMinW = 256;
+
+__device__ __forceinline__ int64_t stream_len(const DecodeArgs& a, int b, bool flag) {
+    int64_t L = __ldg(a.seq_lens + b);
+    if (L < 0 || L > a.max_seq) {
+        if (flag) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : a.max_seq;
+    }
+    return L;
+}
+
+struct StreamWalk {
+    int b, h;          // current unit: sequence b, KV head h
+    int64_t len;       // len_b (clamped)
+    int64_t span;      // len_b rounded up to 8
+    int64_t us;        // first position of the unit
+    int64_t a0;        // first token of this CTA's segment in the unit
+    int64_t end;       // the CTA's positions end here
+    int64_t W;         // positions per CTA
+    bool valid;        // a segment is current
+
+    // Segment [a0, a1) of unit (b, h), a1 <= len.
+    __device__ __forceinline__ int64_t a1() const { return min(len, end - us); }
+    // This segment holds the unit's last tokens (the CTA writes the unit's index entry).
+    __device__ __forceinline__ bool ends_unit() const { return end >= us + span; }
+
+    // Walk start for CTA c of n_cta (lengths flagged by warp 0's lanes only).
+    __device__ __forceinline__ void init(const DecodeArgs& a, int c, int n_cta, int lane, bool flag) {
+        // total positions
+        int64_t tot = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int bb = b0 + lane;
+            int64_t sp = bb < a.B ? ((stream_len(a, bb, flag) + 7) & ~int64_t(7)) : 0;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
+            tot += sp;
+        }
+        tot *= a.Hkv;
+        W = (tot + n_cta - 1) / n_cta;
+        W = max((W + 7) & ~int64_t(7), kStreamMinW);
+        const int64_t P = static_cast<int64_t>(c) * W;
+        valid = P < tot;
+        end = min(P + W, tot);
+        b = 0;
+        h = 0;
+        len = span = us = a0 = 0;
+        if (!valid) return;
+        // the sequence whose units hold position P
+        int64_t base = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int bb = b0 + lane;
+            const int64_t L = bb < a.B ? stream_len(a, bb, false) : 0;
+            const int64_t sp = ((L + 7) & ~int64_t(7)) * a.Hkv;
+            int64_t inc = sp;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(kFullMask, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned hit = __ballot_sync(kFullMask, bb < a.B && base + inc > P);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                b = b0 + l;
+                const int64_t sb = base + __shfl_sync(kFullMask, inc - sp, l);
+                len = __shfl_sync(kFullMask, L, l);
+                span = (len + 7) & ~int64_t(7);
+                h = static_cast<int>((P - sb) / span);
+                us = sb + static_cast<int64_t>(h) * span;
+                a0 = P - us;
+                return;
+            }
+            base += __shfl_sync(kFullMask, inc, 31);
+        }
+        valid = false;  // not reached: P < tot
+    }
+
+    // Next segment (the next unit with tokens), if the CTA's positions go on.
+    __device__ __forceinline__ void next(const DecodeArgs& a) {
+        const int64_t ue = us + span;
+        if (end <= ue) {
+            valid = false;
+            return;
+        }
+        us = ue;
+        a0 = 0;
+        if (++h == a.Hkv) {
+            h = 0;
+            do {
+                ++b;
+                len = b < a.B ? stream_len(a, b, false) : 0;
+            } while (len == 0 && b < a.B);
+            span = (len + 7) & ~int64_t(7);
+            if (b >= a.B) valid = false;  // not reached: end <= total
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, int KB, int VB, int NT, bool MULTI, bool QJL>
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL, bool STREAM>
 __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
     // q is staged in shared memory by the producer for raw K and the dense rotation; with
     // the Walsh-Hadamard rotation each consumer warp reads its query row itself
     constexpr bool Q_STAGED = C::KRAW || (D & (D - 1)) != 0;
+    // the token-balanced schedule (STREAM) serves one query position, one row group, coded
+    // keys without the sketch and the Walsh-Hadamard rotation
+    static_assert(!STREAM || (!MULTI && !QJL && !Q_STAGED), "token-balanced schedule");
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
@@ -733,15 +842,17 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     // heads times L query positions, head-major, contiguous in q and out
     // (the MULTI instantiation serves several query positions or more than kGP rows per
     // unit; the other one is the decode case: one CTA per unit along y, rows = heads)
-    const int vu = blockIdx.y, split = blockIdx.x;
-    const int u = MULTI ? vu / p.q_chunks : vu;
+    // (the token-balanced schedule sets u, b, kvh, qrow0, row0 and t0 per segment)
+    const int split = blockIdx.x;
+    int vu = blockIdx.y;
+    int u = MULTI ? vu / p.q_chunks : vu;
     const int s0 = MULTI ? (vu - u * p.q_chunks) * kGP : 0;
-    const int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
+    int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
     const int G = MULTI ? min(kGP, p.S - s0) : p.G;  // query rows of this CTA
-    const int64_t qrow0 = MULTI ? (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + s0
-                                : static_cast<int64_t>(b) * a.Hq + kvh * G;
-    const int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
-    const int64_t t0 = static_cast<int64_t>(split) * p.chunk;
+    int64_t qrow0 = MULTI ? (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + s0
+                          : static_cast<int64_t>(b) * a.Hq + kvh * G;
+    int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
+    int64_t t0 = STREAM ? 0 : static_cast<int64_t>(split) * p.chunk;
     // This kernel is launched with programmatic stream serialization: it may
     // start while the previous kernel on the stream (e.g. the combine of the
     // previous call, which reads this workspace) still runs.  Until
@@ -781,6 +892,38 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
         // ------------------------------------------------------------ producer
         // (lanes 1-31 issue nothing and never trigger the dependent launch: the
         // CTA's trigger must follow a dependency wait)
+        const uint8_t* kg = static_cast<const uint8_t*>(a.k);
+        // Tile li of the token range [t0, tend): its copies into stage gi % NSTAGE.
+        // (gi: the tile's place in the ring sequence, li: its place in the token range)
+        auto issue = [&](int gi, int li, int64_t tend) {
+            const int s = gi % C::NSTAGE;
+            const int64_t ts = t0 + static_cast<int64_t>(li) * C::TS;
+            const int64_t nv = min(static_cast<int64_t>(C::TS), tend - ts);
+            const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
+            uint8_t* st = stage_ptr(s);
+            const uint32_t vbytes = n8 * C::BPV, nbytes = n8 * 2;
+            if constexpr (C::KRAW) {
+                // whole boxes of TS rows per 64-column block (rows past the tensor read as zero)
+                mbar_arrive_expect_tx(full + s, (D / 64) * C::TS * 128 + vbytes + nbytes);
+#pragma unroll
+                for (int cb = 0; cb < D / 64; ++cb)
+                    tma_g2s_2d(st + cb * C::KREG, &kmap, 64 * cb, static_cast<int>(row0 + ts), full + s);
+            } else {
+                const uint32_t kbytes = n8 * C::BPK;
+                const uint32_t sgbytes = QJL ? n8 * (D / 8) : 0u;
+                mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes + (QJL ? sgbytes + nbytes : 0u));
+                bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
+                bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
+                if constexpr (QJL) {
+                    bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF, a.k_signs + (row0 + ts) * (D / 8), sgbytes,
+                             full + s);
+                    bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF + C::SBUF, a.k_rnorms + row0 + ts, nbytes,
+                             full + s);
+                }
+            }
+            bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
+            bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
+        };
         if (lane == 0) {
             // prologue data first: compact tables, this unit's query block, sign words
             const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
@@ -792,625 +935,682 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             bulk_g2s(pro + C::PRO_V, a.cv.vtab, C::VW * 4, setup);
             if (sbytes) bulk_g2s(pro + C::PRO_S, a.ck.sign_bits, sbytes, setup);
             if (vsbytes) bulk_g2s(pro + C::PRO_S + 64, a.cv.sign_bits, vsbytes, setup);
-            {
-                // While the previous kernel finishes, pull the first NSTAGE tiles of this
-                // split (by max_seq: the lengths are not read yet) into L2.  A prefetch
-                // changes no value any load returns, so it may precede the wait; the
-                // copies into shared memory come after it.
-                const int64_t pf_end = min(min(t0 + p.chunk, a.max_seq), t0 + static_cast<int64_t>(C::NSTAGE) * C::TS);
-                if (pf_end > t0) {
-                    const uint32_t ntok = static_cast<uint32_t>(pf_end - t0);  // a multiple of 8
-                    if constexpr (C::KRAW) {
-                        for (int it = 0; it * C::TS < static_cast<int>(ntok); ++it)
+            if constexpr (STREAM) {
+                // the segments come from every sequence's length: pull the lengths into L2
+                // (whole 16-byte granules of the caller's 256-byte aligned buffer)
+                const uintptr_t l0 = reinterpret_cast<uintptr_t>(a.seq_lens) & ~uintptr_t(15);
+                const uintptr_t l1 = (reinterpret_cast<uintptr_t>(a.seq_lens + a.B) + 15) & ~uintptr_t(15);
+                prefetch_l2(reinterpret_cast<const void*>(l0), static_cast<uint32_t>(l1 - l0 < 4096 ? l1 - l0 : 4096));
+            } else {
+                {
+                    // While the previous kernel finishes, pull the first NSTAGE tiles of this
+                    // split (by max_seq: the lengths are not read yet) into L2.  A prefetch
+                    // changes no value any load returns, so it may precede the wait; the
+                    // copies into shared memory come after it.
+                    const int64_t pf_end = min(min(t0 + p.chunk, a.max_seq), t0 + static_cast<int64_t>(C::NSTAGE) * C::TS);
+                    if (pf_end > t0) {
+                        const uint32_t ntok = static_cast<uint32_t>(pf_end - t0);  // a multiple of 8
+                        if constexpr (C::KRAW) {
+                            for (int it = 0; it * C::TS < static_cast<int>(ntok); ++it)
 #pragma unroll
-                            for (int cb = 0; cb < D / 64; ++cb)
-                                prefetch_l2_2d(&kmap, 64 * cb, static_cast<int>(row0 + t0 + it * C::TS));
-                    } else {
-                        prefetch_l2(static_cast<const uint8_t*>(a.k) + (row0 + t0) * C::BPK, ntok * C::BPK);
-                        prefetch_l2(a.k_norms + row0 + t0, ntok * 2);
+                                for (int cb = 0; cb < D / 64; ++cb)
+                                    prefetch_l2_2d(&kmap, 64 * cb, static_cast<int>(row0 + t0 + it * C::TS));
+                        } else {
+                            prefetch_l2(static_cast<const uint8_t*>(a.k) + (row0 + t0) * C::BPK, ntok * C::BPK);
+                            prefetch_l2(a.k_norms + row0 + t0, ntok * 2);
+                        }
+                        prefetch_l2(a.v_codes + (row0 + t0) * C::BPV, ntok * C::BPV);
+                        prefetch_l2(a.v_norms + row0 + t0, ntok * 2);
                     }
-                    prefetch_l2(a.v_codes + (row0 + t0) * C::BPV, ntok * C::BPV);
-                    prefetch_l2(a.v_norms + row0 + t0, ntok * 2);
+                    // the query block and the 16-byte granule holding seq_lens[b] (allocations
+                    // are 256-byte aligned, so the granule lies inside the caller's buffer)
+                    prefetch_l2(a.q + qrow0 * D, qbytes);
+                    prefetch_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(a.seq_lens + b) & ~uintptr_t(15)), 16);
                 }
-                // the query block and the 16-byte granule holding seq_lens[b] (allocations
-                // are 256-byte aligned, so the granule lies inside the caller's buffer)
-                prefetch_l2(a.q + qrow0 * D, qbytes);
-                prefetch_l2(reinterpret_cast<const void*>(reinterpret_cast<uintptr_t>(a.seq_lens + b) & ~uintptr_t(15)), 16);
-            }
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            allow_dependent_launch();
-            if constexpr (Q_STAGED) {
-                mbar_arrive_expect_tx(setup_q, qbytes);
-                bulk_g2s(pro + C::PRO_Q, a.q + qrow0 * D, qbytes, setup_q);
-            }
-            const uint8_t* kg = static_cast<const uint8_t*>(a.k);
-            // Tile `it` of the token range [t0, tend): its copies into stage it % NSTAGE.
-            auto issue = [&](int it, int64_t tend) {
-                const int s = it % C::NSTAGE;
-                const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
-                const int64_t nv = min(static_cast<int64_t>(C::TS), tend - ts);
-                const uint32_t n8 = static_cast<uint32_t>((nv + 7) & ~int64_t(7));
-                uint8_t* st = stage_ptr(s);
-                const uint32_t vbytes = n8 * C::BPV, nbytes = n8 * 2;
-                if constexpr (C::KRAW) {
-                    // whole boxes of TS rows per 64-column block (rows past the tensor read as zero)
-                    mbar_arrive_expect_tx(full + s, (D / 64) * C::TS * 128 + vbytes + nbytes);
-#pragma unroll
-                    for (int cb = 0; cb < D / 64; ++cb)
-                        tma_g2s_2d(st + cb * C::KREG, &kmap, 64 * cb, static_cast<int>(row0 + ts), full + s);
-                } else {
-                    const uint32_t kbytes = n8 * C::BPK;
-                    const uint32_t sgbytes = QJL ? n8 * (D / 8) : 0u;
-                    mbar_arrive_expect_tx(full + s, kbytes + vbytes + 2 * nbytes + (QJL ? sgbytes + nbytes : 0u));
-                    bulk_g2s(st, kg + (row0 + ts) * C::BPK, kbytes, full + s);
-                    bulk_g2s(st + C::KBUF + C::VBUF, a.k_norms + row0 + ts, nbytes, full + s);
-                    if constexpr (QJL) {
-                        bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF, a.k_signs + (row0 + ts) * (D / 8), sgbytes,
-                                 full + s);
-                        bulk_g2s(st + C::KBUF + C::VBUF + 2 * C::NBUF + C::SBUF, a.k_rnorms + row0 + ts, nbytes,
-                                 full + s);
+                asm volatile("griddepcontrol.wait;" ::: "memory");
+                allow_dependent_launch();
+                if constexpr (Q_STAGED) {
+                    mbar_arrive_expect_tx(setup_q, qbytes);
+                    bulk_g2s(pro + C::PRO_Q, a.q + qrow0 * D, qbytes, setup_q);
+                }
+                // The first ring-full of tiles goes out before the sequence length is known, sized
+                // by max_seq (every copy stays inside the caller's cache); the consumers mask the
+                // tokens past the length, and tiles past it are drained unconsumed.
+                const int pre = pre_tiles(t0, p.chunk, a.max_seq);
+                for (int it = 0; it < pre; ++it) issue(it, it, min(t0 + p.chunk, a.max_seq));
+                t1 = min(clamped_len(a, b), t0 + p.chunk);
+                ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
+                issued = pre;
+                for (int it = pre; it < ntiles; ++it) {
+                    const int s = it % C::NSTAGE;
+                    if (it >= C::NSTAGE && !mbar_wait(empty + s, ((it / C::NSTAGE) - 1) & 1)) {
+                        atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                        *s_abort = 1;
+                        break;
                     }
+                    issue(it, it, t1);
+                    issued = it + 1;
                 }
-                bulk_g2s(st + C::KBUF, a.v_codes + (row0 + ts) * C::BPV, vbytes, full + s);
-                bulk_g2s(st + C::KBUF + C::VBUF + C::NBUF, a.v_norms + row0 + ts, nbytes, full + s);
-            };
-            // The first ring-full of tiles goes out before the sequence length is known, sized
-            // by max_seq (every copy stays inside the caller's cache); the consumers mask the
-            // tokens past the length, and tiles past it are drained unconsumed.
-            const int pre = pre_tiles(t0, p.chunk, a.max_seq);
-            for (int it = 0; it < pre; ++it) issue(it, min(t0 + p.chunk, a.max_seq));
-            t1 = min(clamped_len(a, b), t0 + p.chunk);
-            ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
-            issued = pre;
-            for (int it = pre; it < ntiles; ++it) {
-                const int s = it % C::NSTAGE;
-                if (it >= C::NSTAGE && !mbar_wait(empty + s, ((it / C::NSTAGE) - 1) & 1)) {
-                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
-                    *s_abort = 1;
-                    break;
-                }
-                issue(it, t1);
-                issued = it + 1;
-            }
-            // Tiles issued before the length was known that lie past it are never consumed:
-            // their copies land before the consumers reuse the ring for the merge.
-            for (int it = ntiles; it < pre; ++it) {
-                if (!mbar_wait(full + (it % C::NSTAGE), (it / C::NSTAGE) & 1)) {
-                    atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
-                    *s_abort = 1;
-                    break;
+                // Tiles issued before the length was known that lie past it are never consumed:
+                // their copies land before the consumers reuse the ring for the merge.
+                for (int it = ntiles; it < pre; ++it) {
+                    if (!mbar_wait(full + (it % C::NSTAGE), (it / C::NSTAGE) & 1)) {
+                        atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                        *s_abort = 1;
+                        break;
+                    }
                 }
             }
         }
-        __syncwarp();  // reconverge the producer warp before the block-wide barriers
-        asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+        if constexpr (STREAM) {
+            // Segment by segment: the copies of the segment's tiles (continuing around the
+            // ring), then the arrival on barrier 2 (all copies issued), then, before the next
+            // segment's copies reuse the ring, barrier 3: the consumers' merge of this
+            // segment (which reads the ring) is done.
+            __syncwarp();
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (lane == 0) allow_dependent_launch();
+            StreamWalk sw;
+            sw.init(a, blockIdx.x, p.n_cta, lane, false);
+            int itg = 0;
+            bool stop = false;
+            while (sw.valid) {
+                u = sw.b * a.Hkv + sw.h;
+                row0 = static_cast<int64_t>(u) * a.max_seq;
+                t0 = sw.a0;
+                const int64_t te = sw.a1();
+                const int nt = static_cast<int>((te - t0 + C::TS - 1) / C::TS);
+                if (lane == 0 && !stop) {
+                    for (int it = 0; it < nt; ++it) {
+                        const int gi = itg + it;
+                        if (gi >= C::NSTAGE && !mbar_wait(empty + (gi % C::NSTAGE), ((gi / C::NSTAGE) - 1) & 1)) {
+                            atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                            *s_abort = 1;
+                            stop = true;
+                            break;
+                        }
+                        issue(gi, it, te);
+                        issued = gi + 1;
+                    }
+                }
+                itg += nt;
+                __syncwarp();
+                asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                sw.next(a);
+                if (sw.valid) asm volatile("bar.sync 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+            }
+        } else {
+            __syncwarp();  // reconverge the producer warp before the block-wide barriers
+            asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+        }
     } else {
         // ------------------------------------------------------------ consumers: prologue
         const int ctid = tid;  // 0 .. C::NWC * 32 - 1
         int64_t len = 0;
-        {
-            // Every prologue read of global memory is issued at once (one memory
-            // latency for the CTA, not one per loop iteration).
-            bool ok = __all_sync(kFullMask, mbar_wait(setup, 0));
+        // Every prologue read of global memory is issued at once (one memory
+        // latency for the CTA, not one per loop iteration).
+        bool ok = __all_sync(kFullMask, mbar_wait(setup, 0));
 #ifdef TQ_TIMELINE
-            if (threadIdx.x == 0) {  // slot 1: the SM this CTA runs on
-                unsigned sm;
-                asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
-                tl_t[1] = sm;
-            }
+        if (threadIdx.x == 0) {  // slot 1: the SM this CTA runs on
+            unsigned sm;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+            tl_t[1] = sm;
+        }
 #endif
-            replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
-                                reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
-            asm volatile("griddepcontrol.wait;" ::: "memory");
-            TQ_TL(tl_t, 2);
-            // Past the wait, everything stream-ordered before this kernel is complete: the
-            // combine kernel that follows may start (and read the call's inputs) once every
-            // CTA has triggered, which each CTA does only after one of its threads has
-            // passed this wait.
-            allow_dependent_launch();
-            len = clamped_len(a, b);
-            t1 = min(len, t0 + p.chunk);
+        replicate_tables<C>(reinterpret_cast<const uint32_t*>(pro + C::PRO_K),
+                            reinterpret_cast<const uint32_t*>(pro + C::PRO_V), ktab_s, vtab_s, ctid);
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        TQ_TL(tl_t, 2);
+        // Past the wait, everything stream-ordered before this kernel is complete: the
+        // combine kernel that follows may start (and read the call's inputs) once every
+        // CTA has triggered, which each CTA does only after one of its threads has
+        // passed this wait.
+        allow_dependent_launch();
+        StreamWalk sw;
+        if constexpr (STREAM) sw.init(a, blockIdx.x, p.n_cta, lane, warp == 0);
+        int itg = 0;  // ring position of the segment's first tile
+        // One pass per segment of a unit's tokens: this CTA's split of its unit, or, on the
+        // token-balanced schedule, each unit its positions cover (barrier 3 tells the
+        // producer that the segment's merge no longer reads the ring).
+        for (;;) {
+            if constexpr (STREAM) {
+                if (!sw.valid) break;
+                b = sw.b;
+                kvh = sw.h;
+                u = vu = b * a.Hkv + kvh;
+                qrow0 = static_cast<int64_t>(b) * a.Hq + kvh * G;
+                row0 = static_cast<int64_t>(u) * a.max_seq;
+                t0 = sw.a0;
+                len = sw.len;
+                t1 = sw.a1();
+            } else {
+                len = clamped_len(a, b);
+                t1 = min(len, t0 + p.chunk);
+            }
             ntiles = (t1 > t0) ? static_cast<int>((t1 - t0 + C::TS - 1) / C::TS) : 0;
-            if constexpr (Q_STAGED) ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
-            if (!ok && lane == 0) {
-                atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
-                *s_abort = 1;
-            }
-            rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q), a.q + qrow0 * D,
-                                               reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp,
-                                               lane, ctid);
-            if (MULTI && ctid < kGP) {
-                // Causal end of each query row, as tokens past t0: the rows' positions are the
-                // last L of the sequence (packed tokens, then tail), so every packed token is
-                // visible when L == 1 or the tail is long enough.  Clamped to t1, it also marks
-                // the split's end.
-                const int tail = p.L > 1 ? tail_count(a, b) : 0;
-                const int64_t e = min(packed_visible(len, tail, p.L, (s0 + ctid) % p.L), t1);
-                s_erel[ctid] = e > t0 ? static_cast<int>(e - t0) : 0;
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-        TQ_TL(tl_t, 7);
-
-        const int g = lane >> 2, t = lane & 3;
-        // q' B fragments: Bq[kt][nt][2] (in shared memory for D > 128)
-        uint32_t Bq[C::BQ_SMEM ? 1 : C::KTS][C::NTS][2];
-        const uint32_t bq_a = smem_addr(bq_s);
-#pragma unroll
-        for (int kt = 0; kt < C::KTS; ++kt) {
-#pragma unroll
-            for (int nt = 0; nt < C::NTS; ++nt) {
-                const int qh = (NT == 2) ? g : (g >> 1);
-                const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
-                uint32_t b0, b1;
-                if constexpr (C::KEXP) {
-                    // dims d0, d1 = (D/4) t + 2 kt + {0, 1}; k pair = (K_hi, K_lo) of one dim
-                    const int d0 = (D / 4) * t + 2 * kt;
-                    float v[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const float x = qs[qh * D + d0 + e];
-                        const float hi = __half2float(__float2half_rn(x));
-                        v[e] = lo_part ? (x - hi) : x;
-                    }
-                    if (NT == 2 && lo_part) {  // q_lo multiplies K_hi only
-                        b0 = pack_f16(v[0], 0.0f);
-                        b1 = pack_f16(v[1], 0.0f);
-                    } else {
-                        b0 = pack_f16(v[0], v[0]);
-                        b1 = pack_f16(v[1], v[1]);
-                    }
-                } else {
-                    // coded K: dims (D/4) t + 4 kt + {0..3} (the K-role map); raw K:
-                    // the ldmatrix layout, dims 16 kt + 2 t + {0, 1, 8, 9}
-                    const int base = C::KRAW ? 16 * kt + 2 * t : (D / 4) * t + 4 * kt;
-                    float v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float x = qs[qh * D + base + (C::KRAW ? (e & 1) + 8 * (e >> 1) : e)];
-                        const float hi = __half2float(__float2half_rn(x));
-                        v[e] = lo_part ? (x - hi) : x;
-                    }
-                    b0 = pack_f16(v[0], v[1]);
-                    b1 = pack_f16(v[2], v[3]);
-                }
-                if constexpr (C::BQ_SMEM) {
-                    if (warp == 0) sts64(bq_a + ((kt * C::NTS + nt) * 32 + lane) * 8, b0, b1);
-                } else {
-                    Bq[kt][nt][0] = b0;
-                    Bq[kt][nt][1] = b1;
-                }
-            }
-        }
-        if constexpr (QJL) {
-            // u = S q' for this CTA's query rows, as B fragments of the sketch k-tiles ("How I
-            // built VeloxQuant-MLX", Stage 3: the correction reads <S_j, q> for every sketch
-            // row j).  Sketch k-tile kk, thread (g, t): k = 2t, 2t+1, 2t+8, 2t+9 are sketch rows
-            // j0 .. j0 + 3, j0 = 32 (kk / 2) + 16 (kk % 2) + 4t -- nibble t of the half kk % 2
-            // of the keys' sign word kk / 2.  q' is split into fp16 hi and lo as for the scores.
-            // Warp w takes sketch rows j = 32 w + lane for all rows of q' (S^T rows read
-            // across the lanes, coalesced; q' broadcast from shared memory), then forms the
-            // fragments of k-tiles 2w and 2w + 1 from its lanes by shuffles.
-            const uint32_t ubq_a = smem_addr(ubq_s);
-            for (int w = warp; w < D / 32; w += C::NWC) {
-                float uq[kGP];
-#pragma unroll
-                for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = 0.0f;
-                const float* col = a.ck.sketch_t + 32 * w + lane;
-#pragma unroll 4
-                for (int i = 0; i < D; ++i) {
-                    const float sv = __ldg(col + static_cast<int64_t>(i) * D);
-#pragma unroll
-                    for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv, qs[g2 * D + i], uq[g2]);
-                }
-                const int gg = lane >> 2, tt = lane & 3;
-                const int qh = (NT == 2) ? gg : (gg >> 1);
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int kk = 2 * w + h;
-                    float hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        // sketch row 32 w + 16 h + 4 tt + e of query row qh, from lane 16 h + 4 tt + e
-                        float x = 0.0f;
-#pragma unroll
-                        for (int g2 = 0; g2 < kGP; ++g2) {
-                            const float y = __shfl_sync(kFullMask, uq[g2], 16 * h + 4 * tt + e);
-                            if (g2 == qh) x = y;
-                        }
-                        hi[e] = __half2float(__float2half_rn(x));
-                        lo[e] = x - hi[e];
-                    }
-                    if constexpr (NT == 2) {
-                        sts64(ubq_a + ((kk * 2) * 32 + lane) * 8, pack_f16(hi[0], hi[1]), pack_f16(hi[2], hi[3]));
-                        sts64(ubq_a + ((kk * 2 + 1) * 32 + lane) * 8, pack_f16(lo[0], lo[1]), pack_f16(lo[2], lo[3]));
-                    } else {
-                        const float* v = (gg & 1) ? lo : hi;  // interleaved hi / lo columns
-                        sts64(ubq_a + (kk * 32 + lane) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
-                    }
-                }
-            }
-        }
-        if constexpr (C::BQ_SMEM || QJL) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-
-        float O[C::KT][4];
-#pragma unroll
-        for (int i = 0; i < C::KT; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
-        float m_run[NT], l_run[NT];
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            m_run[j] = -CUDART_INF_F;
-            l_run[j] = 0.0f;
-        }
-        const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
-        // table block: the table address bits ride in the lane offsets (kTBlock is
-        // 64 KB aligned, the V half of a row starts at +128)
-        const uint32_t koff = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) : 0u);
-        const uint32_t lane4 = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) + 128u : 0u);
-
-        // ------------------------------------------------------------ main loop
-        for (int it = 0; it < ntiles; ++it) {
-            const int s = it % C::NSTAGE;
-            // the warp decides together so every later barrier is reached convergently
-            const bool ok = __all_sync(kFullMask, mbar_wait(full + s, (it / C::NSTAGE) & 1));
-            if (!ok) {
-                if (lane == 0) {
+            {
+                if constexpr (Q_STAGED) ok = __all_sync(kFullMask, ok && mbar_wait(setup_q, 0));
+                if (!ok && lane == 0) {
                     atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
                     *s_abort = 1;
                 }
-                break;
+                rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q), a.q + qrow0 * D,
+                                                   reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp,
+                                                   lane, ctid);
+                if (MULTI && ctid < kGP) {
+                    // Causal end of each query row, as tokens past t0: the rows' positions are the
+                    // last L of the sequence (packed tokens, then tail), so every packed token is
+                    // visible when L == 1 or the tail is long enough.  Clamped to t1, it also marks
+                    // the split's end.
+                    const int tail = p.L > 1 ? tail_count(a, b) : 0;
+                    const int64_t e = min(packed_visible(len, tail, p.L, (s0 + ctid) % p.L), t1);
+                    s_erel[ctid] = e > t0 ? static_cast<int>(e - t0) : 0;
+                }
             }
-#ifdef TQ_TIMELINE
-            if (it == 0) TQ_TL(tl_t, 3);
-#endif
-            const uint8_t* st = stage_ptr(s);
-            const uint8_t* kbuf = st;
-            const uint8_t* vbuf = st + C::KBUF;
-            const __half* knrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF);
-            const __half* vnrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF + C::NBUF);
-            const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
-            const int nvalid = static_cast<int>(min(static_cast<int64_t>(C::TS), t1 - ts));
-            const int r0 = warp * 16 * C::MT;
-            if (r0 < nvalid) {
-                // ---- scores for MT m-tiles ----
-                float sc[C::MT][C::NTS][4];
+            asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+            TQ_TL(tl_t, 7);
+
+            const int g = lane >> 2, t = lane & 3;
+            // q' B fragments: Bq[kt][nt][2] (in shared memory for D > 128)
+            uint32_t Bq[C::BQ_SMEM ? 1 : C::KTS][C::NTS][2];
+            const uint32_t bq_a = smem_addr(bq_s);
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
+            for (int kt = 0; kt < C::KTS; ++kt) {
 #pragma unroll
-                    for (int nt = 0; nt < C::NTS; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
-                    const int ra = r0 + 16 * mt + g, rb = ra + 8;
-                    if constexpr (C::KRAW) {
-                        // rows r0 + 16 mt + 0..15 of the swizzled 64-column blocks: lanes 0-7 /
-                        // 8-15 / 16-23 / 24-31 address rows 0-7 / 8-15 / 0-7 / 8-15 at 16-byte
-                        // chunk 2 kl / 2 kl / 2 kl + 1 / 2 kl + 1 of the block, chunk c of
-                        // row r sitting at chunk c ^ (r & 7)
-                        const uint32_t rowa = smem_addr(kbuf) +
-                                              static_cast<uint32_t>((r0 + 16 * mt + (lane & 15)) * 128);
-#pragma unroll
-                        for (int kt = 0; kt < C::KTS; ++kt) {
-                            const int cb = kt >> 2, kl = kt & 3;
-                            const uint32_t chunk = static_cast<uint32_t>(2 * kl) + static_cast<uint32_t>(lane >> 4);
-                            uint32_t a0, a1, a2, a3;
-                            ldmatrix_x4(rowa + cb * C::KREG + ((chunk ^ static_cast<uint32_t>(lane & 7)) << 4), a0, a1,
-                                        a2, a3);
-                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
-                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                            mma16816(sc[mt][0], a0, a1, a2, a3, q00, q01);
-                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], a0, a1, a2, a3, q10, q11);
-                        }
-                    } else {
-                    uint32_t wa[C::KCW], wb[C::KCW];
-                    load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
-                    load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
+                for (int nt = 0; nt < C::NTS; ++nt) {
+                    const int qh = (NT == 2) ? g : (g >> 1);
+                    const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
+                    uint32_t b0, b1;
                     if constexpr (C::KEXP) {
+                        // dims d0, d1 = (D/4) t + 2 kt + {0, 1}; k pair = (K_hi, K_lo) of one dim
+                        const int d0 = (D / 4) * t + 2 * kt;
+                        float v[2];
 #pragma unroll
-                        for (int kt = 0; kt < C::KTS; ++kt) {
-                            // bytes 2(kt&1), 2(kt&1)+1 of word kt/2 are dims d0, d1 of this k-tile
-                            const uint32_t wA = wa[kt >> 1], wB = wb[kt >> 1];
-                            // address = [koff byte 3][koff byte 2 / 0][code][koff byte 0]: with the
-                            // table block the permute alone forms it, else it is added to ktab_a
-                            const uint32_t sel0 = (C::TBLOCK ? 0x7604u : 0x5504u) + ((2u * (kt & 1)) << 4);
-                            const uint32_t sel1 = sel0 + 0x10u;
-                            const uint32_t kb = C::TBLOCK ? 0u : ktab_a;
-                            const uint32_t r0v = lds32(kb + __byte_perm(wA, koff, sel0));
-                            const uint32_t r1v = lds32(kb + __byte_perm(wB, koff, sel0));
-                            const uint32_t r2v = lds32(kb + __byte_perm(wA, koff, sel1));
-                            const uint32_t r3v = lds32(kb + __byte_perm(wB, koff, sel1));
-                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
-                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                            mma16816(sc[mt][0], r0v, r1v, r2v, r3v, q00, q01);
-                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], r0v, r1v, r2v, r3v, q10, q11);
+                        for (int e = 0; e < 2; ++e) {
+                            const float x = qs[qh * D + d0 + e];
+                            const float hi = __half2float(__float2half_rn(x));
+                            v[e] = lo_part ? (x - hi) : x;
+                        }
+                        if (NT == 2 && lo_part) {  // q_lo multiplies K_hi only
+                            b0 = pack_f16(v[0], 0.0f);
+                            b1 = pack_f16(v[1], 0.0f);
+                        } else {
+                            b0 = pack_f16(v[0], v[0]);
+                            b1 = pack_f16(v[1], v[1]);
                         }
                     } else {
+                        // coded K: dims (D/4) t + 4 kt + {0..3} (the K-role map); raw K:
+                        // the ldmatrix layout, dims 16 kt + 2 t + {0, 1, 8, 9}
+                        const int base = C::KRAW ? 16 * kt + 2 * t : (D / 4) * t + 4 * kt;
+                        float v[4];
 #pragma unroll
-                        for (int kt = 0; kt < C::KTS; ++kt) {
-                            uint32_t ah01, ah23, bh01, bh23;
-                            k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23);
-                            k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23);
-                            // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
-                            uint32_t q00, q01, q10 = 0u, q11 = 0u;
-                            q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                            mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
-                            if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
+                        for (int e = 0; e < 4; ++e) {
+                            const float x = qs[qh * D + base + (C::KRAW ? (e & 1) + 8 * (e >> 1) : e)];
+                            const float hi = __half2float(__float2half_rn(x));
+                            v[e] = lo_part ? (x - hi) : x;
                         }
-                        if constexpr (QJL) {
-                            // QJL correction into the same accumulators: row r's A entries are
-                            // +-v_r, v_r = gamma_r sqrt(pi/2) k_alpha / (sqrt(D) n16_K[r]) (the
-                            // accumulator is scaled by n16_K[r] afterwards), sign from bit j
-                            const uint8_t* sg = st + C::KBUF + C::VBUF + 2 * C::NBUF;
-                            const __half* rnm = reinterpret_cast<const __half*>(sg + C::SBUF);
-                            const float kap = 1.2533141373155003f * a.ck.k_alpha * rsqrtf(static_cast<float>(D));
-                            const float nka = __half2float(knrm[ra]), nkb = __half2float(knrm[rb]);
-                            const float fva = nka > 0.0f ? __half2float(rnm[ra]) * kap / nka : 0.0f;
-                            const float fvb = nkb > 0.0f ? __half2float(rnm[rb]) * kap / nkb : 0.0f;
-                            const uint32_t hva = pack_f16(fva, fva), hvb = pack_f16(fvb, fvb);
-                            const uint32_t sga = smem_addr(sg) + static_cast<uint32_t>(ra * (D / 8));
-                            const uint32_t sgb = smem_addr(sg) + static_cast<uint32_t>(rb * (D / 8));
-                            const uint32_t ubq_a = smem_addr(ubq_s);
+                        b0 = pack_f16(v[0], v[1]);
+                        b1 = pack_f16(v[2], v[3]);
+                    }
+                    if constexpr (C::BQ_SMEM) {
+                        if (warp == 0) sts64(bq_a + ((kt * C::NTS + nt) * 32 + lane) * 8, b0, b1);
+                    } else {
+                        Bq[kt][nt][0] = b0;
+                        Bq[kt][nt][1] = b1;
+                    }
+                }
+            }
+            if constexpr (QJL) {
+                // u = S q' for this CTA's query rows, as B fragments of the sketch k-tiles ("How I
+                // built VeloxQuant-MLX", Stage 3: the correction reads <S_j, q> for every sketch
+                // row j).  Sketch k-tile kk, thread (g, t): k = 2t, 2t+1, 2t+8, 2t+9 are sketch rows
+                // j0 .. j0 + 3, j0 = 32 (kk / 2) + 16 (kk % 2) + 4t -- nibble t of the half kk % 2
+                // of the keys' sign word kk / 2.  q' is split into fp16 hi and lo as for the scores.
+                // Warp w takes sketch rows j = 32 w + lane for all rows of q' (S^T rows read
+                // across the lanes, coalesced; q' broadcast from shared memory), then forms the
+                // fragments of k-tiles 2w and 2w + 1 from its lanes by shuffles.
+                const uint32_t ubq_a = smem_addr(ubq_s);
+                for (int w = warp; w < D / 32; w += C::NWC) {
+                    float uq[kGP];
 #pragma unroll
-                            for (int w4 = 0; w4 < D / 32; ++w4) {
-                                const uint32_t wsa = lds32(sga + 4 * w4), wsb = lds32(sgb + 4 * w4);
+                    for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = 0.0f;
+                    const float* col = a.ck.sketch_t + 32 * w + lane;
+#pragma unroll 4
+                    for (int i = 0; i < D; ++i) {
+                        const float sv = __ldg(col + static_cast<int64_t>(i) * D);
 #pragma unroll
-                                for (int h = 0; h < 2; ++h) {
-                                    const int kk = 2 * w4 + h;
-                                    const uint32_t na = wsa >> (16 * h + 4 * t), nb = wsb >> (16 * h + 4 * t);
-                                    // bit b of the nibble -> sign bit of half b (k = 2t + b, 2t + 8 + b)
-                                    const uint32_t a0 = hva ^ (((na & 1u) << 15) | ((na & 2u) << 30));
-                                    const uint32_t a2 = hva ^ (((na & 4u) << 13) | ((na & 8u) << 28));
-                                    const uint32_t a1 = hvb ^ (((nb & 1u) << 15) | ((nb & 2u) << 30));
-                                    const uint32_t a3 = hvb ^ (((nb & 4u) << 13) | ((nb & 8u) << 28));
-                                    uint32_t u00, u01;
-                                    lds64(ubq_a + ((kk * C::NTS) * 32 + lane) * 8, u00, u01);
-                                    mma16816(sc[mt][0], a0, a1, a2, a3, u00, u01);
-                                    if constexpr (C::NTS == 2) {
-                                        uint32_t u10, u11;
-                                        lds64(ubq_a + ((kk * C::NTS + 1) * 32 + lane) * 8, u10, u11);
-                                        mma16816(sc[mt][1], a0, a1, a2, a3, u10, u11);
+                        for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv, qs[g2 * D + i], uq[g2]);
+                    }
+                    const int gg = lane >> 2, tt = lane & 3;
+                    const int qh = (NT == 2) ? gg : (gg >> 1);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int kk = 2 * w + h;
+                        float hi[4], lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            // sketch row 32 w + 16 h + 4 tt + e of query row qh, from lane 16 h + 4 tt + e
+                            float x = 0.0f;
+#pragma unroll
+                            for (int g2 = 0; g2 < kGP; ++g2) {
+                                const float y = __shfl_sync(kFullMask, uq[g2], 16 * h + 4 * tt + e);
+                                if (g2 == qh) x = y;
+                            }
+                            hi[e] = __half2float(__float2half_rn(x));
+                            lo[e] = x - hi[e];
+                        }
+                        if constexpr (NT == 2) {
+                            sts64(ubq_a + ((kk * 2) * 32 + lane) * 8, pack_f16(hi[0], hi[1]), pack_f16(hi[2], hi[3]));
+                            sts64(ubq_a + ((kk * 2 + 1) * 32 + lane) * 8, pack_f16(lo[0], lo[1]), pack_f16(lo[2], lo[3]));
+                        } else {
+                            const float* v = (gg & 1) ? lo : hi;  // interleaved hi / lo columns
+                            sts64(ubq_a + (kk * 32 + lane) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
+                        }
+                    }
+                }
+            }
+            if constexpr (C::BQ_SMEM || QJL) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+
+            float O[C::KT][4];
+#pragma unroll
+            for (int i = 0; i < C::KT; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
+            float m_run[NT], l_run[NT];
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                m_run[j] = -CUDART_INF_F;
+                l_run[j] = 0.0f;
+            }
+            const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
+            // table block: the table address bits ride in the lane offsets (kTBlock is
+            // 64 KB aligned, the V half of a row starts at +128)
+            const uint32_t koff = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) : 0u);
+            const uint32_t lane4 = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) + 128u : 0u);
+
+            // ------------------------------------------------------------ main loop
+            // (after a wait gave up, the token-balanced schedule's later segments skip their tiles)
+            const int nloop = (STREAM && *reinterpret_cast<volatile int*>(s_abort)) ? 0 : ntiles;
+            for (int it = 0; it < nloop; ++it) {
+                const int gi = itg + it;  // the tile's place in the ring sequence
+                const int s = gi % C::NSTAGE;
+                // the warp decides together so every later barrier is reached convergently
+                const bool ok = __all_sync(kFullMask, mbar_wait(full + s, (gi / C::NSTAGE) & 1));
+                if (!ok) {
+                    if (lane == 0) {
+                        atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
+                        *s_abort = 1;
+                    }
+                    break;
+                }
+#ifdef TQ_TIMELINE
+                if (it == 0) TQ_TL(tl_t, 3);
+#endif
+                const uint8_t* st = stage_ptr(s);
+                const uint8_t* kbuf = st;
+                const uint8_t* vbuf = st + C::KBUF;
+                const __half* knrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF);
+                const __half* vnrm = reinterpret_cast<const __half*>(st + C::KBUF + C::VBUF + C::NBUF);
+                const int64_t ts = t0 + static_cast<int64_t>(it) * C::TS;
+                const int nvalid = static_cast<int>(min(static_cast<int64_t>(C::TS), t1 - ts));
+                const int r0 = warp * 16 * C::MT;
+                if (r0 < nvalid) {
+                    // ---- scores for MT m-tiles ----
+                    float sc[C::MT][C::NTS][4];
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+#pragma unroll
+                        for (int nt = 0; nt < C::NTS; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
+                        const int ra = r0 + 16 * mt + g, rb = ra + 8;
+                        if constexpr (C::KRAW) {
+                            // rows r0 + 16 mt + 0..15 of the swizzled 64-column blocks: lanes 0-7 /
+                            // 8-15 / 16-23 / 24-31 address rows 0-7 / 8-15 / 0-7 / 8-15 at 16-byte
+                            // chunk 2 kl / 2 kl / 2 kl + 1 / 2 kl + 1 of the block, chunk c of
+                            // row r sitting at chunk c ^ (r & 7)
+                            const uint32_t rowa = smem_addr(kbuf) +
+                                                  static_cast<uint32_t>((r0 + 16 * mt + (lane & 15)) * 128);
+#pragma unroll
+                            for (int kt = 0; kt < C::KTS; ++kt) {
+                                const int cb = kt >> 2, kl = kt & 3;
+                                const uint32_t chunk = static_cast<uint32_t>(2 * kl) + static_cast<uint32_t>(lane >> 4);
+                                uint32_t a0, a1, a2, a3;
+                                ldmatrix_x4(rowa + cb * C::KREG + ((chunk ^ static_cast<uint32_t>(lane & 7)) << 4), a0, a1,
+                                            a2, a3);
+                                uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                                q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                                mma16816(sc[mt][0], a0, a1, a2, a3, q00, q01);
+                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], a0, a1, a2, a3, q10, q11);
+                            }
+                        } else {
+                        uint32_t wa[C::KCW], wb[C::KCW];
+                        load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
+                        load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
+                        if constexpr (C::KEXP) {
+#pragma unroll
+                            for (int kt = 0; kt < C::KTS; ++kt) {
+                                // bytes 2(kt&1), 2(kt&1)+1 of word kt/2 are dims d0, d1 of this k-tile
+                                const uint32_t wA = wa[kt >> 1], wB = wb[kt >> 1];
+                                // address = [koff byte 3][koff byte 2 / 0][code][koff byte 0]: with the
+                                // table block the permute alone forms it, else it is added to ktab_a
+                                const uint32_t sel0 = (C::TBLOCK ? 0x7604u : 0x5504u) + ((2u * (kt & 1)) << 4);
+                                const uint32_t sel1 = sel0 + 0x10u;
+                                const uint32_t kb = C::TBLOCK ? 0u : ktab_a;
+                                const uint32_t r0v = lds32(kb + __byte_perm(wA, koff, sel0));
+                                const uint32_t r1v = lds32(kb + __byte_perm(wB, koff, sel0));
+                                const uint32_t r2v = lds32(kb + __byte_perm(wA, koff, sel1));
+                                const uint32_t r3v = lds32(kb + __byte_perm(wB, koff, sel1));
+                                uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                                q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                                mma16816(sc[mt][0], r0v, r1v, r2v, r3v, q00, q01);
+                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], r0v, r1v, r2v, r3v, q10, q11);
+                            }
+                        } else {
+#pragma unroll
+                            for (int kt = 0; kt < C::KTS; ++kt) {
+                                uint32_t ah01, ah23, bh01, bh23;
+                                k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23);
+                                k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23);
+                                // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
+                                uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                                q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
+                                mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
+                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
+                            }
+                            if constexpr (QJL) {
+                                // QJL correction into the same accumulators: row r's A entries are
+                                // +-v_r, v_r = gamma_r sqrt(pi/2) k_alpha / (sqrt(D) n16_K[r]) (the
+                                // accumulator is scaled by n16_K[r] afterwards), sign from bit j
+                                const uint8_t* sg = st + C::KBUF + C::VBUF + 2 * C::NBUF;
+                                const __half* rnm = reinterpret_cast<const __half*>(sg + C::SBUF);
+                                const float kap = 1.2533141373155003f * a.ck.k_alpha * rsqrtf(static_cast<float>(D));
+                                const float nka = __half2float(knrm[ra]), nkb = __half2float(knrm[rb]);
+                                const float fva = nka > 0.0f ? __half2float(rnm[ra]) * kap / nka : 0.0f;
+                                const float fvb = nkb > 0.0f ? __half2float(rnm[rb]) * kap / nkb : 0.0f;
+                                const uint32_t hva = pack_f16(fva, fva), hvb = pack_f16(fvb, fvb);
+                                const uint32_t sga = smem_addr(sg) + static_cast<uint32_t>(ra * (D / 8));
+                                const uint32_t sgb = smem_addr(sg) + static_cast<uint32_t>(rb * (D / 8));
+                                const uint32_t ubq_a = smem_addr(ubq_s);
+#pragma unroll
+                                for (int w4 = 0; w4 < D / 32; ++w4) {
+                                    const uint32_t wsa = lds32(sga + 4 * w4), wsb = lds32(sgb + 4 * w4);
+#pragma unroll
+                                    for (int h = 0; h < 2; ++h) {
+                                        const int kk = 2 * w4 + h;
+                                        const uint32_t na = wsa >> (16 * h + 4 * t), nb = wsb >> (16 * h + 4 * t);
+                                        // bit b of the nibble -> sign bit of half b (k = 2t + b, 2t + 8 + b)
+                                        const uint32_t a0 = hva ^ (((na & 1u) << 15) | ((na & 2u) << 30));
+                                        const uint32_t a2 = hva ^ (((na & 4u) << 13) | ((na & 8u) << 28));
+                                        const uint32_t a1 = hvb ^ (((nb & 1u) << 15) | ((nb & 2u) << 30));
+                                        const uint32_t a3 = hvb ^ (((nb & 4u) << 13) | ((nb & 8u) << 28));
+                                        uint32_t u00, u01;
+                                        lds64(ubq_a + ((kk * C::NTS) * 32 + lane) * 8, u00, u01);
+                                        mma16816(sc[mt][0], a0, a1, a2, a3, u00, u01);
+                                        if constexpr (C::NTS == 2) {
+                                            uint32_t u10, u11;
+                                            lds64(ubq_a + ((kk * C::NTS + 1) * 32 + lane) * 8, u10, u11);
+                                            mma16816(sc[mt][1], a0, a1, a2, a3, u10, u11);
+                                        }
                                     }
                                 }
                             }
                         }
-                    }
-                    }
-                }
-                // ---- scale by K norms, mask (tile end, causal limit), tile max ----
-                float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
-                float tmax[NT];
-#pragma unroll
-                for (int j = 0; j < NT; ++j) tmax[j] = -CUDART_INF_F;
-                // this thread's query rows (2t + j, or t when NT == 1): causal ends in the tile
-                // (decode: the tile's end)
-                int lim[NT];
-#pragma unroll
-                for (int j = 0; j < NT; ++j) lim[j] = MULTI ? s_erel[(NT == 2) ? 2 * t + j : t] - it * C::TS : nvalid;
-#pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-#pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int r = r0 + 16 * mt + g + 8 * hr;
-                        const float nk = C::KRAW ? 1.0f : __half2float(knrm[r]);
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            float x;
-                            if constexpr (C::NTS == 2)
-                                x = sc[mt][0][2 * hr + j] + sc[mt][1][2 * hr + j];
-                            else if constexpr (NT == 2)
-                                x = sc[mt][0][2 * hr + j];
-                            else
-                                x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
-                            // lim <= t1 - ts, so this also masks the rows past the tile's end
-                            x = (r < lim[j]) ? x * nk : -CUDART_INF_F;
-                            sv[mt][hr][j] = x;
-                            tmax[j] = fmaxf(tmax[j], x);
                         }
                     }
-                }
+                    // ---- scale by K norms, mask (tile end, causal limit), tile max ----
+                    float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
+                    float tmax[NT];
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 4));
-                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 8));
-                    tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 16));
-                }
-                float alpha[NT], muse[NT];
-                bool rescale = false;
+                    for (int j = 0; j < NT; ++j) tmax[j] = -CUDART_INF_F;
+                    // this thread's query rows (2t + j, or t when NT == 1): causal ends in the tile
+                    // (decode: the tile's end)
+                    int lim[NT];
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const float mn = fmaxf(m_run[j], tmax[j]);
-                    muse[j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
-                    alpha[j] = exp2f(m_run[j] - muse[j]);
-                    rescale |= (alpha[j] != 1.0f);
-                    m_run[j] = mn;
-                    l_run[j] *= alpha[j];
-                }
-                if (__any_sync(kFullMask, rescale)) {
-                    // (MULTI, NT == 1: columns 2t and 2t + 1 both hold row t, hi and lo of P)
-                    const float a1 = (NT == 2 || MULTI) ? alpha[NT - 1] : 1.0f;
+                    for (int j = 0; j < NT; ++j) lim[j] = MULTI ? s_erel[(NT == 2) ? 2 * t + j : t] - it * C::TS : nvalid;
 #pragma unroll
-                    for (int i = 0; i < C::KT; ++i) {
-                        O[i][0] *= alpha[0];
-                        O[i][1] *= a1;
-                        O[i][2] *= alpha[0];
-                        O[i][3] *= a1;
-                    }
-                }
-                // ---- probabilities, P' = p * n16_V, P.V ----
+                    for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
-                for (int mt = 0; mt < C::MT; ++mt) {
-                    const int rbase = r0 + 16 * mt;
-                    if (rbase >= nvalid) break;
-                    float pv[2][NT];
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int r = r0 + 16 * mt + g + 8 * hr;
+                            const float nk = C::KRAW ? 1.0f : __half2float(knrm[r]);
 #pragma unroll
-                    for (int hr = 0; hr < 2; ++hr) {
-                        const int r = rbase + g + 8 * hr;
-                        const bool ok = r < nvalid;
-                        const float nvv = __half2float(vnrm[r]);
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            const float pp = exp2f(sv[mt][hr][j] - muse[j]);
-                            l_run[j] += pp;
-                            pv[hr][j] = ok ? pp * nvv : 0.0f;
-                        }
-                    }
-                    // With several query positions (MULTI), P' is fp16 hi + lo, so the weights
-                    // keep ~2^-22 of their precision: the first rows of a chunk see only a few
-                    // tokens, and one fp16 P would carry their weights' 2^-11 rounding into
-                    // the output.  NT == 1 puts the lo part in the free column 2t + 1, NT == 2
-                    // multiplies V by it in a second mma.  Decode keeps one fp16 P, as fp16
-                    // attention does.
-                    uint32_t x0, x1, pl0 = 0u, pl1 = 0u;
-                    if constexpr (NT == 2) {
-                        if constexpr (MULTI) {
-                            uint32_t y0, y1;
-                            split_f16x2(pv[0][0], pv[0][1], x0, y0);
-                            split_f16x2(pv[1][0], pv[1][1], x1, y1);
-                            pl0 = movmatrix_t(y0);
-                            pl1 = movmatrix_t(y1);
-                        } else {
-                            x0 = pack_f16(pv[0][0], pv[0][1]);
-                            x1 = pack_f16(pv[1][0], pv[1][1]);
-                        }
-                    } else if constexpr (MULTI) {
-                        uint32_t h0, l0;  // (row g, row g + 8) pairs
-                        split_f16x2(pv[0][0], pv[1][0], h0, l0);
-                        x0 = (h0 & 0xffffu) | (l0 << 16);
-                        x1 = (h0 >> 16) | (l0 & 0xffff0000u);
-                    } else {
-                        x0 = pack_f16(pv[0][0], 0.0f);
-                        x1 = pack_f16(pv[1][0], 0.0f);
-                    }
-                    const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
-                    // V of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile, thread g's dims
-                    constexpr bool SPLIT = MULTI && NT == 2;
-                    if constexpr (C::VPAIR) {
-                        constexpr int NSUB = (D / 8 + 15) / 16;  // chunks of up to 16 dims
-#pragma unroll
-                        for (int sub = 0; sub < NSUB; ++sub) {
-                            const int vbit = g * C::VCB + 16 * VB * sub;
-                            const VPairs<VB, C::TBLOCK> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
-                                                 load_bits64(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
-                            const VPairs<VB, C::TBLOCK> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
-                                                 load_bits64(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
-                            constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
-#pragma unroll
-                            for (int k = 0; k < DM_PER_SUB; ++k) {
-                                const int dm = sub * DM_PER_SUB + k;
-                                if (dm < C::KT) {
-                                    const uint32_t a0 = lds32(p01.addr(2 * k, vtab_a, lane4));
-                                    const uint32_t a1 = lds32(p01.addr(2 * k + 1, vtab_a, lane4));
-                                    const uint32_t a2 = lds32(p89.addr(2 * k, vtab_a, lane4));
-                                    const uint32_t a3 = lds32(p89.addr(2 * k + 1, vtab_a, lane4));
-                                    mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
-                                    if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
-                                }
+                            for (int j = 0; j < NT; ++j) {
+                                float x;
+                                if constexpr (C::NTS == 2)
+                                    x = sc[mt][0][2 * hr + j] + sc[mt][1][2 * hr + j];
+                                else if constexpr (NT == 2)
+                                    x = sc[mt][0][2 * hr + j];
+                                else
+                                    x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
+                                // lim <= t1 - ts, so this also masks the rows past the tile's end
+                                x = (r < lim[j]) ? x * nk : -CUDART_INF_F;
+                                sv[mt][hr][j] = x;
+                                tmax[j] = fmaxf(tmax[j], x);
                             }
                         }
-                    } else {
-                        uint32_t v0[C::VCW], v1[C::VCW], v2[C::VCW], v3[C::VCW];
-                        const int vb = g * C::VCB;
-                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t) * C::BPV, vb, v0);
-                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vb, v1);
-                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vb, v2);
-                        load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
+                    }
 #pragma unroll
-                        for (int dm = 0; dm < C::KT; ++dm) {
-                            const uint32_t a0 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm, vtab_a, lane4);
-                            const uint32_t a1 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm + 1, vtab_a, lane4);
-                            const uint32_t a2 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm, vtab_a, lane4);
-                            const uint32_t a3 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm + 1, vtab_a, lane4);
-                            mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
-                            if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
+                    for (int j = 0; j < NT; ++j) {
+                        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 4));
+                        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 8));
+                        tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 16));
+                    }
+                    float alpha[NT], muse[NT];
+                    bool rescale = false;
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const float mn = fmaxf(m_run[j], tmax[j]);
+                        muse[j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
+                        alpha[j] = exp2f(m_run[j] - muse[j]);
+                        rescale |= (alpha[j] != 1.0f);
+                        m_run[j] = mn;
+                        l_run[j] *= alpha[j];
+                    }
+                    if (__any_sync(kFullMask, rescale)) {
+                        // (MULTI, NT == 1: columns 2t and 2t + 1 both hold row t, hi and lo of P)
+                        const float a1 = (NT == 2 || MULTI) ? alpha[NT - 1] : 1.0f;
+#pragma unroll
+                        for (int i = 0; i < C::KT; ++i) {
+                            O[i][0] *= alpha[0];
+                            O[i][1] *= a1;
+                            O[i][2] *= alpha[0];
+                            O[i][3] *= a1;
+                        }
+                    }
+                    // ---- probabilities, P' = p * n16_V, P.V ----
+#pragma unroll
+                    for (int mt = 0; mt < C::MT; ++mt) {
+                        const int rbase = r0 + 16 * mt;
+                        if (rbase >= nvalid) break;
+                        float pv[2][NT];
+#pragma unroll
+                        for (int hr = 0; hr < 2; ++hr) {
+                            const int r = rbase + g + 8 * hr;
+                            const bool ok = r < nvalid;
+                            const float nvv = __half2float(vnrm[r]);
+#pragma unroll
+                            for (int j = 0; j < NT; ++j) {
+                                const float pp = exp2f(sv[mt][hr][j] - muse[j]);
+                                l_run[j] += pp;
+                                pv[hr][j] = ok ? pp * nvv : 0.0f;
+                            }
+                        }
+                        // With several query positions (MULTI), P' is fp16 hi + lo, so the weights
+                        // keep ~2^-22 of their precision: the first rows of a chunk see only a few
+                        // tokens, and one fp16 P would carry their weights' 2^-11 rounding into
+                        // the output.  NT == 1 puts the lo part in the free column 2t + 1, NT == 2
+                        // multiplies V by it in a second mma.  Decode keeps one fp16 P, as fp16
+                        // attention does.
+                        uint32_t x0, x1, pl0 = 0u, pl1 = 0u;
+                        if constexpr (NT == 2) {
+                            if constexpr (MULTI) {
+                                uint32_t y0, y1;
+                                split_f16x2(pv[0][0], pv[0][1], x0, y0);
+                                split_f16x2(pv[1][0], pv[1][1], x1, y1);
+                                pl0 = movmatrix_t(y0);
+                                pl1 = movmatrix_t(y1);
+                            } else {
+                                x0 = pack_f16(pv[0][0], pv[0][1]);
+                                x1 = pack_f16(pv[1][0], pv[1][1]);
+                            }
+                        } else if constexpr (MULTI) {
+                            uint32_t h0, l0;  // (row g, row g + 8) pairs
+                            split_f16x2(pv[0][0], pv[1][0], h0, l0);
+                            x0 = (h0 & 0xffffu) | (l0 << 16);
+                            x1 = (h0 >> 16) | (l0 & 0xffff0000u);
+                        } else {
+                            x0 = pack_f16(pv[0][0], 0.0f);
+                            x1 = pack_f16(pv[1][0], 0.0f);
+                        }
+                        const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
+                        // V of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile, thread g's dims
+                        constexpr bool SPLIT = MULTI && NT == 2;
+                        if constexpr (C::VPAIR) {
+                            constexpr int NSUB = (D / 8 + 15) / 16;  // chunks of up to 16 dims
+#pragma unroll
+                            for (int sub = 0; sub < NSUB; ++sub) {
+                                const int vbit = g * C::VCB + 16 * VB * sub;
+                                const VPairs<VB, C::TBLOCK> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
+                                                     load_bits64(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
+                                const VPairs<VB, C::TBLOCK> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
+                                                     load_bits64(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
+                                constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
+#pragma unroll
+                                for (int k = 0; k < DM_PER_SUB; ++k) {
+                                    const int dm = sub * DM_PER_SUB + k;
+                                    if (dm < C::KT) {
+                                        const uint32_t a0 = lds32(p01.addr(2 * k, vtab_a, lane4));
+                                        const uint32_t a1 = lds32(p01.addr(2 * k + 1, vtab_a, lane4));
+                                        const uint32_t a2 = lds32(p89.addr(2 * k, vtab_a, lane4));
+                                        const uint32_t a3 = lds32(p89.addr(2 * k + 1, vtab_a, lane4));
+                                        mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                                        if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
+                                    }
+                                }
+                            }
+                        } else {
+                            uint32_t v0[C::VCW], v1[C::VCW], v2[C::VCW], v3[C::VCW];
+                            const int vb = g * C::VCB;
+                            load_chunk<C::VCW>(vbuf + (rbase + 2 * t) * C::BPV, vb, v0);
+                            load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vb, v1);
+                            load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vb, v2);
+                            load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
+#pragma unroll
+                            for (int dm = 0; dm < C::KT; ++dm) {
+                                const uint32_t a0 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm, vtab_a, lane4);
+                                const uint32_t a1 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm + 1, vtab_a, lane4);
+                                const uint32_t a2 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm, vtab_a, lane4);
+                                const uint32_t a3 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm + 1, vtab_a, lane4);
+                                mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
+                                if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
+                            }
                         }
                     }
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty + s);
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(empty + s);
-        }
-        // ------------------------------------------------------------ warp totals
-        TQ_TL(tl_t, 4);
+            // ------------------------------------------------------------ warp totals
+            TQ_TL(tl_t, 4);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 4);
-            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 8);
-            l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 16);
-        }
-        if (g == 0) {
+            for (int j = 0; j < NT; ++j) {
+                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 4);
+                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 8);
+                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 16);
+            }
+            if (g == 0) {
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    const int q = (NT == 2) ? 2 * t + j : t;
+                    wm[warp * kGP + q] = m_run[j];
+                    wl[warp * kGP + q] = l_run[j];
+                }
+                if constexpr (NT == 1) {
+                    wm[warp * kGP + 4 + t] = -CUDART_INF_F;
+                    wl[warp * kGP + 4 + t] = 0.0f;
+                }
+            }
+            // every consumer is done with the ring, wm / wl are visible, and the producer has no
+            // copy in flight (barrier 2 counts the producer warp's arrival)
+            asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+            TQ_TL(tl_t, 5);
+            float f[NT];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int q = (NT == 2) ? 2 * t + j : t;
-                wm[warp * kGP + q] = m_run[j];
-                wl[warp * kGP + q] = l_run[j];
+                float M = -CUDART_INF_F;
+                for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+                // the V table holds v_alpha * c: divide it out here, once per output
+                f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M) / a.cv.v_alpha;
             }
-            if constexpr (NT == 1) {
-                wm[warp * kGP + 4 + t] = -CUDART_INF_F;
-                wl[warp * kGP + 4 + t] = 0.0f;
+            // Each warp's O slice goes to shared memory as float2 units (dims 2c, 2c + 1 of one
+            // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
+            // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
+            // of a row parity on the same two banks).
+            float2* slice = reinterpret_cast<float2*>(ring) + warp * (kGP * D / 2);
+#pragma unroll
+            for (int dm = 0; dm < C::KT; ++dm) {
+                const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
+                if constexpr (NT == 2) {
+                    slice[merge_slot<D>(2 * t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
+                    slice[merge_slot<D>(2 * t + 1, c)] = make_float2(f[1] * O[dm][1], f[1] * O[dm][3]);
+                } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
+                    slice[merge_slot<D>(t, c)] = make_float2(f[0] * (O[dm][0] + O[dm][1]), f[0] * (O[dm][2] + O[dm][3]));
+                    slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                } else {
+                    slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
+                    slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                }
             }
-        }
-        // every consumer is done with the ring, wm / wl are visible, and the producer has no
-        // copy in flight (barrier 2 counts the producer warp's arrival)
-        asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
-        TQ_TL(tl_t, 5);
-        float f[NT];
+            asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+            // fixed-order sum of the warp slices, straight into this CTA's partial record: thread i
+            // sums the float4 at physical units 2i, 2i + 1 of every slice (the same swizzled place
+            // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
+            float* part = STREAM ? partial_slot_ptr(a.ws, p, static_cast<int64_t>(blockIdx.x) + u, D)
+                                 : partial_ptr(a.ws, p, vu, split, D);
+            const float4* all4 = reinterpret_cast<const float4*>(ring);
+            float4* part4 = reinterpret_cast<float4*>(part);
+            for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
+                float4 acc = all4[i];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int q = (NT == 2) ? 2 * t + j : t;
-            float M = -CUDART_INF_F;
-            for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
-            // the V table holds v_alpha * c: divide it out here, once per output
-            f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M) / a.cv.v_alpha;
-        }
-        // Each warp's O slice goes to shared memory as float2 units (dims 2c, 2c + 1 of one
-        // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
-        // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
-        // of a row parity on the same two banks).
-        float2* slice = reinterpret_cast<float2*>(ring) + warp * (kGP * D / 2);
-#pragma unroll
-        for (int dm = 0; dm < C::KT; ++dm) {
-            const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
-            if constexpr (NT == 2) {
-                slice[merge_slot<D>(2 * t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
-                slice[merge_slot<D>(2 * t + 1, c)] = make_float2(f[1] * O[dm][1], f[1] * O[dm][3]);
-            } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
-                slice[merge_slot<D>(t, c)] = make_float2(f[0] * (O[dm][0] + O[dm][1]), f[0] * (O[dm][2] + O[dm][3]));
-                slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                for (int w = 1; w < C::NWC; ++w) {
+                    const float4 x = all4[w * (kGP * D / 4) + i];
+                    acc.x += x.x;
+                    acc.y += x.y;
+                    acc.z += x.z;
+                    acc.w += x.w;
+                }
+                const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
+                const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
+                part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
+            }
+            if (tid < kGP) {
+                const int q = tid;
+                float M = -CUDART_INF_F;
+                for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+                float L = 0.0f;
+                for (int w = 0; w < C::NWC; ++w) {
+                    const float mw = wm[w * kGP + q];
+                    if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
+                }
+                part[kGP * D + q] = (q < G) ? M : -CUDART_INF_F;
+                part[kGP * D + kGP + q] = (q < G) ? L : 0.0f;
+            }
+            if constexpr (STREAM) {
+                if (tid == 0 && sw.ends_unit()) {
+                    // the unit's records: slots cf + u .. this CTA's, cf the CTA holding its first position
+                    const int64_t cf = sw.us / sw.W;
+                    *unit_index_ptr(a.ws, p, u) =
+                        make_int2(static_cast<int>(cf) + u, static_cast<int>(static_cast<int64_t>(blockIdx.x) - cf) + 1);
+                }
+                itg += ntiles;
+#ifdef TQ_TIMELINE
+                if (threadIdx.x == 0) tl_t[1] += 1ull << 32;  // segments, above the SM id
+#endif
+                sw.next(a);
+                if (!sw.valid) break;
+                asm volatile("bar.arrive 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
             } else {
-                slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
-                slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                break;
             }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-        // fixed-order sum of the warp slices, straight into this CTA's partial record: thread i
-        // sums the float4 at physical units 2i, 2i + 1 of every slice (the same swizzled place
-        // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
-        float* part = partial_ptr(a.ws, p, vu, split, D);
-        const float4* all4 = reinterpret_cast<const float4*>(ring);
-        float4* part4 = reinterpret_cast<float4*>(part);
-        for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
-            float4 acc = all4[i];
-#pragma unroll
-            for (int w = 1; w < C::NWC; ++w) {
-                const float4 x = all4[w * (kGP * D / 4) + i];
-                acc.x += x.x;
-                acc.y += x.y;
-                acc.z += x.z;
-                acc.w += x.w;
-            }
-            const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
-            const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
-            part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
-        }
-        if (tid < kGP) {
-            const int q = tid;
-            float M = -CUDART_INF_F;
-            for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
-            float L = 0.0f;
-            for (int w = 0; w < C::NWC; ++w) {
-                const float mw = wm[w * kGP + q];
-                if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
-            }
-            part[kGP * D + q] = (q < G) ? M : -CUDART_INF_F;
-            part[kGP * D + kGP + q] = (q < G) ? L : 0.0f;
-        }
+        }  // segments
     }
     __syncthreads();
 #ifdef TQ_TIMELINE
@@ -1436,7 +1636,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
 cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows);
 
 // Launch of one instantiation; split plan for one CTA per SM.
-template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false>
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false, bool STREAM = false>
 cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
@@ -1444,7 +1644,7 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
@@ -1456,7 +1656,7 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.n_split, p.n_units * p.q_chunks);
+    cfg.gridDim = STREAM ? dim3(p.n_cta, 1) : dim3(p.n_split, p.n_units * p.q_chunks);
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     p.decode_smem = C::SMEM;  // the combine kernel sizes its footprint against it
@@ -1466,7 +1666,7 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI, QJL>, a, p, kmap);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM>, a, p, kmap);
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
@@ -1489,9 +1689,35 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
             }                                                                                 \
     }
 
+// The token-balanced schedule's instantiations: one query position, one row group, coded
+// keys, Walsh-Hadamard rotation (power-of-two dims).
+#define TQ_MMA_STREAM_CASE(KB_, VB_)                                                          \
+    if constexpr (mma_fits(D, KB_, VB_) && KB_ != 16 && (D & (D - 1)) == 0) {                 \
+        if (kb == KB_ && vb == VB_) {                                                         \
+            if (nt == 1) return launch_inst<D, KB_, VB_, 1, false, false, true>(a, p, st);    \
+            if (nt == 2) return launch_inst<D, KB_, VB_, 2, false, false, true>(a, p, st);    \
+            return cudaErrorNotSupported;                                                     \
+        }                                                                                     \
+    }
+
 // The (K bits, V bits) schemes with a tensor-core instantiation.
 constexpr int kSchemes[][2] = {{4, 4}, {3, 3}, {2, 2}, {4, 2}, {4, 3}, {8, 3}, {8, 4}, {8, 8}, {8, 2}, {3, 2},
                                {16, 4}, {16, 2}, {16, 3}};
+
+template <int D>
+cudaError_t launch_mma_d_stream(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
+    TQ_MMA_STREAM_CASE(4, 4)
+    TQ_MMA_STREAM_CASE(3, 3)
+    TQ_MMA_STREAM_CASE(2, 2)
+    TQ_MMA_STREAM_CASE(4, 2)
+    TQ_MMA_STREAM_CASE(4, 3)
+    TQ_MMA_STREAM_CASE(8, 3)
+    TQ_MMA_STREAM_CASE(8, 4)
+    TQ_MMA_STREAM_CASE(8, 8)
+    TQ_MMA_STREAM_CASE(8, 2)
+    TQ_MMA_STREAM_CASE(3, 2)
+    return cudaErrorNotSupported;
+}
 
 template <int D>
 cudaError_t launch_mma_d(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int nt, cudaStream_t st) {
@@ -1512,6 +1738,7 @@ cudaError_t launch_mma_d(const DecodeArgs& a, DecodePlan& p, int kb, int vb, int
 }
 
 #undef TQ_MMA_CASE
+#undef TQ_MMA_STREAM_CASE
 
 }  // namespace mma_detail
 }  // namespace tq

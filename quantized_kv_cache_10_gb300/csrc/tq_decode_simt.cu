@@ -17,6 +17,7 @@
 // This path is the correctness baseline and the fallback for shapes the
 // tensor-core kernel does not instantiate.
 #include <atomic>
+#include <algorithm>
 
 #include "tq_decode_common.cuh"
 
@@ -271,7 +272,15 @@ bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int L, int64_t 
     plan.n_split = int((max_seq + chunk - 1) / chunk);
     plan.part_offset = 256;  // after the device error word
     plan.decode_smem = 0;    // set by the tensor-core launcher
-    plan.ws_bytes = plan.part_offset + size_t(vunits) * plan.n_split * kGP * (d + 2) * sizeof(float);
+    // records: n_split per virtual unit, or, for the token-balanced schedule (one query
+    // position, one row group per unit), one per CTA plus one per unit
+    int64_t nrec = vunits * plan.n_split;
+    if (L == 1 && plan.q_chunks == 1) nrec = std::max<int64_t>(nrec, num_sms(device) + int64_t(plan.n_units));
+    plan.n_rec = int(nrec);
+    plan.stream = 0;
+    plan.n_cta = 0;
+    plan.idx_offset = plan.part_offset + size_t(nrec) * kGP * (d + 2) * sizeof(float);
+    plan.ws_bytes = plan.idx_offset + size_t(plan.n_units) * 2 * sizeof(int32_t);
     return true;
 }
 

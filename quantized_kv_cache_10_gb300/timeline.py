@@ -66,8 +66,18 @@ def _report(title, dec, comb, origin):
     late = np.argsort(dec[:, 6])[-4:]
     for j in late:
         e, f, pt = ((int(dec[j, k]) - origin) / 1e3 for k in (0, 3, 6))
-        print(f"  late decode CTA: SM {int(dec[j, 1])}  entry {e:.2f}  first tile {f:.2f}  partial {pt:.2f}")
-    sms = np.bincount(comb[:, 3].astype(np.int64)) if len(comb) else np.zeros(1)
+        print(f"  late decode CTA: SM {int(dec[j, 1]) & 0xffffffff}  entry {e:.2f}  first tile {f:.2f}  "
+              f"partial {pt:.2f}")
+    # token-balanced schedule: segments per CTA (counted above the SM id) and the CTA span
+    # (entry to partial) by segment count
+    nseg = (dec[:, 1].astype(np.uint64) >> np.uint64(32)).astype(np.int64)
+    if nseg.max() > 0:
+        span = (dec[:, 6].astype(np.int64) - dec[:, 0].astype(np.int64)) / 1e3
+        for k in np.unique(nseg):
+            sel = nseg == k
+            print(f"  CTAs with {k} segment(s): {int(sel.sum()):4d}, entry-to-partial median "
+                  f"{np.median(span[sel]):.2f} us, max {span[sel].max():.2f} us")
+    sms = np.bincount(comb[:, 3].astype(np.int64) & 0xffffffff) if len(comb) else np.zeros(1)
     print(f"  combine CTAs per SM: at most {sms.max()}; SMs with more than one: {int((sms > 1).sum())}")
 
 
