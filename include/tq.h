@@ -94,9 +94,26 @@ void tq_codec_destroy(tq_codec *codec);
 
 /* Codec parameters; any output pointer may be NULL.  bytes_per_vec is the
  * packed row size dim*bits/8 (dim*2 for bits == 16); is_wht is 1 for the
- * Hadamard rotation, 0 for the dense one. */
+ * Hadamard rotation, 0 for the dense one; *centroids_host points at the
+ * codec's own host copy of its 2^bits fp32 centroids, ascending (NULL for
+ * bits == 16), valid until tq_codec_destroy. */
 tq_status tq_codec_info(const tq_codec *codec, int *dim, int *bits, int *bytes_per_vec,
-                        int *is_wht);
+                        int *is_wht, const float **centroids_host);
+
+/* The rotation of the codec (host copies; either pointer may be NULL):
+ * signs [dim] int8 (+1/-1) for the Walsh-Hadamard rotation, dense_q
+ * [dim*dim] fp32 row-major Q (z = Q k) for the dense one; the pointer of the
+ * other kind is left untouched.  ("How I built VeloxQuant-MLX", Stage 1.) */
+tq_status tq_codec_export_rotation(const tq_codec *codec, int8_t *signs, float *dense_q);
+
+/* The Lloyd-Max codebook of N(0,1) with 2^bits levels, built on the host as
+ * tq_codec_create builds it ("How I built VeloxQuant-MLX", Stage 2: cell
+ * boundaries at the midpoints of neighbouring centroids, each centroid the
+ * conditional mean of its cell), without a device:
+ *   centroids  [2^bits] fp32 ascending, RN of the fp64 solution
+ *   midpoints  [2^bits - 1] fp64 (c_i + c_{i+1}) / 2 of the fp32 centroids, or NULL
+ * bits in 1..8.  Errors: TQ_ERR_INVALID_ARG. */
+tq_status tq_codebook_gaussian(int bits, float *centroids, double *midpoints);
 
 /* Copies the codec's host tables out (any pointer may be NULL):
  *   signs      [dim] int8 (+1/-1), WHT codecs only (left untouched otherwise)

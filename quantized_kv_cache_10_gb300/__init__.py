@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "TQError", "Codec", "tq_version", "tq_codec_create", "tq_codec_destroy", "tq_codec_info",
-    "tq_codec_export", "tq_encode", "tq_encode_append", "tq_encode_append_kv", "tq_dequant",
+    "tq_codec_export", "tq_codec_export_rotation", "tq_codebook_gaussian", "tq_encode", "tq_encode_append",
+    "tq_encode_append_kv", "tq_dequant",
     "tq_decode_attend_workspace_bytes", "tq_workspace_init", "tq_decode_attend",
     "tq_get_device_error", "tq_decode_attend_noalloc", "tq_decode_attend_tail",
     "tq_decode_attend_multi", "tq_decode_attend_multi_workspace_bytes", "tq_codec_create_qjl",
@@ -43,8 +44,11 @@ _sig = {
     "tq_status_string": (C.c_char_p, [_i32]),
     "tq_codec_create": (_i32, [_i32, _i32, _u64, C.POINTER(_vp)]),
     "tq_codec_destroy": (None, [_vp]),
-    "tq_codec_info": (_i32, [_vp, C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32)]),
+    "tq_codec_info": (_i32, [_vp, C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32), C.POINTER(_i32),
+                             C.POINTER(C.POINTER(C.c_float))]),
     "tq_codec_export": (_i32, [_vp, _vp, _vp, _vp, _vp]),
+    "tq_codec_export_rotation": (_i32, [_vp, _vp, _vp]),
+    "tq_codebook_gaussian": (_i32, [_i32, _vp, _vp]),
     "tq_encode": (_i32, [_vp, _vp, _i64, _i64, _vp, _i64, _vp, _vp]),
     "tq_encode_append": (_i32, [_vp, _vp, _i32, _i32, _i32, _vp, _i64, _vp, _vp, _vp, _vp]),
     "tq_debug_set_timeline": (_i32, [_vp, _sz]),
@@ -138,7 +142,7 @@ class Codec:
     def __init__(self, handle: int):
         self._h = handle
         d, b, bpv, w = _i32(), _i32(), _i32(), _i32()
-        _check(_lib.tq_codec_info(handle, C.byref(d), C.byref(b), C.byref(bpv), C.byref(w)), "tq_codec_info")
+        _check(_lib.tq_codec_info(handle, C.byref(d), C.byref(b), C.byref(bpv), C.byref(w), None), "tq_codec_info")
         self.dim, self.bits, self.bytes_per_vec, self.is_wht = d.value, b.value, bpv.value, bool(w.value)
 
     @property
@@ -184,7 +188,33 @@ def tq_codec_destroy(codec: Codec):
 
 
 def tq_codec_info(codec: Codec) -> dict:
-    return dict(dim=codec.dim, bits=codec.bits, bytes_per_vec=codec.bytes_per_vec, is_wht=codec.is_wht)
+    """dim, bits, bytes_per_vec, is_wht and the centroids (a numpy copy of the codec's host table)."""
+    import numpy as np
+    ptr = C.POINTER(C.c_float)()
+    _check(_lib.tq_codec_info(codec.handle, None, None, None, None, C.byref(ptr)), "tq_codec_info")
+    cent = np.ctypeslib.as_array(ptr, shape=(1 << codec.bits,)).copy() if ptr else None
+    return dict(dim=codec.dim, bits=codec.bits, bytes_per_vec=codec.bytes_per_vec, is_wht=codec.is_wht,
+                centroids=cent)
+
+
+def tq_codec_export_rotation(codec: Codec) -> dict:
+    """The codec's rotation: signs (Walsh-Hadamard) or dense Q, as numpy arrays."""
+    import numpy as np
+    d = codec.dim
+    s = np.zeros(d, dtype=np.int8)
+    q = np.zeros((d, d), dtype=np.float32)
+    _check(_lib.tq_codec_export_rotation(codec.handle, s.ctypes.data, q.ctypes.data), "tq_codec_export_rotation")
+    return dict(signs=s if codec.is_wht else None, dense_q=None if codec.is_wht else q)
+
+
+def tq_codebook_gaussian(bits: int) -> dict:
+    """The Lloyd-Max codebook of N(0,1) with 2^bits levels as the library builds it (host only)."""
+    import numpy as np
+    n = 1 << min(max(bits, 0), 8)  # buffers for the valid range; the library checks bits
+    c = np.zeros(n, dtype=np.float32)
+    m = np.zeros(max(n - 1, 1), dtype=np.float64)
+    _check(_lib.tq_codebook_gaussian(bits, c.ctypes.data, m.ctypes.data), "tq_codebook_gaussian")
+    return dict(centroids=c, midpoints=m[: n - 1])
 
 
 def tq_codec_export(codec: Codec) -> dict:

@@ -51,8 +51,8 @@ int tq_e2e_decode_steps(const tq_codec* ck, const tq_codec* cv, int B, int n_q_h
                         double* host_seconds, double* h2d_bytes_per_step, double* d2h_bytes_per_step) {
     if (!ck || !cv || R <= 0 || steps <= 0 || pending_batch <= 0) return TQ_ERR_INVALID_ARG;
     int dim = 0, kbits = 0, vbits = 0, kbpv = 0, vbpv = 0, wht = 0;
-    tq_codec_info(ck, &dim, &kbits, &kbpv, &wht);
-    tq_codec_info(cv, &dim, &vbits, &vbpv, &wht);
+    tq_codec_info(ck, &dim, &kbits, &kbpv, &wht, nullptr);
+    tq_codec_info(cv, &dim, &vbits, &vbpv, &wht, nullptr);
     if (kbits == 16) return TQ_ERR_UNSUPPORTED;  // raw keys are copied, not encoded: not driven here
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t units = static_cast<size_t>(B) * n_kv_heads;

@@ -8,11 +8,11 @@
 //    a random Gaussian matrix), by Householder reflections with the signs of
 //    R's diagonal made positive.
 //  * Lloyd-Max codebook of N(0,1) with 2^bits levels ("How I built
-//    VeloxQuant-MLX", The Core Idea): boundaries are midpoints, centroids are
-//    conditional means.  Here the conditional means use the closed form
-//    E[X | a < X < b] = (phi(a) - phi(b)) / (Phi(b) - Phi(a)); a few Lloyd
-//    steps are followed by Newton steps on the same fixed-point conditions
-//    (plain Lloyd steps converge far too slowly at 256 levels).
+//    VeloxQuant-MLX", The Core Idea and Stage 2): boundaries are midpoints,
+//    centroids are conditional means, with the closed form
+//    E[X | a < X < b] = (phi(a) - phi(b)) / (Phi(b) - Phi(a)).  Solved for the
+//    thresholds of the positive half line by damped Newton steps from the
+//    companding (Panter-Dite) start, not by Lloyd's alternation.
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -43,13 +43,6 @@ constexpr double kInvSqrt2 = 0.70710678118654752440084436210485;
 
 double pdf(double x) { return std::isinf(x) ? 0.0 : std::exp(-0.5 * x * x) * kInvSqrt2Pi; }
 double upper_tail(double x) { return 0.5 * std::erfc(x * kInvSqrt2); }  // P(X > x)
-
-// Probability mass of (a, b), computed from the tail nearer to the cell.
-double cell_mass(double a, double b) {
-    if (a >= 0.0) return upper_tail(a) - upper_tail(b);
-    if (b <= 0.0) return upper_tail(-b) - upper_tail(-a);
-    return 1.0 - upper_tail(-a) - upper_tail(b);
-}
 
 }  // namespace
 
@@ -123,58 +116,109 @@ int dense_rotation(int dim, uint64_t seed, std::vector<float>& qout) {
     return 0;
 }
 
+// Lloyd-Max codebook of N(0,1) with n = 2^bits levels ("How I built VeloxQuant-MLX",
+// Stage 2: boundaries are the midpoints of neighbouring centroids, each centroid the
+// conditional mean of its cell).  The density is even, so the codebook is antisymmetric
+// and only the positive half line is solved: m = n/2 cells (t_{j-1}, t_j), t_0 = 0,
+// t_m = +inf, with the m - 1 inner thresholds as the unknowns,
+//   F_j(t) = t_j - (mu_j + mu_{j+1}) / 2 = 0,   mu_j = E[X | t_{j-1} < X < t_j],
+// started from the companding (Panter-Dite) point density p^(1/3) -- for N(0,1) a
+// normal of variance 3, so t_j = sqrt(3) Phi^-1(1/2 + j/n) -- and solved by damped
+// Newton steps (tridiagonal Jacobian; a step is halved while it does not lower max|F|).
+namespace {
+
+// E[X | a < X < b] for 0 <= a < b <= inf, its cell mass and the partial derivatives.
+struct HalfCell {
+    double mass, mean, d_lo, d_hi;  // d_lo = d mean / d a, d_hi = d mean / d b
+};
+
+HalfCell half_cell(double a, double b) {
+    HalfCell h;
+    h.mass = upper_tail(a) - upper_tail(b);
+    const double pa = pdf(a), pb = pdf(b);
+    h.mean = (pa - pb) / h.mass;
+    h.d_lo = pa * (h.mean - a) / h.mass;
+    h.d_hi = std::isinf(b) ? 0.0 : pb * (b - h.mean) / h.mass;
+    return h;
+}
+
+// x >= 0 with P(X > x) = q, 0 < q <= 1/2 (bisection; the tail is decreasing).
+double upper_quantile(double q) {
+    double lo = 0.0, hi = 40.0;
+    for (int it = 0; it < 200 && hi - lo > 0.0; ++it) {
+        const double mid = 0.5 * (lo + hi);
+        if (mid == lo || mid == hi) break;
+        (upper_tail(mid) > q ? lo : hi) = mid;
+    }
+    return 0.5 * (lo + hi);
+}
+
+}  // namespace
+
 void lloyd_max_gaussian(int bits, std::vector<double>& c) {
-    const int n = 1 << bits;
+    const int n = 1 << bits, m = n / 2;
     c.assign(n, 0.0);
     if (n == 1) return;
-    for (int i = 0; i < n; ++i) c[i] = -3.0 + 6.0 * double(i) / double(n - 1);
-    std::vector<double> lo(n), hi(n), D(n), E(n), cp(n), dp(n);
-    auto cells = [&]() {
-        for (int i = 0; i < n; ++i) {
-            lo[i] = (i == 0) ? -INFINITY : 0.5 * (c[i - 1] + c[i]);
-            hi[i] = (i == n - 1) ? INFINITY : 0.5 * (c[i] + c[i + 1]);
-            D[i] = cell_mass(lo[i], hi[i]);
-            E[i] = (pdf(lo[i]) - pdf(hi[i])) / D[i];
+    // t[0] = 0, t[1..m-1] unknown, t[m] = inf
+    std::vector<double> t(m + 1), F(m), sub(m), dia(m), sup(m), step(m), trial(m + 1);
+    t[0] = 0.0;
+    t[m] = INFINITY;
+    const double s3 = std::sqrt(3.0);
+    for (int j = 1; j < m; ++j) t[j] = s3 * upper_quantile(0.5 - double(j) / double(n));
+    std::vector<HalfCell> cell(m + 1);
+    auto residual = [&](const std::vector<double>& tt) {
+        for (int j = 1; j <= m; ++j) cell[j] = half_cell(tt[j - 1], tt[j]);
+        double r = 0.0;
+        for (int j = 1; j < m; ++j) {
+            F[j] = tt[j] - 0.5 * (cell[j].mean + cell[j + 1].mean);
+            r = std::fmax(r, std::fabs(F[j]));
         }
+        return r;
     };
-    for (int it = 0; it < 200; ++it) {
-        cells();
-        double mv = 0.0;
-        for (int i = 0; i < n; ++i) {
-            mv = std::fmax(mv, std::fabs(E[i] - c[i]));
-            c[i] = E[i];
+    double r = residual(t);
+    for (int it = 0; it < 100 && r > 0.0; ++it) {
+        // Jacobian rows j = 1 .. m-1: dF_j / dt_{j-1}, dt_j, dt_{j+1}
+        for (int j = 1; j < m; ++j) {
+            sub[j] = (j > 1) ? -0.5 * cell[j].d_lo : 0.0;
+            dia[j] = 1.0 - 0.5 * (cell[j].d_hi + cell[j + 1].d_lo);
+            sup[j] = (j + 1 < m) ? -0.5 * cell[j + 1].d_hi : 0.0;
+            step[j] = -F[j];
         }
-        if (mv < 1e-14) break;
-    }
-    for (int it = 0; it < 60; ++it) {
-        cells();
-        // Tridiagonal Newton system for F_i = c_i - E_i(c_{i-1}, c_i, c_{i+1}).
-        for (int i = 0; i < n; ++i) {
-            double dEa = (i == 0) ? 0.0 : pdf(lo[i]) * (E[i] - lo[i]) / D[i];
-            double dEb = (i == n - 1) ? 0.0 : pdf(hi[i]) * (hi[i] - E[i]) / D[i];
-            double diag = 1.0 - 0.5 * (dEa + dEb), lower = -0.5 * dEa, upper = -0.5 * dEb;
-            double r = E[i] - c[i];
-            if (i == 0) {
-                cp[i] = upper / diag;
-                dp[i] = r / diag;
-            } else {
-                double den = diag - lower * cp[i - 1];
-                cp[i] = upper / den;
-                dp[i] = (r - lower * dp[i - 1]) / den;
+        // tridiagonal elimination, then back substitution
+        for (int j = 2; j < m; ++j) {
+            const double f = sub[j] / dia[j - 1];
+            dia[j] -= f * sup[j - 1];
+            step[j] -= f * step[j - 1];
+        }
+        for (int j = m - 1; j >= 1; --j) step[j] = (step[j] - ((j + 1 < m) ? sup[j] * step[j + 1] : 0.0)) / dia[j];
+        // damping: keep the thresholds increasing and max|F| falling
+        double lam = 1.0, rn = r, smax = 0.0;
+        for (int tries = 0; tries < 40; ++tries, lam *= 0.5) {
+            bool ordered = true;
+            trial[0] = 0.0;
+            trial[m] = INFINITY;
+            for (int j = 1; j < m; ++j) {
+                trial[j] = t[j] + lam * step[j];
+                if (!(trial[j] > trial[j - 1])) ordered = false;
             }
+            if (!ordered) continue;
+            rn = residual(trial);
+            if (rn < r) break;
         }
-        for (int i = n - 2; i >= 0; --i) dp[i] -= cp[i] * dp[i + 1];
-        double mv = 0.0;
-        for (int i = 0; i < n; ++i) {
-            c[i] += dp[i];
-            mv = std::fmax(mv, std::fabs(dp[i]));
+        smax = 0.0;
+        for (int j = 1; j < m; ++j) smax = std::fmax(smax, std::fabs(trial[j] - t[j]));
+        if (!(rn < r)) {  // no decrease: at the rounding floor
+            residual(t);
+            break;
         }
-        if (mv < 1e-15) break;
+        t.swap(trial);
+        r = rn;
+        if (smax < 1e-16) break;
     }
-    for (int i = 0; i < n / 2; ++i) {  // exact antisymmetry
-        double v = 0.5 * (c[n - 1 - i] - c[i]);
-        c[n - 1 - i] = v;
-        c[i] = -v;
+    residual(t);  // the cells of the final thresholds
+    for (int j = 1; j <= m; ++j) {
+        c[m - 1 + j] = cell[j].mean;
+        c[m - j] = -cell[j].mean;
     }
 }
 
@@ -352,12 +396,29 @@ void tq_codec_destroy(tq_codec* c) {
     delete c;
 }
 
-tq_status tq_codec_info(const tq_codec* c, int* dim, int* bits, int* bytes_per_vec, int* is_wht) {
+tq_status tq_codec_info(const tq_codec* c, int* dim, int* bits, int* bytes_per_vec, int* is_wht,
+                        const float** centroids_host) {
     if (!c) return TQ_ERR_INVALID_ARG;
     if (dim) *dim = c->dim;
     if (bits) *bits = c->bits;
     if (bytes_per_vec) *bytes_per_vec = c->bytes_per_vec;
     if (is_wht) *is_wht = c->is_wht;
+    if (centroids_host) *centroids_host = (c->bits != 16) ? c->centroids.data() : nullptr;
+    return TQ_OK;
+}
+
+tq_status tq_codec_export_rotation(const tq_codec* c, int8_t* signs, float* dense_q) {
+    return tq_codec_export(c, signs, dense_q, nullptr, nullptr);
+}
+
+tq_status tq_codebook_gaussian(int bits, float* centroids, double* midpoints) {
+    if (bits < 1 || bits > 8 || !centroids) return TQ_ERR_INVALID_ARG;
+    std::vector<double> c64;
+    tq::lloyd_max_gaussian(bits, c64);
+    const int n = 1 << bits;
+    for (int i = 0; i < n; ++i) centroids[i] = float(c64[i]);
+    if (midpoints)
+        for (int i = 0; i + 1 < n; ++i) midpoints[i] = (double(centroids[i]) + double(centroids[i + 1])) * 0.5;
     return TQ_OK;
 }
 

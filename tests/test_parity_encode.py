@@ -39,6 +39,13 @@ def test_codec_tables_match_oracle():
                 np.testing.assert_array_equal(t["signs"], o["signs"])
             else:
                 np.testing.assert_array_equal(t["dense_q"], o["Q"])
+            # the same tables through tq_codec_info (host centroids) and tq_codec_export_rotation
+            np.testing.assert_array_equal(tq.tq_codec_info(c)["centroids"], t["centroids"])
+            r = tq.tq_codec_export_rotation(c)
+            if c.is_wht:
+                np.testing.assert_array_equal(r["signs"], t["signs"])
+            else:
+                np.testing.assert_array_equal(r["dense_q"], t["dense_q"])
 
 
 @pytest.mark.parametrize("d,bits", [(64, 4), (128, 2), (128, 3), (128, 4), (128, 8), (96, 3), (96, 8),
