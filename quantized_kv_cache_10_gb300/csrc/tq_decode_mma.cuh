@@ -216,10 +216,10 @@ constexpr int stage_bytes(int D, int KB, int VB, int ts, bool qjl = false) {
 // function serves the kernel (constexpr) and the host's support test.
 struct Layout {
     int nwc, krows, vrows, ktab, vtab, kw, vw, pro, bqb, ubq, fixed, mt, ts, stage, nstage, smem;
-    // 8-bit K ("table block"): both lookup tables share one 64 KB block at the
-    // fixed shared address kTBlock -- K in the first 128 B of each 256-B row, V
-    // in the second -- so that a byte permute forms a whole K address and one
-    // mask-or a whole V address.  The small regions and `g` stages sit below
+    // 8-bit K and pairs of 4-bit K ("table block"): both lookup tables share one
+    // 64 KB block at the fixed shared address kTBlock -- K in the first 128 B of
+    // each 256-B row, V in the second -- so that a byte permute forms a whole K
+    // address and one mask-or a whole V address.  The small regions and `g` stages sit below
     // the block, the other `na` stages above it.
     bool tblock;
     int small, g, na;
@@ -268,8 +268,9 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
 }
 
 constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
-    if (KB == 8) {
+    if (KB == 8 || (KB == 4 && !qjl && !multi)) {
         // the table block, when it holds at least as many stages as the linear layout would
+        // (4-bit keys: a pair of codes is one byte, so the same byte permute forms the address)
         const Layout t2 = make_tblock_layout(D, KB, VB, 2, multi), t1 = make_tblock_layout(D, KB, VB, 1, multi);
         const Layout t = (D <= 128 && t2.nstage >= 3) ? t2 : t1;
         if (t.nstage >= 3) return t;
@@ -378,6 +379,9 @@ struct Cfg {
     static constexpr int NSTAGE = L.nstage;
     static constexpr int SMEM = L.smem;
     static constexpr bool TBLOCK = L.tblock;
+    // K lookups addressed by one byte permute of the code word: 8-bit codes, or pairs of
+    // 4-bit codes (one byte) in the table block
+    static constexpr bool KPERM = KEXP || (KB == 4 && TBLOCK);
     static constexpr int SMALL = L.small, G_BELOW = L.g, N_ABOVE = L.na;
     static_assert(STAGE >= KBUF + VBUF + 2 * NBUF + SBUF + RBUF, "stage size");
     static_assert(!QJL || (KB <= 4 && D % 32 == 0), "the QJL sketch rides on 2-4 bit keys");
@@ -454,18 +458,34 @@ struct VPairs {
     }
 };
 
-// 64 bits of a row starting at bit `bit` (row 4-byte aligned; may read 12 bytes past).
-__device__ __forceinline__ uint64_t load_bits64(const uint8_t* row, int bit) {
+// Bits [bit, bit + 32 NW - (bit & 31)) of a row (4-byte aligned) in the low bits of the
+// result: NW words, the fewest that hold the field the caller uses (at most 64 bits).
+template <int NW>
+__device__ __forceinline__ uint64_t load_bits_w(const uint8_t* row, int bit) {
+    static_assert(NW >= 1 && NW <= 3, "words");
     const uint32_t* p = reinterpret_cast<const uint32_t*>(row) + (bit >> 5);
     const int sh = bit & 31;
-    const uint32_t w0 = p[0], w1 = p[1];
-    uint32_t lo = w0, hi = w1;
-    if (sh) {
-        const uint32_t w2 = p[2];
-        lo = __funnelshift_r(w0, w1, sh);
-        hi = __funnelshift_r(w1, w2, sh);
-    }
+    const uint32_t w0 = p[0];
+    const uint32_t w1 = (NW > 1) ? p[1] : 0u;
+    const uint32_t w2 = (NW > 2) ? p[2] : 0u;
+    const uint32_t lo = __funnelshift_r(w0, w1, sh);
+    const uint32_t hi = __funnelshift_r(w1, w2, sh);
     return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
+// Words a thread's V-role field spans at most: min(16, D/8) dims of VB bits at bit
+// g * (D/8) VB + 16 VB sub of the row, over the eight g and the NSUB chunks.
+constexpr int v_field_words(int D, int VB) {
+    const int nsub = (D / 8 + 15) / 16;
+    const int nb = (D / 8 < 16 ? D / 8 : 16) * VB;
+    int m = 1;
+    for (int g = 0; g < 8; ++g)
+        for (int sub = 0; sub < nsub; ++sub) {
+            const int sh = (g * (D / 8) * VB + 16 * VB * sub) % 32;
+            const int w = (sh + nb + 31) / 32;
+            m = w > m ? w : m;
+        }
+    return m;
 }
 
 // Loads NW 32-bit words of a row chunk starting at bit `bit` of the row (row
@@ -541,7 +561,8 @@ __device__ __forceinline__ void replicate_one(const uint32_t* src, uint8_t* dst,
 template <typename C>
 __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const uint32_t* vcompact, uint8_t* ktab_s,
                                                  uint8_t* vtab_s, int ctid) {
-    if constexpr (C::KROWS > 0) replicate_one<C, C::KROWS, 1, C::KPAIR ? 128 : 256>(kcompact, ktab_s, ctid);
+    if constexpr (C::KROWS > 0)
+        replicate_one<C, C::KROWS, 1, (C::KPAIR && !C::TBLOCK) ? 128 : 256>(kcompact, ktab_s, ctid);
     replicate_one<C, C::VROWS, 1, C::TBLOCK ? 256 : 128>(vcompact, vtab_s, ctid);
 }
 
@@ -780,6 +801,17 @@ struct StreamWalk {
     }
 };
 
+// Warp-merge area of the token-balanced schedule: beside the ring when it fits, so that
+// the producer keeps filling the ring with the next segment's tiles while the consumers
+// merge a segment (rows 4..7 of a warp's slice are zero with up to four query heads and
+// are not stored).  0: the merge reuses the ring, and the producer waits for it.
+template <int D, int KB, int VB, int NT, bool QJL, bool MULTI, bool STREAM>
+constexpr int stream_merge_bytes() {
+    using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
+    const int bytes = C::NWC * ((NT == 2) ? kGP : 4) * D * 4;
+    return (STREAM && C::SMEM + bytes <= kSmemLimit) ? bytes : 0;
+}
+
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
@@ -793,6 +825,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     // the token-balanced schedule (STREAM) serves one query position, one row group, coded
     // keys without the sketch and the Walsh-Hadamard rotation
     static_assert(!STREAM || (!MULTI && !QJL && !Q_STAGED), "token-balanced schedule");
+    constexpr bool SEP = stream_merge_bytes<D, KB, VB, NT, QJL, MULTI, STREAM>() > 0;
+    constexpr int SROWS = (SEP && NT == 1) ? 4 : kGP;  // rows of a warp's merge slice
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
@@ -1004,9 +1038,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
         }
         if constexpr (STREAM) {
             // Segment by segment: the copies of the segment's tiles (continuing around the
-            // ring), then the arrival on barrier 2 (all copies issued), then, before the next
-            // segment's copies reuse the ring, barrier 3: the consumers' merge of this
-            // segment (which reads the ring) is done.
+            // ring); where the merge reuses the ring, then the arrival on barrier 2 (all
+            // copies issued) and, before the next segment's copies, barrier 3: the
+            // consumers' merge of this segment is done.
             __syncwarp();
             asm volatile("griddepcontrol.wait;" ::: "memory");
             if (lane == 0) allow_dependent_launch();
@@ -1035,9 +1069,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 }
                 itg += nt;
                 __syncwarp();
-                asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                if constexpr (!SEP) asm volatile("bar.arrive 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
                 sw.next(a);
-                if (sw.valid) asm volatile("bar.sync 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                if (!SEP && sw.valid) asm volatile("bar.sync 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
             }
         } else {
             __syncwarp();  // reconverge the producer warp before the block-wide barriers
@@ -1283,10 +1317,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                         uint32_t wa[C::KCW], wb[C::KCW];
                         load_k_chunk<D, KB, C::KCW>(kbuf, ra, t, wa);
                         load_k_chunk<D, KB, C::KCW>(kbuf, rb, t, wb);
-                        if constexpr (C::KEXP) {
+                        if constexpr (C::KPERM) {
 #pragma unroll
                             for (int kt = 0; kt < C::KTS; ++kt) {
                                 // bytes 2(kt&1), 2(kt&1)+1 of word kt/2 are dims d0, d1 of this k-tile
+                                // (4-bit keys: the pairs of dims d0, d0 + 1 and d0 + 2, d0 + 3)
                                 const uint32_t wA = wa[kt >> 1], wB = wb[kt >> 1];
                                 // address = [koff byte 3][koff byte 2 / 0][code][koff byte 0]: with the
                                 // table block the permute alone forms it, else it is added to ktab_a
@@ -1467,10 +1502,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
 #pragma unroll
                             for (int sub = 0; sub < NSUB; ++sub) {
                                 const int vbit = g * C::VCB + 16 * VB * sub;
-                                const VPairs<VB, C::TBLOCK> p01(load_bits64(vbuf + (rbase + 2 * t) * C::BPV, vbit),
-                                                     load_bits64(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
-                                const VPairs<VB, C::TBLOCK> p89(load_bits64(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
-                                                     load_bits64(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
+                                constexpr int VW = v_field_words(D, VB);  // words per field (2 at D 128, 3 bits)
+                                const VPairs<VB, C::TBLOCK> p01(load_bits_w<VW>(vbuf + (rbase + 2 * t) * C::BPV, vbit),
+                                                     load_bits_w<VW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
+                                const VPairs<VB, C::TBLOCK> p89(load_bits_w<VW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
+                                                     load_bits_w<VW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
                                 constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
 #pragma unroll
                                 for (int k = 0; k < DM_PER_SUB; ++k) {
@@ -1528,8 +1564,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 }
             }
             // every consumer is done with the ring, wm / wl are visible, and the producer has no
-            // copy in flight (barrier 2 counts the producer warp's arrival)
-            asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+            // copy in flight (barrier 2 counts the producer warp's arrival); with a merge area of
+            // its own the producer goes on, and the consumers alone meet
+            if constexpr (SEP)
+                asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+            else
+                asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
             TQ_TL(tl_t, 5);
             float f[NT];
 #pragma unroll
@@ -1544,7 +1584,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
             // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
             // of a row parity on the same two banks).
-            float2* slice = reinterpret_cast<float2*>(ring) + warp * (kGP * D / 2);
+            float2* const merge_base = reinterpret_cast<float2*>(SEP ? smem + C::SMEM : ring);
+            float2* slice = merge_base + warp * (SROWS * D / 2);
 #pragma unroll
             for (int dm = 0; dm < C::KT; ++dm) {
                 const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
@@ -1556,7 +1597,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                     slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
                 } else {
                     slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
-                    slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                    if constexpr (SROWS == kGP) slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
@@ -1565,19 +1606,23 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
             float* part = STREAM ? partial_slot_ptr(a.ws, p, static_cast<int64_t>(blockIdx.x) + u, D)
                                  : partial_ptr(a.ws, p, vu, split, D);
-            const float4* all4 = reinterpret_cast<const float4*>(ring);
+            const float4* all4 = reinterpret_cast<const float4*>(merge_base);
             float4* part4 = reinterpret_cast<float4*>(part);
             for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
+                const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
+                if (SROWS < kGP && row >= SROWS) {  // rows with no query head
+                    part4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    continue;
+                }
                 float4 acc = all4[i];
 #pragma unroll
                 for (int w = 1; w < C::NWC; ++w) {
-                    const float4 x = all4[w * (kGP * D / 4) + i];
+                    const float4 x = all4[w * (SROWS * D / 4) + i];
                     acc.x += x.x;
                     acc.y += x.y;
                     acc.z += x.z;
                     acc.w += x.w;
                 }
-                const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
                 const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
                 part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
             }
@@ -1606,7 +1651,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
 #endif
                 sw.next(a);
                 if (!sw.valid) break;
-                asm volatile("bar.arrive 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                if constexpr (SEP) {
+                    // the slices are read: the next segment's merge may overwrite them
+                    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+                } else {
+                    asm volatile("bar.arrive 3, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                }
             } else {
                 break;
             }
@@ -1643,9 +1693,10 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
+    constexpr int SMEM = C::SMEM + stream_merge_bytes<D, KB, VB, NT, QJL, MULTI, STREAM>();
     if (!(configured.load() & bit)) {
         cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
@@ -1658,8 +1709,8 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = STREAM ? dim3(p.n_cta, 1) : dim3(p.n_split, p.n_units * p.q_chunks);
     cfg.blockDim = dim3(C::NTHREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
-    p.decode_smem = C::SMEM;  // the combine kernel sizes its footprint against it
+    cfg.dynamicSmemBytes = SMEM;
+    p.decode_smem = SMEM;  // the combine kernel sizes its footprint against it
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
