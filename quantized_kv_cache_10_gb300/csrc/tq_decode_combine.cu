@@ -127,12 +127,12 @@ __device__ __forceinline__ void to_rotated_units(const DecodeArgs& a, float (&x)
 // decode CTA is resident, and only if a combine CTA fits beside one does it start there
 // (scoring the tail during the decode); otherwise its CTAs wait for the first SMs the
 // decode grid frees and pile up there, several per SM, keeping the next call's decode
-// CTAs off those SMs.  So it uses at most 64 registers per thread up to d = 192 (one
+// CTAs off those SMs.  So it uses at most 64 registers per thread up to d = 160 (one
 // warp per SM sub-partition fits beside three 144-register decode warps), the same
 // shared-memory split as the decode kernel, and a shared-memory pad sized at launch
 // so that exactly one combine CTA fits beside a decode CTA.
 template <int VPL>
-__global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 6 ? 8 : 4)) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
+__global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 5 ? 8 : 4)) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
@@ -238,19 +238,21 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 6 ? 8 : 4)) decode
 #pragma unroll
         for (int v = 0; v < VPL; ++v) tail_o[v] = ot[v];
     }
+    // This row's records: n_split of them, or, on the token-balanced schedule, those of the
+    // CTAs whose positions cover the unit (none while the sequence is empty), found from
+    // the lengths here, before the wait, while the decode kernel runs.
+    int ns = p.n_split;
+    int64_t rec0 = static_cast<int64_t>(vu) * p.n_split;
+    if (p.stream) {
+        int64_t first;
+        stream_unit_ctas(a, p.n_cta, b, kvh, lane, first, ns);
+        rec0 = first + u;
+    }
     // wait for this call's decode grid (and the visibility of its records)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     TQ_TL(tl_t, 1);
-    // the unit's records: n_split of them, or, on the token-balanced schedule, the slots
-    // its index entry lists (none while the sequence is empty)
-    int ns = p.n_split;
     const int rec = kGP * (D + 2);
-    const float* base = partial_ptr(a.ws, p, vu, 0, D);
-    if (p.stream) {
-        const int2 ix = __ldcg(unit_index_ptr(a.ws, p, u));
-        ns = (__ldg(a.seq_lens + b) > 0) ? ix.y : 0;
-        base = partial_slot_ptr(a.ws, p, ns > 0 ? ix.x : 0, D);
-    }
+    const float* base = partial_slot_ptr(a.ws, p, rec0, D);
     const float* ob = base + g * D + lane * VPL;
 
     constexpr int CH = VPL <= 4 ? 5 : (VPL <= 8 ? 4 : 2);

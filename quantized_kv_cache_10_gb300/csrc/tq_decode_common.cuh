@@ -35,12 +35,137 @@ __device__ __forceinline__ float* partial_slot_ptr(void* ws, const DecodePlan& p
     return base + slot * (kGP * (d + 2));
 }
 
-// {first slot, count} of unit u's records under the token-balanced schedule.
-__device__ __forceinline__ int2* unit_index_ptr(void* ws, const DecodePlan& p, int u) {
-    return reinterpret_cast<int2*>(static_cast<char*>(ws) + p.idx_offset) + u;
+__device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int32_t*>(ws); }
+
+// Token-balanced schedule (several sequences, one query position, tensor-core kernel)
+// The units' tokens are laid end to end in unit order (u = b * Hkv + h), unit u
+// spanning len_b rounded up to a multiple of 8 positions, and CTA c takes positions
+// [c W, (c + 1) W), W = the total over the CTAs rounded up to 8 (at least kStreamMinW).
+// Every boundary is a multiple of 8, so each segment of a unit starts on an 8-token
+// boundary (16-byte aligned copies) and holds at least one real token.  Every warp that
+// needs the segments walks them itself (warp-collective, same result in each).
+constexpr int64_t kStreamMinW = 256;
+
+__device__ __forceinline__ int64_t stream_len(const DecodeArgs& a, int b, bool flag) {
+    int64_t L = __ldg(a.seq_lens + b);
+    if (L < 0 || L > a.max_seq) {
+        if (flag) atomicOr(error_ptr(a.ws), TQ_DEVERR_SEQ_LEN);
+        L = L < 0 ? 0 : a.max_seq;
+    }
+    return L;
 }
 
-__device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int32_t*>(ws); }
+// Total positions (all units) and the positions per CTA, W (warp-collective).
+__device__ __forceinline__ void stream_extent(const DecodeArgs& a, int n_cta, int lane, bool flag, int64_t& tot,
+                                              int64_t& W) {
+    tot = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        const int bb = b0 + lane;
+        int64_t sp = bb < a.B ? ((stream_len(a, bb, flag) + 7) & ~int64_t(7)) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
+        tot += sp;
+    }
+    tot *= a.Hkv;
+    W = (tot + n_cta - 1) / n_cta;
+    W = max((W + 7) & ~int64_t(7), kStreamMinW);
+}
+
+// The CTAs whose positions cover unit (b, h): the first and their count (0 when the
+// sequence is empty) -- its records are slots first + u .. first + u + count - 1
+// (warp-collective).
+__device__ __forceinline__ void stream_unit_ctas(const DecodeArgs& a, int n_cta, int b, int h, int lane,
+                                                 int64_t& first, int& count) {
+    int64_t tot, W;
+    stream_extent(a, n_cta, lane, false, tot, W);
+    // positions before sequence b: its units start there
+    int64_t before = 0;
+    for (int b0 = 0; b0 < b; b0 += 32) {
+        const int bb = b0 + lane;
+        int64_t sp = bb < b ? ((stream_len(a, bb, false) + 7) & ~int64_t(7)) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
+        before += sp;
+    }
+    const int64_t span = (stream_len(a, b, false) + 7) & ~int64_t(7);
+    const int64_t us = before * a.Hkv + static_cast<int64_t>(h) * span;
+    first = us / W;
+    count = span > 0 ? static_cast<int>((us + span - 1) / W - first + 1) : 0;
+}
+
+struct StreamWalk {
+    int b, h;          // current unit: sequence b, KV head h
+    int64_t len;       // len_b (clamped)
+    int64_t span;      // len_b rounded up to 8
+    int64_t us;        // first position of the unit
+    int64_t a0;        // first token of this CTA's segment in the unit
+    int64_t end;       // the CTA's positions end here
+    int64_t W;         // positions per CTA
+    bool valid;        // a segment is current
+
+    // Segment [a0, a1) of unit (b, h), a1 <= len.
+    __device__ __forceinline__ int64_t a1() const { return min(len, end - us); }
+
+    // Walk start for CTA c of n_cta (lengths flagged by warp 0's lanes only).
+    __device__ __forceinline__ void init(const DecodeArgs& a, int c, int n_cta, int lane, bool flag) {
+        int64_t tot;
+        stream_extent(a, n_cta, lane, flag, tot, W);
+        const int64_t P = static_cast<int64_t>(c) * W;
+        valid = P < tot;
+        end = min(P + W, tot);
+        b = 0;
+        h = 0;
+        len = span = us = a0 = 0;
+        if (!valid) return;
+        // the sequence whose units hold position P
+        int64_t base = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            const int bb = b0 + lane;
+            const int64_t L = bb < a.B ? stream_len(a, bb, false) : 0;
+            const int64_t sp = ((L + 7) & ~int64_t(7)) * a.Hkv;
+            int64_t inc = sp;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(kFullMask, inc, o);
+                if (lane >= o) inc += y;
+            }
+            const unsigned hit = __ballot_sync(kFullMask, bb < a.B && base + inc > P);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                b = b0 + l;
+                const int64_t sb = base + __shfl_sync(kFullMask, inc - sp, l);
+                len = __shfl_sync(kFullMask, L, l);
+                span = (len + 7) & ~int64_t(7);
+                h = static_cast<int>((P - sb) / span);
+                us = sb + static_cast<int64_t>(h) * span;
+                a0 = P - us;
+                return;
+            }
+            base += __shfl_sync(kFullMask, inc, 31);
+        }
+        valid = false;  // not reached: P < tot
+    }
+
+    // Next segment (the next unit with tokens), if the CTA's positions go on.
+    __device__ __forceinline__ void next(const DecodeArgs& a) {
+        const int64_t ue = us + span;
+        if (end <= ue) {
+            valid = false;
+            return;
+        }
+        us = ue;
+        a0 = 0;
+        if (++h == a.Hkv) {
+            h = 0;
+            do {
+                ++b;
+                len = b < a.B ? stream_len(a, b, false) : 0;
+            } while (len == 0 && b < a.B);
+            span = (len + 7) & ~int64_t(7);
+            if (b >= a.B) valid = false;  // not reached: end <= total
+        }
+    }
+};
 
 // Clamped sequence length of batch b (flags out-of-range values).
 __device__ __forceinline__ int64_t clamped_len(const DecodeArgs& a, int b) {

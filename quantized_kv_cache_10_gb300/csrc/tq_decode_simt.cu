@@ -279,8 +279,7 @@ bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int L, int64_t 
     plan.n_rec = int(nrec);
     plan.stream = 0;
     plan.n_cta = 0;
-    plan.idx_offset = plan.part_offset + size_t(nrec) * kGP * (d + 2) * sizeof(float);
-    plan.ws_bytes = plan.idx_offset + size_t(plan.n_units) * 2 * sizeof(int32_t);
+    plan.ws_bytes = plan.part_offset + size_t(nrec) * kGP * (d + 2) * sizeof(float);
     return true;
 }
 

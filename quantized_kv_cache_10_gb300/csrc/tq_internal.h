@@ -111,12 +111,10 @@ struct DecodePlan {
     // Token-balanced schedule (tensor-core kernel, one query position, several sequences):
     // the units' tokens laid end to end, unit u = b * Hkv + h spanning len_b rounded up to
     // 8 positions, and CTA c of n_cta takes an equal share of the positions.  Its records
-    // are at slots c + u; unit u's slots are listed at idx_offset ({first slot, count}
-    // per unit, written by the CTA that holds the unit's last tokens).
+    // are at slots c + u (the combine finds a unit's CTAs from the same lengths).
     int stream;          // 1: token-balanced schedule, 0: n_split splits of chunk tokens per unit
     int n_cta;           // CTAs of the token-balanced schedule
     int n_rec;           // partial records the workspace holds
-    size_t idx_offset;   // byte offset of the per-unit {first slot, count} pairs
 };
 
 // Split-K plan (independent of the kernel chosen, so the workspace size only
