@@ -39,12 +39,21 @@ __device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int
 
 // Token-balanced schedule (several sequences, one query position, tensor-core kernel)
 // The units' tokens are laid end to end in unit order (u = b * Hkv + h), unit u
-// spanning len_b rounded up to a multiple of 8 positions, and CTA c takes positions
+// spanning kStreamOvh positions that hold no token and then len_b rounded up to a
+// multiple of 8 (an empty sequence spans nothing), and CTA c takes positions
 // [c W, (c + 1) W), W = the total over the CTAs rounded up to 8 (at least kStreamMinW).
-// Every boundary is a multiple of 8, so each segment of a unit starts on an 8-token
-// boundary (16-byte aligned copies) and holds at least one real token.  Every warp that
-// needs the segments walks them itself (warp-collective, same result in each).
+// The positions without tokens stand for the fixed cost of starting a unit (its queries,
+// a partial record), so a CTA that starts more units gets fewer tokens.  Every boundary
+// is a multiple of 8, so each segment of a unit starts on an 8-token boundary (16-byte
+// aligned copies) and holds at least one real token.  Every warp that needs the
+// segments walks them itself (warp-collective, same result in each).
 constexpr int64_t kStreamMinW = 256;
+constexpr int64_t kStreamOvh = 320;
+
+// Positions of one unit of a sequence of len tokens.
+__device__ __forceinline__ int64_t stream_unit_ext(int64_t len) {
+    return len > 0 ? kStreamOvh + ((len + 7) & ~int64_t(7)) : 0;
+}
 
 __device__ __forceinline__ int64_t stream_len(const DecodeArgs& a, int b, bool flag) {
     int64_t L = __ldg(a.seq_lens + b);
@@ -61,7 +70,7 @@ __device__ __forceinline__ void stream_extent(const DecodeArgs& a, int n_cta, in
     tot = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int bb = b0 + lane;
-        int64_t sp = bb < a.B ? ((stream_len(a, bb, flag) + 7) & ~int64_t(7)) : 0;
+        int64_t sp = bb < a.B ? stream_unit_ext(stream_len(a, bb, flag)) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
         tot += sp;
@@ -82,29 +91,29 @@ __device__ __forceinline__ void stream_unit_ctas(const DecodeArgs& a, int n_cta,
     int64_t before = 0;
     for (int b0 = 0; b0 < b; b0 += 32) {
         const int bb = b0 + lane;
-        int64_t sp = bb < b ? ((stream_len(a, bb, false) + 7) & ~int64_t(7)) : 0;
+        int64_t sp = bb < b ? stream_unit_ext(stream_len(a, bb, false)) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
         before += sp;
     }
-    const int64_t span = (stream_len(a, b, false) + 7) & ~int64_t(7);
-    const int64_t us = before * a.Hkv + static_cast<int64_t>(h) * span;
-    first = us / W;
-    count = span > 0 ? static_cast<int>((us + span - 1) / W - first + 1) : 0;
+    const int64_t ext = stream_unit_ext(stream_len(a, b, false));
+    const int64_t us = before * a.Hkv + static_cast<int64_t>(h) * ext;  // the unit's first position
+    first = (us + kStreamOvh) / W;                                      // ... holding a token
+    count = ext > 0 ? static_cast<int>((us + ext - 1) / W - first + 1) : 0;
 }
 
 struct StreamWalk {
     int b, h;          // current unit: sequence b, KV head h
     int64_t len;       // len_b (clamped)
-    int64_t span;      // len_b rounded up to 8
-    int64_t us;        // first position of the unit
+    int64_t ext;       // positions of the unit (kStreamOvh + len_b rounded up to 8)
+    int64_t us;        // first position of the unit (its tokens start at us + kStreamOvh)
     int64_t a0;        // first token of this CTA's segment in the unit
     int64_t end;       // the CTA's positions end here
     int64_t W;         // positions per CTA
     bool valid;        // a segment is current
 
     // Segment [a0, a1) of unit (b, h), a1 <= len.
-    __device__ __forceinline__ int64_t a1() const { return min(len, end - us); }
+    __device__ __forceinline__ int64_t a1() const { return min(len, end - (us + kStreamOvh)); }
 
     // Walk start for CTA c of n_cta (lengths flagged by warp 0's lanes only).
     __device__ __forceinline__ void init(const DecodeArgs& a, int c, int n_cta, int lane, bool flag) {
@@ -115,14 +124,14 @@ struct StreamWalk {
         end = min(P + W, tot);
         b = 0;
         h = 0;
-        len = span = us = a0 = 0;
+        len = ext = us = a0 = 0;
         if (!valid) return;
         // the sequence whose units hold position P
         int64_t base = 0;
         for (int b0 = 0; b0 < a.B; b0 += 32) {
             const int bb = b0 + lane;
             const int64_t L = bb < a.B ? stream_len(a, bb, false) : 0;
-            const int64_t sp = ((L + 7) & ~int64_t(7)) * a.Hkv;
+            const int64_t sp = stream_unit_ext(L) * a.Hkv;
             int64_t inc = sp;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -135,10 +144,12 @@ struct StreamWalk {
                 b = b0 + l;
                 const int64_t sb = base + __shfl_sync(kFullMask, inc - sp, l);
                 len = __shfl_sync(kFullMask, L, l);
-                span = (len + 7) & ~int64_t(7);
-                h = static_cast<int>((P - sb) / span);
-                us = sb + static_cast<int64_t>(h) * span;
-                a0 = P - us;
+                ext = stream_unit_ext(len);
+                h = static_cast<int>((P - sb) / ext);
+                us = sb + static_cast<int64_t>(h) * ext;
+                const int64_t r0 = us + kStreamOvh;  // the unit's first token
+                a0 = P > r0 ? P - r0 : 0;
+                valid = end > r0;  // else the CTA's positions end before any token
                 return;
             }
             base += __shfl_sync(kFullMask, inc, 31);
@@ -146,9 +157,9 @@ struct StreamWalk {
         valid = false;  // not reached: P < tot
     }
 
-    // Next segment (the next unit with tokens), if the CTA's positions go on.
+    // Next segment (the next unit with tokens), if the CTA's positions reach its tokens.
     __device__ __forceinline__ void next(const DecodeArgs& a) {
-        const int64_t ue = us + span;
+        const int64_t ue = us + ext;
         if (end <= ue) {
             valid = false;
             return;
@@ -161,9 +172,13 @@ struct StreamWalk {
                 ++b;
                 len = b < a.B ? stream_len(a, b, false) : 0;
             } while (len == 0 && b < a.B);
-            span = (len + 7) & ~int64_t(7);
-            if (b >= a.B) valid = false;  // not reached: end <= total
+            ext = stream_unit_ext(len);
+            if (b >= a.B) {  // not reached: end <= total
+                valid = false;
+                return;
+            }
         }
+        valid = end > us + kStreamOvh;
     }
 };
 

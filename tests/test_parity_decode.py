@@ -72,22 +72,26 @@ def test_decode_edge_lengths(lens):
 
 
 # Several sequences take the token-balanced schedule (one CTA per SM over all units'
-# tokens laid end to end): CTAs that cover many short units, units split over several
-# CTAs, empty and 1..9-token sequences, more than 32 sequences (the length scan runs
-# over chunks of 32), and long units whose tiles wrap the ring across segments.
-@pytest.mark.parametrize("B,S,lens_seed,kb,vb,G", [
-    (40, 320, 3, 4, 2, 4),     # short ragged sequences: several units per CTA
-    (5, 1032, 4, 8, 3, 8),     # a few units of ~1K tokens: segments inside units
-    (3, 8192, 5, 4, 2, 4),     # long units: many tiles per segment, ring wrap
-    (33, 256, 6, 3, 3, 2),     # d 256 below (the parametrised d)
+# tokens laid end to end): CTAs that cover several short units (up to 4 segments, with
+# the merge beside the ring and, for 8-bit keys, in it), units split over several CTAs,
+# empty and 1..9-token sequences, more than 32 sequences (the length scan runs over
+# chunks of 32), and long units whose tiles wrap the ring across segments.
+@pytest.mark.parametrize("B,Hkv,S,lens_seed,kb,vb,G", [
+    (64, 8, 128, 7, 4, 2, 4),     # 512 short units: up to 4 segments per CTA
+    (48, 8, 200, 8, 8, 3, 8),     # the same with 8-bit keys (merge in the ring)
+    (40, 2, 320, 3, 4, 2, 4),     # short ragged sequences
+    (5, 2, 1032, 4, 8, 3, 8),     # a few units of ~1K tokens: segments inside units
+    (3, 2, 8192, 5, 4, 2, 4),     # long units: many tiles per segment, ring wrap
+    (33, 2, 256, 6, 3, 3, 2),     # d 256 (3-bit keys and values)
+    (96, 4, 96, 9, 3, 3, 2),      # d 256 with several segments per CTA
 ])
-def test_decode_token_balanced_schedule(B, S, lens_seed, kb, vb, G):
+def test_decode_token_balanced_schedule(B, Hkv, S, lens_seed, kb, vb, G):
     d = 256 if (kb, vb) == (3, 3) else 128
     rng = np.random.default_rng(lens_seed)
     lens = rng.integers(0, S + 1, size=B).astype(np.int32)
     edge = [0, 1, 7, 8, 9, S]
     lens[:min(B, len(edge))] = edge[:B]
-    w = tq_inputs.Workload("t", B=B, Hq=2 * G, Hkv=2, d=d, S=S, k_bits=kb, v_bits=vb, k_outliers=True)
+    w = tq_inputs.Workload("t", B=B, Hq=Hkv * G, Hkv=Hkv, d=d, S=S, k_bits=kb, v_bits=vb, k_outliers=True)
     got, ref, ws = _run_small(w, lens=lens)
     for b in range(B):
         if lens[b] == 0:
