@@ -50,6 +50,39 @@ __device__ __forceinline__ void load_vec(const float* p, float (&v)[N]) {
     }
 }
 
+// VPL consecutive fp16 values (a lane's dims of one row) as packed pairs, bypassing L1:
+// one 4-, 8- or 16-byte load where VPL allows (the rows are 16-byte aligned).
+template <int VPL>
+__device__ __forceinline__ void load_halves(const uint16_t* p, uint32_t (&h)[(VPL + 1) / 2]) {
+    if constexpr (VPL % 8 == 0) {
+#pragma unroll
+        for (int i = 0; i < VPL / 8; ++i) {
+            const uint4 x = __ldcg(reinterpret_cast<const uint4*>(p) + i);
+            h[4 * i] = x.x;
+            h[4 * i + 1] = x.y;
+            h[4 * i + 2] = x.z;
+            h[4 * i + 3] = x.w;
+        }
+    } else if constexpr (VPL == 4) {
+        const uint2 x = __ldcg(reinterpret_cast<const uint2*>(p));
+        h[0] = x.x;
+        h[1] = x.y;
+    } else if constexpr (VPL == 2) {
+        h[0] = __ldcg(reinterpret_cast<const unsigned int*>(p));
+    } else {
+#pragma unroll
+        for (int i = 0; i < (VPL + 1) / 2; ++i) {
+            const uint32_t lo = __ldcg(p + 2 * i);
+            const uint32_t hi = (2 * i + 1 < VPL) ? __ldcg(p + 2 * i + 1) : 0u;
+            h[i] = lo | (hi << 16);
+        }
+    }
+}
+
+__device__ __forceinline__ float half_at(const uint32_t* h, int v) {
+    return __half2float(__ushort_as_half(static_cast<uint16_t>(h[v >> 1] >> (16 * (v & 1)))));
+}
+
 // Online merge of one more partial (m_s, l_s, o_s) into (m, l, acc).
 template <int VPL>
 __device__ __forceinline__ void merge_state(float& m, float& l, float (&acc)[VPL], float ms, float ls,
@@ -131,8 +164,12 @@ __device__ __forceinline__ void to_rotated_units(const DecodeArgs& a, float (&x)
 // warp per SM sub-partition fits beside three 144-register decode warps), the same
 // shared-memory split as the decode kernel, and a shared-memory pad sized at launch
 // so that exactly one combine CTA fits beside a decode CTA.
-template <int VPL>
-__global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 5 ? 8 : 4)) decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
+// WIDE: the instantiation for decode kernels that fill their SMs (the token-balanced
+// schedule), beside which no combine CTA runs anyway: eight tail tokens per warp and round
+// instead of two, for four times fewer round trips to memory (up to 128 registers).
+template <int VPL, bool WIDE>
+__global__ void __launch_bounds__(kCombineWarps * 32, (WIDE ? 4 : (VPL <= 5 ? 8 : 4)))
+    decode_combine_kernel(const DecodeArgs a, const DecodePlan p) {
     constexpr int D = 32 * VPL;
     __shared__ __align__(16) float s_o[kCombineWarps][D];
     __shared__ float s_m[kCombineWarps], s_l[kCombineWarps];
@@ -194,21 +231,17 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 5 ? 8 : 4)) decode
             ot[v] = 0.0f;
         }
         // TCH tokens per round with all their loads in flight (one memory latency per round)
-        constexpr int TCH = VPL <= 2 ? 4 : 2;
+        constexpr int TCH = WIDE ? (VPL >= 16 ? 4 : 8) : (VPL <= 2 ? 4 : 2);
+        constexpr int HW = (VPL + 1) / 2;  // packed fp16 pairs per row slice
         for (int n0 = warp; n0 < ntot; n0 += kCombineWarps * TCH) {
-            float kv[TCH][VPL], vv[TCH][VPL];
+            uint32_t kh[TCH][HW], vh[TCH][HW];
 #pragma unroll
             for (int j = 0; j < TCH; ++j) {
                 const int n = n0 + j * kCombineWarps;
                 if (n < ntot) {
                     const int64_t row = (n < nvis) ? (tail_row0 + n) : new_row;
-                    const uint16_t* kr = ((n < nvis) ? a.k_tail : a.k_new) + row * D + lane * VPL;
-                    const uint16_t* vr = ((n < nvis) ? a.v_tail : a.v_new) + row * D + lane * VPL;
-#pragma unroll
-                    for (int v = 0; v < VPL; ++v) {
-                        kv[j][v] = __half2float(__ushort_as_half(__ldcg(kr + v)));
-                        vv[j][v] = __half2float(__ushort_as_half(__ldcg(vr + v)));
-                    }
+                    load_halves<VPL>(((n < nvis) ? a.k_tail : a.k_new) + row * D + lane * VPL, kh[j]);
+                    load_halves<VPL>(((n < nvis) ? a.v_tail : a.v_new) + row * D + lane * VPL, vh[j]);
                 }
             }
 #pragma unroll
@@ -216,7 +249,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 5 ? 8 : 4)) decode
                 if (n0 + j * kCombineWarps < ntot) {
                     float part = 0.0f;
 #pragma unroll
-                    for (int v = 0; v < VPL; ++v) part = fmaf(qv[v], kv[j][v], part);
+                    for (int v = 0; v < VPL; ++v) part = fmaf(qv[v], half_at(kh[j], v), part);
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(kFullMask, part, off);
                     const float mn = fmaxf(mt, part);
@@ -224,7 +257,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (VPL <= 5 ? 8 : 4)) decode
                     const float pw = exp2f(part - mn);
                     lt = fmaf(lt, al, pw);
 #pragma unroll
-                    for (int v = 0; v < VPL; ++v) ot[v] = fmaf(ot[v], al, pw * vv[j][v]);
+                    for (int v = 0; v < VPL; ++v) ot[v] = fmaf(ot[v], al, pw * half_at(vh[j], v));
                     mt = mn;
                 }
             }
@@ -410,7 +443,7 @@ int combine_pad_bytes(int decode_smem, int static_bytes) {
     return (pad + 127) / 128 * 128;
 }
 
-template <int VPL>
+template <int VPL, bool WIDE>
 cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
     // The L1 / shared-memory split of an SM is set for the CTAs it holds, and a CTA whose
     // kernel prefers another split waits for an idle SM: the combine asks for the same
@@ -420,7 +453,7 @@ cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     if (!(configured.load() & bit)) {
-        const cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel<VPL>,
+        const cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel<VPL, WIDE>,
                                                    cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
@@ -436,24 +469,29 @@ cudaError_t launch_vpl(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<VPL>, a, p);
+    return cudaLaunchKernelEx(&cfg, decode_combine_kernel<VPL, WIDE>, a, p);
+}
+
+template <bool WIDE>
+cudaError_t launch_wide(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
+    switch (a.cv.dim / 32) {
+        case 1: return launch_vpl<1, WIDE>(a, p, st);
+        case 2: return launch_vpl<2, WIDE>(a, p, st);
+        case 3: return launch_vpl<3, WIDE>(a, p, st);
+        case 4: return launch_vpl<4, WIDE>(a, p, st);
+        case 5: return launch_vpl<5, WIDE>(a, p, st);
+        case 6: return launch_vpl<6, WIDE>(a, p, st);
+        case 7: return launch_vpl<7, WIDE>(a, p, st);
+        case 8: return launch_vpl<8, WIDE>(a, p, st);
+        case 16: return launch_vpl<16, WIDE>(a, p, st);
+        default: return cudaErrorNotSupported;
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_decode_combine(const DecodeArgs& a, const DecodePlan& p, cudaStream_t st) {
-    switch (a.cv.dim / 32) {
-        case 1: return launch_vpl<1>(a, p, st);
-        case 2: return launch_vpl<2>(a, p, st);
-        case 3: return launch_vpl<3>(a, p, st);
-        case 4: return launch_vpl<4>(a, p, st);
-        case 5: return launch_vpl<5>(a, p, st);
-        case 6: return launch_vpl<6>(a, p, st);
-        case 7: return launch_vpl<7>(a, p, st);
-        case 8: return launch_vpl<8>(a, p, st);
-        case 16: return launch_vpl<16>(a, p, st);
-        default: return cudaErrorNotSupported;
-    }
+    return p.stream ? launch_wide<true>(a, p, st) : launch_wide<false>(a, p, st);
 }
 
 }  // namespace tq
