@@ -871,11 +871,13 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 prefetch_l2(reinterpret_cast<const void*>(l0), static_cast<uint32_t>(l1 - l0 < 4096 ? l1 - l0 : 4096));
             } else {
                 {
-                    // While the previous kernel finishes, pull the first NSTAGE tiles of this
-                    // split (by max_seq: the lengths are not read yet) into L2.  A prefetch
-                    // changes no value any load returns, so it may precede the wait; the
-                    // copies into shared memory come after it.
-                    const int64_t pf_end = min(min(t0 + p.chunk, a.max_seq), t0 + static_cast<int64_t>(C::NSTAGE) * C::TS);
+                    // While the previous kernel finishes, pull the first tile of this split
+                    // (by max_seq: the lengths are not read yet) into L2 -- only the first:
+                    // all CTAs' first tiles then arrive within the overlap, and the next ones
+                    // stream once the copies start.  A prefetch changes no value any load
+                    // returns, so it may precede the wait; the copies into shared memory
+                    // come after it.
+                    const int64_t pf_end = min(min(t0 + p.chunk, a.max_seq), t0 + static_cast<int64_t>(C::TS));
                     if (pf_end > t0) {
                         const uint32_t ntok = static_cast<uint32_t>(pf_end - t0);  // a multiple of 8
                         if constexpr (C::KRAW) {
