@@ -223,6 +223,12 @@ struct Layout {
     // the block, the other `na` stages above it.
     bool tblock;
     int small, g, na;
+    // 2-4 bit K ("based" tables): the K and V pair tables (128-B rows) at the same fixed
+    // address kTBlock, the larger first and the other at kTBlock + its size, so that each
+    // table's base bits ride in the lane offset and an address is a mask-or (no add).
+    // Small regions and `g` stages below, `na` stages above kTBlock + tt.
+    bool based;
+    int kbase, vbase, tt;
 };
 
 // Shared address where the dynamic shared memory starts on this GPU (the
@@ -236,6 +242,7 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false, bool multi
 constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
     Layout L{};
     L.tblock = true;
+    L.based = false;
     L.nwc = nwc_for(D, KB);
     L.krows = 256;
     L.vrows = (VB <= 4) ? (1 << (2 * VB)) : 256;
@@ -264,6 +271,36 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
     }
     L.nstage = (L.na * L.stage >= L.nwc * kGP * D * 4) ? L.g + L.na : 0;
     L.smem = 2 * kTBlock + L.na * L.stage - kSmemBase;
+    return L;
+}
+
+constexpr Layout make_based_layout(const Layout& lin, int D, int KB, int VB, bool qjl, int mt) {
+    Layout L = lin;
+    L.based = true;
+    L.tblock = false;
+    // the larger table first: the other's base (the larger's size, a power of two) and
+    // its offsets (below its own, smaller, size) never share a bit
+    L.kbase = (L.ktab >= L.vtab) ? 0 : L.vtab;
+    L.vbase = (L.ktab >= L.vtab) ? L.ktab : 0;
+    L.tt = L.ktab + L.vtab;
+    L.small = kGP * D * 4 + 1024 + L.pro + L.bqb + L.ubq;
+    L.fixed = L.small;
+    L.mt = mt;
+    L.ts = L.nwc * 16 * mt;
+    L.stage = stage_bytes(D, KB, VB, L.ts, qjl);
+    const int below = kTBlock - kSmemBase - L.small;
+    const int above_max = (kSmemBase + kSmemLimit - kTBlock - L.tt) / L.stage;
+    L.g = below > 0 ? below / L.stage : 0;
+    L.na = above_max;
+    if (L.g > 4) L.g = 4;
+    if (L.g + L.na > 4) L.na = 4 - L.g;
+    // the warp merge uses the stages above the tables as one contiguous area
+    while (L.na * L.stage < L.nwc * kGP * D * 4 && L.g > 0 && L.na < above_max) {
+        --L.g;
+        ++L.na;
+    }
+    L.nstage = (L.na * L.stage >= L.nwc * kGP * D * 4) ? L.g + L.na : 0;
+    L.smem = kTBlock + L.tt + L.na * L.stage - kSmemBase;
     return L;
 }
 
@@ -306,9 +343,16 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
     L.nstage = ns > cap ? cap : ns;
     L.smem = L.fixed + L.nstage * L.stage;
     L.tblock = false;
+    L.based = false;
+    L.kbase = L.vbase = L.tt = 0;
     L.small = 0;
     L.g = 0;
     L.na = L.nstage;
+    if (KB <= 4) {
+        // the based tables when they keep as many stages of the same size
+        const Layout b = make_based_layout(L, D, KB, VB, qjl, L.mt);
+        if (b.nstage >= L.nstage) return b;
+    }
     return L;
 }
 
@@ -379,6 +423,9 @@ struct Cfg {
     static constexpr int NSTAGE = L.nstage;
     static constexpr int SMEM = L.smem;
     static constexpr bool TBLOCK = L.tblock;
+    static constexpr bool BASED = L.based;
+    static constexpr int KBASE = L.kbase, VBASE = L.vbase, TT = L.tt;
+    static constexpr int VMODE = TBLOCK ? 1 : BASED ? 2 : 0;  // V table addressing (v_role)
     // K lookups addressed by one byte permute of the code word: 8-bit codes, or pairs of
     // 4-bit codes (one byte) in the table block
     static constexpr bool KPERM = KEXP || (KB == 4 && TBLOCK);
@@ -408,23 +455,25 @@ __device__ __forceinline__ void k_role(const uint32_t (&w)[KCW], int kt, uint32_
 // ---------------------------------------------------------------------------
 // Dequant: V role (one dim of two tokens a, b)
 // ---------------------------------------------------------------------------
-// TB: table-block layout (256-B rows, lane4 already holds the table address
-// bits and the lane offset, so an address is one shift and one or).
-template <int VB, int VCW, bool TB>
+// MODE: where the V table sits.  0: anywhere (the table address is added), 1: the table
+// block (256-B rows), 2: the based tables (128-B rows); in 1 and 2 lane4 already holds
+// the table's address bits and the lane offset, so an address is one shift and one or.
+template <int VB, int VCW, int MODE>
 __device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint32_t (&wb)[VCW], int j,
                                            uint32_t tab, uint32_t lane4) {
     const int s = VB * j;
     const uint32_t m = (1u << VB) - 1u;
-    constexpr int RS = TB ? 8 : 7;
+    constexpr int RS = (MODE == 1) ? 8 : 7;
+    const uint32_t t = (MODE == 0) ? tab : 0u;
     if constexpr (VB <= 4) {
         const uint32_t ca = bits_at<VCW>(wa, s) & m;
         const uint32_t cb = bits_at<VCW>(wb, s) & m;
-        return lds32((TB ? 0u : tab) + (((ca | (cb << VB)) << RS) | lane4));
+        return lds32(t + (((ca | (cb << VB)) << RS) | lane4));
     } else {
         const uint32_t ca = bits_at<VCW>(wa, s) & m;
         const uint32_t cb = bits_at<VCW>(wb, s) & m;
-        const uint32_t va = lds32((TB ? 0u : tab) + ((ca << RS) | lane4));
-        const uint32_t vb = lds32((TB ? 0u : tab) + ((cb << RS) | lane4));
+        const uint32_t va = lds32(t + ((ca << RS) | lane4));
+        const uint32_t vb = lds32(t + ((cb << RS) | lane4));
         return __byte_perm(va, vb, 0x7610);
     }
 }
@@ -433,7 +482,7 @@ __device__ __forceinline__ uint32_t v_role(const uint32_t (&wa)[VCW], const uint
 // 64-bit values) are interleaved once into z_even / z_odd whose field i
 // (2*VB bits) is code_a | code_b << VB of dim 2i / 2i+1; each pair is then one
 // shift and one mask.
-template <int VB, bool TB>
+template <int VB, int MODE>
 struct VPairs {
     static constexpr uint64_t even_mask() {
         uint64_t m = 0;
@@ -447,14 +496,14 @@ struct VPairs {
         zo = ((a >> VB) & me) | (b & ~me);
     }
     // shared-memory address of the pair-table slot for dim j (0..15) of the chunk
-    // (TB: 256-B rows and lane4 carrying the table address, so no add)
+    // (MODE 1 / 2: lane4 carrying the table address, so no add; v_role's modes)
     __device__ __forceinline__ uint32_t addr(int j, uint32_t tab, uint32_t lane4) const {
-        constexpr int RS = TB ? 8 : 7;
+        constexpr int RS = (MODE == 1) ? 8 : 7;
         const uint64_t z = (j & 1) ? zo : ze;
         const int s = VB * (j & ~1);
         const uint32_t x = (s >= RS) ? static_cast<uint32_t>(z >> (s - RS)) : static_cast<uint32_t>(z << (RS - s));
         const uint32_t f = (x & (((1u << (2 * VB)) - 1u) << RS)) | lane4;
-        return TB ? f : tab + f;
+        return (MODE != 0) ? f : tab + f;
     }
 };
 
@@ -724,9 +773,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     extern __shared__ __align__(1024) uint8_t smem[];
     const uint32_t sbase = smem_addr(smem);
     // table block (8-bit K): the tables at shared address kTBlock, the rest around them
-    uint8_t* ktab_s = C::TBLOCK ? smem + (static_cast<uint32_t>(kTBlock) - sbase) : smem;
-    uint8_t* vtab_s = C::TBLOCK ? ktab_s + 128 : ktab_s + C::KTAB;
-    float* qs = reinterpret_cast<float*>(C::TBLOCK ? smem : vtab_s + C::VTAB);  // [kGP][D]
+    // (based tables: at kTBlock + KBASE / VBASE)
+    uint8_t* ktab_s = C::TBLOCK  ? smem + (static_cast<uint32_t>(kTBlock) - sbase)
+                      : C::BASED ? smem + (static_cast<uint32_t>(kTBlock + C::KBASE) - sbase)
+                                 : smem;
+    uint8_t* vtab_s = C::TBLOCK  ? ktab_s + 128
+                      : C::BASED ? smem + (static_cast<uint32_t>(kTBlock + C::VBASE) - sbase)
+                                 : ktab_s + C::KTAB;
+    float* qs = reinterpret_cast<float*>((C::TBLOCK || C::BASED) ? smem : vtab_s + C::VTAB);  // [kGP][D]
     uint8_t* misc = reinterpret_cast<uint8_t*>(qs) + C::QBYTES;
     uint64_t* full = reinterpret_cast<uint64_t*>(misc);                  // [NSTAGE <= 8]
     uint64_t* empty = full + 8;                                          // [NSTAGE <= 8]
@@ -743,14 +797,16 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     if constexpr (C::KRAW)  // the swizzled K blocks need 1024-byte aligned shared addresses
         below += (1024u - (smem_addr(below) & 1023u)) & 1023u;
     // stages G_BELOW .. NSTAGE-1, contiguous (also the warp-merge area)
-    uint8_t* ring = C::TBLOCK ? smem + (static_cast<uint32_t>(2 * kTBlock) - sbase) : below;
+    constexpr uint32_t kAbove = C::TBLOCK ? 2u * kTBlock : static_cast<uint32_t>(kTBlock + C::TT);
+    uint8_t* ring = (C::TBLOCK || C::BASED) ? smem + (kAbove - sbase) : below;
     auto stage_ptr = [&](int s) -> uint8_t* {
-        return (C::TBLOCK && s < C::G_BELOW) ? below + s * C::STAGE : ring + (s - C::G_BELOW) * C::STAGE;
+        return ((C::TBLOCK || C::BASED) && s < C::G_BELOW) ? below + s * C::STAGE
+                                                             : ring + (s - C::G_BELOW) * C::STAGE;
     };
-    if constexpr (C::TBLOCK) {
+    if constexpr (C::TBLOCK || C::BASED) {
         // the layout was sized for the dynamic shared memory starting at kSmemBase
         if (sbase + C::SMALL + C::G_BELOW * C::STAGE > static_cast<uint32_t>(kTBlock) ||
-            static_cast<uint32_t>(2 * kTBlock + C::N_ABOVE * C::STAGE) > sbase + C::SMEM) {
+            kAbove + C::N_ABOVE * C::STAGE > sbase + C::SMEM) {
             if (threadIdx.x == 0) atomicOr(error_ptr(a.ws), TQ_DEVERR_LAYOUT);
             return;
         }
@@ -1153,8 +1209,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
             // table block: the table address bits ride in the lane offsets (kTBlock is
             // 64 KB aligned, the V half of a row starts at +128)
-            const uint32_t koff = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) : 0u);
-            const uint32_t lane4 = uint32_t(lane * 4) | (C::TBLOCK ? uint32_t(kTBlock) + 128u : 0u);
+            const uint32_t koff = uint32_t(lane * 4) | (C::TBLOCK  ? uint32_t(kTBlock)
+                                                        : C::BASED ? uint32_t(kTBlock + C::KBASE)
+                                                                   : 0u);
+            const uint32_t lane4 = uint32_t(lane * 4) | (C::TBLOCK  ? uint32_t(kTBlock) + 128u
+                                                         : C::BASED ? uint32_t(kTBlock + C::VBASE)
+                                                                    : 0u);
 
             // ------------------------------------------------------------ main loop
             // (after a wait gave up, the token-balanced schedule's later segments skip their tiles)
@@ -1237,8 +1297,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
 #pragma unroll
                             for (int kt = 0; kt < C::KTS; ++kt) {
                                 uint32_t ah01, ah23, bh01, bh23;
-                                k_role<KB, C::KCW>(wa, kt, ktab_a, koff, ah01, ah23);
-                                k_role<KB, C::KCW>(wb, kt, ktab_a, koff, bh01, bh23);
+                                // (based tables: the table's address bits are in koff)
+                                k_role<KB, C::KCW>(wa, kt, C::BASED ? 0u : ktab_a, koff, ah01, ah23);
+                                k_role<KB, C::KCW>(wb, kt, C::BASED ? 0u : ktab_a, koff, bh01, bh23);
                                 // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
                                 uint32_t q00, q01, q10 = 0u, q11 = 0u;
                                 q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
@@ -1399,9 +1460,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                             for (int sub = 0; sub < NSUB; ++sub) {
                                 const int vbit = g * C::VCB + 16 * VB * sub;
                                 constexpr int VW = v_field_words(D, VB);  // words per field (2 at D 128, 3 bits)
-                                const VPairs<VB, C::TBLOCK> p01(load_bits_w<VW>(vbuf + (rbase + 2 * t) * C::BPV, vbit),
+                                const VPairs<VB, C::VMODE> p01(load_bits_w<VW>(vbuf + (rbase + 2 * t) * C::BPV, vbit),
                                                      load_bits_w<VW>(vbuf + (rbase + 2 * t + 1) * C::BPV, vbit));
-                                const VPairs<VB, C::TBLOCK> p89(load_bits_w<VW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
+                                const VPairs<VB, C::VMODE> p89(load_bits_w<VW>(vbuf + (rbase + 2 * t + 8) * C::BPV, vbit),
                                                      load_bits_w<VW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vbit));
                                 constexpr int DM_PER_SUB = 8;  // 16 dims = 8 m-tiles of two rows
 #pragma unroll
@@ -1426,10 +1487,10 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                             load_chunk<C::VCW>(vbuf + (rbase + 2 * t + 9) * C::BPV, vb, v3);
 #pragma unroll
                             for (int dm = 0; dm < C::KT; ++dm) {
-                                const uint32_t a0 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm, vtab_a, lane4);
-                                const uint32_t a1 = v_role<VB, C::VCW, C::TBLOCK>(v0, v1, 2 * dm + 1, vtab_a, lane4);
-                                const uint32_t a2 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm, vtab_a, lane4);
-                                const uint32_t a3 = v_role<VB, C::VCW, C::TBLOCK>(v2, v3, 2 * dm + 1, vtab_a, lane4);
+                                const uint32_t a0 = v_role<VB, C::VCW, C::VMODE>(v0, v1, 2 * dm, vtab_a, lane4);
+                                const uint32_t a1 = v_role<VB, C::VCW, C::VMODE>(v0, v1, 2 * dm + 1, vtab_a, lane4);
+                                const uint32_t a2 = v_role<VB, C::VCW, C::VMODE>(v2, v3, 2 * dm, vtab_a, lane4);
+                                const uint32_t a3 = v_role<VB, C::VCW, C::VMODE>(v2, v3, 2 * dm + 1, vtab_a, lane4);
                                 mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
                                 if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
                             }
