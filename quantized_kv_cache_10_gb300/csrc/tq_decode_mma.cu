@@ -198,6 +198,14 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
     // the QJL sketch (one row group, one query position, 16-byte aligned sketch fields)
     const bool multi = p.L > 1 || p.q_chunks > 1;
     int nt = (p.S > 4 ? 2 : 1) + (multi ? 2 : 0);
+    // several query positions with 8-bit keys at d <= 128 and an even number of row groups:
+    // two groups per CTA, one dequantised tile feeding both groups' contractions
+    int rg = 1;
+    if (multi && a.ck.bits == 8 && a.cv.dim <= 128 && (a.cv.dim & (a.cv.dim - 1)) == 0 && p.q_chunks % 2 == 0 &&
+        !a.k_signs) {
+        nt = 7;
+        rg = 2;
+    }
     if (a.k_signs) {
         const auto al16 = [](const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; };
         if (multi || !al16(a.k_signs) || !al16(a.k_rnorms)) return cudaErrorNotSupported;  // SIMT
@@ -208,7 +216,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
     int dev = 0;
     cudaGetDevice(&dev);
     const int64_t sms = num_sms(dev);
-    const int64_t ctas = int64_t(p.n_units) * p.q_chunks;  // CTAs per split
+    const int64_t ctas = int64_t(p.n_units) * (p.q_chunks / rg);  // CTAs per split
     int64_t ns = (sms + ctas - 1) / ctas;
     // several row groups per unit (each re-reads the unit's tiles, mostly from L2):
     // keep the grid to one wave

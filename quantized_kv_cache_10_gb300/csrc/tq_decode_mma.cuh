@@ -237,9 +237,9 @@ struct Layout {
 constexpr int kSmemBase = 1024;
 constexpr int kTBlock = 65536;
 
-constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false, bool multi = false);
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl = false, bool multi = false, int rg = 1);
 
-constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
+constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi, int rg = 1) {
     Layout L{};
     L.tblock = true;
     L.based = false;
@@ -253,8 +253,8 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
     L.pro = al128(L.kw * 4) + al128(L.vw * 4) + al128(kGP * D * 2) + 128;
     // q' B fragments in shared memory: D > 128, or several query positions (q_hi and q_lo
     // n-tiles, which registers would not hold beside the rest)
-    L.bqb = (D > 128 || multi) ? (D / 8) * 2 * 256 : 0;
-    L.small = kGP * D * 4 + 1024 + L.pro + L.bqb;
+    L.bqb = (D > 128 || multi) ? (D / 8) * 2 * 256 * rg : 0;
+    L.small = kGP * D * 4 * rg + 1024 + L.pro + L.bqb;
     L.fixed = L.small;
     L.mt = mt;
     L.ts = L.nwc * 16 * mt;
@@ -274,7 +274,7 @@ constexpr Layout make_tblock_layout(int D, int KB, int VB, int mt, bool multi) {
     return L;
 }
 
-constexpr Layout make_based_layout(const Layout& lin, int D, int KB, int VB, bool qjl, int mt) {
+constexpr Layout make_based_layout(const Layout& lin, int D, int KB, int VB, bool qjl, int mt, int rg) {
     Layout L = lin;
     L.based = true;
     L.tblock = false;
@@ -283,7 +283,7 @@ constexpr Layout make_based_layout(const Layout& lin, int D, int KB, int VB, boo
     L.kbase = (L.ktab >= L.vtab) ? 0 : L.vtab;
     L.vbase = (L.ktab >= L.vtab) ? L.ktab : 0;
     L.tt = L.ktab + L.vtab;
-    L.small = kGP * D * 4 + 1024 + L.pro + L.bqb + L.ubq;
+    L.small = kGP * D * 4 * rg + 1024 + L.pro + L.bqb + L.ubq;
     L.fixed = L.small;
     L.mt = mt;
     L.ts = L.nwc * 16 * mt;
@@ -304,11 +304,11 @@ constexpr Layout make_based_layout(const Layout& lin, int D, int KB, int VB, boo
     return L;
 }
 
-constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
+constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi, int rg) {
     if (KB == 8 || (KB == 4 && !qjl && !multi)) {
         // the table block, when it holds at least as many stages as the linear layout would
         // (4-bit keys: a pair of codes is one byte, so the same byte permute forms the address)
-        const Layout t2 = make_tblock_layout(D, KB, VB, 2, multi), t1 = make_tblock_layout(D, KB, VB, 1, multi);
+        const Layout t2 = make_tblock_layout(D, KB, VB, 2, multi, rg), t1 = make_tblock_layout(D, KB, VB, 1, multi, rg);
         const Layout t = (D <= 128 && t2.nstage >= 3) ? t2 : t1;
         if (t.nstage >= 3) return t;
     }
@@ -328,11 +328,11 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
     // per (k-tile, n-tile)) instead of registers
     // (also with the QJL sketch, whose own fragments and per-row values need the registers)
     // (and for 8-bit K with several query positions: q_hi and q_lo n-tiles)
-    L.bqb = (D > 128 || qjl || (multi && KB == 8)) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 : 0;
+    L.bqb = (D > 128 || qjl || (multi && KB == 8)) ? ((KB == 8) ? D / 8 : D / 16) * 2 * 256 * rg : 0;
     // keys with the QJL sketch: the B fragments of u = S q' (D / 16 k-tiles, up to two n-tiles)
     L.ubq = qjl ? (D / 16) * 2 * 256 : 0;
     // (+1024 for raw K: the ring is aligned to 1024 B at run time)
-    L.fixed = L.ktab + L.vtab + kGP * D * 4 + 1024 + L.pro + L.bqb + L.ubq + (KB == 16 ? 1024 : 0);
+    L.fixed = L.ktab + L.vtab + kGP * D * 4 * rg + 1024 + L.pro + L.bqb + L.ubq + (KB == 16 ? 1024 : 0);
     // two m-tiles per warp per stage when three such stages fit (so two are in
     // flight while one is consumed), else one
     L.mt = (KB != 16 && D <= 128 && L.fixed + 3 * stage_bytes(D, KB, VB, L.nwc * 32, qjl) <= kSmemLimit) ? 2 : 1;
@@ -350,7 +350,7 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
     L.na = L.nstage;
     if (KB <= 4) {
         // the based tables when they keep as many stages of the same size
-        const Layout b = make_based_layout(L, D, KB, VB, qjl, L.mt);
+        const Layout b = make_based_layout(L, D, KB, VB, qjl, L.mt, rg);
         if (b.nstage >= L.nstage) return b;
     }
     return L;
@@ -360,10 +360,16 @@ constexpr Layout make_layout(int D, int KB, int VB, bool qjl, bool multi) {
 constexpr bool mma_fits(int D, int KB, int VB, bool qjl = false, bool multi = false) {
     return (KB != 16 || D % 64 == 0) && (!qjl || KB <= 4) && make_layout(D, KB, VB, qjl, multi).nstage >= 2;
 }
+// ... and the instantiation with two row groups per CTA (several query positions, 8-bit K)
+constexpr bool mma_fits_rg2(int D, int KB, int VB) {
+    return KB == 8 && D <= 128 && make_layout(D, KB, VB, false, true, 2).nstage >= 3;
+}
 
-template <int D, int KB, int VB, int NT, bool QJL = false, bool MULTI = false>
+// RG: groups of kGP query rows a CTA serves at once (2: one dequantised tile feeds both
+// groups' contractions; the instantiation with several query positions and 8-bit keys)
+template <int D, int KB, int VB, int NT, bool QJL = false, bool MULTI = false, int RG = 1>
 struct Cfg {
-    static constexpr Layout L = make_layout(D, KB, VB, QJL, MULTI);
+    static constexpr Layout L = make_layout(D, KB, VB, QJL, MULTI, RG);
     static constexpr int NWC = L.nwc;               // consumer warps
     static constexpr int NTHREADS = (NWC + 1) * 32;
     // register budget per thread: 8-bit K at d <= 128 measured fastest at 144 (17.3 vs 18.3 us
@@ -411,7 +417,8 @@ struct Cfg {
     static constexpr int RBUF = QJL ? al128(TS * 2) : 0;
     static constexpr int UBQ = L.ubq;
     static constexpr int STAGE = L.stage;
-    static constexpr int QBYTES = kGP * D * 4;      // q' fp32, later the merged O
+    static constexpr int QBYTES = kGP * D * 4 * RG;  // q' fp32 of every row group
+    static constexpr int RGS = RG;                   // row groups (q' fragment stride)
     static constexpr int KW = L.kw, VW = L.vw;
     static constexpr int PRO = L.pro;
     static constexpr int PRO_K = 0;                              // offsets inside the prologue area
@@ -617,23 +624,23 @@ __device__ __forceinline__ void replicate_tables(const uint32_t* kcompact, const
 
 // q' = R q * log2(e) * scale / sqrt(D) for the G query heads of the unit into
 // qs[kGP][D] (rows >= G zero), with every global load in flight at once.
-template <int D, int NWC, bool RAW>
+template <int D, int NWC, bool RAW, int ROWS = kGP>
 __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16_t* qg, const uint16_t* qglob,
                                                const uint32_t* signs, int G, float* qs, int warp, int lane, int ctid) {
     constexpr int NTH = NWC * 32;
     if constexpr (RAW) {
         // raw fp16 K is scored in the original basis: q' = q * log2(e) * scale
         const float f = kLog2e * a.scale;
-        for (int i = ctid; i < kGP * D; i += NTH)
+        for (int i = ctid; i < ROWS * D; i += NTH)
             qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) * f : 0.0f;
     } else if constexpr ((D & (D - 1)) == 0) {
         // Power-of-two dims always carry the Walsh-Hadamard rotation, the others the dense
-        // one.  Warp w < G rotates query row w in registers, straight from global memory
+        // one.  Warp w rotates query rows w, w + NWC, ... < G in registers, straight from global memory
         // (lane l holds dims [VPL l, VPL (l + 1))): H (s . q) by butterflies of stride < VPL
         // inside the lane and the rest across lanes, natural (Sylvester) order.
         constexpr int VPL = D / 32;
-        if (warp < G) {
-            const uint16_t* src = qglob + warp * D + lane * VPL;
+        for (int row = warp; row < G; row += NWC) {
+            const uint16_t* src = qglob + row * D + lane * VPL;
             float x[VPL];
             if constexpr (VPL == 8) {
                 const uint4 u = *reinterpret_cast<const uint4*>(src);
@@ -674,11 +681,11 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
                 }
             }
             const float f = kLog2e * a.scale / (static_cast<float>(D) * a.ck.k_alpha);
-            float* dst = qs + warp * D + lane * VPL;
+            float* dst = qs + row * D + lane * VPL;
 #pragma unroll
             for (int v = 0; v < VPL; ++v) dst[v] = x[v] * f;
         }
-        for (int i = G * D + ctid; i < kGP * D; i += NTH) qs[i] = 0.0f;
+        for (int i = G * D + ctid; i < ROWS * D; i += NTH) qs[i] = 0.0f;
     } else {
         // dense: stage q in qs, then each thread forms whole columns j of Q q
         for (int i = ctid; i < kGP * D; i += NTH)
@@ -718,10 +725,12 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
 // registers, or from the shared-memory copy when C::BQ_SMEM.
 template <typename C, typename BQ>
 __device__ __forceinline__ void q_frag(const BQ& Bq, uint32_t bq_a, int kt, int lane, uint32_t& q00, uint32_t& q01,
-                                       uint32_t& q10, uint32_t& q11) {
+                                       uint32_t& q10, uint32_t& q11, int rg = 0) {
     if constexpr (C::BQ_SMEM) {
-        lds64(bq_a + ((kt * C::NTS) * 32 + lane) * 8, q00, q01);
-        if constexpr (C::NTS == 2) lds64(bq_a + ((kt * C::NTS + 1) * 32 + lane) * 8, q10, q11);
+        // (row group rg's fragments follow group 0's within each k-tile)
+        const int f0 = (kt * C::RGS + rg) * C::NTS;
+        lds64(bq_a + (f0 * 32 + lane) * 8, q00, q01);
+        if constexpr (C::NTS == 2) lds64(bq_a + ((f0 + 1) * 32 + lane) * 8, q10, q11);
     } else {
         q00 = Bq[kt][0][0];
         q01 = Bq[kt][0][1];
@@ -758,10 +767,14 @@ constexpr int stream_merge_bytes() {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, int KB, int VB, int NT, bool MULTI, bool QJL, bool STREAM>
-__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL, bool STREAM, int RG>
+__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
-    using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
+    using C = Cfg<D, KB, VB, NT, QJL, MULTI, RG>;
+    // two row groups per CTA: several query positions, 8-bit keys (their byte-permute
+    // lookups and q' fragments in shared memory), one schedule per unit
+    static_assert(RG == 1 || (RG == 2 && MULTI && C::KEXP && C::BQ_SMEM && !STREAM && !QJL &&
+                              (D & (D - 1)) == 0), "row groups");
     // q is staged in shared memory by the producer for raw K and the dense rotation; with
     // the Walsh-Hadamard rotation each consumer warp reads its query row itself
     constexpr bool Q_STAGED = C::KRAW || (D & (D - 1)) != 0;
@@ -787,9 +800,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     uint64_t* setup = full + 16;                                         // codec tables, sign words
     uint64_t* setup_q = full + 17;                                       // the query block
     int* s_erel = reinterpret_cast<int*>(misc + 160);                    // [kGP] causal ends
+    int* s_erel1 = reinterpret_cast<int*>(misc + 976);                   // [kGP] the second row group's
     float* wm = reinterpret_cast<float*>(misc + 256);                    // [C::NWC][kGP]
     float* wl = wm + C::NWC * kGP;                                         // [C::NWC][kGP]
     int* s_abort = reinterpret_cast<int*>(wl + C::NWC * kGP);
+    static_assert(256 + 2 * C::NWC * kGP * 4 + 4 <= 976, "misc area: the second group's causal ends");
     uint8_t* pro = misc + C::MISC;                                       // prologue landing area
     uint8_t* bq_s = pro + C::PRO;                                    // q' fragments (D > 128)
     uint8_t* ubq_s = bq_s + C::BQB;                                      // u = S q' fragments (QJL)
@@ -827,12 +842,15 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
     // (the MULTI instantiation serves several query positions or more than kGP rows per
     // unit; the other one is the decode case: one CTA per unit along y, rows = heads)
     // (the token-balanced schedule sets u, b, kvh, qrow0, row0 and t0 per segment)
+    // (with RG row groups a CTA serves chunks c0 .. c0 + RG - 1 of its unit: records vu + rg)
     const int split = blockIdx.x;
-    int vu = blockIdx.y;
-    int u = MULTI ? vu / p.q_chunks : vu;
+    int u = MULTI ? static_cast<int>(blockIdx.y) / (p.q_chunks / RG) : static_cast<int>(blockIdx.y);
+    int vu = MULTI ? u * p.q_chunks + (static_cast<int>(blockIdx.y) - u * (p.q_chunks / RG)) * RG
+                   : static_cast<int>(blockIdx.y);
     const int s0 = MULTI ? (vu - u * p.q_chunks) * kGP : 0;
     int b = u / a.Hkv, kvh = u - (u / a.Hkv) * a.Hkv;
-    const int G = MULTI ? min(kGP, p.S - s0) : p.G;  // query rows of this CTA
+    const int G = MULTI ? min(kGP, p.S - s0) : p.G;  // query rows of this CTA (its first group)
+    const int G1 = (RG == 2) ? min(kGP, p.S - s0 - kGP) : 0;  // the second group's rows
     int64_t qrow0 = MULTI ? (static_cast<int64_t>(b) * a.Hq + static_cast<int64_t>(kvh) * p.G) * p.L + s0
                           : static_cast<int64_t>(b) * a.Hq + kvh * G;
     int64_t row0 = static_cast<int64_t>(u) * a.max_seq;
@@ -910,7 +928,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
         };
         if (lane == 0) {
             // prologue data first: compact tables, this unit's query block, sign words
-            const uint32_t qbytes = static_cast<uint32_t>(G * D * 2);
+            const uint32_t qbytes = static_cast<uint32_t>((G + G1) * D * 2);
             // sign words: K codec's at PRO_S, V codec's at PRO_S + 64 (<= 64 B each, D <= 512)
             const uint32_t sbytes = (a.ck.is_wht && !C::KRAW) ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
             const uint32_t vsbytes = a.cv.is_wht ? 16u * ((D / 32 * 4 + 15) / 16) : 0u;
@@ -1080,17 +1098,18 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                     atomicOr(error_ptr(a.ws), TQ_DEVERR_TIMEOUT);
                     *s_abort = 1;
                 }
-                rotate_queries<D, C::NWC, C::KRAW>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q), a.q + qrow0 * D,
-                                                   reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G, qs, warp,
-                                                   lane, ctid);
-                if (MULTI && ctid < kGP) {
+                rotate_queries<D, C::NWC, C::KRAW, kGP * RG>(a, reinterpret_cast<const uint16_t*>(pro + C::PRO_Q),
+                                                             a.q + qrow0 * D,
+                                                             reinterpret_cast<const uint32_t*>(pro + C::PRO_S), G + G1,
+                                                             qs, warp, lane, ctid);
+                if (MULTI && ctid < kGP * RG) {
                     // Causal end of each query row, as tokens past t0: the rows' positions are the
                     // last L of the sequence (packed tokens, then tail), so every packed token is
                     // visible when L == 1 or the tail is long enough.  Clamped to t1, it also marks
-                    // the split's end.
+                    // the split's end.  (The second row group's ends sit at s_erel1.)
                     const int tail = p.L > 1 ? tail_count(a, b) : 0;
                     const int64_t e = min(packed_visible(len, tail, p.L, (s0 + ctid) % p.L), t1);
-                    s_erel[ctid] = e > t0 ? static_cast<int>(e - t0) : 0;
+                    (ctid < kGP ? s_erel : s_erel1)[ctid % kGP] = e > t0 ? static_cast<int>(e - t0) : 0;
                 }
             }
             asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
@@ -1101,10 +1120,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             uint32_t Bq[C::BQ_SMEM ? 1 : C::KTS][C::NTS][2];
             const uint32_t bq_a = smem_addr(bq_s);
 #pragma unroll
+            for (int rg = 0; rg < RG; ++rg) {
+#pragma unroll
             for (int kt = 0; kt < C::KTS; ++kt) {
 #pragma unroll
                 for (int nt = 0; nt < C::NTS; ++nt) {
-                    const int qh = (NT == 2) ? g : (g >> 1);
+                    const int qh = rg * kGP + ((NT == 2) ? g : (g >> 1));
                     const bool lo_part = (NT == 2) ? (nt == 1) : ((g & 1) != 0);
                     uint32_t b0, b1;
                     if constexpr (C::KEXP) {
@@ -1139,12 +1160,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                         b1 = pack_f16(v[2], v[3]);
                     }
                     if constexpr (C::BQ_SMEM) {
-                        if (warp == 0) sts64(bq_a + ((kt * C::NTS + nt) * 32 + lane) * 8, b0, b1);
+                        // (row group rg's fragments after group 0's in each k-tile; warp rg writes them)
+                        if (warp == rg) sts64(bq_a + (((kt * RG + rg) * C::NTS + nt) * 32 + lane) * 8, b0, b1);
                     } else {
                         Bq[kt][nt][0] = b0;
                         Bq[kt][nt][1] = b1;
                     }
                 }
+            }
             }
             if constexpr (QJL) {
                 // u = S q' for this CTA's query rows, as B fragments of the sketch k-tiles ("How I
@@ -1197,14 +1220,17 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
             }
             if constexpr (C::BQ_SMEM || QJL) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
-            float O[C::KT][4];
+            float O[RG][C::KT][4];  // per row group
+            float m_run[RG][NT], l_run[RG][NT];
 #pragma unroll
-            for (int i = 0; i < C::KT; ++i) O[i][0] = O[i][1] = O[i][2] = O[i][3] = 0.0f;
-            float m_run[NT], l_run[NT];
+            for (int rg = 0; rg < RG; ++rg) {
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                m_run[j] = -CUDART_INF_F;
-                l_run[j] = 0.0f;
+                for (int i = 0; i < C::KT; ++i) O[rg][i][0] = O[rg][i][1] = O[rg][i][2] = O[rg][i][3] = 0.0f;
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    m_run[rg][j] = -CUDART_INF_F;
+                    l_run[rg][j] = 0.0f;
+                }
             }
             const uint32_t ktab_a = smem_addr(ktab_s), vtab_a = smem_addr(vtab_s);
             // table block: the table address bits ride in the lane offsets (kTBlock is
@@ -1244,11 +1270,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 const int r0 = warp * 16 * C::MT;
                 if (r0 < nvalid) {
                     // ---- scores for MT m-tiles ----
-                    float sc[C::MT][C::NTS][4];
+                    float sc[RG][C::MT][C::NTS][4];
 #pragma unroll
                     for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
-                        for (int nt = 0; nt < C::NTS; ++nt) sc[mt][nt][0] = sc[mt][nt][1] = sc[mt][nt][2] = sc[mt][nt][3] = 0.0f;
+                        for (int rg = 0; rg < RG; ++rg)
+#pragma unroll
+                            for (int nt = 0; nt < C::NTS; ++nt)
+                                sc[rg][mt][nt][0] = sc[rg][mt][nt][1] = sc[rg][mt][nt][2] = sc[rg][mt][nt][3] = 0.0f;
                         const int ra = r0 + 16 * mt + g, rb = ra + 8;
                         if constexpr (C::KRAW) {
                             // rows r0 + 16 mt + 0..15 of the swizzled 64-column blocks: lanes 0-7 /
@@ -1266,8 +1295,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                             a2, a3);
                                 uint32_t q00, q01, q10 = 0u, q11 = 0u;
                                 q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                                mma16816(sc[mt][0], a0, a1, a2, a3, q00, q01);
-                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], a0, a1, a2, a3, q10, q11);
+                                mma16816(sc[0][mt][0], a0, a1, a2, a3, q00, q01);
+                                if constexpr (C::NTS == 2) mma16816(sc[0][mt][1], a0, a1, a2, a3, q10, q11);
                             }
                         } else {
                         uint32_t wa[C::KCW], wb[C::KCW];
@@ -1288,10 +1317,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                 const uint32_t r1v = lds32(kb + __byte_perm(wB, koff, sel0));
                                 const uint32_t r2v = lds32(kb + __byte_perm(wA, koff, sel1));
                                 const uint32_t r3v = lds32(kb + __byte_perm(wB, koff, sel1));
-                                uint32_t q00, q01, q10 = 0u, q11 = 0u;
-                                q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                                mma16816(sc[mt][0], r0v, r1v, r2v, r3v, q00, q01);
-                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], r0v, r1v, r2v, r3v, q10, q11);
+                                // (every row group's contraction takes the same dequantised operand)
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg) {
+                                    uint32_t q00, q01, q10 = 0u, q11 = 0u;
+                                    q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11, rg);
+                                    mma16816(sc[rg][mt][0], r0v, r1v, r2v, r3v, q00, q01);
+                                    if constexpr (C::NTS == 2) mma16816(sc[rg][mt][1], r0v, r1v, r2v, r3v, q10, q11);
+                                }
                             }
                         } else {
 #pragma unroll
@@ -1303,8 +1336,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                 // A regs: {row g: k 2t,2t+1}, {row g+8: k 2t,2t+1}, {row g: k 2t+8,2t+9}, {row g+8: ...}
                                 uint32_t q00, q01, q10 = 0u, q11 = 0u;
                                 q_frag<C>(Bq, bq_a, kt, lane, q00, q01, q10, q11);
-                                mma16816(sc[mt][0], ah01, bh01, ah23, bh23, q00, q01);
-                                if constexpr (C::NTS == 2) mma16816(sc[mt][1], ah01, bh01, ah23, bh23, q10, q11);
+                                mma16816(sc[0][mt][0], ah01, bh01, ah23, bh23, q00, q01);
+                                if constexpr (C::NTS == 2) mma16816(sc[0][mt][1], ah01, bh01, ah23, bh23, q10, q11);
                             }
                             if constexpr (QJL) {
                                 // QJL correction into the same accumulators: row r's A entries are
@@ -1334,11 +1367,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                         const uint32_t a3 = hvb ^ (((nb & 4u) << 13) | ((nb & 8u) << 28));
                                         uint32_t u00, u01;
                                         lds64(ubq_a + ((kk * C::NTS) * 32 + lane) * 8, u00, u01);
-                                        mma16816(sc[mt][0], a0, a1, a2, a3, u00, u01);
+                                        mma16816(sc[0][mt][0], a0, a1, a2, a3, u00, u01);
                                         if constexpr (C::NTS == 2) {
                                             uint32_t u10, u11;
                                             lds64(ubq_a + ((kk * C::NTS + 1) * 32 + lane) * 8, u10, u11);
-                                            mma16816(sc[mt][1], a0, a1, a2, a3, u10, u11);
+                                            mma16816(sc[0][mt][1], a0, a1, a2, a3, u10, u11);
                                         }
                                     }
                                 }
@@ -1347,7 +1380,12 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                         }
                     }
                     // ---- scale by K norms, mask (tile end, causal limit), tile max ----
-                    float sv[C::MT][2][NT];  // [m-tile][row g / g+8][query slot]
+                    // (per row group: each has its own rows, causal ends and running state)
+                    float sv[RG][C::MT][2][NT];  // [group][m-tile][row g / g+8][query slot]
+                    float muse[RG][NT];
+#pragma unroll
+                    for (int rg = 0; rg < RG; ++rg) {
+                    const int* erel = (rg == 0) ? s_erel : s_erel1;
                     float tmax[NT];
 #pragma unroll
                     for (int j = 0; j < NT; ++j) tmax[j] = -CUDART_INF_F;
@@ -1355,7 +1393,7 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                     // (decode: the tile's end)
                     int lim[NT];
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) lim[j] = MULTI ? s_erel[(NT == 2) ? 2 * t + j : t] - it * C::TS : nvalid;
+                    for (int j = 0; j < NT; ++j) lim[j] = MULTI ? erel[(NT == 2) ? 2 * t + j : t] - it * C::TS : nvalid;
 #pragma unroll
                     for (int mt = 0; mt < C::MT; ++mt) {
 #pragma unroll
@@ -1366,14 +1404,14 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                             for (int j = 0; j < NT; ++j) {
                                 float x;
                                 if constexpr (C::NTS == 2)
-                                    x = sc[mt][0][2 * hr + j] + sc[mt][1][2 * hr + j];
+                                    x = sc[rg][mt][0][2 * hr + j] + sc[rg][mt][1][2 * hr + j];
                                 else if constexpr (NT == 2)
-                                    x = sc[mt][0][2 * hr + j];
+                                    x = sc[rg][mt][0][2 * hr + j];
                                 else
-                                    x = sc[mt][0][2 * hr] + sc[mt][0][2 * hr + 1];
+                                    x = sc[rg][mt][0][2 * hr] + sc[rg][mt][0][2 * hr + 1];
                                 // lim <= t1 - ts, so this also masks the rows past the tile's end
                                 x = (r < lim[j]) ? x * nk : -CUDART_INF_F;
-                                sv[mt][hr][j] = x;
+                                sv[rg][mt][hr][j] = x;
                                 tmax[j] = fmaxf(tmax[j], x);
                             }
                         }
@@ -1384,33 +1422,37 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                         tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 8));
                         tmax[j] = fmaxf(tmax[j], __shfl_xor_sync(kFullMask, tmax[j], 16));
                     }
-                    float alpha[NT], muse[NT];
+                    float alpha[NT];
                     bool rescale = false;
 #pragma unroll
                     for (int j = 0; j < NT; ++j) {
-                        const float mn = fmaxf(m_run[j], tmax[j]);
-                        muse[j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
-                        alpha[j] = exp2f(m_run[j] - muse[j]);
+                        const float mn = fmaxf(m_run[rg][j], tmax[j]);
+                        muse[rg][j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
+                        alpha[j] = exp2f(m_run[rg][j] - muse[rg][j]);
                         rescale |= (alpha[j] != 1.0f);
-                        m_run[j] = mn;
-                        l_run[j] *= alpha[j];
+                        m_run[rg][j] = mn;
+                        l_run[rg][j] *= alpha[j];
                     }
                     if (__any_sync(kFullMask, rescale)) {
                         // (MULTI, NT == 1: columns 2t and 2t + 1 both hold row t, hi and lo of P)
                         const float a1 = (NT == 2 || MULTI) ? alpha[NT - 1] : 1.0f;
 #pragma unroll
                         for (int i = 0; i < C::KT; ++i) {
-                            O[i][0] *= alpha[0];
-                            O[i][1] *= a1;
-                            O[i][2] *= alpha[0];
-                            O[i][3] *= a1;
+                            O[rg][i][0] *= alpha[0];
+                            O[rg][i][1] *= a1;
+                            O[rg][i][2] *= alpha[0];
+                            O[rg][i][3] *= a1;
                         }
+                    }
                     }
                     // ---- probabilities, P' = p * n16_V, P.V ----
 #pragma unroll
                     for (int mt = 0; mt < C::MT; ++mt) {
                         const int rbase = r0 + 16 * mt;
                         if (rbase >= nvalid) break;
+                        uint32_t pb0[RG], pb1[RG], pl0[RG], pl1[RG];  // P fragments per row group
+#pragma unroll
+                        for (int rg = 0; rg < RG; ++rg) {
                         float pv[2][NT];
 #pragma unroll
                         for (int hr = 0; hr < 2; ++hr) {
@@ -1419,8 +1461,8 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                             const float nvv = __half2float(vnrm[r]);
 #pragma unroll
                             for (int j = 0; j < NT; ++j) {
-                                const float pp = exp2f(sv[mt][hr][j] - muse[j]);
-                                l_run[j] += pp;
+                                const float pp = exp2f(sv[rg][mt][hr][j] - muse[rg][j]);
+                                l_run[rg][j] += pp;
                                 pv[hr][j] = ok ? pp * nvv : 0.0f;
                             }
                         }
@@ -1430,14 +1472,16 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                         // the output.  NT == 1 puts the lo part in the free column 2t + 1, NT == 2
                         // multiplies V by it in a second mma.  Decode keeps one fp16 P, as fp16
                         // attention does.
-                        uint32_t x0, x1, pl0 = 0u, pl1 = 0u;
+                        uint32_t x0, x1;
+                        pl0[rg] = 0u;
+                        pl1[rg] = 0u;
                         if constexpr (NT == 2) {
                             if constexpr (MULTI) {
                                 uint32_t y0, y1;
                                 split_f16x2(pv[0][0], pv[0][1], x0, y0);
                                 split_f16x2(pv[1][0], pv[1][1], x1, y1);
-                                pl0 = movmatrix_t(y0);
-                                pl1 = movmatrix_t(y1);
+                                pl0[rg] = movmatrix_t(y0);
+                                pl1[rg] = movmatrix_t(y1);
                             } else {
                                 x0 = pack_f16(pv[0][0], pv[0][1]);
                                 x1 = pack_f16(pv[1][0], pv[1][1]);
@@ -1451,7 +1495,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                             x0 = pack_f16(pv[0][0], 0.0f);
                             x1 = pack_f16(pv[1][0], 0.0f);
                         }
-                        const uint32_t pb0 = movmatrix_t(x0), pb1 = movmatrix_t(x1);
+                        pb0[rg] = movmatrix_t(x0);
+                        pb1[rg] = movmatrix_t(x1);
+                        }
                         // V of tokens 2t, 2t+1, 2t+8, 2t+9 of this m-tile, thread g's dims
                         constexpr bool SPLIT = MULTI && NT == 2;
                         if constexpr (C::VPAIR) {
@@ -1473,8 +1519,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                         const uint32_t a1 = lds32(p01.addr(2 * k + 1, vtab_a, lane4));
                                         const uint32_t a2 = lds32(p89.addr(2 * k, vtab_a, lane4));
                                         const uint32_t a3 = lds32(p89.addr(2 * k + 1, vtab_a, lane4));
-                                        mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
-                                        if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+                                        for (int rg = 0; rg < RG; ++rg) {
+                                            mma16816(O[rg][dm], a0, a1, a2, a3, pb0[rg], pb1[rg]);
+                                            if constexpr (SPLIT) mma16816(O[rg][dm], a0, a1, a2, a3, pl0[rg], pl1[rg]);
+                                        }
                                     }
                                 }
                             }
@@ -1491,8 +1540,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                                 const uint32_t a1 = v_role<VB, C::VCW, C::VMODE>(v0, v1, 2 * dm + 1, vtab_a, lane4);
                                 const uint32_t a2 = v_role<VB, C::VCW, C::VMODE>(v2, v3, 2 * dm, vtab_a, lane4);
                                 const uint32_t a3 = v_role<VB, C::VCW, C::VMODE>(v2, v3, 2 * dm + 1, vtab_a, lane4);
-                                mma16816(O[dm], a0, a1, a2, a3, pb0, pb1);
-                                if constexpr (SPLIT) mma16816(O[dm], a0, a1, a2, a3, pl0, pl1);
+#pragma unroll
+                                for (int rg = 0; rg < RG; ++rg) {
+                                    mma16816(O[rg][dm], a0, a1, a2, a3, pb0[rg], pb1[rg]);
+                                    if constexpr (SPLIT) mma16816(O[rg][dm], a0, a1, a2, a3, pl0[rg], pl1[rg]);
+                                }
                             }
                         }
                     }
@@ -1500,100 +1552,108 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty + s);
             }
-            // ------------------------------------------------------------ warp totals
-            TQ_TL(tl_t, 4);
+            // (row group by row group: one partial record each)
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 4);
-                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 8);
-                l_run[j] += __shfl_xor_sync(kFullMask, l_run[j], 16);
-            }
-            if (g == 0) {
+            for (int rg = 0; rg < RG; ++rg) {
+                // ------------------------------------------------------------ warp totals
+                TQ_TL(tl_t, 4);
+#pragma unroll
+                for (int j = 0; j < NT; ++j) {
+                    l_run[rg][j] += __shfl_xor_sync(kFullMask, l_run[rg][j], 4);
+                    l_run[rg][j] += __shfl_xor_sync(kFullMask, l_run[rg][j], 8);
+                    l_run[rg][j] += __shfl_xor_sync(kFullMask, l_run[rg][j], 16);
+                }
+                if (g == 0) {
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const int q = (NT == 2) ? 2 * t + j : t;
+                        wm[warp * kGP + q] = m_run[rg][j];
+                        wl[warp * kGP + q] = l_run[rg][j];
+                    }
+                    if constexpr (NT == 1) {
+                        wm[warp * kGP + 4 + t] = -CUDART_INF_F;
+                        wl[warp * kGP + 4 + t] = 0.0f;
+                    }
+                }
+                // every consumer is done with the ring, wm / wl are visible, and the producer has no
+                // copy in flight (barrier 2 counts the producer warp's arrival); with a merge area of
+                // its own the producer goes on, and the consumers alone meet
+                // (a second row group: the consumers alone, the producer arrived once)
+                if (SEP || rg > 0)
+                    asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+                else
+                    asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
+                TQ_TL(tl_t, 5);
+                float f[NT];
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
                     const int q = (NT == 2) ? 2 * t + j : t;
-                    wm[warp * kGP + q] = m_run[j];
-                    wl[warp * kGP + q] = l_run[j];
+                    float M = -CUDART_INF_F;
+                    for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+                    // the V table holds v_alpha * c: divide it out here, once per output
+                    f[j] = (m_run[rg][j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[rg][j] - M) / a.cv.v_alpha;
                 }
-                if constexpr (NT == 1) {
-                    wm[warp * kGP + 4 + t] = -CUDART_INF_F;
-                    wl[warp * kGP + 4 + t] = 0.0f;
+                // Each warp's O slice goes to shared memory as float2 units (dims 2c, 2c + 1 of one
+                // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
+                // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
+                // of a row parity on the same two banks).
+                float2* const merge_base = reinterpret_cast<float2*>(SEP ? smem + C::SMEM : ring);
+                float2* slice = merge_base + warp * (SROWS * D / 2);
+#pragma unroll
+                for (int dm = 0; dm < C::KT; ++dm) {
+                    const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
+                    if constexpr (NT == 2) {
+                        slice[merge_slot<D>(2 * t, c)] = make_float2(f[0] * O[rg][dm][0], f[0] * O[rg][dm][2]);
+                        slice[merge_slot<D>(2 * t + 1, c)] = make_float2(f[1] * O[rg][dm][1], f[1] * O[rg][dm][3]);
+                    } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
+                        slice[merge_slot<D>(t, c)] = make_float2(f[0] * (O[rg][dm][0] + O[rg][dm][1]), f[0] * (O[rg][dm][2] + O[rg][dm][3]));
+                        slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                    } else {
+                        slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[rg][dm][0], f[0] * O[rg][dm][2]);
+                        if constexpr (SROWS == kGP) slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                    }
                 }
-            }
-            // every consumer is done with the ring, wm / wl are visible, and the producer has no
-            // copy in flight (barrier 2 counts the producer warp's arrival); with a merge area of
-            // its own the producer goes on, and the consumers alone meet
-            if constexpr (SEP)
                 asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-            else
-                asm volatile("bar.sync 2, %0;" ::"n"((C::NWC + 1) * 32) : "memory");
-            TQ_TL(tl_t, 5);
-            float f[NT];
+                // fixed-order sum of the warp slices, straight into this CTA's partial record: thread i
+                // sums the float4 at physical units 2i, 2i + 1 of every slice (the same swizzled place
+                // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
+                float* part = STREAM ? partial_slot_ptr(a.ws, p, static_cast<int64_t>(blockIdx.x) + u, D)
+                                     : partial_ptr(a.ws, p, vu + rg, split, D);
+                const float4* all4 = reinterpret_cast<const float4*>(merge_base);
+                float4* part4 = reinterpret_cast<float4*>(part);
+                for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
+                    const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
+                    if (SROWS < kGP && row >= SROWS) {  // rows with no query head
+                        part4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        continue;
+                    }
+                    float4 acc = all4[i];
 #pragma unroll
-            for (int j = 0; j < NT; ++j) {
-                const int q = (NT == 2) ? 2 * t + j : t;
-                float M = -CUDART_INF_F;
-                for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
-                // the V table holds v_alpha * c: divide it out here, once per output
-                f[j] = (m_run[j] == -CUDART_INF_F) ? 0.0f : exp2f(m_run[j] - M) / a.cv.v_alpha;
-            }
-            // Each warp's O slice goes to shared memory as float2 units (dims 2c, 2c + 1 of one
-            // row) at merge_slot(): row-major with the low bits of c XOR-ed, so that the 16 lanes
-            // of a half-warp store to 16 distinct bank pairs (row-major without it put every lane
-            // of a row parity on the same two banks).
-            float2* const merge_base = reinterpret_cast<float2*>(SEP ? smem + C::SMEM : ring);
-            float2* slice = merge_base + warp * (SROWS * D / 2);
-#pragma unroll
-            for (int dm = 0; dm < C::KT; ++dm) {
-                const int c = (D / 16) * g + dm;  // dims (D/8) g + 2 dm + {0, 1}
-                if constexpr (NT == 2) {
-                    slice[merge_slot<D>(2 * t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
-                    slice[merge_slot<D>(2 * t + 1, c)] = make_float2(f[1] * O[dm][1], f[1] * O[dm][3]);
-                } else if constexpr (MULTI) {  // columns 2t, 2t + 1: the hi and lo parts of row t's P
-                    slice[merge_slot<D>(t, c)] = make_float2(f[0] * (O[dm][0] + O[dm][1]), f[0] * (O[dm][2] + O[dm][3]));
-                    slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
-                } else {
-                    slice[merge_slot<D>(t, c)] = make_float2(f[0] * O[dm][0], f[0] * O[dm][2]);
-                    if constexpr (SROWS == kGP) slice[merge_slot<D>(4 + t, c)] = make_float2(0.0f, 0.0f);
+                    for (int w = 1; w < C::NWC; ++w) {
+                        const float4 x = all4[w * (SROWS * D / 4) + i];
+                        acc.x += x.x;
+                        acc.y += x.y;
+                        acc.z += x.z;
+                        acc.w += x.w;
+                    }
+                    const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
+                    part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
                 }
-            }
-            asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
-            // fixed-order sum of the warp slices, straight into this CTA's partial record: thread i
-            // sums the float4 at physical units 2i, 2i + 1 of every slice (the same swizzled place
-            // in each) and stores it at its logical place (units c0 and c0 ^ 1 of the row)
-            float* part = STREAM ? partial_slot_ptr(a.ws, p, static_cast<int64_t>(blockIdx.x) + u, D)
-                                 : partial_ptr(a.ws, p, vu, split, D);
-            const float4* all4 = reinterpret_cast<const float4*>(merge_base);
-            float4* part4 = reinterpret_cast<float4*>(part);
-            for (int i = tid; i < kGP * D / 4; i += C::NWC * 32) {
-                const int row = (2 * i) / (D / 2), cp = (2 * i) % (D / 2);
-                if (SROWS < kGP && row >= SROWS) {  // rows with no query head
-                    part4[i] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                    continue;
+                if (tid < kGP) {
+                    const int q = tid;
+                    float M = -CUDART_INF_F;
+                    for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
+                    float L = 0.0f;
+                    for (int w = 0; w < C::NWC; ++w) {
+                        const float mw = wm[w * kGP + q];
+                        if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
+                    }
+                    const int Gg = (rg == 0) ? G : G1;  // rows of this group
+                    part[kGP * D + q] = (q < Gg) ? M : -CUDART_INF_F;
+                    part[kGP * D + kGP + q] = (q < Gg) ? L : 0.0f;
                 }
-                float4 acc = all4[i];
-#pragma unroll
-                for (int w = 1; w < C::NWC; ++w) {
-                    const float4 x = all4[w * (SROWS * D / 4) + i];
-                    acc.x += x.x;
-                    acc.y += x.y;
-                    acc.z += x.z;
-                    acc.w += x.w;
-                }
-                const int c0 = merge_slot<D>(row, cp) - row * (D / 2);  // the swizzle is an involution
-                part4[row * (D / 4) + (c0 >> 1)] = (c0 & 1) ? make_float4(acc.z, acc.w, acc.x, acc.y) : acc;
-            }
-            if (tid < kGP) {
-                const int q = tid;
-                float M = -CUDART_INF_F;
-                for (int w = 0; w < C::NWC; ++w) M = fmaxf(M, wm[w * kGP + q]);
-                float L = 0.0f;
-                for (int w = 0; w < C::NWC; ++w) {
-                    const float mw = wm[w * kGP + q];
-                    if (mw != -CUDART_INF_F) L += wl[w * kGP + q] * exp2f(mw - M);
-                }
-                part[kGP * D + q] = (q < G) ? M : -CUDART_INF_F;
-                part[kGP * D + kGP + q] = (q < G) ? L : 0.0f;
+                // the next group rewrites wm / wl and the slices once every thread is done with them
+                if (RG > 1 && rg + 1 < RG) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
             }
             if constexpr (STREAM) {
                 itg += ntiles;
@@ -1637,16 +1697,16 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI>::MAXREG))
 cudaError_t encode_raw_k_map(CUtensorMap* map, const void* k, int dim, int64_t rows, int box_rows);
 
 // Launch of one instantiation; split plan for one CTA per SM.
-template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false, bool STREAM = false>
+template <int D, int KB, int VB, int NT, bool MULTI, bool QJL = false, bool STREAM = false, int RG = 1>
 cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
-    using C = Cfg<D, KB, VB, NT, QJL, MULTI>;
+    using C = Cfg<D, KB, VB, NT, QJL, MULTI, RG>;
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaGetDevice(&dev);
     const uint64_t bit = 1ull << (dev & 63);
     constexpr int SMEM = C::SMEM + stream_merge_bytes<D, KB, VB, NT, QJL, MULTI, STREAM>();
     if (!(configured.load() & bit)) {
-        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM>,
+        cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM, RG>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
@@ -1658,7 +1718,7 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = STREAM ? dim3(p.n_cta, 1) : dim3(p.n_split, p.n_units * p.q_chunks);
+    cfg.gridDim = STREAM ? dim3(p.n_cta, 1) : dim3(p.n_split, p.n_units * (p.q_chunks / RG));
     cfg.blockDim = dim3(C::NTHREADS);
     cfg.dynamicSmemBytes = SMEM;
     p.decode_smem = SMEM;  // the combine kernel sizes its footprint against it
@@ -1668,7 +1728,7 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM>, a, p, kmap);
+    return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, KB, VB, NT, MULTI, QJL, STREAM, RG>, a, p, kmap);
 }
 
 #define TQ_MMA_CASE(KB_, VB_)                                                                 \
@@ -1682,6 +1742,10 @@ cudaError_t launch_inst(const DecodeArgs& a, DecodePlan& p, cudaStream_t st) {
                     if constexpr (mma_fits(D, KB_, VB_, false, true))                         \
                         return nt == 3 ? launch_inst<D, KB_, VB_, 1, true>(a, p, st)              \
                                        : launch_inst<D, KB_, VB_, 2, true>(a, p, st);             \
+                    return cudaErrorNotSupported;                                             \
+                case 7:                                                                       \
+                    if constexpr (KB_ == 8 && (D & (D - 1)) == 0 && mma_fits_rg2(D, KB_, VB_)) \
+                        return launch_inst<D, KB_, VB_, 2, true, false, false, 2>(a, p, st);  \
                     return cudaErrorNotSupported;                                             \
                 default:                                                                      \
                     if constexpr (KB_ <= 4 && (D & (D - 1)) == 0 && mma_fits(D, KB_, VB_, true)) \

@@ -60,7 +60,7 @@ def _run(w, L, lens, tail_lens=None, max_tail=0, seed=700):
     return got, ref, ws
 
 
-@pytest.mark.parametrize("G,L", [(1, 2), (4, 2), (8, 4), (2, 7), (8, 5)])
+@pytest.mark.parametrize("G,L", [(1, 2), (4, 2), (8, 4), (2, 7), (8, 5), (3, 10)])
 @pytest.mark.parametrize("kb,vb", [(8, 3), (4, 4), (16, 4), (3, 2)])
 def test_multi_small_all_outputs(G, L, kb, vb):
     # lengths: a long sequence, an empty one, one shorter than L, one ending inside a tile
