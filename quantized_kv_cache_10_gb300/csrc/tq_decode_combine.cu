@@ -317,21 +317,30 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (WIDE ? 4 : (VPL <= 5 ? 8 
         s_l[warp] = l;
     }
     __syncthreads();
-    if (warp != 0) return;
-    m = -CUDART_INF_F;
-    l = 0.0f;
+    // the dense inverse rotation is shared by the four warps; the Walsh-Hadamard one is
+    // warp 0's alone
+    const bool dense = !((VPL & (VPL - 1)) == 0 && a.cv.is_wht);
+    if (!dense && warp != 0) return;
+    if (warp == 0) {
+        m = -CUDART_INF_F;
+        l = 0.0f;
 #pragma unroll
-    for (int v = 0; v < VPL; ++v) acc[v] = 0.0f;
+        for (int v = 0; v < VPL; ++v) acc[v] = 0.0f;
 #pragma unroll
-    for (int w = 0; w < kCombineWarps; ++w) {
-        float os[VPL];
+        for (int w = 0; w < kCombineWarps; ++w) {
+            float os[VPL];
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) os[v] = s_o[w][lane * VPL + v];
-        merge_state<VPL>(m, l, acc, s_m[w], s_l[w], os);
+            for (int v = 0; v < VPL; ++v) os[v] = s_o[w][lane * VPL + v];
+            merge_state<VPL>(m, l, acc, s_m[w], s_l[w], os);
+        }
+        const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;  // seq_len 0: zero output
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) acc[v] *= inv;
+        if (dense) {  // the merged row for every warp (warp 0 has read the states)
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) s_o[0][lane * VPL + v] = acc[v];
+        }
     }
-    const float inv = (l > 0.0f) ? 1.0f / l : 0.0f;  // seq_len 0: zero output
-#pragma unroll
-    for (int v = 0; v < VPL; ++v) acc[v] *= inv;
 
     float res[VPL];
     bool done = false;
@@ -367,20 +376,36 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (WIDE ? 4 : (VPL <= 5 ? 8 
         }
     }
     if (!done) {
-        // Q^T acc / sqrt(d): column c of the output is sum_j Q[j][c] acc[j], j ascending
+        // Q^T acc / sqrt(d): column c of the output is sum_j Q[j][c] acc[j]; warp w sums the
+        // quarter j in [w D/4, (w + 1) D/4) ascending (Q rows across the lanes, acc[j] a
+        // broadcast from shared memory), and warp 0 adds the four in a fixed order
+        __syncthreads();
         const float f = rsqrtf(static_cast<float>(D));
+        constexpr int JW = (D + kCombineWarps - 1) / kCombineWarps;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) res[v] = 0.0f;
         const float* qcol = a.cv.q + lane * VPL;
-        for (int src = 0; src < 32; ++src) {
 #pragma unroll
-            for (int w = 0; w < VPL; ++w) {
-                const float xj = __shfl_sync(kFullMask, acc[w], src);
-                const float* qrow = qcol + static_cast<int64_t>(src * VPL + w) * D;
+        for (int jj = 0; jj < JW; ++jj) {  // (unrolled: every load of the quarter in flight at once)
+            const int j = warp * JW + jj;
+            if (j < D) {
+                const float xj = s_o[0][j];
+                const float* qrow = qcol + static_cast<int64_t>(j) * D;
 #pragma unroll
                 for (int v = 0; v < VPL; ++v) res[v] = fmaf(__ldg(qrow + v), xj, res[v]);
             }
         }
+        __syncthreads();  // every warp has read the merged row
+        if (warp != 0) {
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) s_o[warp][lane * VPL + v] = res[v];
+        }
+        __syncthreads();
+        if (warp != 0) return;
+#pragma unroll
+        for (int w = 1; w < kCombineWarps; ++w)
+#pragma unroll
+            for (int v = 0; v < VPL; ++v) res[v] += s_o[w][lane * VPL + v];
 #pragma unroll
         for (int v = 0; v < VPL; ++v) res[v] *= f;
     }
