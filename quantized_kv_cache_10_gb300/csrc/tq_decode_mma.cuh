@@ -691,32 +691,38 @@ __device__ __forceinline__ void rotate_queries(const DecodeArgs& a, const uint16
         for (int i = ctid; i < kGP * D; i += NTH)
             qs[i] = (i < G * D) ? __half2float(__ushort_as_half(qg[i])) : 0.0f;
         asm volatile("bar.sync 1, %0;" ::"n"(NWC * 32) : "memory");
-        constexpr int CPT = (D + NTH - 1) / NTH;  // columns per thread
-        float acc[CPT][kGP];
+        // (when D divides the threads twice or more, each column's rows are split between
+        // RS threads: each loads the column, then forms kGP / RS of its rows)
+        constexpr int RS = (NTH >= 4 * D) ? 4 : (NTH >= 2 * D) ? 2 : 1;
+        constexpr int RPT = kGP / RS;             // rows per thread
+        constexpr int CPT = (D * RS + NTH - 1) / NTH;  // (column, row slice) items per thread
+        float acc[CPT][RPT];
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
-            const int j = ctid + NTH * c;
+            const int item = ctid + NTH * c;
+            const int j = item % D, g0 = (item / D) * RPT;
 #pragma unroll
-            for (int g = 0; g < kGP; ++g) acc[c][g] = 0.0f;
-            if (j < D) {
+            for (int g = 0; g < RPT; ++g) acc[c][g] = 0.0f;
+            if (item < D * RS) {
                 float col[D];
 #pragma unroll
                 for (int i = 0; i < D; ++i) col[i] = __ldg(a.ck.qt + static_cast<int64_t>(i) * D + j);
 #pragma unroll
-                for (int g = 0; g < kGP; ++g)
-                    if (g < G)
+                for (int g = 0; g < RPT; ++g)
+                    if (g0 + g < G)
 #pragma unroll
-                        for (int i = 0; i < D; ++i) acc[c][g] = fmaf(col[i], qs[g * D + i], acc[c][g]);
+                        for (int i = 0; i < D; ++i) acc[c][g] = fmaf(col[i], qs[(g0 + g) * D + i], acc[c][g]);
             }
         }
         asm volatile("bar.sync 1, %0;" ::"n"(NWC * 32) : "memory");
         const float f = kLog2e * a.scale * rsqrtf(static_cast<float>(D)) / a.ck.k_alpha;
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
-            const int j = ctid + NTH * c;
-            if (j < D)
+            const int item = ctid + NTH * c;
+            const int j = item % D, g0 = (item / D) * RPT;
+            if (item < D * RS)
 #pragma unroll
-                for (int g = 0; g < kGP; ++g) qs[g * D + j] = acc[c][g] * f;
+                for (int g = 0; g < RPT; ++g) qs[(g0 + g) * D + j] = acc[c][g] * f;
         }
     }
 }
