@@ -1179,8 +1179,9 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
                 // u = S q' for this CTA's query rows, as B fragments of the sketch k-tiles ("How I
                 // built VeloxQuant-MLX", Stage 3: the correction reads <S_j, q> for every sketch
                 // row j).  Sketch k-tile kk, thread (g, t): k = 2t, 2t+1, 2t+8, 2t+9 are sketch rows
-                // j0 .. j0 + 3, j0 = 32 (kk / 2) + 16 (kk % 2) + 4t -- nibble t of the half kk % 2
-                // of the keys' sign word kk / 2.  q' is split into fp16 hi and lo as for the scores.
+                // 32 (kk / 2) + b, b = 4t + 2 (kk % 2) + 0, 16, 1, 17 -- bits b of the keys' sign
+                // word kk / 2, so that the two bits of an A register sit 16 apart and one shift puts
+                // them on its fp16 sign bits.  q' is split into fp16 hi and lo as for the scores.
                 // Warp w takes sketch rows j = 32 w + lane for all rows of q' (S^T rows read
                 // across the lanes, coalesced; q' broadcast from shared memory), then forms the
                 // fragments of k-tiles 2w and 2w + 1 from its lanes by shuffles.
@@ -1204,11 +1205,11 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
                         float hi[4], lo[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            // sketch row 32 w + 16 h + 4 tt + e of query row qh, from lane 16 h + 4 tt + e
+                            // sketch row 32 w + b of query row qh, from lane b = 4 tt + 2 h + (e / 2) + 16 (e % 2)
                             float x = 0.0f;
 #pragma unroll
                             for (int g2 = 0; g2 < kGP; ++g2) {
-                                const float y = __shfl_sync(kFullMask, uq[g2], 16 * h + 4 * tt + e);
+                                const float y = __shfl_sync(kFullMask, uq[g2], 4 * tt + 2 * h + (e >> 1) + 16 * (e & 1));
                                 if (g2 == qh) x = y;
                             }
                             hi[e] = __half2float(__float2half_rn(x));
@@ -1359,18 +1360,20 @@ __global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
                                 const uint32_t sga = smem_addr(sg) + static_cast<uint32_t>(ra * (D / 8));
                                 const uint32_t sgb = smem_addr(sg) + static_cast<uint32_t>(rb * (D / 8));
                                 const uint32_t ubq_a = smem_addr(ubq_s);
+                                const int sh0 = 15 - 4 * t;  // bit 4t of a sign word -> bit 15
 #pragma unroll
                                 for (int w4 = 0; w4 < D / 32; ++w4) {
                                     const uint32_t wsa = lds32(sga + 4 * w4), wsb = lds32(sgb + 4 * w4);
 #pragma unroll
                                     for (int h = 0; h < 2; ++h) {
                                         const int kk = 2 * w4 + h;
-                                        const uint32_t na = wsa >> (16 * h + 4 * t), nb = wsb >> (16 * h + 4 * t);
-                                        // bit b of the nibble -> sign bit of half b (k = 2t + b, 2t + 8 + b)
-                                        const uint32_t a0 = hva ^ (((na & 1u) << 15) | ((na & 2u) << 30));
-                                        const uint32_t a2 = hva ^ (((na & 4u) << 13) | ((na & 8u) << 28));
-                                        const uint32_t a1 = hvb ^ (((nb & 1u) << 15) | ((nb & 2u) << 30));
-                                        const uint32_t a3 = hvb ^ (((nb & 4u) << 13) | ((nb & 8u) << 28));
+                                        // bits b, b + 16 (b = 4t + 2h) -> the sign bits of k = 2t, 2t + 1;
+                                        // bits b + 1, b + 17 -> those of k = 2t + 8, 2t + 9
+                                        const int s0 = sh0 - 2 * h;
+                                        const uint32_t a0 = hva ^ ((wsa << s0) & 0x80008000u);
+                                        const uint32_t a2 = hva ^ ((wsa << (s0 - 1)) & 0x80008000u);
+                                        const uint32_t a1 = hvb ^ ((wsb << s0) & 0x80008000u);
+                                        const uint32_t a3 = hvb ^ ((wsb << (s0 - 1)) & 0x80008000u);
                                         uint32_t u00, u01;
                                         lds64(ubq_a + ((kk * C::NTS) * 32 + lane) * 8, u00, u01);
                                         mma16816(sc[0][mt][0], a0, a1, a2, a3, u00, u01);
