@@ -773,8 +773,10 @@ constexpr int stream_merge_bytes() {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
+// (the token-balanced schedule's walk state does not fit the 144-register budget of the
+// 8-bit-key decode: those instantiations take 168, one CTA of 9 warps per SM either way)
 template <int D, int KB, int VB, int NT, bool MULTI, bool QJL, bool STREAM, int RG>
-__global__ void __maxnreg__((Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
+__global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL, MULTI, RG>::MAXREG))
     decode_mma_kernel(const DecodeArgs a, const DecodePlan p, const __grid_constant__ CUtensorMap kmap) {
     using C = Cfg<D, KB, VB, NT, QJL, MULTI, RG>;
     // two row groups per CTA: several query positions, 8-bit keys (their byte-permute
