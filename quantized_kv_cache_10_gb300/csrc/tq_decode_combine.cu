@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32, (WIDE ? 4 : (VPL <= 5 ? 8 
     int64_t rec0 = static_cast<int64_t>(vu) * p.n_split;
     if (p.stream) {
         int64_t first;
-        stream_unit_ctas(a, p.n_cta, b, kvh, lane, first, ns);
+        stream_unit_ctas(a, p.n_cta, p.stream_ovh, b, kvh, lane, first, ns);
         rec0 = first + u;
     }
     // wait for this call's decode grid (and the visibility of its records)

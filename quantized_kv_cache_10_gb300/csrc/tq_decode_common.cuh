@@ -39,20 +39,22 @@ __device__ __forceinline__ int32_t* error_ptr(void* ws) { return static_cast<int
 
 // Token-balanced schedule (several sequences, one query position, tensor-core kernel)
 // The units' tokens are laid end to end in unit order (u = b * Hkv + h), unit u
-// spanning kStreamOvh positions that hold no token and then len_b rounded up to a
+// spanning ovh positions that hold no token and then len_b rounded up to a
 // multiple of 8 (an empty sequence spans nothing), and CTA c takes positions
 // [c W, (c + 1) W), W = the total over the CTAs rounded up to 8 (at least kStreamMinW).
 // The positions without tokens stand for the fixed cost of starting a unit (its queries,
-// a partial record), so a CTA that starts more units gets fewer tokens.  Every boundary
+// a partial record), so a CTA that starts more units gets fewer tokens (ovh, a multiple
+// of 8, is the plan's: that cost is a time, so its size in tokens follows the loop's
+// rate).  Every boundary
 // is a multiple of 8, so each segment of a unit starts on an 8-token boundary (16-byte
 // aligned copies) and holds at least one real token.  Every warp that needs the
 // segments walks them itself (warp-collective, same result in each).
 constexpr int64_t kStreamMinW = 256;
-constexpr int64_t kStreamOvh = 320;
 
-// Positions of one unit of a sequence of len tokens.
-__device__ __forceinline__ int64_t stream_unit_ext(int64_t len) {
-    return len > 0 ? kStreamOvh + ((len + 7) & ~int64_t(7)) : 0;
+// Positions of one unit of a sequence of len tokens (ovh: the positions without tokens
+// at a unit's start, the plan's stream_ovh).
+__device__ __forceinline__ int64_t stream_unit_ext(int64_t ovh, int64_t len) {
+    return len > 0 ? ovh + ((len + 7) & ~int64_t(7)) : 0;
 }
 
 __device__ __forceinline__ int64_t stream_len(const DecodeArgs& a, int b, bool flag) {
@@ -65,12 +67,12 @@ __device__ __forceinline__ int64_t stream_len(const DecodeArgs& a, int b, bool f
 }
 
 // Total positions (all units) and the positions per CTA, W (warp-collective).
-__device__ __forceinline__ void stream_extent(const DecodeArgs& a, int n_cta, int lane, bool flag, int64_t& tot,
-                                              int64_t& W) {
+__device__ __forceinline__ void stream_extent(const DecodeArgs& a, int n_cta, int64_t ovh, int lane, bool flag,
+                                              int64_t& tot, int64_t& W) {
     tot = 0;
     for (int b0 = 0; b0 < a.B; b0 += 32) {
         const int bb = b0 + lane;
-        int64_t sp = bb < a.B ? stream_unit_ext(stream_len(a, bb, flag)) : 0;
+        int64_t sp = bb < a.B ? stream_unit_ext(ovh, stream_len(a, bb, flag)) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
         tot += sp;
@@ -83,42 +85,44 @@ __device__ __forceinline__ void stream_extent(const DecodeArgs& a, int n_cta, in
 // The CTAs whose positions cover unit (b, h): the first and their count (0 when the
 // sequence is empty) -- its records are slots first + u .. first + u + count - 1
 // (warp-collective).
-__device__ __forceinline__ void stream_unit_ctas(const DecodeArgs& a, int n_cta, int b, int h, int lane,
-                                                 int64_t& first, int& count) {
+__device__ __forceinline__ void stream_unit_ctas(const DecodeArgs& a, int n_cta, int64_t ovh, int b, int h,
+                                                 int lane, int64_t& first, int& count) {
     int64_t tot, W;
-    stream_extent(a, n_cta, lane, false, tot, W);
+    stream_extent(a, n_cta, ovh, lane, false, tot, W);
     // positions before sequence b: its units start there
     int64_t before = 0;
     for (int b0 = 0; b0 < b; b0 += 32) {
         const int bb = b0 + lane;
-        int64_t sp = bb < b ? stream_unit_ext(stream_len(a, bb, false)) : 0;
+        int64_t sp = bb < b ? stream_unit_ext(ovh, stream_len(a, bb, false)) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sp += __shfl_xor_sync(kFullMask, sp, o);
         before += sp;
     }
-    const int64_t ext = stream_unit_ext(stream_len(a, b, false));
+    const int64_t ext = stream_unit_ext(ovh, stream_len(a, b, false));
     const int64_t us = before * a.Hkv + static_cast<int64_t>(h) * ext;  // the unit's first position
-    first = (us + kStreamOvh) / W;                                      // ... holding a token
+    first = (us + ovh) / W;                                             // ... holding a token
     count = ext > 0 ? static_cast<int>((us + ext - 1) / W - first + 1) : 0;
 }
 
 struct StreamWalk {
     int b, h;          // current unit: sequence b, KV head h
     int64_t len;       // len_b (clamped)
-    int64_t ext;       // positions of the unit (kStreamOvh + len_b rounded up to 8)
-    int64_t us;        // first position of the unit (its tokens start at us + kStreamOvh)
+    int64_t ext;       // positions of the unit (ovh + len_b rounded up to 8)
+    int64_t us;        // first position of the unit (its tokens start at us + ovh)
+    int64_t ovh;       // positions without tokens at a unit's start
     int64_t a0;        // first token of this CTA's segment in the unit
     int64_t end;       // the CTA's positions end here
     int64_t W;         // positions per CTA
     bool valid;        // a segment is current
 
     // Segment [a0, a1) of unit (b, h), a1 <= len.
-    __device__ __forceinline__ int64_t a1() const { return min(len, end - (us + kStreamOvh)); }
+    __device__ __forceinline__ int64_t a1() const { return min(len, end - (us + ovh)); }
 
     // Walk start for CTA c of n_cta (lengths flagged by warp 0's lanes only).
-    __device__ __forceinline__ void init(const DecodeArgs& a, int c, int n_cta, int lane, bool flag) {
+    __device__ __forceinline__ void init(const DecodeArgs& a, int c, int n_cta, int64_t ovh_, int lane, bool flag) {
         int64_t tot;
-        stream_extent(a, n_cta, lane, flag, tot, W);
+        ovh = ovh_;
+        stream_extent(a, n_cta, ovh, lane, flag, tot, W);
         const int64_t P = static_cast<int64_t>(c) * W;
         valid = P < tot;
         end = min(P + W, tot);
@@ -131,7 +135,7 @@ struct StreamWalk {
         for (int b0 = 0; b0 < a.B; b0 += 32) {
             const int bb = b0 + lane;
             const int64_t L = bb < a.B ? stream_len(a, bb, false) : 0;
-            const int64_t sp = stream_unit_ext(L) * a.Hkv;
+            const int64_t sp = stream_unit_ext(ovh, L) * a.Hkv;
             int64_t inc = sp;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
@@ -144,10 +148,10 @@ struct StreamWalk {
                 b = b0 + l;
                 const int64_t sb = base + __shfl_sync(kFullMask, inc - sp, l);
                 len = __shfl_sync(kFullMask, L, l);
-                ext = stream_unit_ext(len);
+                ext = stream_unit_ext(ovh, len);
                 h = static_cast<int>((P - sb) / ext);
                 us = sb + static_cast<int64_t>(h) * ext;
-                const int64_t r0 = us + kStreamOvh;  // the unit's first token
+                const int64_t r0 = us + ovh;  // the unit's first token
                 a0 = P > r0 ? P - r0 : 0;
                 valid = end > r0;  // else the CTA's positions end before any token
                 return;
@@ -172,13 +176,13 @@ struct StreamWalk {
                 ++b;
                 len = b < a.B ? stream_len(a, b, false) : 0;
             } while (len == 0 && b < a.B);
-            ext = stream_unit_ext(len);
+            ext = stream_unit_ext(ovh, len);
             if (b >= a.B) {  // not reached: end <= total
                 valid = false;
                 return;
             }
         }
-        valid = end > us + kStreamOvh;
+        valid = end > us + ovh;
     }
 };
 

@@ -41,6 +41,11 @@
 
 namespace tq {
 
+// Positions without tokens per unit on the token-balanced schedule, at d <= 128 (scaled by
+// 128 / d) and at d 256.
+constexpr int kStreamOvhD128 = 768;
+constexpr int kStreamOvhD256 = 320;
+
 // ---------------------------------------------------------------------------
 // Host: compact decode tables, built once per codec.
 // The tensor cores take fp16 operands, and a centroid rounded to fp16 is off
@@ -240,6 +245,9 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
         sms + int64_t(p.n_units) <= p0.n_rec) {
         p.stream = 1;
         p.n_cta = static_cast<int>(sms);
+        // the fixed cost of starting a unit (its queries, the segment's merge and record),
+        // in tokens of the loop at this head dim
+        p.stream_ovh = (d <= 128 ? kStreamOvhD128 * (128 / d) : kStreamOvhD256) & ~7;
         switch (d) {
             case 64: e = launch_mma_d_stream_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
             case 128: e = launch_mma_d_stream_extern<128>(a, p, a.ck.bits, a.cv.bits, nt, st); break;
@@ -249,6 +257,7 @@ cudaError_t launch_decode_mma(const DecodeArgs& a, DecodePlan& p, cudaStream_t s
         if (e != cudaErrorNotSupported) return e;
         p.stream = 0;
         p.n_cta = 0;
+        p.stream_ovh = 0;
     }
     switch (a.cv.dim) {
         case 64: e = launch_mma_d_extern<64>(a, p, a.ck.bits, a.cv.bits, nt, st); break;

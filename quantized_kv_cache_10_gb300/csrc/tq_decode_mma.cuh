@@ -1023,7 +1023,7 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
             asm volatile("griddepcontrol.wait;" ::: "memory");
             if (lane == 0) allow_dependent_launch();
             StreamWalk sw;
-            sw.init(a, blockIdx.x, p.n_cta, lane, false);
+            sw.init(a, blockIdx.x, p.n_cta, p.stream_ovh, lane, false);
             int itg = 0;
             bool stop = false;
             while (sw.valid) {
@@ -1079,7 +1079,7 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
         // passed this wait.
         allow_dependent_launch();
         StreamWalk sw;
-        if constexpr (STREAM) sw.init(a, blockIdx.x, p.n_cta, lane, warp == 0);
+        if constexpr (STREAM) sw.init(a, blockIdx.x, p.n_cta, p.stream_ovh, lane, warp == 0);
         int itg = 0;  // ring position of the segment's first tile
         // One pass per segment of a unit's tokens: this CTA's split of its unit, or, on the
         // token-balanced schedule, each unit its positions cover (barrier 3 tells the

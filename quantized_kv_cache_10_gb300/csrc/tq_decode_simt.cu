@@ -279,6 +279,7 @@ bool make_decode_plan(int d, int device, int B, int Hq, int Hkv, int L, int64_t 
     plan.n_rec = int(nrec);
     plan.stream = 0;
     plan.n_cta = 0;
+    plan.stream_ovh = 0;
     plan.ws_bytes = plan.part_offset + size_t(nrec) * kGP * (d + 2) * sizeof(float);
     return true;
 }

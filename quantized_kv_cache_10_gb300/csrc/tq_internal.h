@@ -109,11 +109,13 @@ struct DecodePlan {
     size_t part_offset;  // byte offset of the split-K partial records
     int decode_smem;     // dynamic shared memory of the decode kernel launched (0: unknown)
     // Token-balanced schedule (tensor-core kernel, one query position, several sequences):
-    // the units' tokens laid end to end, unit u = b * Hkv + h spanning len_b rounded up to
-    // 8 positions, and CTA c of n_cta takes an equal share of the positions.  Its records
-    // are at slots c + u (the combine finds a unit's CTAs from the same lengths).
+    // the units' tokens laid end to end, unit u = b * Hkv + h spanning stream_ovh positions
+    // without tokens (the fixed cost of starting a unit) and len_b rounded up to 8, and CTA
+    // c of n_cta takes an equal share of the positions.  Its records are at slots c + u
+    // (the combine finds a unit's CTAs from the same lengths).
     int stream;          // 1: token-balanced schedule, 0: n_split splits of chunk tokens per unit
     int n_cta;           // CTAs of the token-balanced schedule
+    int stream_ovh;      // positions without tokens per unit (a multiple of 8)
     int n_rec;           // partial records the workspace holds
 };
 
