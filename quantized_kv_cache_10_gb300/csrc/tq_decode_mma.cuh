@@ -1193,11 +1193,16 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
 #pragma unroll
                     for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = 0.0f;
                     const float* col = a.ck.sketch_t + 32 * w + lane;
-#pragma unroll 4
-                    for (int i = 0; i < D; ++i) {
-                        const float sv = __ldg(col + static_cast<int64_t>(i) * D);
+                    // (16 loads in flight before their fmas: S^T comes from L2, one round trip
+                    // per batch; the sums still run over i ascending)
+                    for (int i0 = 0; i0 < D; i0 += 16) {
+                        float sv[16];
 #pragma unroll
-                        for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv, qs[g2 * D + i], uq[g2]);
+                        for (int k = 0; k < 16; ++k) sv[k] = __ldg(col + static_cast<int64_t>(i0 + k) * D);
+#pragma unroll
+                        for (int k = 0; k < 16; ++k)
+#pragma unroll
+                            for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv[k], qs[g2 * D + i0 + k], uq[g2]);
                     }
                     const int gg = lane >> 2, tt = lane & 3;
                     const int qh = (NT == 2) ? gg : (gg >> 1);
