@@ -159,6 +159,10 @@ __device__ __forceinline__ void lds64(uint32_t addr, uint32_t& a, uint32_t& b) {
     asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
 
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t a) {
+    asm volatile("st.shared.b32 [%0], %1;" ::"r"(addr), "r"(a) : "memory");
+}
+
 __device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
     asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
 }
@@ -1188,14 +1192,22 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
                 // across the lanes, coalesced; q' broadcast from shared memory), then forms the
                 // fragments of k-tiles 2w and 2w + 1 from its lanes by shuffles.
                 const uint32_t ubq_a = smem_addr(ubq_s);
-                for (int w = warp; w < D / 32; w += C::NWC) {
+                // With enough warps each block of 32 sketch rows is summed by two warps over the
+                // two halves of i (16 loads of S^T in flight per batch, from L2); the second
+                // warp's partial sums pass through the block's own fragment area, which the
+                // first warp reads before it writes the fragments there.
+                constexpr int NB = D / 32;
+                constexpr bool HALVES = 2 * NB <= C::NWC;
+                constexpr int RQ = (NT == 2) ? kGP : 4;                   // rows that hold a query
+                constexpr uint32_t PBYTES = (NT == 2) ? 1024u : 512u;     // a block's fragment area
+                const int part = HALVES ? warp / NB : 0;
+                for (int w = (HALVES ? warp % NB : warp); w < NB && part < 2; w += (HALVES ? NB : C::NWC)) {
                     float uq[kGP];
 #pragma unroll
                     for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = 0.0f;
                     const float* col = a.ck.sketch_t + 32 * w + lane;
-                    // (16 loads in flight before their fmas: S^T comes from L2, one round trip
-                    // per batch; the sums still run over i ascending)
-                    for (int i0 = 0; i0 < D; i0 += 16) {
+                    const int i_beg = HALVES ? part * (D / 2) : 0, i_end = HALVES ? i_beg + D / 2 : D;
+                    for (int i0 = i_beg; i0 < i_end; i0 += 16) {
                         float sv[16];
 #pragma unroll
                         for (int k = 0; k < 16; ++k) sv[k] = __ldg(col + static_cast<int64_t>(i0 + k) * D);
@@ -1203,6 +1215,18 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
                         for (int k = 0; k < 16; ++k)
 #pragma unroll
                             for (int g2 = 0; g2 < kGP; ++g2) uq[g2] = fmaf(sv[k], qs[g2 * D + i0 + k], uq[g2]);
+                    }
+                    if (HALVES) {
+                        const uint32_t pa = ubq_a + static_cast<uint32_t>(w) * PBYTES;
+                        if (part == 1) {
+#pragma unroll
+                            for (int g2 = 0; g2 < RQ; ++g2) sts32(pa + (g2 * 32 + lane) * 4, __float_as_uint(uq[g2]));
+                        }
+                        asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
+                        if (part == 1) break;
+#pragma unroll
+                        for (int g2 = 0; g2 < RQ; ++g2) uq[g2] += __uint_as_float(lds32(pa + (g2 * 32 + lane) * 4));
+                        __syncwarp();
                     }
                     const int gg = lane >> 2, tt = lane & 3;
                     const int qh = (NT == 2) ? gg : (gg >> 1);
@@ -1230,7 +1254,10 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
                             sts64(ubq_a + (kk * 32 + lane) * 8, pack_f16(v[0], v[1]), pack_f16(v[2], v[3]));
                         }
                     }
+                    if (HALVES) break;
                 }
+                // the warps without a block meet the halves' barrier too
+                if (HALVES && warp >= 2 * NB) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
             }
             if constexpr (C::BQ_SMEM || QJL) asm volatile("bar.sync 1, %0;" ::"n"(C::NWC * 32) : "memory");
 
