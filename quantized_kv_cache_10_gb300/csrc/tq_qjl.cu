@@ -18,7 +18,6 @@
 namespace tq {
 namespace {
 
-constexpr int kWarps = 8;
 constexpr unsigned kFull = 0xffffffffu;
 
 // x * 2^24 as an exact integer (every finite fp16 value is a multiple of 2^-24).
@@ -35,73 +34,113 @@ __device__ __forceinline__ int code_at(const uint8_t* row, int i, int bits) {
     return static_cast<int>((w >> sh) & ((1u << bits) - 1u));
 }
 
-// One warp per key vector (grid-stride); E = dim / 32.
+// Keys in batches of KB per warp (grid-stride over batches); E = dim / 32.  Per key the
+// warp forms the exact rotation and the fp32 residual (kept for the batch in shared
+// memory); then lane k runs key k's fp64 norm chain (so that one fp64 instruction serves
+// KB keys), and the sketch chains of all KB keys run together, each S^T load feeding KB
+// of them.  Every chain keeps its order (i ascending), so the results are the same bits.
 template <int E>
-__global__ void __launch_bounds__(kWarps * 32)
+struct QjlShape {
+    static constexpr int D = 32 * E;
+    static constexpr int WARPS = E >= 16 ? 2 : (E >= 8 ? 4 : 8);  // warps per CTA
+    static constexpr int KB = E >= 16 ? 4 : 8;                    // keys per batch
+    static constexpr int RS = D + 1;                              // residual row stride (floats)
+};
+
+template <int E>
+__global__ void __launch_bounds__(QjlShape<E>::WARPS * 32)
     qjl_sketch_kernel(const uint16_t* x, int64_t n, int64_t xstride, const uint8_t* codes, int64_t cstride,
                       const uint16_t* norms, const float* centroids, const uint32_t* sign_bits, const float* st,
                       int bits, uint8_t* signs, int64_t sstride, uint16_t* rnorms) {
-    constexpr int D = 32 * E;
-    __shared__ long long s_w[kWarps][D];
-    __shared__ float s_rho[kWarps][D];
+    using Q = QjlShape<E>;
+    constexpr int D = Q::D, KB = Q::KB, RS = Q::RS;
+    __shared__ long long s_w[Q::WARPS][D];
+    __shared__ float s_rho[Q::WARPS][KB * RS];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     long long* w = s_w[warp];
     float* rho = s_rho[warp];
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * kWarps + warp; v < n;
-         v += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const uint16_t* xr = x + v * xstride;
+    const int64_t nbatch = (n + KB - 1) / KB;
+    for (int64_t bt = static_cast<int64_t>(blockIdx.x) * Q::WARPS + warp; bt < nbatch;
+         bt += static_cast<int64_t>(gridDim.x) * Q::WARPS) {
+        const int64_t v0 = bt * KB;
+        const int nk = static_cast<int>(n - v0 < KB ? n - v0 : KB);
+        for (int k = 0; k < KB; ++k) {
+            float* rk = rho + k * RS;
+            if (k >= nk) {  // rows past the last key: zeros (their sums are not stored)
+                for (int i = lane; i < D; i += 32) rk[i] = 0.0f;
+                continue;
+            }
+            const int64_t v = v0 + k;
+            const uint16_t* xr = x + v * xstride;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int i = lane + 32 * e;
-            const long long k = f16_fixed(xr[i]);
-            w[i] = ((__ldg(sign_bits + (i >> 5)) >> (i & 31)) & 1u) ? -k : k;
-        }
-        __syncwarp();
-        // Sylvester butterfly in natural order, exact in int64 (|w| < 2^48)
-        for (int hh = 1; hh < D; hh <<= 1) {
-            for (int i = lane; i < D / 2; i += 32) {
-                const int lo = (i / hh) * (2 * hh) + (i % hh);
-                const long long a = w[lo], b = w[lo + hh];
-                w[lo] = a + b;
-                w[lo + hh] = a - b;
+            for (int e = 0; e < E; ++e) {
+                const int i = lane + 32 * e;
+                const long long kx = f16_fixed(xr[i]);
+                w[i] = ((__ldg(sign_bits + (i >> 5)) >> (i & 31)) & 1u) ? -kx : kx;
             }
             __syncwarp();
-        }
-        const double n16 = static_cast<double>(__half2float(__ushort_as_half(norms[v])));
-        const uint8_t* cr = codes + v * cstride;
+            // Sylvester butterfly in natural order, exact in int64 (|w| < 2^48)
+            for (int hh = 1; hh < D; hh <<= 1) {
+                for (int i = lane; i < D / 2; i += 32) {
+                    const int lo = (i / hh) * (2 * hh) + (i % hh);
+                    const long long a = w[lo], b = w[lo + hh];
+                    w[lo] = a + b;
+                    w[lo + hh] = a - b;
+                }
+                __syncwarp();
+            }
+            const double n16 = static_cast<double>(__half2float(__ushort_as_half(norms[v])));
+            const uint8_t* cr = codes + v * cstride;
 #pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const int i = lane + 32 * e;
-            const double c = static_cast<double>(__ldg(centroids + code_at(cr, i, bits)));
-            rho[i] = __double2float_rn(__fma_rn(-n16, c, static_cast<double>(w[i]) * 0x1.0p-24));
+            for (int e = 0; e < E; ++e) {
+                const int i = lane + 32 * e;
+                const double c = static_cast<double>(__ldg(centroids + code_at(cr, i, bits)));
+                rk[i] = __double2float_rn(__fma_rn(-n16, c, static_cast<double>(w[i]) * 0x1.0p-24));
+            }
+            __syncwarp();  // w is rewritten by the next key
         }
-        __syncwarp();
-        if (lane == 0) {
+        // residual norms: lane k, key k's fp64 chain over i ascending (rows RS apart:
+        // the lanes read distinct banks)
+        if (lane < nk) {
+            const float* rk = rho + lane * RS;
             double g2 = 0.0;
             for (int i = 0; i < D; ++i) {
-                const double r = static_cast<double>(rho[i]);
+                const double r = static_cast<double>(rk[i]);
                 g2 = __fma_rn(r, r, g2);
             }
-            rnorms[v] = __half_as_ushort(__double2half(sqrt(g2 / static_cast<double>(D))));
+            rnorms[v0 + lane] = __half_as_ushort(__double2half(sqrt(g2 / static_cast<double>(D))));
         }
-        // t_j for j = lane + 32 kk, each an fp32 fma chain over i ascending; S^T rows are
-        // read across the lanes (coalesced)
-        float t[E];
+        // t_j of every key of the batch, j = lane + 32 kk, each an fp32 fma chain over i
+        // ascending; S^T rows are read across the lanes (coalesced), each load feeding KB keys
+        float t[KB][E];
 #pragma unroll
-        for (int kk = 0; kk < E; ++kk) t[kk] = 0.0f;
+        for (int k = 0; k < KB; ++k)
+#pragma unroll
+            for (int kk = 0; kk < E; ++kk) t[k][kk] = 0.0f;
+#pragma unroll 2
         for (int i = 0; i < D; ++i) {
-            const float r = rho[i];
             const float* row = st + static_cast<int64_t>(i) * D + lane;
+            float sv[E];
 #pragma unroll
-            for (int kk = 0; kk < E; ++kk) t[kk] = __fmaf_rn(__ldg(row + 32 * kk), r, t[kk]);
-        }
-        uint32_t* sw = reinterpret_cast<uint32_t*>(signs + v * sstride);
+            for (int kk = 0; kk < E; ++kk) sv[kk] = __ldg(row + 32 * kk);
 #pragma unroll
-        for (int kk = 0; kk < E; ++kk) {
-            const uint32_t word = __ballot_sync(kFull, t[kk] < 0.0f);
-            if (lane == 0) sw[kk] = word;
+            for (int k = 0; k < KB; ++k) {
+                const float r = rho[k * RS + i];
+#pragma unroll
+                for (int kk = 0; kk < E; ++kk) t[k][kk] = __fmaf_rn(sv[kk], r, t[k][kk]);
+            }
         }
-        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            if (k >= nk) break;
+            uint32_t* sw = reinterpret_cast<uint32_t*>(signs + (v0 + k) * sstride);
+#pragma unroll
+            for (int kk = 0; kk < E; ++kk) {
+                const uint32_t word = __ballot_sync(kFull, t[k][kk] < 0.0f);
+                if (lane == 0) sw[kk] = word;
+            }
+        }
+        __syncwarp();  // the residual rows are rewritten by the next batch
     }
 }
 
@@ -109,12 +148,14 @@ template <int E>
 cudaError_t launch_e(const tq_codec* c, const uint16_t* x, int64_t n, int64_t xstride, const uint8_t* codes,
                      int64_t cstride, const uint16_t* norms, uint8_t* signs, int64_t sstride, uint16_t* rnorms,
                      cudaStream_t st) {
-    const int64_t want = (n + kWarps - 1) / kWarps;
+    using Q = QjlShape<E>;
+    const int64_t nbatch = (n + Q::KB - 1) / Q::KB;
+    const int64_t want = (nbatch + Q::WARPS - 1) / Q::WARPS;
     const int64_t cap = int64_t(num_sms(c->device)) * 16;
     const int grid = static_cast<int>(want < cap ? want : cap);
-    qjl_sketch_kernel<E><<<grid, kWarps * 32, 0, st>>>(x, n, xstride, codes, cstride, norms, c->d_centroids,
-                                                        c->d_sign_bits, c->d_sketch_t, c->bits, signs, sstride,
-                                                        rnorms);
+    qjl_sketch_kernel<E><<<grid, Q::WARPS * 32, 0, st>>>(x, n, xstride, codes, cstride, norms, c->d_centroids,
+                                                          c->d_sign_bits, c->d_sketch_t, c->bits, signs, sstride,
+                                                          rnorms);
     return cudaGetLastError();
 }
 
