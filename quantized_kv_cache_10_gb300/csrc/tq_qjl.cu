@@ -42,8 +42,8 @@ __device__ __forceinline__ int code_at(const uint8_t* row, int i, int bits) {
 template <int E>
 struct QjlShape {
     static constexpr int D = 32 * E;
-    static constexpr int WARPS = E >= 16 ? 2 : (E >= 8 ? 4 : 8);  // warps per CTA
-    static constexpr int KB = E >= 16 ? 4 : 8;                    // keys per batch
+    static constexpr int WARPS = E >= 16 ? 2 : 4;                 // warps per CTA
+    static constexpr int KB = E >= 16 ? 4 : (E >= 8 ? 8 : 16);    // keys per batch
     static constexpr int RS = D + 1;                              // residual row stride (floats)
 };
 
