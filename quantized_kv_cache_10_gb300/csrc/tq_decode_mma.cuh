@@ -149,6 +149,16 @@ __device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint
     lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx.ftz: relative
+// error ~2^-22, subnormal results flushed to zero, 2^-inf = 0).  The softmax weights it
+// forms are rounded to fp16 for the P.V contraction, and the flushed ones are below
+// 2^-126 of the running maximum.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ uint32_t lds32(uint32_t addr) {
     uint32_t v;
     asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(addr));
@@ -1471,7 +1481,7 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
                     for (int j = 0; j < NT; ++j) {
                         const float mn = fmaxf(m_run[rg][j], tmax[j]);
                         muse[rg][j] = (mn == -CUDART_INF_F) ? 0.0f : mn;
-                        alpha[j] = exp2f(m_run[rg][j] - muse[rg][j]);
+                        alpha[j] = ex2_approx(m_run[rg][j] - muse[rg][j]);
                         rescale |= (alpha[j] != 1.0f);
                         m_run[rg][j] = mn;
                         l_run[rg][j] *= alpha[j];
@@ -1504,7 +1514,7 @@ __global__ void __maxnreg__(((STREAM && KB == 8) ? 168 : Cfg<D, KB, VB, NT, QJL,
                             const float nvv = __half2float(vnrm[r]);
 #pragma unroll
                             for (int j = 0; j < NT; ++j) {
-                                const float pp = exp2f(sv[rg][mt][hr][j] - muse[rg][j]);
+                                const float pp = ex2_approx(sv[rg][mt][hr][j] - muse[rg][j]);
                                 l_run[rg][j] += pp;
                                 pv[hr][j] = ok ? pp * nvv : 0.0f;
                             }
