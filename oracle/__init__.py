@@ -17,11 +17,13 @@ What it computes, and from which pages (titles and sections):
     ("anyone still talking about mlx-swift-lm?") fixes what the fused kernel
     must equal.
 
-Parity status: every function is pinned by tests in tests/test_oracle_*.py
-except the dense (non-power-of-two) rotation, whose only pins are
-orthogonality, the Q R = G factorisation and agreement with an independent
-Householder factorisation -- "parity unpinned" beyond that, because the pages
-print no worked example for it.
+Parity status: every function is pinned by tests in tests/test_oracle_*.py and
+tests/test_codebook.py.  The dense (non-power-of-two) rotation is pinned to
+numpy's Householder QR of the same seeded Gaussian (sign-fixed, orthogonal) and,
+as applied in encode, to an independent fp64 product z = Q k, the exact norm and
+the threshold scale D / sqrt(d).  Which orthogonal matrix (the Gaussian stream,
+the QR sign convention) is a reading of ours: the pages print no worked example
+of it.
 """
 from __future__ import annotations
 
